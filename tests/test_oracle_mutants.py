@@ -1,0 +1,52 @@
+"""Planted mistakes: each mutant of the oracle's C source must fail a pin.
+
+A mutant is the oracle source with one plausible slip (a wrong index, a
+dropped term, a flipped sign, a transposed operand).  It is compiled to a
+temporary library on the CPU and the pin suite is run against it; the test
+passes only if the pins reject every mutant.  Nothing here touches a GPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+from oracle.build import SRC
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "gqa_head_interleaved": ("int h = kvh * G + g;", "int h = g * j->Hk + kvh;"),
+    "gather_offset_shift": ("int off = i % bs;", "int off = (i + 1) % bs;"),
+    "gather_block_off_by_one": ("int64_t phys = table[i / bs];", "int64_t phys = table[(i + 1) / bs];"),
+    "cache_layout_transposed": ("int64_t row = ((phys * Hk + kvh) * bs + off) * (int64_t)D;",
+                                "int64_t row = ((phys * bs + off) * Hk + kvh) * (int64_t)D;"),
+    "scale_dropped": ("z[i] = scale * dot;", "z[i] = dot;"),
+    "softmax_sign": ("double p = exp(z[i] - m);", "double p = exp(m - z[i]);"),
+    "normaliser_dropped": ("        o[d] /= l;\n}", "        o[d] /= 1.0;\n}"),
+    "merge_weight_drops_l": ("double w = lp[p] * exp(mp[p] - M);", "double w = exp(mp[p] - M);"),
+    "blocks_floor_plus_one": ("return (n_tokens + block_size - 1) / block_size;",
+                              "return n_tokens / block_size + 1;"),
+    "f16_exponent_bias": ("v = ldexp((double)(m | 0x400), e - 25);", "v = ldexp((double)(m | 0x400), e - 24);"),
+    "scatter_block_offset_swapped": ("size_t dst = (size_t)(((b * num_kv_heads + h) * block_size + o)) * row;",
+                                     "size_t dst = (size_t)(((o * num_kv_heads + h) * block_size + b)) * row;"),
+    "copy_direction_swapped": ("memcpy((char *)k_caches[l] + (size_t)dst * block_bytes,\n                   (const char *)k_caches[l] + (size_t)src * block_bytes",
+                               "memcpy((char *)k_caches[l] + (size_t)src * block_bytes,\n                   (const char *)k_caches[l] + (size_t)dst * block_bytes"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutant_src = tmp_path / "mutant.c"
+    mutant_src.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-std=c11", "-O1", "-fPIC", "-shared", "-D_POSIX_C_SOURCE=200809L",
+                    str(mutant_src), "-o", str(lib), "-lm", "-lpthread"], check=True)
+    env = dict(os.environ, PKV_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
