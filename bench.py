@@ -1,0 +1,545 @@
+"""Benchmark of the paged decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: copy-on-write block
+copies (when the step has any), the scatter of the new tokens into their
+slots, and paged decode attention (single pass, or partition pass plus
+log-sum-exp reduce).  Default workload: the Llama-7B-shaped fp16 decode
+(batch 64, 32 heads, head_dim 128, block 16, lengths U{128..2048}, 100 steps).
+
+Prints ONE JSON line (rank 0).  value = algorithmic bytes of the step / device
+time of the step, with every input resident in HBM; L2 is flushed (256 MiB
+write) before every step, outside the timed events.  roofline = the decode
+kernel's own algorithmic bytes per launch / its mean launch time against the
+measured HBM copy bandwidth.  e2e = the same metric with the step's inputs
+copied from pinned host memory and the output read back inside the timed
+region.  cpu_baseline = the CPU oracle on a bounded sample of the same steps.
+
+--impl reference times the oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, PagedDecodeWorkload, get  # noqa: E402
+from workloads.runner import DeviceState, algorithmic_bytes  # noqa: E402
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak); seq-steps/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+SEED_BASE = 311 * 100
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=95)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="llama7b_f16")
+    ap.add_argument("--block-size", type=int, default=0)
+    ap.add_argument("--partition-size", type=int, default=-1, help="-1: the preset's choice")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--identity-tables", action="store_true",
+                    help="place every sequence's blocks contiguously (gather-overhead comparison)")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def local_device():
+    lr = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(lr)
+    return torch.device("cuda", lr)
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def run_native(args):
+    dist, rank, world = dist_setup()
+    dev = local_device()
+    cfg = get(args.config)
+    if args.block_size:
+        cfg = cfg.with_(block_size=args.block_size)
+    seed = SEED_BASE + CONFIGS.index(get(args.config)) + 1000 * rank
+    total = args.warmup + args.steps
+    w = PagedDecodeWorkload(cfg, seed, total_steps=max(total, cfg.steps),
+                            contiguous=args.identity_tables)
+    P = cfg.partition_size if args.partition_size < 0 else args.partition_size
+    out_dtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[cfg.dtype]
+    state = DeviceState(cfg, w, seed, device=dev, out_dtype=out_dtype)
+    host_inputs = [w.next_step() for _ in range(total)]
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(cfg, state, host_inputs, args.cpu_seconds, seed)
+
+    steps = [state.to_device(inp) for inp in host_inputs]
+    import paged_kv_cache_311_gb300 as pkv
+    for s in steps:
+        state.ensure_workspace(s.max_context_len, P)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    out_bytes = torch.tensor([], dtype=out_dtype).element_size()
+
+    # warm-up
+    for s in steps[:args.warmup]:
+        state.run_step(s, partition_size=P)
+    torch.cuda.synchronize()
+    state.status.zero_()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches = 0
+    decode_launches = []
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    for i, s in enumerate(steps[args.warmup:]):
+        flush.fill_(i)
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        if s.cow_pairs is not None:
+            pkv.copy_blocks([state.k_cache], [state.v_cache], s.cow_pairs,
+                            device_status=state.status)
+            launches += 1
+        pkv.reshape_and_cache(s.key, s.value, state.k_cache, state.v_cache, s.slot_mapping,
+                              device_status=state.status)
+        launches += 1
+        e1.record(stream)
+        pkv.paged_attention_decode(state.out, s.q, state.k_cache, state.v_cache, s.block_tables,
+                                   s.context_lens, cfg.softmax_scale,
+                                   max_context_len=s.max_context_len, partition_size=P,
+                                   workspace=state.workspace, device_status=state.status)
+        n = pkv.last_decode_launches()
+        decode_launches.append(n)
+        launches += n
+        e2.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    if state.status.item() != 0:
+        raise RuntimeError(f"device status {state.status.item()} during the timed steps")
+
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    tot_ms = sum(step_ms)
+    bytes_step, bytes_dec, seqs = 0, 0, 0
+    for s, n in zip(steps[args.warmup:], decode_launches):
+        Pp = _split_partition(P, s.max_context_len, n)
+        ab = algorithmic_bytes(cfg, s.host, w.num_seqs, split_partition=Pp, out_bytes=out_bytes)
+        bytes_step += ab["total"]
+        bytes_dec += ab["attention"]
+        seqs += w.num_seqs
+    t_max = max_over_ranks(dist, tot_ms / 1e3)
+    bytes_all = sum_over_ranks(dist, bytes_step)
+    seqs_all = sum_over_ranks(dist, seqs)
+    value = bytes_all / t_max / 1e9
+    dec_mean_ms = sum(dec_ms) / len(dec_ms)
+    achieved = bytes_dec / len(dec_ms) / (dec_mean_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(state, steps[args.warmup:], host_inputs[args.warmup:], P, flush, bytes_step)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max * 1e3 / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "kv_dtype": cfg.dtype, "num_seqs": w.num_seqs,
+                       "num_heads": cfg.num_heads, "num_kv_heads": cfg.num_kv_heads,
+                       "head_dim": cfg.head_dim, "block_size": cfg.block_size,
+                       "partition_size": P, "decode_launches_per_step": decode_launches[0],
+                       "parallelism": f"replicas x{world} (sequences sharded, no collective)",
+                       "l2": "flushed (256 MiB write) before every timed step, outside the events",
+                       "block_placement": "contiguous" if args.identity_tables else "random"},
+            "seq_steps_per_s": round(seqs_all / t_max, 1),
+            "pct_of_peak": round(100 * value / peak, 2),
+            "roofline": {"bound": "hbm", "kernel": "pa_decode_kernel" + ("+pa_reduce_kernel" if decode_launches[0] == 2 else ""),
+                         "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                         "traffic": traffic_for(cfg, bytes_dec / len(dec_ms)),
+                         "algorithmic_bytes_per_launch": int(bytes_dec / len(dec_ms)),
+                         "mean_launch_ms": round(dec_mean_ms, 5)},
+            "clocks": clk,
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _split_partition(P, max_len, launches):
+    if launches != 2:
+        return 0
+    return P if P > 0 else 512
+
+
+def traffic_for(cfg, algo_bytes):
+    """Per-launch DRAM traffic of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source for this workload."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "paged_kv_cache_311_gb300", "csrc", "pa_decode.cuh")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    e = d.get(cfg.name)
+    if not e or e.get("source_sha") != h:
+        return None
+    return e.get("bytes_per_launch")
+
+
+def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
+    """Same step, inputs from pinned host memory, output read back, all timed."""
+    import paged_kv_cache_311_gb300 as pkv
+    cfg = state.cfg
+    stream = torch.cuda.current_stream()
+    dev = state.device
+    pinned = []
+    for s in steps:
+        d = {k: getattr(s, k).cpu().pin_memory() for k in
+             ("q", "key", "value", "slot_mapping", "block_tables", "context_lens")}
+        if s.cow_pairs is not None:
+            d["cow_pairs"] = s.cow_pairs.cpu().pin_memory()
+        pinned.append(d)
+    dev_bufs = {k: torch.empty_like(getattr(steps[0], k)) for k in
+                ("q", "slot_mapping", "context_lens")}
+    out_host = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
+    h2d = d2h = 0
+    total_ms = 0.0
+    for i, (s, hp) in enumerate(zip(steps, pinned)):
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q = torch.empty(hp["q"].shape, dtype=hp["q"].dtype, device=dev)
+        q.copy_(hp["q"], non_blocking=True)
+        key = torch.empty(hp["key"].shape, dtype=hp["key"].dtype, device=dev)
+        key.copy_(hp["key"], non_blocking=True)
+        val = torch.empty(hp["value"].shape, dtype=hp["value"].dtype, device=dev)
+        val.copy_(hp["value"], non_blocking=True)
+        sm = torch.empty(hp["slot_mapping"].shape, dtype=torch.int64, device=dev)
+        sm.copy_(hp["slot_mapping"], non_blocking=True)
+        bt = torch.empty(hp["block_tables"].shape, dtype=torch.int32, device=dev)
+        bt.copy_(hp["block_tables"], non_blocking=True)
+        cl = torch.empty(hp["context_lens"].shape, dtype=torch.int32, device=dev)
+        cl.copy_(hp["context_lens"], non_blocking=True)
+        nb = sum(t.numel() * t.element_size() for t in hp.values())
+        if "cow_pairs" in hp:
+            cp = torch.empty(hp["cow_pairs"].shape, dtype=torch.int64, device=dev)
+            cp.copy_(hp["cow_pairs"], non_blocking=True)
+            pkv.copy_blocks([state.k_cache], [state.v_cache], cp, device_status=state.status)
+        pkv.reshape_and_cache(key, val, state.k_cache, state.v_cache, sm, device_status=state.status)
+        pkv.paged_attention_decode(state.out, q, state.k_cache, state.v_cache, bt, cl,
+                                   cfg.softmax_scale, max_context_len=s.max_context_len,
+                                   partition_size=P, workspace=state.workspace,
+                                   device_status=state.status)
+        out_host.copy_(state.out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        total_ms += e0.elapsed_time(e1)
+        h2d += nb
+        d2h += out_host.numel() * out_host.element_size()
+    n = len(steps)
+    return {"value": round(bytes_step / (total_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d / n), "d2h_bytes_per_step": int(d2h / n),
+            "ms_per_step": round(total_ms / n, 5)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def _raw(t):
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+class _OracleStepper:
+    """Host copy of the blocks that `seqs` touch over `inputs`, advanced step
+    by step with the oracle's own copy-on-write copies and scatter, and the
+    oracle's attention for those sequences."""
+
+    def __init__(self, cfg, num_blocks, seqs, inputs, k_blocks_fn, v_blocks_fn):
+        bs = cfg.block_size
+        blocks = set()
+        for inp in inputs:
+            for s in seqs:
+                L = int(inp.context_lens[s])
+                blocks.update(int(b) for b in inp.block_tables[s][:-(-L // bs)])
+            for a, b in inp.cow_pairs:
+                if int(b) in blocks or int(a) in blocks:
+                    blocks.update((int(a), int(b)))
+        self.blocks = np.array(sorted(blocks), dtype=np.int64)
+        self.local = np.full(num_blocks, -1, dtype=np.int64)
+        self.local[self.blocks] = np.arange(self.blocks.size)
+        self.k = k_blocks_fn(self.blocks)
+        self.v = v_blocks_fn(self.blocks)
+        self.cfg, self.seqs = cfg, np.array(seqs, dtype=np.int64)
+
+    def step(self, inp, q, key, value, nthreads):
+        import oracle
+        bs = self.cfg.block_size
+        if inp.cow_pairs.shape[0]:
+            loc = self.local[inp.cow_pairs]
+            loc = loc[loc[:, 1] >= 0]
+            if loc.shape[0]:
+                oracle.copy_blocks([self.k], [self.v], loc)
+        sm = inp.slot_mapping
+        lb = self.local[sm // bs]
+        slots = np.where(lb >= 0, lb * bs + sm % bs, -1)
+        oracle.reshape_and_cache(key, value, self.k, self.v, slots)
+        t = inp.block_tables[self.seqs]
+        tables = np.where(t >= 0, self.local[np.maximum(t, 0)], -1).astype(np.int32)
+        out, st = oracle.paged_attention(q[self.seqs], self.k, self.v, self.cfg.dtype, tables,
+                                         inp.context_lens[self.seqs], self.cfg.num_kv_heads,
+                                         float(np.float32(self.cfg.softmax_scale)),
+                                         nthreads=nthreads)
+        return out
+
+
+def _sample_bytes(cfg, inp, seqs):
+    """Algorithmic bytes of the oracle's share of one step (its sequences)."""
+    sub = _restrict(inp, seqs)
+    return algorithmic_bytes(cfg, sub, len(seqs))["total"]
+
+
+def _restrict(inp, seqs):
+    from workloads.gen import StepInputs
+    seqs = np.asarray(seqs)
+    keep = np.isin(inp.token_seq, seqs)
+    pairs = inp.cow_pairs
+    if pairs.shape[0]:
+        mine = set()
+        for s in seqs:
+            mine.update(int(b) for b in inp.block_tables[s] if b >= 0)
+        pairs = pairs[[int(b) in mine for b in pairs[:, 1]]].reshape(-1, 2)
+    return StepInputs(step=inp.step, slot_mapping=inp.slot_mapping[keep],
+                      token_seq=inp.token_seq[keep], token_pos=inp.token_pos[keep],
+                      context_lens=inp.context_lens[seqs], block_tables=inp.block_tables[seqs],
+                      cow_pairs=pairs, max_context_len=int(inp.context_lens[seqs].max()))
+
+
+def cpu_baseline(cfg, state, host_inputs, budget_s, seed):
+    """The oracle, as it stands, on whole steps of this workload (copies,
+    scatter and attention over every sequence, the same values as the GPU
+    run) until about budget_s seconds of it are spent."""
+    from workloads import step_values
+    nthreads = os.cpu_count() or 1
+    seqs = list(range(state.w.num_seqs))
+
+    def take(cache):
+        def f(blocks):
+            idx = torch.as_tensor(blocks, device=cache.device)
+            return _raw(cache.index_select(0, idx))
+        return f
+
+    st = _OracleStepper(cfg, state.w.num_blocks, seqs, host_inputs, take(state.k_cache),
+                        take(state.v_cache))
+    done, t_used, nbytes = 0, 0.0, 0
+    for inp in host_inputs:
+        q, k, v = step_values(cfg, seed, inp, state.w.num_seqs, device=state.device)
+        q, k, v = _raw(q), _raw(k), _raw(v)
+        t0 = time.perf_counter()
+        st.step(inp, q, k, v, nthreads)
+        t_used += time.perf_counter() - t0
+        nbytes += algorithmic_bytes(cfg, inp, state.w.num_seqs)["total"]
+        done += 1
+        if t_used >= budget_s:
+            break
+    return {"value": round(nbytes / t_used / 1e9, 4), "unit": "GB/s", "cores": nthreads,
+            "kind": "oracle", "seconds": round(t_used, 2),
+            "sample": f"steps 0..{done - 1} of {cfg.name}: all {state.w.num_seqs} sequences, "
+                      f"copy-on-write + scatter + fp64 attention (C, {nthreads} threads)"}
+
+
+# -------------------------------------------------------- reference arm
+def run_reference(args):
+    """The oracle as the reference arm: each step runs the oracle (as it
+    stands, all host cores) on a fixed sample of the step's sequences, sized
+    so that warm-up plus timed steps end within about three minutes."""
+    dist, rank, world = dist_setup()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    from workloads import TAG_CACHE_K, TAG_CACHE_V, normal, step_values
+    cfg = get(args.config)
+    if args.block_size:
+        cfg = cfg.with_(block_size=args.block_size)
+    seed = SEED_BASE + CONFIGS.index(get(args.config))
+    total = args.warmup + args.steps
+    w = PagedDecodeWorkload(cfg, seed, total_steps=max(total, cfg.steps))
+    inputs = [w.next_step() for _ in range(total)]
+    nthreads = os.cpu_count() or 1
+    shape = (cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
+
+    def fill(tag):
+        def f(blocks):
+            x = normal((blocks.size,) + shape, cfg.dtype, seed, tag, 0, device="cpu")
+            return _raw(x)
+        return f
+
+    def stepper(seqs):
+        return _OracleStepper(cfg, w.num_blocks, seqs, inputs, fill(TAG_CACHE_K), fill(TAG_CACHE_V))
+
+    def values(inp):
+        q, k, v = step_values(cfg, seed, inp, w.num_seqs, device="cpu")
+        return _raw(q), _raw(k), _raw(v)
+
+    # calibrate: one thread's time for one sequence, then size the sample
+    probe = stepper([0])
+    q, k, v = values(inputs[0])
+    t0 = time.perf_counter()
+    probe.step(inputs[0], q, k, v, 1)
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    per_step = 150.0 / max(total, 1)
+    n = int(max(1, min(w.num_seqs, per_step * nthreads / t1)))
+    n = max(1, (n // nthreads) * nthreads) if n >= nthreads else n
+    seqs = list(range(n))
+    st = stepper(seqs)
+    times, nbytes = [], 0
+    for i, inp in enumerate(inputs):
+        q, k, v = values(inp)
+        t0 = time.perf_counter()
+        st.step(inp, q, k, v, nthreads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes += _sample_bytes(cfg, inp, seqs)
+    tot = sum(times)
+    value = nbytes / tot / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot * 1e3 / len(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "kv_dtype": cfg.dtype, "num_seqs": w.num_seqs,
+                       "sampled_seqs": n, "num_heads": cfg.num_heads,
+                       "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
+                       "block_size": cfg.block_size},
+            "seq_steps_per_s": round(n * len(times) / tot, 2),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
+                             "kind": "oracle",
+                             "sample": f"sequences 0..{n - 1} of {w.num_seqs} of every step: "
+                                       "copy-on-write + scatter + fp64 attention"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache decode library (libpkv.so), sm_103a.
+ *
+ * The operations follow the PagedAttention pages:
+ *   - "PagedAttention: Efficient LLM Serving with vLLM", section "The
+ *     PagedAttention Algorithm", Steps 1-5: the KV cache is cut into blocks
+ *     of a fixed number of tokens that may sit anywhere in GPU memory; a
+ *     per-sequence page table maps logical block j to its physical block;
+ *     attention gathers K/V from the scattered blocks through that table.
+ *   - same page, "Advanced Features", KV-Cache Sharing (Copy-on-Write):
+ *     sequences share blocks until one of them writes.
+ *   - "Efficient Memory Management for Large Language Model Serving with
+ *     PagedAttention" (card), "Key ideas": blocks addressed through a
+ *     per-sequence block table; prefix blocks shared across sequences.
+ *
+ * Conventions shared by every call
+ *   - Layouts are dense and row-major.  One KV cache (K or V) of one layer is
+ *     [num_blocks, num_kv_heads, block_size, head_dim]: the block_size x
+ *     head_dim rows of one (block, kv head) are contiguous.  A token at
+ *     logical position i of sequence s sits in physical block
+ *     block_tables[s * max_blocks_per_seq + i / block_size] at row
+ *     i % block_size; its slot number is block * block_size + i % block_size.
+ *   - Pointers are DEVICE pointers unless stated otherwise.  The caller owns
+ *     every buffer, including the workspace; the library allocates no device
+ *     memory and keeps no per-call state.  Every call is asynchronous on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream) and returns
+ *     after enqueueing its kernels.
+ *   - Host-side argument errors return a negative pkv_status and enqueue
+ *     nothing.  Data-dependent errors found on the GPU (a block id or slot
+ *     out of range, an inconsistent context length, a bounded wait that ran
+ *     out) are OR-ed into *device_status (may be NULL: not reported) with the
+ *     PKV_DEV_* bits; the kernels skip the offending element and never trap.
+ *     Read *device_status after synchronising the stream.
+ *   - Element types: q, k_cache, v_cache share kv_dtype; arithmetic is fp32
+ *     (fp32 accumulation for fp16/bf16 inputs).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_EINVAL = -1,        /* bad pointer, size, shape or alignment */
+    PKV_EUNSUPPORTED = -2,  /* valid request outside the built kernel set */
+    PKV_ECUDA = -3,         /* a CUDA runtime/driver call failed */
+    PKV_EWORKSPACE = -4     /* workspace missing or too small */
+} pkv_status;
+
+/* Bits OR-ed into *device_status by the kernels. */
+#define PKV_DEV_BAD_BLOCK 1u        /* block id outside [0, num_blocks) */
+#define PKV_DEV_BAD_SLOT 2u         /* slot outside [0, num_blocks * block_size) */
+#define PKV_DEV_TIMEOUT 4u          /* a bounded wait on a TMA barrier gave up */
+#define PKV_DEV_BAD_CONTEXT_LEN 8u  /* context_lens[s] < 0 or beyond the table / max */
+
+/* Supported shapes of the decode kernel. */
+#define PKV_DEFAULT_PARTITION 512    /* tokens per split-context partition */
+
+/*
+ * Bytes of workspace pkv_paged_attention_decode needs for these sizes.
+ * partition_size: as passed to the decode call (0 = automatic; the size
+ * returned then covers whichever path the automatic choice takes).
+ * Returns 0 if no workspace is needed or on invalid sizes.
+ */
+size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_heads, int max_context_len,
+                                           int head_dim, int partition_size);
+
+/*
+ * paged_attention_decode -- single-query attention of every running sequence
+ * over its paged K/V ("The PagedAttention Algorithm", Step 5).
+ *
+ * For query head h of sequence s, with G = num_heads / num_kv_heads and
+ * kv head h / G, over the L = context_lens[s] tokens at logical positions
+ * 0..L-1:
+ *     out[s,h,:] = sum_i softmax_i(scale * q[s,h,:] . k_i) * v_i
+ * L = 0 gives a zero row.
+ *
+ *   out        [num_seqs, num_heads, head_dim] of out_dtype (written)
+ *   q          [num_seqs, num_heads, head_dim] of kv_dtype
+ *   k_cache, v_cache  [num_blocks, num_kv_heads, block_size, head_dim] of
+ *              kv_dtype, 16-byte aligned
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]; entries past
+ *              ceil(L / block_size) are never read
+ *   context_lens  int32 [num_seqs], each in [0, max_context_len]
+ *   max_context_len  host-side upper bound of context_lens (sizes the grid);
+ *              must be <= max_blocks_per_seq * block_size
+ *   scale      softmax scale (e.g. 1/sqrt(head_dim))
+ *   partition_size  0 = automatic; otherwise tokens per split-context
+ *              partition (multiple of 32 and of block_size): each partition
+ *              is reduced separately and the partials are merged by a
+ *              log-sum-exp reduce kernel.  A value >= max_context_len forces
+ *              the single-pass kernel.
+ *   workspace  device buffer of at least
+ *              pkv_paged_attention_workspace_bytes(...) bytes when the split
+ *              path runs (may be NULL otherwise)
+ * Supported: head_dim in {64, 128}; block_size in {8, 16, 32};
+ * num_heads / num_kv_heads in {1, 2, 4, 8}; dtypes as pkv_dtype.
+ * Device errors: PKV_DEV_BAD_BLOCK / PKV_DEV_BAD_CONTEXT_LEN -> that
+ * sequence's output rows (for the kv head group touched) are zero.
+ */
+int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const void *k_cache,
+                               const void *v_cache, int kv_dtype, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, int max_context_len, float scale,
+                               int partition_size, void *workspace, size_t workspace_bytes,
+                               uint32_t *device_status, void *stream);
+
+/*
+ * reshape_and_cache -- write each new token's key/value rows into its slot
+ * ("The PagedAttention Algorithm", Step 2: generated tokens fill the block).
+ *
+ *   key, value   [num_tokens, num_kv_heads, head_dim] of dtype, 16-byte aligned
+ *   k_cache, v_cache  [num_blocks, num_kv_heads, block_size, head_dim]
+ *   slot_mapping int64 [num_tokens]; slot = block * block_size + row.
+ *                A negative slot marks a padding token: skipped, no error.
+ *                A slot >= num_blocks * block_size: skipped, PKV_DEV_BAD_SLOT.
+ * Bit-exact copy.  Two tokens with the same slot in one call: undefined.
+ */
+int pkv_reshape_and_cache(const void *key, const void *value, void *k_cache, void *v_cache,
+                          int dtype, const int64_t *slot_mapping, int num_tokens,
+                          int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                          uint32_t *device_status, void *stream);
+
+/*
+ * copy_blocks -- copy-on-write block copies ("Advanced Features", KV-Cache
+ * Sharing (Copy-on-Write): shared pages until write, like fork()).
+ *
+ *   k_caches, v_caches  HOST arrays of num_layers DEVICE pointers, one K and
+ *                one V cache per layer, each 16-byte aligned
+ *   src_dst_pairs  int64 [num_pairs, 2] (device): block dst of every layer's
+ *                K and V cache becomes a copy of block src
+ *   block_bytes  bytes of one block of one cache (num_kv_heads * block_size *
+ *                head_dim * element size), a multiple of 16
+ * Pairs with an id outside [0, num_blocks): skipped, PKV_DEV_BAD_BLOCK.
+ * Caller contract: destinations are distinct and no destination is also a
+ * source in the same call.
+ */
+int pkv_copy_blocks(void *const *k_caches, void *const *v_caches, int num_layers,
+                    const int64_t *src_dst_pairs, int num_pairs, size_t block_bytes,
+                    int64_t num_blocks, uint32_t *device_status, void *stream);
+
+/* Static, NUL-terminated description of a pkv_status value. */
+const char *pkv_status_string(int status);
+
+/* Number of kernels the last successful pkv_paged_attention_decode call on
+ * this host thread enqueued (1 = single pass, 2 = partition pass + reduce). */
+int pkv_last_decode_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,204 @@
+"""paged_kv_cache_311_gb300 -- GB300-native paged KV-cache decode attention.
+
+A thin ctypes binding over ``libpkv.so`` (C ABI in ``include/pkv.h``).  Every
+step of the path runs in the library's CUDA kernels; this module only turns
+torch tensors into pointers, sizes and the current CUDA stream.  torch is
+used for device memory and streams, nothing else.  There is no CPU fallback:
+calling into the library without a built ``libpkv.so`` raises.
+
+Operations (PagedAttention: Efficient LLM Serving with vLLM, "The
+PagedAttention Algorithm" and "Advanced Features"):
+  paged_attention_decode  single-query attention over a block-table-mapped cache
+  reshape_and_cache       scatter of new tokens' K/V into their slots
+  copy_blocks             copy-on-write copy of shared blocks
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Sequence
+
+import torch
+
+from .build import library_path
+
+__all__ = [
+    "PkvError", "load_library", "paged_attention_decode", "reshape_and_cache", "copy_blocks",
+    "paged_attention_workspace_bytes", "status_string", "last_decode_launches",
+    "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "HEADER_PATH",
+]
+
+HEADER_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                           "include", "pkv.h")
+
+PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
+_DTYPE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_TIMEOUT, DEV_BAD_CONTEXT_LEN = 1, 2, 4, 8
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Loads libpkv.so (built by ``paged_kv_cache_311_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise ImportError(f"libpkv.so not built at {p}; run python -m paged_kv_cache_311_gb300.build")
+    L = ctypes.CDLL(p)
+    vp, i32, i64, u64, f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                              ctypes.c_float)
+    L.pkv_paged_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.pkv_paged_attention_workspace_bytes.restype = u64
+    L.pkv_paged_attention_decode.argtypes = [vp, i32, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
+                                             i32, i32, i64, i32, f32, i32, vp, u64, vp, vp]
+    L.pkv_paged_attention_decode.restype = i32
+    L.pkv_reshape_and_cache.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, vp, vp]
+    L.pkv_reshape_and_cache.restype = i32
+    L.pkv_copy_blocks.argtypes = [vp, vp, i32, vp, i32, u64, i64, vp, vp]
+    L.pkv_copy_blocks.restype = i32
+    L.pkv_status_string.argtypes = [i32]
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_last_decode_launches.argtypes = []
+    L.pkv_last_decode_launches.restype = i32
+    if path is None:
+        _lib = L
+    return L
+
+
+def declared_functions(header: str = HEADER_PATH) -> list:
+    """Names of the functions include/pkv.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return load_library().pkv_status_string(int(status)).decode()
+
+
+def last_decode_launches() -> int:
+    return int(load_library().pkv_last_decode_launches())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise PkvError(rc, what)
+
+
+def _need_cuda(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def paged_attention_workspace_bytes(num_seqs: int, num_heads: int, max_context_len: int,
+                                    head_dim: int, partition_size: int = 0) -> int:
+    return int(load_library().pkv_paged_attention_workspace_bytes(
+        num_seqs, num_heads, max_context_len, head_dim, partition_size))
+
+
+def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, scale: float,
+                           block_size: Optional[int] = None, num_kv_heads: Optional[int] = None,
+                           *, max_context_len: Optional[int] = None, partition_size: int = 0,
+                           workspace: Optional[torch.Tensor] = None,
+                           device_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[s, h] = attention of q[s, h] over sequence s's paged K/V.
+
+    q, out: [B, H, D]; k_cache, v_cache: [NB, Hk, bs, D]; block_tables int32
+    [B, MB]; context_lens int32 [B].  ``max_context_len`` is a host-side bound
+    of context_lens (read from the device, with a sync, if omitted).  A
+    workspace is allocated here when the split-context path needs one and
+    none is given.  device_status: optional uint32/int32 [1] tensor that the
+    kernels OR error bits into."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, workspace, device_status)
+    B, H, D = q.shape
+    NB, Hk, bs, D2 = k_cache.shape
+    if block_size is not None and block_size != bs:
+        raise ValueError("block_size does not match k_cache")
+    if num_kv_heads is not None and num_kv_heads != Hk:
+        raise ValueError("num_kv_heads does not match k_cache")
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, H, D):
+        raise ValueError("shape mismatch")
+    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise ValueError("q, k_cache and v_cache must share a dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0
+    if workspace is None:
+        nbytes = paged_attention_workspace_bytes(B, H, max_context_len, D, partition_size)
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    L = load_library()
+    rc = L.pkv_paged_attention_decode(
+        _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[k_cache.dtype],
+        _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), B, H, Hk, D, bs, NB,
+        int(max_context_len), float(scale), int(partition_size), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(device_status), _stream(stream))
+    _check(rc, "pkv_paged_attention_decode")
+    return out
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, slot_mapping: torch.Tensor, *,
+                      device_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k_cache/v_cache[slot // bs, :, slot % bs, :] = key/value[t] for every slot >= 0."""
+    _need_cuda(key, value, k_cache, v_cache, slot_mapping, device_status)
+    T, Hk, D = key.shape
+    NB, Hk2, bs, D2 = k_cache.shape
+    if (Hk2, D2) != (Hk, D) or value.shape != key.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if key.dtype != k_cache.dtype or value.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise ValueError("dtype mismatch")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    rc = load_library().pkv_reshape_and_cache(
+        _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _DTYPE[k_cache.dtype],
+        _ptr(slot_mapping), T, Hk, D, bs, NB, _ptr(device_status), _stream(stream))
+    _check(rc, "pkv_reshape_and_cache")
+
+
+def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor],
+                src_dst_pairs: torch.Tensor, *, device_status: Optional[torch.Tensor] = None,
+                stream=None) -> None:
+    """Block dst of every layer's K and V cache becomes a copy of block src."""
+    if len(k_caches) != len(v_caches) or not k_caches:
+        raise ValueError("need one K and one V cache per layer")
+    _need_cuda(*k_caches, *v_caches, src_dst_pairs, device_status)
+    if src_dst_pairs.dtype != torch.int64:
+        raise ValueError("src_dst_pairs must be int64")
+    shape = tuple(k_caches[0].shape)
+    for c in list(k_caches) + list(v_caches):
+        if tuple(c.shape) != shape or c.dtype != k_caches[0].dtype:
+            raise ValueError("all caches must share shape and dtype")
+    nl = len(k_caches)
+    kp = (ctypes.c_void_p * nl)(*[c.data_ptr() for c in k_caches])
+    vp = (ctypes.c_void_p * nl)(*[c.data_ptr() for c in v_caches])
+    block_bytes = k_caches[0][0].numel() * k_caches[0].element_size()
+    rc = load_library().pkv_copy_blocks(kp, vp, nl, _ptr(src_dst_pairs),
+                                        int(src_dst_pairs.numel() // 2), block_bytes, shape[0],
+                                        _ptr(device_status), _stream(stream))
+    _check(rc, "pkv_copy_blocks")

@@ -1,0 +1,68 @@
+// cache_ops.cuh -- the two cache-maintenance kernels: the scatter of new
+// tokens into their slots and the copy-on-write block copy.
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+// reshape_and_cache (PagedAttention: Efficient LLM Serving with vLLM, "The
+// PagedAttention Algorithm", Step 2): token t's rows key[t, h, :] and
+// value[t, h, :] go to row slot % bs of physical block slot / bs, head h.
+// One CTA per token; 16-byte vectors, so each (token, head) row is a run of
+// D * e / 16 coalesced vector stores.
+__global__ void __launch_bounds__(128)
+reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                         uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                         const int64_t *__restrict__ slot_mapping, int num_kv_heads,
+                         int row_vecs, int block_size, int64_t num_blocks, uint32_t *status)
+{
+    const int t = blockIdx.x;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0)
+        return;  // padding token
+    if (slot >= num_blocks * (int64_t)block_size) {
+        if (threadIdx.x == 0)
+            report(status, PKV_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t b = slot / block_size;
+    const int o = (int)(slot % block_size);
+    const int total = num_kv_heads * row_vecs;
+    const int64_t src0 = (int64_t)t * total;
+    for (int v = threadIdx.x; v < total; v += blockDim.x) {
+        const int h = v / row_vecs, c = v % row_vecs;
+        const int64_t dst = ((b * num_kv_heads + h) * block_size + o) * row_vecs + c;
+        k_cache[dst] = key[src0 + v];
+        v_cache[dst] = value[src0 + v];
+    }
+}
+
+constexpr int kCopyMaxLayers = 128;
+
+struct CopyBlocksParams {
+    uint4 *k[kCopyMaxLayers];
+    uint4 *v[kCopyMaxLayers];
+};
+
+// copy_blocks ("Advanced Features", KV-Cache Sharing (Copy-on-Write)): grid
+// (pair, layer, cache); each CTA copies one whole block of one cache.
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(const __grid_constant__ CopyBlocksParams ptrs, const int64_t *__restrict__ pairs,
+                   int64_t block_vecs, int64_t num_blocks, uint32_t *status)
+{
+    const int pr = blockIdx.x, layer = blockIdx.y, which = blockIdx.z;
+    const int64_t src = pairs[2 * pr], dst = pairs[2 * pr + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && layer == 0 && which == 0)
+            report(status, PKV_DEV_BAD_BLOCK);
+        return;
+    }
+    uint4 *base = which == 0 ? ptrs.k[layer] : ptrs.v[layer];
+    const uint4 *s = base + src * block_vecs;
+    uint4 *d = base + dst * block_vecs;
+    for (int64_t i = threadIdx.x; i < block_vecs; i += blockDim.x)
+        d[i] = s[i];
+}
+
+}  // namespace pkv

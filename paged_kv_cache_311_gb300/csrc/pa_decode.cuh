@@ -1,0 +1,512 @@
+// pa_decode.cuh -- paged decode attention for sm_103a.
+//
+// What it computes (PagedAttention: Efficient LLM Serving with vLLM, "The
+// PagedAttention Algorithm", Steps 4-5): for every sequence s and query head
+// h, softmax(scale * q[s,h] . k_i) weighted sum of v_i over the sequence's
+// logical tokens i < L_s, where token i lives in physical block
+// block_tables[s][i / bs], row i % bs, of a cache laid out
+// [num_blocks, Hk, bs, D].
+//
+// Kernel design (one CTA per (context partition, kv head, sequence)):
+//   * The CTA owns the G = H / Hk query heads of one kv head, so every K/V
+//     byte is read from HBM once and feeds G heads.
+//   * Each warp streams its own tiles of TILE tokens through an S-stage ring
+//     in shared memory.  Lane 0 of the warp is the producer: for each tile it
+//     issues one TMA (cp.async.bulk.tensor.5d) load per block-box of K and of
+//     V, with 128-byte swizzling so that both the token-per-lane reads of the
+//     QK phase and the dim-per-lane reads of the PV phase are free of bank
+//     conflicts.  Block ids come from a copy of the partition's slice of the
+//     block table staged in shared memory when the CTA starts.
+//   * QK: LPT = 32 / TILE lanes per token, each taking a fixed subset of the
+//     row's 16-byte pieces; q (pre-scaled by scale * log2 e) is read from
+//     shared memory as broadcasts; packed fp32x2 FMAs, fp32 accumulation.
+//   * Online softmax per tile in the log2 domain (exp2), probabilities staged
+//     in shared memory as (p, p) pairs.
+//   * PV: every lane owns D / 32 output dims for all G heads and walks the
+//     tile's tokens; packed fp32x2 FMAs.
+//   * End of CTA: warps merge (max, sum, acc) through shared memory; the
+//     single-pass kernel writes the normalised output, the split-context
+//     kernel writes (max, sum, unnormalised acc) to the workspace for the
+//     log-sum-exp reduce kernel.
+//   * Reduction order depends only on logical token positions, so results
+//     are bit-identical under any physical placement of the blocks.
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+struct DecodeParams {
+    void *out;
+    const void *q;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *ws_ml;     // split path: [B][H][NP][2] = (max, sum) in the log2 domain
+    float *ws_acc;    // split path: [B][H][NP][D] unnormalised accumulators
+    uint32_t *status;
+    int64_t num_blocks;
+    int num_seqs, num_heads, num_kv_heads;
+    int max_blocks_per_seq;
+    int max_context_len;
+    int partition_size;  // tokens per CTA along the context
+    int num_partitions;  // grid.x
+    int out_dtype;
+    int split;           // nonzero: write partials to the workspace
+    float qscale;        // softmax scale * log2(e)
+};
+
+#ifndef PKV_DECODE_TILE
+#define PKV_DECODE_TILE 16
+#endif
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+#ifndef PKV_DECODE_STAGE_BUDGET
+#define PKV_DECODE_STAGE_BUDGET 98304
+#endif
+
+template <typename T, int D, int BS, int G>
+struct DecodeCfg {
+    static constexpr int E = Elem<T>::bytes;
+    static constexpr int TILE = PKV_DECODE_TILE;   // tokens per warp tile
+    static constexpr int NW = PKV_DECODE_WARPS;    // warps per CTA
+    static constexpr int ROW = D * E;              // bytes of one token row
+    static constexpr int CHUNKS = ROW / 128;       // 128-byte swizzle atoms per row
+    static constexpr int EPP = 16 / E;             // elements per 16-byte piece
+    static constexpr int NPC = ROW / 16;           // pieces per row
+    static constexpr int LPT = 32 / TILE;          // lanes per token in QK
+    static constexpr int PCL = 8 / LPT;            // pieces per chunk per lane
+    static constexpr int BOX_ROWS = BS < TILE ? BS : TILE;
+    static constexpr int BOXES = TILE / BOX_ROWS;
+    static constexpr int BOX_BYTES = BOX_ROWS * ROW;
+    static constexpr int TILE_BYTES = TILE * ROW;  // K (or V) of one tile
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int S0 = PKV_DECODE_STAGE_BUDGET / (NW * STAGE_BYTES);
+    static constexpr int S = S0 < 2 ? 2 : (S0 > 8 ? 8 : S0);  // ring depth per warp
+    static constexpr int DPL = D / 32;             // PV dims per lane
+    static constexpr int QROW = G * EPP * 4 + 16;  // bytes per q piece row (padded)
+    static constexpr int TABLE_CAP = 1024;         // block-table entries per CTA
+
+    static constexpr int OFF_STAGES = 0;
+    static constexpr int STAGES_BYTES = NW * S * STAGE_BYTES;
+    static constexpr int OFF_Q = STAGES_BYTES;
+    static constexpr int OFF_P = OFF_Q + ((NPC * QROW + 127) / 128) * 128;
+    static constexpr int OFF_TABLE = OFF_P + NW * TILE * G * 8;
+    static constexpr int OFF_BAR = OFF_TABLE + TABLE_CAP * 4;
+    static constexpr int OFF_FLAG = OFF_BAR + NW * S * 8;
+    static constexpr int SMEM_USED = OFF_FLAG + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+
+    static_assert(ROW % 128 == 0, "rows must be whole 128-byte swizzle atoms");
+    static_assert(TILE % BOX_ROWS == 0 && BOX_ROWS % 8 == 0, "box rows");
+    static_assert(BOX_BYTES % 1024 == 0, "TMA 128B-swizzle boxes need 1024-byte alignment");
+    static_assert(D % 64 == 0 && DPL % 2 == 0, "head_dim");
+    static_assert(NW * G * (D + 2) * 4 <= STAGES_BYTES, "merge scratch fits in the ring");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+// Host-visible description of the config (for the TMA box and launch).
+template <typename T, int D, int BS, int G>
+struct DecodeShape {
+    using C = DecodeCfg<T, D, BS, G>;
+    static constexpr int box_rows = C::BOX_ROWS;
+    static constexpr int threads = C::NW * 32;
+    static constexpr int smem = C::SMEM_BYTES;
+    static constexpr int tile = C::TILE;
+};
+
+__device__ __forceinline__ void store_out(void *out, int dtype, int64_t i, float v)
+{
+    if (dtype == PKV_F32)
+        static_cast<float *>(out)[i] = v;
+    else if (dtype == PKV_F16)
+        static_cast<__half *>(out)[i] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
+}
+
+// Writes the result of a CTA that cannot produce one (bad length / block):
+// zeros for the single pass, an "invalid" (max = -inf, sum = -1) marker for
+// the split path.
+template <int D, int G>
+__device__ void write_invalid(const DecodeParams &p, int seq, int kvh, int part)
+{
+    const int nthr = blockDim.x;
+    for (int idx = threadIdx.x; idx < G * D; idx += nthr) {
+        const int h = kvh * G + idx / D, d = idx % D;
+        const int64_t sh = (int64_t)seq * p.num_heads + h;
+        if (!p.split) {
+            store_out(p.out, p.out_dtype, sh * D + d, 0.f);
+        } else {
+            p.ws_acc[(sh * p.num_partitions + part) * D + d] = 0.f;
+            if (d == 0) {
+                p.ws_ml[(sh * p.num_partitions + part) * 2 + 0] = -INFINITY;
+                p.ws_ml[(sh * p.num_partitions + part) * 2 + 1] = -1.f;
+            }
+        }
+    }
+}
+
+template <typename T, int D, int BS, int G>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, G>::NW * 32)
+pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                 const __grid_constant__ CUtensorMap tmv)
+{
+    using C = DecodeCfg<T, D, BS, G>;
+    constexpr int NW = C::NW, S = C::S, TILE = C::TILE, LPT = C::LPT;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int L = p.context_lens[seq];
+    if (L < 0 || L > p.max_context_len) {
+        if (part == 0 && kvh == 0 && tid == 0)
+            report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+        if (!p.split)
+            write_invalid<D, G>(p, seq, kvh, part);
+        return;  // split path: the reduce kernel sees the bad length itself
+    }
+    const int tok0 = part * p.partition_size;
+    const int tok_end = min(tok0 + p.partition_size, L);
+    if (tok0 >= tok_end) {
+        if (!p.split && part == 0)
+            write_invalid<D, G>(p, seq, kvh, part);  // L == 0: zero output
+        return;
+    }
+
+    // ---- stage the block-table slice and the pre-scaled queries
+    const int j0 = tok0 / BS;
+    const int nblk = (tok_end - tok0 + BS - 1) / BS;
+    int32_t *table_s = reinterpret_cast<int32_t *>(smem + C::OFF_TABLE);
+    const int32_t *bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + j0;
+    int bad = 0;
+    for (int i = tid; i < nblk; i += NW * 32) {
+        int b = bt[i];
+        if (b < 0 || (int64_t)b >= p.num_blocks) {
+            bad = 1;
+            b = 0;
+        }
+        table_s[i] = b;
+    }
+    const T *qp = static_cast<const T *>(p.q) + ((int64_t)seq * p.num_heads + kvh * G) * D;
+    for (int i = tid; i < G * D; i += NW * 32) {
+        const int h = i / D, d = i % D;
+        const float v = to_float(qp[i]) * p.qscale;
+        float *dst = reinterpret_cast<float *>(smem + C::OFF_Q + (d / C::EPP) * C::QROW);
+        dst[h * C::EPP + d % C::EPP] = v;
+    }
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR) + warp * S;
+    uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + C::OFF_FLAG);
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    if (tid == 0) {
+        *cta_flag = 0;
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
+    if (__syncthreads_or(bad)) {
+        if (tid == 0)
+            report(p.status, PKV_DEV_BAD_BLOCK);
+        write_invalid<D, G>(p, seq, kvh, part);
+        return;
+    }
+
+    // ---- per-warp tile stream
+    const int ntok = tok_end - tok0;
+    const int ntiles = (ntok + TILE - 1) / TILE;
+    const int my_n = warp < ntiles ? (ntiles - 1 - warp) / NW + 1 : 0;
+    uint8_t *stages = smem + C::OFF_STAGES + warp * S * C::STAGE_BYTES;
+
+    auto issue = [&](int i, int st) {
+        const int t0 = tok0 + (warp + i * NW) * TILE;
+        uint8_t *kd = stages + st * C::STAGE_BYTES;
+        uint8_t *vd = kd + C::TILE_BYTES;
+        const int nbox = min(C::BOXES, (tok_end - t0 + C::BOX_ROWS - 1) / C::BOX_ROWS);
+        mbar_arrive_expect_tx(&bars[st], (uint32_t)(nbox * 2 * C::BOX_BYTES));
+        for (int b = 0; b < nbox; ++b) {
+            const int tok = t0 + b * C::BOX_ROWS;
+            const int phys = table_s[tok / BS - j0];
+            const int row0 = tok % BS;
+            tma_load_5d(kd + b * C::BOX_BYTES, &tmk, &bars[st], 0, row0, 0, kvh, phys);
+            tma_load_5d(vd + b * C::BOX_BYTES, &tmv, &bars[st], 0, row0, 0, kvh, phys);
+        }
+    };
+    if (lane == 0) {
+        const int pre = my_n < S ? my_n : S;
+        for (int i = 0; i < pre; ++i)
+            issue(i, i);
+    }
+
+    float m[G], lsum[G];
+    float2 acc[G][C::DPL / 2];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        lsum[h] = 0.f;
+#pragma unroll
+        for (int k = 0; k < C::DPL / 2; ++k)
+            acc[h][k] = make_float2(0.f, 0.f);
+    }
+
+    const int ti = lane / LPT;           // token of this lane in QK
+    const int sub = lane % LPT;          // which piece subset of the row
+    const int qbox = ti / C::BOX_ROWS, qr = ti % C::BOX_ROWS;
+    const uint32_t qbase = smem_u32(smem + C::OFF_Q);
+    const uint32_t pbase = smem_u32(smem + C::OFF_P) + warp * TILE * G * 8;
+    constexpr int VBYTES = C::DPL * C::E;           // PV bytes per lane per row
+    const int vq = (lane * VBYTES) >> 4, vin = (lane * VBYTES) & 15;
+
+    int failed_at = -1;
+    for (int i = 0; i < my_n; ++i) {
+        const int st = i % S;
+        if (!mbar_wait_bounded(&bars[st], (uint32_t)((i / S) & 1))) {
+            failed_at = i;
+            break;
+        }
+        const int t0 = tok0 + (warp + i * NW) * TILE;
+        const int nvalid = min(TILE, tok_end - t0);
+        const uint32_t kbase = smem_u32(stages + st * C::STAGE_BYTES);
+        const uint32_t vbase = kbase + C::TILE_BYTES;
+
+        // ---- QK for token ti
+        float2 s2[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+            s2[h] = make_float2(0.f, 0.f);
+        const uint32_t krow = kbase + qbox * C::BOX_BYTES + qr * 128;
+#pragma unroll
+        for (int c2 = 0; c2 < C::CHUNKS; ++c2) {
+#pragma unroll
+            for (int i4 = 0; i4 < C::PCL; ++i4) {
+                const int pc = sub * C::PCL + i4;
+                const uint4 kw = lds128(krow + c2 * C::BOX_ROWS * 128 + ((pc ^ (qr & 7)) << 4));
+                const uint32_t qa = qbase + (c2 * 8 + pc) * C::QROW;
+                if constexpr (C::E == 2) {
+                    const float2 k0 = Unpack<T>::pair(kw.x), k1 = Unpack<T>::pair(kw.y);
+                    const float2 k2 = Unpack<T>::pair(kw.z), k3 = Unpack<T>::pair(kw.w);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float4 qa0 = lds128f(qa + h * 32);
+                        const float4 qa1 = lds128f(qa + h * 32 + 16);
+                        s2[h] = ffma2(make_float2(qa0.x, qa0.y), k0, s2[h]);
+                        s2[h] = ffma2(make_float2(qa0.z, qa0.w), k1, s2[h]);
+                        s2[h] = ffma2(make_float2(qa1.x, qa1.y), k2, s2[h]);
+                        s2[h] = ffma2(make_float2(qa1.z, qa1.w), k3, s2[h]);
+                    }
+                } else {
+                    const float2 k0 = make_float2(__uint_as_float(kw.x), __uint_as_float(kw.y));
+                    const float2 k1 = make_float2(__uint_as_float(kw.z), __uint_as_float(kw.w));
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float4 qa0 = lds128f(qa + h * 16);
+                        s2[h] = ffma2(make_float2(qa0.x, qa0.y), k0, s2[h]);
+                        s2[h] = ffma2(make_float2(qa0.z, qa0.w), k1, s2[h]);
+                    }
+                }
+            }
+        }
+
+        // ---- online softmax over this tile (log2 domain)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float s = s2[h].x + s2[h].y;
+            if constexpr (LPT > 1) {
+#pragma unroll
+                for (int off = 1; off < LPT; off <<= 1)
+                    s += __shfl_xor_sync(0xffffffffu, s, off);
+            }
+            s = ti < nvalid ? s : -INFINITY;
+            float tm = s;
+#pragma unroll
+            for (int off = LPT; off < 32; off <<= 1)
+                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
+            const float mn = fmaxf(m[h], tm);
+            const float alpha = exp2f(m[h] - mn);
+            const float pr = exp2f(s - mn);
+            lsum[h] = lsum[h] * alpha + (sub == 0 ? pr : 0.f);
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int k = 0; k < C::DPL / 2; ++k)
+                acc[h][k] = fmul2(acc[h][k], a2);
+            m[h] = mn;
+            if (sub == 0)
+                asm volatile("st.shared.v2.f32 [%0], {%1, %1};" ::"r"(pbase + (ti * G + h) * 8),
+                             "f"(pr)
+                             : "memory");
+        }
+        __syncwarp();
+
+        // ---- PV: this lane's D/32 dims of every head
+        for (int t = 0; t < nvalid; ++t) {
+            const int bx = t / C::BOX_ROWS, r = t % C::BOX_ROWS;
+            const uint32_t va = vbase + bx * C::BOX_BYTES + ((vq >> 3) * C::BOX_ROWS + r) * 128 +
+                                ((((vq & 7) ^ (r & 7)) << 4) | vin);
+            float2 vf[C::DPL / 2];
+            if constexpr (C::E == 2) {
+                if constexpr (VBYTES == 8) {
+                    const uint2 w = lds64(va);
+                    vf[0] = Unpack<T>::pair(w.x);
+                    vf[1] = Unpack<T>::pair(w.y);
+                } else {
+                    vf[0] = Unpack<T>::pair(lds32(va));
+                }
+            } else {
+                if constexpr (VBYTES == 16) {
+                    const float4 w = lds128f(va);
+                    vf[0] = make_float2(w.x, w.y);
+                    vf[1] = make_float2(w.z, w.w);
+                } else {
+                    vf[0] = lds64f(va);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float2 pp = lds64f(pbase + (t * G + h) * 8);
+#pragma unroll
+                for (int k = 0; k < C::DPL / 2; ++k)
+                    acc[h][k] = ffma2(pp, vf[k], acc[h][k]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && i + S < my_n) {
+            fence_proxy_async_smem();
+            issue(i + S, st);
+        }
+    }
+
+    if (failed_at >= 0) {
+        // Drain the loads this warp still has in flight before the CTA may
+        // exit, then mark the CTA's result invalid.
+        const int last = min(my_n, failed_at + S);
+        for (int i = failed_at; i < last; ++i)
+            mbar_wait_bounded(&bars[i % S], (uint32_t)((i / S) & 1), 200000000ull);
+        if (lane == 0) {
+            report(p.status, PKV_DEV_TIMEOUT);
+            atomicOr(cta_flag, 1u);
+        }
+    }
+
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], off);
+    }
+    __syncthreads();  // every warp is done with its ring: reuse it as merge scratch
+    const bool failed = *reinterpret_cast<volatile uint32_t *>(cta_flag) != 0;
+    float *mw = reinterpret_cast<float *>(smem + C::OFF_STAGES);
+    float *lw = mw + NW * G;
+    float *aw = lw + NW * G;
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            mw[warp * G + h] = m[h];
+            lw[warp * G + h] = lsum[h];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int k = 0; k < C::DPL / 2; ++k)
+            *reinterpret_cast<float2 *>(&aw[(warp * G + h) * D + lane * C::DPL + 2 * k]) =
+                acc[h][k];
+    }
+    __syncthreads();
+
+    for (int idx = tid; idx < G * D; idx += NW * 32) {
+        const int h = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            M = fmaxf(M, mw[w * G + h]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float mwh = mw[w * G + h];
+            if (mwh != -INFINITY) {
+                const float f = exp2f(mwh - M);
+                num += f * aw[(w * G + h) * D + d];
+                den += f * lw[w * G + h];
+            }
+        }
+        const int64_t sh = (int64_t)seq * p.num_heads + kvh * G + h;
+        if (!p.split) {
+            store_out(p.out, p.out_dtype, sh * D + d, (failed || den == 0.f) ? 0.f : num / den);
+        } else {
+            const int64_t slot = sh * p.num_partitions + part;
+            p.ws_acc[slot * D + d] = failed ? 0.f : num;
+            if (d == 0) {
+                p.ws_ml[slot * 2 + 0] = failed ? -INFINITY : M;
+                p.ws_ml[slot * 2 + 1] = failed ? -1.f : den;
+            }
+        }
+    }
+}
+
+// Log-sum-exp merge of the split-context partials: one warp per (seq, head).
+template <int D>
+__global__ void __launch_bounds__(128) pa_reduce_kernel(const __grid_constant__ DecodeParams p)
+{
+    constexpr int DPL = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
+    if (sh >= (int64_t)p.num_seqs * p.num_heads)
+        return;
+    const int seq = (int)(sh / p.num_heads);
+    const int L = p.context_lens[seq];
+    const bool bad_len = L < 0 || L > p.max_context_len;
+    const int np = bad_len ? 0 : (L + p.partition_size - 1) / p.partition_size;
+    const float *ml = p.ws_ml + sh * p.num_partitions * 2;
+    const float *accp = p.ws_acc + sh * p.num_partitions * D;
+
+    float M = -INFINITY;
+    int invalid = 0;
+    for (int i = lane; i < np; i += 32) {
+        const float mi = ml[2 * i], li = ml[2 * i + 1];
+        invalid |= li < 0.f;
+        M = fmaxf(M, mi);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    invalid = __any_sync(0xffffffffu, invalid);
+
+    float num[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k)
+        num[k] = 0.f;
+    float den = 0.f;
+    if (!invalid) {
+        for (int i = 0; i < np; ++i) {
+            const float mi = ml[2 * i];
+            if (mi == -INFINITY)
+                continue;
+            const float f = exp2f(mi - M);
+            den += f * ml[2 * i + 1];
+            const float *a = accp + (int64_t)i * D + lane * DPL;
+            if constexpr (DPL == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(a);
+                num[0] += f * v.x;
+                num[1] += f * v.y;
+                num[2] += f * v.z;
+                num[3] += f * v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(a);
+                num[0] += f * v.x;
+                num[1] += f * v.y;
+            }
+        }
+    }
+    const bool zero = invalid || den == 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k)
+        store_out(p.out, p.out_dtype, sh * D + lane * DPL + k, zero ? 0.f : num[k] / den);
+}
+
+}  // namespace pkv

@@ -1,0 +1,100 @@
+// pkv_host.cuh -- host-side launch plumbing shared by the translation units:
+// TMA descriptor encoding for a [num_blocks, Hk, bs, D] cache and the
+// compile-time dispatch of the decode kernel over (head_dim, block size, G).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "pa_decode.cuh"
+
+namespace pkv {
+
+struct DecodeLaunch {
+    DecodeParams p;
+    const void *k_cache;
+    const void *v_cache;
+    int head_dim;
+    int block_size;
+    int group;
+    cudaStream_t stream;
+};
+
+// Encodes a 5-D TMA descriptor over one cache [NB, Hk, bs, D] (row = D * e
+// bytes) whose box is one block's `box_rows` rows of one kv head, written to
+// shared memory as [chunk][row][128 bytes] with 128-byte swizzling.
+// Dimension order (innermost first): elements of a 128-byte chunk, row of
+// the block, 128-byte chunk of the row, kv head, block.
+int encode_kv_map(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                  int head_dim, int block_size, int num_kv_heads, int64_t num_blocks, int box_rows);
+
+// Marks a kernel as allowed to use `bytes` of dynamic shared memory on the
+// current device (cached per device).
+int ensure_smem_attr(const void *func, int bytes, unsigned long long *done_mask);
+
+int launch_decode_f32(const DecodeLaunch &a);
+int launch_decode_f16(const DecodeLaunch &a);
+int launch_decode_bf16(const DecodeLaunch &a);
+
+template <typename T, int D, int BS, int G>
+int run_decode(const DecodeLaunch &a)
+{
+    using Sh = DecodeShape<T, D, BS, G>;
+    const DecodeParams &p = a.p;
+    alignas(64) CUtensorMap tmk;
+    alignas(64) CUtensorMap tmv;
+    int rc = encode_kv_map(&tmk, a.k_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
+                           p.num_blocks, Sh::box_rows);
+    if (rc)
+        return rc;
+    rc = encode_kv_map(&tmv, a.v_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
+                       p.num_blocks, Sh::box_rows);
+    if (rc)
+        return rc;
+    static unsigned long long done = 0;
+    auto kern = pa_decode_kernel<T, D, BS, G>;
+    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), Sh::smem, &done);
+    if (rc)
+        return rc;
+    dim3 grid(p.num_partitions, p.num_kv_heads, p.num_seqs);
+    kern<<<grid, Sh::threads, Sh::smem, a.stream>>>(p, tmk, tmv);
+    if (p.split) {
+        const long long pairs = (long long)p.num_seqs * p.num_heads;
+        pa_reduce_kernel<D><<<(unsigned)((pairs + 3) / 4), 128, 0, a.stream>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+template <typename T, int D, int BS>
+int dispatch_group(const DecodeLaunch &a)
+{
+    switch (a.group) {
+    case 1: return run_decode<T, D, BS, 1>(a);
+    case 2: return run_decode<T, D, BS, 2>(a);
+    case 4: return run_decode<T, D, BS, 4>(a);
+    case 8: return run_decode<T, D, BS, 8>(a);
+    default: return PKV_EUNSUPPORTED;
+    }
+}
+
+template <typename T, int D>
+int dispatch_block(const DecodeLaunch &a)
+{
+    switch (a.block_size) {
+    case 8: return dispatch_group<T, D, 8>(a);
+    case 16: return dispatch_group<T, D, 16>(a);
+    case 32: return dispatch_group<T, D, 32>(a);
+    default: return PKV_EUNSUPPORTED;
+    }
+}
+
+template <typename T>
+int dispatch_decode(const DecodeLaunch &a)
+{
+    switch (a.head_dim) {
+    case 64: return dispatch_block<T, 64>(a);
+    case 128: return dispatch_block<T, 128>(a);
+    default: return PKV_EUNSUPPORTED;
+    }
+}
+
+}  // namespace pkv

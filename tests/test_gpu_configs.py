@@ -1,0 +1,56 @@
+"""The five workload presets at full size on the GPU, in the launch
+configuration the benchmark times: sampled sequences checked against the
+oracle step by step (scatter, copy-on-write copies and attention)."""
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_support import TOL, SampledOracle, max_err
+from workloads import CONFIGS, PagedDecodeWorkload
+from workloads.runner import DeviceState
+
+pytestmark = pytest.mark.gpu
+
+SEED_BASE = 311 * 100
+
+
+def run_config(cfg, seed, steps, samples, partition_size=None, pool_blocks=None):
+    w = PagedDecodeWorkload(cfg, seed, total_steps=max(steps, 1), pool_blocks=pool_blocks)
+    state = DeviceState(cfg, w, seed)
+    inputs = [w.next_step() for _ in range(steps)]
+    rng = np.random.default_rng(seed)
+    seqs = sorted(rng.choice(w.num_seqs, size=min(samples, w.num_seqs), replace=False).tolist())
+    orc = SampledOracle(state, seqs, inputs)       # snapshot before any library kernel runs
+    worst = 0.0
+    for inp in inputs:
+        ds = state.to_device(inp, value_device="cpu")   # same values for both sides
+        state.run_step(ds, partition_size=partition_size)
+        torch.cuda.synchronize()
+        assert state.status.item() == 0
+        orc.apply_step(inp, ds.key.cpu(), ds.value.cpu())
+        ref = orc.attention(inp, ds.q.cpu())
+        got = state.out[seqs].to(torch.float64).cpu().numpy()
+        err = max_err(got, ref)
+        worst = max(worst, err)
+        assert err <= TOL[cfg.dtype], f"{cfg.name} step {inp.step}: max err {err}"
+    return worst
+
+
+def test_tiny_f32_every_sequence():
+    cfg = CONFIGS[0]
+    run_config(cfg, SEED_BASE + 0, steps=cfg.steps, samples=cfg.num_seqs)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_preset_sampled(idx):
+    cfg = CONFIGS[idx]
+    run_config(cfg, SEED_BASE + idx, steps=3, samples=6)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_long_context_sampled(bs):
+    cfg = CONFIGS[4].with_(block_size=bs)
+    free = torch.cuda.mem_get_info()[0]
+    pool_bytes = min(cfg.pool_value, 0.8 * free)
+    nb = int(pool_bytes // (2 * cfg.block_bytes))
+    run_config(cfg, SEED_BASE + 4, steps=2, samples=2, pool_blocks=nb)

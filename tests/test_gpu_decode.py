@@ -1,0 +1,136 @@
+"""GPU parity of paged_attention_decode against the CPU oracle.
+
+Bars: max-abs error <= 1e-5 for fp32 K/V and <= 2e-3 for fp16/bf16 K/V with
+fp32 output; fp16/bf16 output within one unit in the last place of the
+oracle's value in that dtype; bit-identical results under physical block
+permutation and prefix aliasing; L = 1 returns the value row exactly."""
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_support import TOL, gpu_decode, max_err, oracle_decode, ulp_bound
+from tests.util import logical_kv, small_case
+
+pytestmark = pytest.mark.gpu
+
+
+def lens_for(bs):
+    return (1, bs - 1, bs, bs + 1, 3 * bs + 5, 100, 511, 512, 513)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_decode_matrix(dtype, D, bs, G):
+    lens = lens_for(bs)
+    case = small_case(100 + D + bs + G, dtype=dtype, B=len(lens), H=2 * G, Hk=2, D=D, bs=bs,
+                      lens=lens)
+    ref, st = oracle_decode(case)
+    assert st == 0
+    for P in (0, 32, 4096):           # automatic, forced split (tiny partitions), forced single
+        got, gst, launches = gpu_decode(case, partition_size=P)
+        assert gst == 0
+        assert launches == (2 if P == 32 else 1) or P == 0
+        err = max_err(got, ref)
+        assert err <= TOL[dtype], f"P={P} max err {err}"
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_half_output_within_one_ulp(dtype):
+    case = small_case(3, dtype=dtype, B=4, H=8, Hk=2, D=128, bs=16, lens=(7, 300, 64, 1000))
+    ref, _ = oracle_decode(case)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    for P in (0, 64):
+        got, st, _ = gpu_decode(case, partition_size=P, out_dtype=tdt)
+        assert st == 0
+        rne = torch.from_numpy(ref).to(tdt).to(torch.float64).numpy()
+        assert np.all(np.abs(got - rne) <= ulp_bound(ref, tdt))
+
+
+def test_long_context_split_path():
+    lens = (4097, 16384 + 511, 9000)
+    case = small_case(9, dtype="bf16", B=3, H=16, Hk=2, D=128, bs=16, lens=lens)
+    ref, _ = oracle_decode(case)
+    for P in (0, 512, 1024):
+        got, st, launches = gpu_decode(case, partition_size=P)
+        assert st == 0 and launches == 2
+        assert max_err(got, ref) <= TOL["bf16"]
+
+
+def test_empty_and_single_token():
+    case = small_case(4, dtype="f32", B=4, H=4, Hk=4, D=64, bs=16, lens=(0, 1, 1, 0))
+    for P in (0, 32):
+        got, st, _ = gpu_decode(case, partition_size=P)
+        assert st == 0
+        assert not got[0].any() and not got[3].any()
+        for s in (1, 2):
+            _, V = logical_kv(case, s)
+            np.testing.assert_array_equal(got[s], V[0])   # exactly v_0
+
+
+def test_permutation_is_bit_exact():
+    case = small_case(5, dtype="bf16", B=3, H=8, Hk=1, D=128, bs=16, lens=(70, 513, 1200))
+    base, _, _ = gpu_decode(case, partition_size=512)
+    NB = case["k_cache"].shape[0]
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(1))
+    moved = dict(case)
+    moved["k_cache"] = torch.empty_like(case["k_cache"]); moved["k_cache"][perm] = case["k_cache"]
+    moved["v_cache"] = torch.empty_like(case["v_cache"]); moved["v_cache"][perm] = case["v_cache"]
+    t = case["block_tables"]
+    moved["block_tables"] = np.where(t >= 0, perm.numpy()[np.maximum(t, 0)], -1).astype(np.int32)
+    got, st, _ = gpu_decode(moved, partition_size=512)
+    assert st == 0
+    np.testing.assert_array_equal(got, base)
+
+
+def test_prefix_aliasing_is_bit_exact():
+    g = torch.Generator().manual_seed(6)
+    bs, Hk, H, D = 16, 2, 8, 128
+    kc = torch.randn(16, Hk, bs, D, generator=g).to(torch.bfloat16)
+    vc = torch.randn(16, Hk, bs, D, generator=g).to(torch.bfloat16)
+    kc[4:8] = kc[0:4]; vc[4:8] = vc[0:4]
+    q = torch.randn(1, H, D, generator=g).to(torch.bfloat16).repeat(2, 1, 1)
+    base = dict(q=q, k_cache=kc, v_cache=vc, dtype="bf16", bs=bs, Hk=Hk, scale=0.088388,
+                context_lens=np.array([4 * bs + 3, 4 * bs + 3], np.int32))
+    dup = dict(base, block_tables=np.array([[0, 1, 2, 3, 8], [4, 5, 6, 7, 8]], np.int32))
+    ali = dict(base, block_tables=np.array([[0, 1, 2, 3, 8], [0, 1, 2, 3, 8]], np.int32))
+    a, _, _ = gpu_decode(dup)
+    b, _, _ = gpu_decode(ali)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(a[0], a[1])
+
+
+def test_bad_block_and_length_are_reported():
+    import paged_kv_cache_311_gb300 as pkv
+    case = small_case(7, dtype="f16", B=3, H=4, Hk=2, D=128, bs=16, lens=(40, 40, 40))
+    good, _, _ = gpu_decode(case)
+    bad = dict(case)
+    t = case["block_tables"].copy()
+    t[1, 2] = case["k_cache"].shape[0] + 5
+    bad["block_tables"] = t
+    for P in (0, 32):
+        got, st, _ = gpu_decode(bad, partition_size=P)
+        assert st & pkv.DEV_BAD_BLOCK
+        assert not got[1].any()
+        np.testing.assert_array_equal(got[0], good[0])
+    lens = case["context_lens"].copy()
+    lens[2] = 41                                # beyond max_context_len passed below
+    bl = dict(case, context_lens=lens)
+    for P in (0, 32):
+        got, st, _ = gpu_decode(bl, partition_size=P, max_context_len=40)
+        assert st & pkv.DEV_BAD_CONTEXT_LEN
+        assert not got[2].any()
+        np.testing.assert_array_equal(got[0], good[0])
+
+
+def test_host_validation_rejects_bad_arguments():
+    import paged_kv_cache_311_gb300 as pkv
+    case = small_case(8, dtype="f16", B=2, H=4, Hk=2, D=128, bs=16, lens=(5, 6))
+    with pytest.raises(pkv.PkvError) as e:
+        gpu_decode(case, partition_size=48)     # not a multiple of 32
+    assert e.value.status == -1
+    odd = small_case(8, dtype="f16", B=2, H=6, Hk=2, D=128, bs=16, lens=(5, 6))   # G = 3
+    with pytest.raises(pkv.PkvError) as e:
+        gpu_decode(odd)
+    assert e.value.status == -2

@@ -104,7 +104,8 @@ class PagedDecodeWorkload:
     """
 
     def __init__(self, cfg: DecodeConfig, seed: int, *, pool_blocks: Optional[int] = None,
-                 total_steps: Optional[int] = None, num_seqs: Optional[int] = None):
+                 total_steps: Optional[int] = None, num_seqs: Optional[int] = None,
+                 contiguous: bool = False):
         self.cfg = cfg
         self.seed = int(seed)
         self.rng = np.random.Generator(np.random.Philox(self.seed))
@@ -147,6 +148,23 @@ class PagedDecodeWorkload:
 
         # Initial placement.
         self.seqs: List[_Seq] = []
+        self.reserved_next: Optional[List[int]] = None
+        if contiguous:
+            # Every sequence owns one run of consecutive blocks big enough for
+            # its whole run (the layout of a contiguous, non-paged cache).
+            if cfg.kind != "plain":
+                raise ValueError("contiguous placement is defined for plain workloads only")
+            need = [_blocks_for(int(L) + self.total_steps, self.bs) for L in self.init_lens]
+            if sum(need) > nb:
+                raise ValueError("pool too small for contiguous placement")
+            base = 0
+            self.reserved_next = []
+            for L, n in zip(self.init_lens, need):
+                k = _blocks_for(int(L), self.bs)
+                self.seqs.append(_Seq(table=list(range(base, base + k)), length=int(L)))
+                self.reserved_next.append(base + k)
+                base += n
+            return
         if cfg.kind == "shared_prefix":
             self.refcount = np.zeros(nb, dtype=np.int32)
             S = cfg.samples_per_prompt
@@ -232,7 +250,11 @@ class PagedDecodeWorkload:
         pos = q.length
         j, o = divmod(pos, self.bs)
         if o == 0:
-            b = self.free.pop()
+            if self.reserved_next is not None:
+                b = self.reserved_next[s]
+                self.reserved_next[s] += 1
+            else:
+                b = self.free.pop()
             q.table.append(b)
             if self.refcount is not None:
                 self.refcount[b] = 1
