@@ -50,6 +50,7 @@ def parse_args():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="llama7b_f16")
     ap.add_argument("--block-size", type=int, default=0)
+    ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling cases)")
     ap.add_argument("--partition-size", type=int, default=-1, help="-1: the preset's choice")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -159,7 +160,8 @@ def run_native(args):
     seed = SEED_BASE + CONFIGS.index(get(args.config)) + 1000 * rank
     total = args.warmup + args.steps
     w = PagedDecodeWorkload(cfg, seed, total_steps=max(total, cfg.steps),
-                            contiguous=args.identity_tables)
+                            contiguous=args.identity_tables, num_seqs=args.num_seqs or None,
+                            pool_blocks=_pool_blocks(cfg, dev))
     P = cfg.partition_size if args.partition_size < 0 else args.partition_size
     out_dtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[cfg.dtype]
     state = DeviceState(cfg, w, seed, device=dev, out_dtype=out_dtype)
@@ -191,8 +193,10 @@ def run_native(args):
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index) if rank == 0 else None
+    torch.cuda.nvtx.range_push("timed_steps")
     for i, s in enumerate(steps[args.warmup:]):
         flush.fill_(i)
+        _preroll()
         e0, e1, e2 = ev[i]
         e0.record(stream)
         if s.cow_pairs is not None:
@@ -212,6 +216,7 @@ def run_native(args):
         launches += n
         e2.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop() if clocks else None
@@ -250,6 +255,7 @@ def run_native(args):
                        "num_heads": cfg.num_heads, "num_kv_heads": cfg.num_kv_heads,
                        "head_dim": cfg.head_dim, "block_size": cfg.block_size,
                        "partition_size": P, "decode_launches_per_step": decode_launches[0],
+                       "pool_gb": round(2 * w.num_blocks * cfg.block_bytes / 1e9, 3),
                        "parallelism": f"replicas x{world} (sequences sharded, no collective)",
                        "l2": "flushed (256 MiB write) before every timed step, outside the events",
                        "block_placement": "contiguous" if args.identity_tables else "random"},
@@ -269,6 +275,24 @@ def run_native(args):
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def _preroll():
+    """Keeps the GPU busy for ~0.3 ms before a timed step so that the host has
+    enqueued the whole step before its first event is reached: the events
+    then time the kernels, not Python's launch overhead."""
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(600_000)
+
+
+def _pool_blocks(cfg, dev):
+    """Pools given in bytes (the long-context preset, ~60 GB) shrink to 80% of
+    the free device memory when the GPU has less room."""
+    if cfg.pool != "bytes":
+        return None
+    free = torch.cuda.mem_get_info(dev)[0]
+    return int(min(cfg.pool_value, 0.8 * free) // (2 * cfg.block_bytes))
 
 
 def _split_partition(P, max_len, launches):
