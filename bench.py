@@ -8,7 +8,7 @@ log-sum-exp reduce).  Default workload: the Llama-7B-shaped fp16 decode
 
 Prints ONE JSON line (rank 0).  value = algorithmic bytes of the step / device
 time of the step, with every input resident in HBM; L2 is flushed (256 MiB
-write) before every step, outside the timed events.  roofline = the decode
+read) before every step, outside the timed events.  roofline = the decode
 kernel's own algorithmic bytes per launch / its mean launch time against the
 measured HBM copy bandwidth.  e2e = the same metric with the step's inputs
 copied from pinned host memory and the output read back inside the timed
@@ -175,7 +175,7 @@ def run_native(args):
     import paged_kv_cache_311_gb300 as pkv
     for s in steps:
         state.ensure_workspace(s.max_context_len, P)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
     out_bytes = torch.tensor([], dtype=out_dtype).element_size()
 
@@ -195,7 +195,7 @@ def run_native(args):
     clocks = ClockSampler(dev.index) if rank == 0 else None
     torch.cuda.nvtx.range_push("timed_steps")
     for i, s in enumerate(steps[args.warmup:]):
-        flush.fill_(i)
+        _flush_l2(flush)
         _preroll()
         e0, e1, e2 = ev[i]
         e0.record(stream)
@@ -257,7 +257,7 @@ def run_native(args):
                        "partition_size": P, "decode_launches_per_step": decode_launches[0],
                        "pool_gb": round(2 * w.num_blocks * cfg.block_bytes / 1e9, 3),
                        "parallelism": f"replicas x{world} (sequences sharded, no collective)",
-                       "l2": "flushed (256 MiB write) before every timed step, outside the events",
+                       "l2": "flushed (256 MiB read) before every timed step, outside the events",
                        "block_placement": "contiguous" if args.identity_tables else "random"},
             "seq_steps_per_s": round(seqs_all / t_max, 1),
             "pct_of_peak": round(100 * value / peak, 2),
@@ -275,6 +275,13 @@ def run_native(args):
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def _flush_l2(buf):
+    """Evicts the decode step's data from L2 by reading a 256 MiB buffer (twice
+    the L2).  A read leaves clean lines behind, so the timed kernels do not pay
+    for writing flush data back to DRAM."""
+    torch.sum(buf, dtype=torch.int64)
 
 
 def _preroll():
@@ -302,8 +309,10 @@ def _split_partition(P, max_len, launches):
 
 
 def traffic_for(cfg, algo_bytes):
-    """Per-launch DRAM traffic of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source for this workload."""
+    """Per-launch DRAM traffic (read + write) of the decode kernel, from the
+    committed ncu capture's traffic / algorithmic-bytes ratio scaled to this
+    run's launches; None unless that capture was taken on the current kernel
+    source for this workload."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
         with open(path) as f:
@@ -316,7 +325,7 @@ def traffic_for(cfg, algo_bytes):
     e = d.get(cfg.name)
     if not e or e.get("source_sha") != h:
         return None
-    return e.get("bytes_per_launch")
+    return int(e["traffic_per_algorithmic_byte"] * algo_bytes)
 
 
 def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
@@ -338,7 +347,7 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
     h2d = d2h = 0
     total_ms = 0.0
     for i, (s, hp) in enumerate(zip(steps, pinned)):
-        flush.fill_(i)
+        _flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         q = torch.empty(hp["q"].shape, dtype=hp["q"].dtype, device=dev)
