@@ -147,6 +147,43 @@ int pkv_copy_blocks(void *const *k_caches, void *const *v_caches, int num_layers
                     const int64_t *src_dst_pairs, int num_pairs, size_t block_bytes,
                     int64_t num_blocks, uint32_t *device_status, void *stream);
 
+/*
+ * paged_attention_decode_static -- the same attention as
+ * pkv_paged_attention_decode, for callers that cannot allocate device
+ * memory.  (The pages have no counterpart; this is a convenience of this
+ * library.)  Callers of this kind include code running while a stream is
+ * captured into a CUDA graph (cudaMalloc is not allowed during capture),
+ * plugins whose host engine owns all device memory and gives them none, and
+ * latency-critical loops that must not call cudaMalloc because it may
+ * synchronise the device.
+ *
+ * It always takes the split-context path and keeps the partials in a buffer
+ * that lives inside libpkv.so: pkv_static_workspace_capacity() bytes (32 MiB)
+ * on every GPU that uses it, held until the process exits.  It calls no
+ * allocator.  The first call on a device looks up that buffer's address for
+ * the device (cudaGetSymbolAddress); make that first call before any stream
+ * capture begins.
+ *
+ * Arguments as for pkv_paged_attention_decode, without the workspace;
+ * partition_size 0 means PKV_DEFAULT_PARTITION tokens.  Returns
+ * PKV_EWORKSPACE when num_seqs * num_heads * ceil(max_context_len /
+ * partition_size) * (2 + head_dim) * 4 bytes (plus alignment) exceed the
+ * capacity.  All calls on one device share the buffer: calls whose kernels
+ * may overlap on the GPU (different streams without ordering) race and give
+ * wrong results; calls ordered on one stream are safe.  The buffer keeps the
+ * last call's partials; nothing in it needs to start at zero.
+ */
+int pkv_paged_attention_decode_static(void *out, int out_dtype, const void *q,
+                                      const void *k_cache, const void *v_cache, int kv_dtype,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *context_lens, int num_seqs, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int64_t num_blocks, int max_context_len, float scale,
+                                      int partition_size, uint32_t *device_status, void *stream);
+
+/* Bytes of the library-owned buffer pkv_paged_attention_decode_static uses. */
+size_t pkv_static_workspace_capacity(void);
+
 /* Static, NUL-terminated description of a pkv_status value. */
 const char *pkv_status_string(int status);
 
