@@ -131,7 +131,8 @@ int pkv_reshape_and_cache(const void *key, const void *value, void *k_cache, voi
 
 /*
  * copy_blocks -- copy-on-write block copies ("Advanced Features", KV-Cache
- * Sharing (Copy-on-Write): shared pages until write, like fork()).
+ * Sharing (Copy-on-Write): sharers keep one copy of a block until one of
+ * them writes to it, the way a forked process shares memory pages).
  *
  *   k_caches, v_caches  HOST arrays of num_layers DEVICE pointers, one K and
  *                one V cache per layer, each 16-byte aligned

@@ -9,7 +9,7 @@ Plain Python bookkeeping of physical blocks, written from the pages:
 * a page table maps logical block j to a physical block that may sit anywhere
   (same page, Step 4);
 * sequences that share a prefix share its blocks; a shared block is copied on
-  its first write, like fork() (same page, "Advanced Features", KV-Cache
+  its first write, the way a forked process shares memory pages (same page, "Advanced Features", KV-Cache
   Sharing (Copy-on-Write)).
 
 The refcount rule for the copy: a write into a block whose refcount is above
