@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--block-size", type=int, default=0)
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling cases)")
     ap.add_argument("--partition-size", type=int, default=-1, help="-1: the preset's choice")
+    ap.add_argument("--engine", default="auto", choices=["auto", "cuda_core", "tensor_core"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -173,6 +174,7 @@ def run_native(args):
 
     steps = [state.to_device(inp) for inp in host_inputs]
     import paged_kv_cache_311_gb300 as pkv
+    pkv.set_decode_engine(args.engine)
     for s in steps:
         state.ensure_workspace(s.max_context_len, P)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -213,6 +215,7 @@ def run_native(args):
                                    workspace=state.workspace, device_status=state.status)
         n = pkv.last_decode_launches()
         decode_launches.append(n)
+        engine_used = pkv.last_decode_engine()
         launches += n
         e2.record(stream)
     torch.cuda.synchronize()
@@ -255,6 +258,7 @@ def run_native(args):
                        "num_heads": cfg.num_heads, "num_kv_heads": cfg.num_kv_heads,
                        "head_dim": cfg.head_dim, "block_size": cfg.block_size,
                        "partition_size": P, "decode_launches_per_step": decode_launches[0],
+                       "engine": engine_used,
                        "pool_gb": round(2 * w.num_blocks * cfg.block_bytes / 1e9, 3),
                        "parallelism": f"replicas x{world} (sequences sharded, no collective)",
                        "l2": "flushed (256 MiB read) before every timed step, outside the events",

@@ -185,6 +185,18 @@ int pkv_paged_attention_decode_static(void *out, int out_dtype, const void *q,
 /* Bytes of the library-owned buffer pkv_paged_attention_decode_static uses. */
 size_t pkv_static_workspace_capacity(void);
 
+/*
+ * Engine of the decode kernel, process-wide (tests and benchmarks compare the
+ * two): 0 = automatic (tensor cores for 16-bit caches when num_heads /
+ * num_kv_heads >= 4, CUDA cores otherwise), 1 = CUDA cores, 2 = tensor cores
+ * (16-bit caches only; fp32 caches then return PKV_EUNSUPPORTED).
+ * Returns PKV_EINVAL for other values.
+ */
+int pkv_decode_set_engine(int engine);
+
+/* Engine (1 or 2) of the last successful decode call on this host thread. */
+int pkv_last_decode_engine(void);
+
 /* Static, NUL-terminated description of a pkv_status value. */
 const char *pkv_status_string(int status);
 

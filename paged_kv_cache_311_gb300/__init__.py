@@ -26,6 +26,7 @@ from .build import library_path
 __all__ = [
     "PkvError", "load_library", "paged_attention_decode", "reshape_and_cache", "copy_blocks",
     "paged_attention_workspace_bytes", "status_string", "last_decode_launches",
+    "set_decode_engine", "last_decode_engine",
     "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "HEADER_PATH",
 ]
 
@@ -70,6 +71,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_status_string.restype = ctypes.c_char_p
     L.pkv_last_decode_launches.argtypes = []
     L.pkv_last_decode_launches.restype = i32
+    L.pkv_last_decode_engine.argtypes = []
+    L.pkv_last_decode_engine.restype = i32
+    L.pkv_decode_set_engine.argtypes = [i32]
+    L.pkv_decode_set_engine.restype = i32
     if path is None:
         _lib = L
     return L
@@ -88,6 +93,19 @@ def status_string(status: int) -> str:
 
 def last_decode_launches() -> int:
     return int(load_library().pkv_last_decode_launches())
+
+
+ENGINES = {"auto": 0, "cuda_core": 1, "tensor_core": 2}
+
+
+def set_decode_engine(engine: str) -> None:
+    """Process-wide engine of the decode kernel: "auto", "cuda_core" or "tensor_core"."""
+    _check(load_library().pkv_decode_set_engine(ENGINES[engine]), "pkv_decode_set_engine")
+
+
+def last_decode_engine() -> str:
+    code = int(load_library().pkv_last_decode_engine())
+    return {1: "cuda_core", 2: "tensor_core"}.get(code, "none")
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -2,28 +2,33 @@
 //
 // What it computes (PagedAttention: Efficient LLM Serving with vLLM, "The
 // PagedAttention Algorithm", Steps 4-5): for every sequence s and query head
-// h, softmax(scale * q[s,h] . k_i) weighted sum of v_i over the sequence's
-// logical tokens i < L_s, where token i lives in physical block
-// block_tables[s][i / bs], row i % bs, of a cache laid out
-// [num_blocks, Hk, bs, D].
+// h, the softmax(scale * q[s,h] . k_i)-weighted sum of v_i over the
+// sequence's logical tokens i < L_s, where token i lives in physical block
+// block_tables[s][i / bs], row i % bs, of a cache laid out [num_blocks, Hk,
+// bs, D].
 //
 // Kernel design (one CTA per (context partition, kv head, sequence)):
 //   * The CTA owns the G = H / Hk query heads of one kv head, so every K/V
 //     byte is read from HBM once and feeds G heads.
-//   * Each warp streams its own tiles of TILE tokens through an S-stage ring
-//     in shared memory.  Lane 0 of the warp is the producer: for each tile it
-//     issues one TMA (cp.async.bulk.tensor.5d) load per block-box of K and of
-//     V, with 128-byte swizzling so that both the token-per-lane reads of the
-//     QK phase and the dim-per-lane reads of the PV phase are free of bank
-//     conflicts.  Block ids come from a copy of the partition's slice of the
-//     block table staged in shared memory when the CTA starts.
-//   * QK: LPT = 32 / TILE lanes per token, each taking a fixed subset of the
-//     row's 16-byte pieces; q (pre-scaled by scale * log2 e) is read from
-//     shared memory as broadcasts; packed fp32x2 FMAs, fp32 accumulation.
-//   * Online softmax per tile in the log2 domain (exp2), probabilities staged
-//     in shared memory as (p, p) pairs.
-//   * PV: every lane owns D / 32 output dims for all G heads and walks the
-//     tile's tokens; packed fp32x2 FMAs.
+//   * Each warp streams its own tiles of 16 tokens through an S-stage ring in
+//     shared memory.  Lane 0 of the warp is the producer: per tile it issues
+//     one TMA load (cp.async.bulk.tensor.5d) per block-box of K and of V,
+//     completing on the stage's mbarrier.  The tensor map writes each box as
+//     [128-byte chunk][row][128 bytes] with 128-byte swizzling, which makes
+//     both token-major and dim-major shared-memory reads conflict-free.
+//     Block ids come from the partition's slice of the block table, staged in
+//     shared memory when the CTA starts.
+//   * Two interchangeable per-warp engines consume a tile:
+//       CcEngine (CUDA cores): QK with two lanes per token and q broadcast
+//         from shared memory, PV with D/32 dims of all G heads per lane,
+//         packed fp32x2 FMAs; for fp32 caches and small G.
+//       TcEngine (tensor cores, mma.sync m16n8k16): for 16-bit caches, the
+//         tile is the M = 16 dimension and the (up to 8) query heads the
+//         N = 8 dimension: S^T = K q^T from ldmatrix'd K, O^T += V^T P^T with
+//         ldmatrix.trans'd V and P^T transposed in registers (movmatrix).  P
+//         is split into a 16-bit high part and a 16-bit remainder so that the
+//         products keep fp32-level accuracy; accumulation is fp32.
+//     Both run the online softmax per tile in the log2 domain (exp2).
 //   * End of CTA: warps merge (max, sum, acc) through shared memory; the
 //     single-pass kernel writes the normalised output, the split-context
 //     kernel writes (max, sum, unnormalised acc) to the workspace for the
@@ -31,6 +36,8 @@
 //   * Reduction order depends only on logical token positions, so results
 //     are bit-identical under any physical placement of the blocks.
 #pragma once
+
+#include <type_traits>
 
 #include "pkv_device.cuh"
 
@@ -55,43 +62,43 @@ struct DecodeParams {
     float qscale;        // softmax scale * log2(e)
 };
 
-#ifndef PKV_DECODE_TILE
-#define PKV_DECODE_TILE 16
+enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2 };
+
+#ifndef PKV_DECODE_STAGE_BUDGET_CC
+#define PKV_DECODE_STAGE_BUDGET_CC 98304
 #endif
-#ifndef PKV_DECODE_WARPS
-#define PKV_DECODE_WARPS 4
-#endif
-#ifndef PKV_DECODE_STAGE_BUDGET
-#define PKV_DECODE_STAGE_BUDGET 98304
+#ifndef PKV_DECODE_STAGE_BUDGET_TC
+#define PKV_DECODE_STAGE_BUDGET_TC 98304
 #endif
 
-template <typename T, int D, int BS, int G>
+template <typename T, int D, int BS, int G, bool TC>
 struct DecodeCfg {
     static constexpr int E = Elem<T>::bytes;
-    static constexpr int TILE = PKV_DECODE_TILE;   // tokens per warp tile
-    static constexpr int NW = PKV_DECODE_WARPS;    // warps per CTA
+    static constexpr int TILE = 16;                // tokens per warp tile
+    static constexpr int NW = 4;                   // warps per CTA
     static constexpr int ROW = D * E;              // bytes of one token row
     static constexpr int CHUNKS = ROW / 128;       // 128-byte swizzle atoms per row
     static constexpr int EPP = 16 / E;             // elements per 16-byte piece
     static constexpr int NPC = ROW / 16;           // pieces per row
-    static constexpr int LPT = 32 / TILE;          // lanes per token in QK
-    static constexpr int PCL = 8 / LPT;            // pieces per chunk per lane
     static constexpr int BOX_ROWS = BS < TILE ? BS : TILE;
     static constexpr int BOXES = TILE / BOX_ROWS;
     static constexpr int BOX_BYTES = BOX_ROWS * ROW;
     static constexpr int TILE_BYTES = TILE * ROW;  // K (or V) of one tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int S0 = PKV_DECODE_STAGE_BUDGET / (NW * STAGE_BYTES);
+    static constexpr int BUDGET = TC ? PKV_DECODE_STAGE_BUDGET_TC : PKV_DECODE_STAGE_BUDGET_CC;
+    static constexpr int S0 = BUDGET / (NW * STAGE_BYTES);
     static constexpr int S = S0 < 2 ? 2 : (S0 > 8 ? 8 : S0);  // ring depth per warp
-    static constexpr int DPL = D / 32;             // PV dims per lane
-    static constexpr int QROW = G * EPP * 4 + 16;  // bytes per q piece row (padded)
     static constexpr int TABLE_CAP = 1024;         // block-table entries per CTA
+    // CUDA-core engine: shared-memory q (padded rows) and (p, p) pairs.
+    static constexpr int QROW = G * EPP * 4 + 16;
+    static constexpr int Q_BYTES = TC ? 0 : ((NPC * QROW + 127) / 128) * 128;
+    static constexpr int P_BYTES = TC ? 0 : NW * TILE * G * 8;
 
     static constexpr int OFF_STAGES = 0;
     static constexpr int STAGES_BYTES = NW * S * STAGE_BYTES;
     static constexpr int OFF_Q = STAGES_BYTES;
-    static constexpr int OFF_P = OFF_Q + ((NPC * QROW + 127) / 128) * 128;
-    static constexpr int OFF_TABLE = OFF_P + NW * TILE * G * 8;
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;
+    static constexpr int OFF_TABLE = OFF_P + P_BYTES;
     static constexpr int OFF_BAR = OFF_TABLE + TABLE_CAP * 4;
     static constexpr int OFF_FLAG = OFF_BAR + NW * S * 8;
     static constexpr int SMEM_USED = OFF_FLAG + 16;
@@ -100,19 +107,26 @@ struct DecodeCfg {
     static_assert(ROW % 128 == 0, "rows must be whole 128-byte swizzle atoms");
     static_assert(TILE % BOX_ROWS == 0 && BOX_ROWS % 8 == 0, "box rows");
     static_assert(BOX_BYTES % 1024 == 0, "TMA 128B-swizzle boxes need 1024-byte alignment");
-    static_assert(D % 64 == 0 && DPL % 2 == 0, "head_dim");
+    static_assert(D % 64 == 0, "head_dim");
+    static_assert(!TC || (E == 2 && G <= 8), "tensor-core engine: 16-bit caches, G <= 8");
     static_assert(NW * G * (D + 2) * 4 <= STAGES_BYTES, "merge scratch fits in the ring");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+
+    // Shared-memory address of 16-byte piece `q` of token row `t` of a tile.
+    __device__ __forceinline__ static uint32_t addr(uint32_t base, int t, int q)
+    {
+        const int bx = t / BOX_ROWS, r = t % BOX_ROWS;
+        return base + bx * BOX_BYTES + ((q >> 3) * BOX_ROWS + r) * 128 + (((q & 7) ^ (r & 7)) << 4);
+    }
 };
 
 // Host-visible description of the config (for the TMA box and launch).
-template <typename T, int D, int BS, int G>
+template <typename T, int D, int BS, int G, bool TC>
 struct DecodeShape {
-    using C = DecodeCfg<T, D, BS, G>;
+    using C = DecodeCfg<T, D, BS, G, TC>;
     static constexpr int box_rows = C::BOX_ROWS;
     static constexpr int threads = C::NW * 32;
     static constexpr int smem = C::SMEM_BYTES;
-    static constexpr int tile = C::TILE;
 };
 
 __device__ __forceinline__ void store_out(void *out, int dtype, int64_t i, float v)
@@ -147,13 +161,314 @@ __device__ void write_invalid(const DecodeParams &p, int seq, int kvh, int part)
     }
 }
 
+// ------------------------------------------------------------ CUDA cores
 template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(DecodeCfg<T, D, BS, G>::NW * 32)
+struct CcEngine {
+    using C = DecodeCfg<T, D, BS, G, false>;
+    static constexpr int LPT = 32 / C::TILE;   // lanes per token in QK
+    static constexpr int PCL = 8 / LPT;        // pieces per 128-byte chunk per lane
+    static constexpr int DPL = D / 32;         // PV dims per lane
+    static constexpr int VBYTES = DPL * C::E;  // PV bytes per lane per row
+
+    float m[G], lsum[G];
+    float2 acc[G][DPL / 2];
+    uint32_t qbase, pbase;
+    int ti, sub, vq, vin;
+
+    // Stages q (pre-scaled by scale * log2 e) as [piece][head][EPP] fp32.
+    __device__ static void stage_q(const DecodeParams &p, uint8_t *smem, int seq, int kvh)
+    {
+        const T *qp = static_cast<const T *>(p.q) + ((int64_t)seq * p.num_heads + kvh * G) * D;
+        for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+            const int h = i / D, d = i % D;
+            float *dst = reinterpret_cast<float *>(smem + C::OFF_Q + (d / C::EPP) * C::QROW);
+            dst[h * C::EPP + d % C::EPP] = to_float(qp[i]) * p.qscale;
+        }
+    }
+
+    __device__ void init(const DecodeParams &, uint8_t *smem, int, int, int warp, int lane)
+    {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            m[h] = -INFINITY;
+            lsum[h] = 0.f;
+#pragma unroll
+            for (int k = 0; k < DPL / 2; ++k)
+                acc[h][k] = make_float2(0.f, 0.f);
+        }
+        ti = lane / LPT;
+        sub = lane % LPT;
+        qbase = smem_u32(smem + C::OFF_Q);
+        pbase = smem_u32(smem + C::OFF_P) + warp * C::TILE * G * 8;
+        vq = (lane * VBYTES) >> 4;
+        vin = (lane * VBYTES) & 15;
+    }
+
+    __device__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, int lane)
+    {
+        // ---- QK for token ti
+        float2 s2[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+            s2[h] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c2 = 0; c2 < C::CHUNKS; ++c2) {
+#pragma unroll
+            for (int i4 = 0; i4 < PCL; ++i4) {
+                const int pc = sub * PCL + i4;
+                const uint4 kw = lds128(C::addr(kbase, ti, c2 * 8 + pc));
+                const uint32_t qa = qbase + (c2 * 8 + pc) * C::QROW;
+                if constexpr (C::E == 2) {
+                    const float2 k0 = Unpack<T>::pair(kw.x), k1 = Unpack<T>::pair(kw.y);
+                    const float2 k2 = Unpack<T>::pair(kw.z), k3 = Unpack<T>::pair(kw.w);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float4 qa0 = lds128f(qa + h * 32);
+                        const float4 qa1 = lds128f(qa + h * 32 + 16);
+                        s2[h] = ffma2(make_float2(qa0.x, qa0.y), k0, s2[h]);
+                        s2[h] = ffma2(make_float2(qa0.z, qa0.w), k1, s2[h]);
+                        s2[h] = ffma2(make_float2(qa1.x, qa1.y), k2, s2[h]);
+                        s2[h] = ffma2(make_float2(qa1.z, qa1.w), k3, s2[h]);
+                    }
+                } else {
+                    const float2 k0 = make_float2(__uint_as_float(kw.x), __uint_as_float(kw.y));
+                    const float2 k1 = make_float2(__uint_as_float(kw.z), __uint_as_float(kw.w));
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float4 qa0 = lds128f(qa + h * 16);
+                        s2[h] = ffma2(make_float2(qa0.x, qa0.y), k0, s2[h]);
+                        s2[h] = ffma2(make_float2(qa0.z, qa0.w), k1, s2[h]);
+                    }
+                }
+            }
+        }
+
+        // ---- online softmax over this tile (log2 domain)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float s = s2[h].x + s2[h].y;
+#pragma unroll
+            for (int off = 1; off < LPT; off <<= 1)
+                s += __shfl_xor_sync(0xffffffffu, s, off);
+            s = ti < nvalid ? s : -INFINITY;
+            float tm = s;
+#pragma unroll
+            for (int off = LPT; off < 32; off <<= 1)
+                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
+            const float mn = fmaxf(m[h], tm);
+            const float alpha = exp2f(m[h] - mn);
+            const float pr = exp2f(s - mn);
+            lsum[h] = lsum[h] * alpha + (sub == 0 ? pr : 0.f);
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int k = 0; k < DPL / 2; ++k)
+                acc[h][k] = fmul2(acc[h][k], a2);
+            m[h] = mn;
+            if (sub == 0)
+                asm volatile("st.shared.v2.f32 [%0], {%1, %1};" ::"r"(pbase + (ti * G + h) * 8),
+                             "f"(pr)
+                             : "memory");
+        }
+        __syncwarp();
+
+        // ---- PV: this lane's D/32 dims of every head
+        for (int t = 0; t < nvalid; ++t) {
+            const uint32_t va = C::addr(vbase, t, vq) + vin;
+            float2 vf[DPL / 2];
+            if constexpr (C::E == 2) {
+                if constexpr (VBYTES == 8) {
+                    const uint2 w = lds64(va);
+                    vf[0] = Unpack<T>::pair(w.x);
+                    vf[1] = Unpack<T>::pair(w.y);
+                } else {
+                    vf[0] = Unpack<T>::pair(lds32(va));
+                }
+            } else {
+                if constexpr (VBYTES == 16) {
+                    const float4 w = lds128f(va);
+                    vf[0] = make_float2(w.x, w.y);
+                    vf[1] = make_float2(w.z, w.w);
+                } else {
+                    vf[0] = lds64f(va);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float2 pp = lds64f(pbase + (t * G + h) * 8);
+#pragma unroll
+                for (int k = 0; k < DPL / 2; ++k)
+                    acc[h][k] = ffma2(pp, vf[k], acc[h][k]);
+            }
+        }
+    }
+
+    // Per-warp (max, sum, acc) of every head into the merge scratch.
+    __device__ void finish(float *mw, float *lw, float *aw, int warp, int lane)
+    {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], off);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                mw[warp * G + h] = m[h];
+                lw[warp * G + h] = lsum[h];
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int k = 0; k < DPL / 2; ++k)
+                *reinterpret_cast<float2 *>(&aw[(warp * G + h) * D + lane * DPL + 2 * k]) = acc[h][k];
+        }
+    }
+};
+
+// ---------------------------------------------------------- tensor cores
+template <typename T, int D, int BS, int G>
+struct TcEngine {
+    using C = DecodeCfg<T, D, BS, G, true>;
+    static constexpr int KS = D / 16;   // k-steps of QK = m-tiles of PV
+
+    uint32_t qf[KS][2];   // q^T B-fragments: rows g (< G), dims 16 ks + 2c (+8)
+    float o[KS][4];       // O^T C-fragments: dims 16 mt + g (+8), rows 2c, 2c+1
+    float m[2], lsum[2];  // rows 2c, 2c+1
+    float qscale;
+    int g, c;
+
+    __device__ static void stage_q(const DecodeParams &, uint8_t *, int, int) {}
+
+    __device__ void init(const DecodeParams &p, uint8_t *, int seq, int kvh, int, int lane)
+    {
+        g = lane >> 2;
+        c = lane & 3;
+        qscale = p.qscale;
+        const uint32_t *qp = reinterpret_cast<const uint32_t *>(
+            static_cast<const T *>(p.q) + ((int64_t)seq * p.num_heads + kvh * G + g) * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qf[ks][0] = g < G ? qp[(16 * ks + 2 * c) / 2] : 0u;
+            qf[ks][1] = g < G ? qp[(16 * ks + 2 * c + 8) / 2] : 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                o[ks][j] = 0.f;
+        }
+        m[0] = m[1] = -INFINITY;
+        lsum[0] = lsum[1] = 0.f;
+    }
+
+    __device__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, int lane)
+    {
+        // ---- S^T (16 tokens x 8 query rows) = K q^T
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int t = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int dq = lane >> 4;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(C::addr(kbase, t, 2 * ks + dq), a);
+                Mma<T>::run(s, a, qf[ks][0], qf[ks][1]);
+            }
+        }
+
+        // ---- online softmax: this lane holds tokens g, g + 8 of rows 2c, 2c+1
+        const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
+        float p0[2], p1[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float x0 = ok0 ? s[j] * qscale : -INFINITY;
+            const float x1 = ok1 ? s[2 + j] * qscale : -INFINITY;
+            float tm = fmaxf(x0, x1);
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+            const float mn = fmaxf(m[j], tm);
+            const float alpha = exp2f(m[j] - mn);
+            p0[j] = exp2f(x0 - mn);
+            p1[j] = exp2f(x1 - mn);
+            lsum[j] = lsum[j] * alpha + p0[j] + p1[j];
+            m[j] = mn;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][j] *= alpha;
+                o[mt][2 + j] *= alpha;
+            }
+        }
+
+        // ---- rows of V past the valid tokens may hold anything (even NaN
+        // bit patterns); zero them so that 0 * v stays 0 in the PV products.
+        if (nvalid < C::TILE) {
+            for (int idx = lane; idx < (C::TILE - nvalid) * C::NPC; idx += 32) {
+                const int t = nvalid + idx / C::NPC, q = idx % C::NPC;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(C::addr(vbase, t, q)),
+                             "r"(0u)
+                             : "memory");
+            }
+            __syncwarp();
+        }
+
+        // ---- P^T B-fragments: P = hi + lo in the cache's 16-bit type
+        const uint32_t h0 = Mma<T>::pack(p0[0], p0[1]);  // tokens g,   rows 2c, 2c+1
+        const uint32_t h1 = Mma<T>::pack(p1[0], p1[1]);  // tokens g+8, rows 2c, 2c+1
+        const float2 f0 = Mma<T>::unpack(h0), f1 = Mma<T>::unpack(h1);
+        const uint32_t l0 = Mma<T>::pack(p0[0] - f0.x, p0[1] - f0.y);
+        const uint32_t l1 = Mma<T>::pack(p1[0] - f1.x, p1[1] - f1.y);
+        const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
+        const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
+
+        // ---- O^T (D dims x 8 rows) += V^T P^T
+        {
+            const int t = (lane & 7) + (lane >> 4) * 8;
+            const int dq = (lane >> 3) & 1;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t a[4];
+                ldsm_x4_trans(C::addr(vbase, t, 2 * mt + dq), a);
+                Mma<T>::run(o[mt], a, bh0, bh1);
+                Mma<T>::run(o[mt], a, bl0, bl1);
+            }
+        }
+    }
+
+    __device__ void finish(float *mw, float *lw, float *aw, int warp, int lane)
+    {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 4);
+            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 8);
+            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int row = 2 * c + j;
+            if (row < G) {
+                if (g == 0) {
+                    mw[warp * G + row] = m[j];
+                    lw[warp * G + row] = lsum[j];
+                }
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    aw[(warp * G + row) * D + 16 * mt + g] = o[mt][j];
+                    aw[(warp * G + row) * D + 16 * mt + g + 8] = o[mt][2 + j];
+                }
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------ the kernel
+template <typename T, int D, int BS, int G, bool TC>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, G, TC>::NW * 32)
 pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv)
 {
-    using C = DecodeCfg<T, D, BS, G>;
-    constexpr int NW = C::NW, S = C::S, TILE = C::TILE, LPT = C::LPT;
+    using C = DecodeCfg<T, D, BS, G, TC>;
+    using Eng = typename std::conditional<TC, TcEngine<T, D, BS, G>, CcEngine<T, D, BS, G>>::type;
+    constexpr int NW = C::NW, S = C::S, TILE = C::TILE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -177,7 +492,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
         return;
     }
 
-    // ---- stage the block-table slice and the pre-scaled queries
+    // ---- stage the block-table slice (and, for the CUDA-core engine, q)
     const int j0 = tok0 / BS;
     const int nblk = (tok_end - tok0 + BS - 1) / BS;
     int32_t *table_s = reinterpret_cast<int32_t *>(smem + C::OFF_TABLE);
@@ -191,13 +506,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
         }
         table_s[i] = b;
     }
-    const T *qp = static_cast<const T *>(p.q) + ((int64_t)seq * p.num_heads + kvh * G) * D;
-    for (int i = tid; i < G * D; i += NW * 32) {
-        const int h = i / D, d = i % D;
-        const float v = to_float(qp[i]) * p.qscale;
-        float *dst = reinterpret_cast<float *>(smem + C::OFF_Q + (d / C::EPP) * C::QROW);
-        dst[h * C::EPP + d % C::EPP] = v;
-    }
+    Eng::stage_q(p, smem, seq, kvh);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR) + warp * S;
     uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + C::OFF_FLAG);
     if (lane == 0) {
@@ -243,24 +552,8 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
             issue(i, i);
     }
 
-    float m[G], lsum[G];
-    float2 acc[G][C::DPL / 2];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m[h] = -INFINITY;
-        lsum[h] = 0.f;
-#pragma unroll
-        for (int k = 0; k < C::DPL / 2; ++k)
-            acc[h][k] = make_float2(0.f, 0.f);
-    }
-
-    const int ti = lane / LPT;           // token of this lane in QK
-    const int sub = lane % LPT;          // which piece subset of the row
-    const int qbox = ti / C::BOX_ROWS, qr = ti % C::BOX_ROWS;
-    const uint32_t qbase = smem_u32(smem + C::OFF_Q);
-    const uint32_t pbase = smem_u32(smem + C::OFF_P) + warp * TILE * G * 8;
-    constexpr int VBYTES = C::DPL * C::E;           // PV bytes per lane per row
-    const int vq = (lane * VBYTES) >> 4, vin = (lane * VBYTES) & 15;
+    Eng eng;
+    eng.init(p, smem, seq, kvh, warp, lane);
 
     int failed_at = -1;
     for (int i = 0; i < my_n; ++i) {
@@ -272,107 +565,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
         const int t0 = tok0 + (warp + i * NW) * TILE;
         const int nvalid = min(TILE, tok_end - t0);
         const uint32_t kbase = smem_u32(stages + st * C::STAGE_BYTES);
-        const uint32_t vbase = kbase + C::TILE_BYTES;
-
-        // ---- QK for token ti
-        float2 s2[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-            s2[h] = make_float2(0.f, 0.f);
-        const uint32_t krow = kbase + qbox * C::BOX_BYTES + qr * 128;
-#pragma unroll
-        for (int c2 = 0; c2 < C::CHUNKS; ++c2) {
-#pragma unroll
-            for (int i4 = 0; i4 < C::PCL; ++i4) {
-                const int pc = sub * C::PCL + i4;
-                const uint4 kw = lds128(krow + c2 * C::BOX_ROWS * 128 + ((pc ^ (qr & 7)) << 4));
-                const uint32_t qa = qbase + (c2 * 8 + pc) * C::QROW;
-                if constexpr (C::E == 2) {
-                    const float2 k0 = Unpack<T>::pair(kw.x), k1 = Unpack<T>::pair(kw.y);
-                    const float2 k2 = Unpack<T>::pair(kw.z), k3 = Unpack<T>::pair(kw.w);
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float4 qa0 = lds128f(qa + h * 32);
-                        const float4 qa1 = lds128f(qa + h * 32 + 16);
-                        s2[h] = ffma2(make_float2(qa0.x, qa0.y), k0, s2[h]);
-                        s2[h] = ffma2(make_float2(qa0.z, qa0.w), k1, s2[h]);
-                        s2[h] = ffma2(make_float2(qa1.x, qa1.y), k2, s2[h]);
-                        s2[h] = ffma2(make_float2(qa1.z, qa1.w), k3, s2[h]);
-                    }
-                } else {
-                    const float2 k0 = make_float2(__uint_as_float(kw.x), __uint_as_float(kw.y));
-                    const float2 k1 = make_float2(__uint_as_float(kw.z), __uint_as_float(kw.w));
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float4 qa0 = lds128f(qa + h * 16);
-                        s2[h] = ffma2(make_float2(qa0.x, qa0.y), k0, s2[h]);
-                        s2[h] = ffma2(make_float2(qa0.z, qa0.w), k1, s2[h]);
-                    }
-                }
-            }
-        }
-
-        // ---- online softmax over this tile (log2 domain)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float s = s2[h].x + s2[h].y;
-            if constexpr (LPT > 1) {
-#pragma unroll
-                for (int off = 1; off < LPT; off <<= 1)
-                    s += __shfl_xor_sync(0xffffffffu, s, off);
-            }
-            s = ti < nvalid ? s : -INFINITY;
-            float tm = s;
-#pragma unroll
-            for (int off = LPT; off < 32; off <<= 1)
-                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
-            const float mn = fmaxf(m[h], tm);
-            const float alpha = exp2f(m[h] - mn);
-            const float pr = exp2f(s - mn);
-            lsum[h] = lsum[h] * alpha + (sub == 0 ? pr : 0.f);
-            const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-            for (int k = 0; k < C::DPL / 2; ++k)
-                acc[h][k] = fmul2(acc[h][k], a2);
-            m[h] = mn;
-            if (sub == 0)
-                asm volatile("st.shared.v2.f32 [%0], {%1, %1};" ::"r"(pbase + (ti * G + h) * 8),
-                             "f"(pr)
-                             : "memory");
-        }
-        __syncwarp();
-
-        // ---- PV: this lane's D/32 dims of every head
-        for (int t = 0; t < nvalid; ++t) {
-            const int bx = t / C::BOX_ROWS, r = t % C::BOX_ROWS;
-            const uint32_t va = vbase + bx * C::BOX_BYTES + ((vq >> 3) * C::BOX_ROWS + r) * 128 +
-                                ((((vq & 7) ^ (r & 7)) << 4) | vin);
-            float2 vf[C::DPL / 2];
-            if constexpr (C::E == 2) {
-                if constexpr (VBYTES == 8) {
-                    const uint2 w = lds64(va);
-                    vf[0] = Unpack<T>::pair(w.x);
-                    vf[1] = Unpack<T>::pair(w.y);
-                } else {
-                    vf[0] = Unpack<T>::pair(lds32(va));
-                }
-            } else {
-                if constexpr (VBYTES == 16) {
-                    const float4 w = lds128f(va);
-                    vf[0] = make_float2(w.x, w.y);
-                    vf[1] = make_float2(w.z, w.w);
-                } else {
-                    vf[0] = lds64f(va);
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float2 pp = lds64f(pbase + (t * G + h) * 8);
-#pragma unroll
-                for (int k = 0; k < C::DPL / 2; ++k)
-                    acc[h][k] = ffma2(pp, vf[k], acc[h][k]);
-            }
-        }
+        eng.tile(kbase, kbase + C::TILE_BYTES, nvalid, lane);
         __syncwarp();
         if (lane == 0 && i + S < my_n) {
             fence_proxy_async_smem();
@@ -392,31 +585,12 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
         }
     }
 
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], off);
-    }
     __syncthreads();  // every warp is done with its ring: reuse it as merge scratch
     const bool failed = *reinterpret_cast<volatile uint32_t *>(cta_flag) != 0;
     float *mw = reinterpret_cast<float *>(smem + C::OFF_STAGES);
     float *lw = mw + NW * G;
     float *aw = lw + NW * G;
-    if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            mw[warp * G + h] = m[h];
-            lw[warp * G + h] = lsum[h];
-        }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int k = 0; k < C::DPL / 2; ++k)
-            *reinterpret_cast<float2 *>(&aw[(warp * G + h) * D + lane * C::DPL + 2 * k]) =
-                acc[h][k];
-    }
+    eng.finish(mw, lw, aw, warp, lane);
     __syncthreads();
 
     for (int idx = tid; idx < G * D; idx += NW * 32) {

@@ -58,6 +58,8 @@ int sm_count(int dev)
 }
 
 thread_local int g_last_decode_launches = 0;
+thread_local int g_last_decode_engine = 0;
+std::atomic<int> g_engine_override{0};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -139,6 +141,16 @@ const char *pkv_status_string(int status)
 
 int pkv_last_decode_launches(void) { return g_last_decode_launches; }
 
+int pkv_last_decode_engine(void) { return g_last_decode_engine; }
+
+int pkv_decode_set_engine(int engine)
+{
+    if (engine < kEngineAuto || engine > kEngineTensorCore)
+        return PKV_EINVAL;
+    g_engine_override.store(engine, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
 size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_heads, int max_context_len,
                                            int head_dim, int partition_size)
 {
@@ -161,6 +173,7 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
                                uint32_t *device_status, void *stream)
 {
     g_last_decode_launches = 0;
+    g_last_decode_engine = 0;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
         return PKV_EINVAL;
     if (!valid_dtype(out_dtype) || !valid_dtype(kv_dtype))
@@ -247,7 +260,10 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     a.head_dim = head_dim;
     a.block_size = block_size;
     a.group = group;
+    a.engine = g_engine_override.load(std::memory_order_relaxed);
     a.stream = static_cast<cudaStream_t>(stream);
+    int engine_used = 0;
+    a.engine_used = &engine_used;
 
     int rc;
     switch (kv_dtype) {
@@ -255,8 +271,10 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     case PKV_F16: rc = launch_decode_f16(a); break;
     default: rc = launch_decode_bf16(a); break;
     }
-    if (rc == PKV_OK)
+    if (rc == PKV_OK) {
         g_last_decode_launches = p.split ? 2 : 1;
+        g_last_decode_engine = engine_used;
+    }
     return rc;
 }
 

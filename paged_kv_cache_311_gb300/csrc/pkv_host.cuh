@@ -16,7 +16,9 @@ struct DecodeLaunch {
     int head_dim;
     int block_size;
     int group;
+    int engine;          // Engine: kEngineAuto, kEngineCudaCore or kEngineTensorCore
     cudaStream_t stream;
+    int *engine_used;    // out: the engine that ran
 };
 
 // Encodes a 5-D TMA descriptor over one cache [NB, Hk, bs, D] (row = D * e
@@ -35,10 +37,10 @@ int launch_decode_f32(const DecodeLaunch &a);
 int launch_decode_f16(const DecodeLaunch &a);
 int launch_decode_bf16(const DecodeLaunch &a);
 
-template <typename T, int D, int BS, int G>
+template <typename T, int D, int BS, int G, bool TC>
 int run_decode(const DecodeLaunch &a)
 {
-    using Sh = DecodeShape<T, D, BS, G>;
+    using Sh = DecodeShape<T, D, BS, G, TC>;
     const DecodeParams &p = a.p;
     alignas(64) CUtensorMap tmk;
     alignas(64) CUtensorMap tmv;
@@ -51,7 +53,7 @@ int run_decode(const DecodeLaunch &a)
     if (rc)
         return rc;
     static unsigned long long done = 0;
-    auto kern = pa_decode_kernel<T, D, BS, G>;
+    auto kern = pa_decode_kernel<T, D, BS, G, TC>;
     rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), Sh::smem, &done);
     if (rc)
         return rc;
@@ -61,17 +63,36 @@ int run_decode(const DecodeLaunch &a)
         const long long pairs = (long long)p.num_seqs * p.num_heads;
         pa_reduce_kernel<D><<<(unsigned)((pairs + 3) / 4), 128, 0, a.stream>>>(p);
     }
+    if (a.engine_used)
+        *a.engine_used = TC ? kEngineTensorCore : kEngineCudaCore;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+// Engine choice: tensor cores for 16-bit caches once G >= 4 query heads share
+// a kv head (the contraction is then dense enough that CUDA cores, not HBM,
+// bound the CUDA-core engine); CUDA cores otherwise.  `a.engine` overrides.
+template <typename T, int D, int BS, int G>
+int run_engine(const DecodeLaunch &a)
+{
+    if constexpr (Elem<T>::bytes == 2) {
+        const bool tc = a.engine == kEngineTensorCore || (a.engine == kEngineAuto && G >= 4);
+        if (tc)
+            return run_decode<T, D, BS, G, true>(a);
+    } else {
+        if (a.engine == kEngineTensorCore)
+            return PKV_EUNSUPPORTED;
+    }
+    return run_decode<T, D, BS, G, false>(a);
 }
 
 template <typename T, int D, int BS>
 int dispatch_group(const DecodeLaunch &a)
 {
     switch (a.group) {
-    case 1: return run_decode<T, D, BS, 1>(a);
-    case 2: return run_decode<T, D, BS, 2>(a);
-    case 4: return run_decode<T, D, BS, 4>(a);
-    case 8: return run_decode<T, D, BS, 8>(a);
+    case 1: return run_engine<T, D, BS, 1>(a);
+    case 2: return run_engine<T, D, BS, 2>(a);
+    case 4: return run_engine<T, D, BS, 4>(a);
+    case 8: return run_engine<T, D, BS, 8>(a);
     default: return PKV_EUNSUPPORTED;
     }
 }

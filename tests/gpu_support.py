@@ -14,8 +14,10 @@ from tests.util import raw_np
 TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
 
 
-def gpu_decode(case, partition_size=0, out_dtype=torch.float32, max_context_len=None):
+def gpu_decode(case, partition_size=0, out_dtype=torch.float32, max_context_len=None,
+               engine="auto"):
     import paged_kv_cache_311_gb300 as pkv
+    pkv.set_decode_engine(engine)
     dev = torch.device("cuda")
     q = case["q"].to(dev)
     kc = case["k_cache"].to(dev)
@@ -25,9 +27,15 @@ def gpu_decode(case, partition_size=0, out_dtype=torch.float32, max_context_len=
     out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     mcl = int(max(case["context_lens"])) if max_context_len is None else max_context_len
-    pkv.paged_attention_decode(out, q, kc, vc, bt, cl, case["scale"], max_context_len=mcl,
-                               partition_size=partition_size, device_status=st)
+    try:
+        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, case["scale"], max_context_len=mcl,
+                                   partition_size=partition_size, device_status=st)
+    finally:
+        ran = pkv.last_decode_engine()
+        pkv.set_decode_engine("auto")
     torch.cuda.synchronize()
+    if engine != "auto":
+        assert ran == engine, (ran, engine)
     return out.to(torch.float64).cpu().numpy(), int(st.item()), pkv.last_decode_launches()
 
 

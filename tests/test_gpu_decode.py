@@ -18,18 +18,22 @@ def lens_for(bs):
     return (1, bs - 1, bs, bs + 1, 3 * bs + 5, 100, 511, 512, 513)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+ENGINE_CASES = [(dt, e) for dt in ("f32", "f16", "bf16") for e in ("cuda_core", "tensor_core")
+                if not (dt == "f32" and e == "tensor_core")]
+
+
+@pytest.mark.parametrize("dtype,engine", ENGINE_CASES)
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-def test_decode_matrix(dtype, D, bs, G):
+def test_decode_matrix(dtype, engine, D, bs, G):
     lens = lens_for(bs)
     case = small_case(100 + D + bs + G, dtype=dtype, B=len(lens), H=2 * G, Hk=2, D=D, bs=bs,
                       lens=lens)
     ref, st = oracle_decode(case)
     assert st == 0
     for P in (0, 32, 4096):           # automatic, forced split (tiny partitions), forced single
-        got, gst, launches = gpu_decode(case, partition_size=P)
+        got, gst, launches = gpu_decode(case, partition_size=P, engine=engine)
         assert gst == 0
         assert launches == (2 if P == 32 else 1) or P == 0
         err = max_err(got, ref)
@@ -37,31 +41,35 @@ def test_decode_matrix(dtype, D, bs, G):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_half_output_within_one_ulp(dtype):
+@pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])
+def test_half_output_within_one_ulp(dtype, engine):
     case = small_case(3, dtype=dtype, B=4, H=8, Hk=2, D=128, bs=16, lens=(7, 300, 64, 1000))
     ref, _ = oracle_decode(case)
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
     for P in (0, 64):
-        got, st, _ = gpu_decode(case, partition_size=P, out_dtype=tdt)
+        got, st, _ = gpu_decode(case, partition_size=P, out_dtype=tdt, engine=engine)
         assert st == 0
         rne = torch.from_numpy(ref).to(tdt).to(torch.float64).numpy()
         assert np.all(np.abs(got - rne) <= ulp_bound(ref, tdt))
 
 
-def test_long_context_split_path():
+@pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])
+def test_long_context_split_path(engine):
     lens = (4097, 16384 + 511, 9000)
     case = small_case(9, dtype="bf16", B=3, H=16, Hk=2, D=128, bs=16, lens=lens)
     ref, _ = oracle_decode(case)
     for P in (0, 512, 1024):
-        got, st, launches = gpu_decode(case, partition_size=P)
+        got, st, launches = gpu_decode(case, partition_size=P, engine=engine)
         assert st == 0 and launches == 2
         assert max_err(got, ref) <= TOL["bf16"]
 
 
-def test_empty_and_single_token():
-    case = small_case(4, dtype="f32", B=4, H=4, Hk=4, D=64, bs=16, lens=(0, 1, 1, 0))
+@pytest.mark.parametrize("dtype,engine", [("f32", "cuda_core"), ("bf16", "cuda_core"),
+                                          ("bf16", "tensor_core"), ("f16", "tensor_core")])
+def test_empty_and_single_token(dtype, engine):
+    case = small_case(4, dtype=dtype, B=4, H=8, Hk=2, D=64, bs=16, lens=(0, 1, 1, 0))
     for P in (0, 32):
-        got, st, _ = gpu_decode(case, partition_size=P)
+        got, st, _ = gpu_decode(case, partition_size=P, engine=engine)
         assert st == 0
         assert not got[0].any() and not got[3].any()
         for s in (1, 2):
@@ -69,9 +77,10 @@ def test_empty_and_single_token():
             np.testing.assert_array_equal(got[s], V[0])   # exactly v_0
 
 
-def test_permutation_is_bit_exact():
+@pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])
+def test_permutation_is_bit_exact(engine):
     case = small_case(5, dtype="bf16", B=3, H=8, Hk=1, D=128, bs=16, lens=(70, 513, 1200))
-    base, _, _ = gpu_decode(case, partition_size=512)
+    base, _, _ = gpu_decode(case, partition_size=512, engine=engine)
     NB = case["k_cache"].shape[0]
     perm = torch.randperm(NB, generator=torch.Generator().manual_seed(1))
     moved = dict(case)
@@ -79,12 +88,13 @@ def test_permutation_is_bit_exact():
     moved["v_cache"] = torch.empty_like(case["v_cache"]); moved["v_cache"][perm] = case["v_cache"]
     t = case["block_tables"]
     moved["block_tables"] = np.where(t >= 0, perm.numpy()[np.maximum(t, 0)], -1).astype(np.int32)
-    got, st, _ = gpu_decode(moved, partition_size=512)
+    got, st, _ = gpu_decode(moved, partition_size=512, engine=engine)
     assert st == 0
     np.testing.assert_array_equal(got, base)
 
 
-def test_prefix_aliasing_is_bit_exact():
+@pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])
+def test_prefix_aliasing_is_bit_exact(engine):
     g = torch.Generator().manual_seed(6)
     bs, Hk, H, D = 16, 2, 8, 128
     kc = torch.randn(16, Hk, bs, D, generator=g).to(torch.bfloat16)
@@ -95,22 +105,23 @@ def test_prefix_aliasing_is_bit_exact():
                 context_lens=np.array([4 * bs + 3, 4 * bs + 3], np.int32))
     dup = dict(base, block_tables=np.array([[0, 1, 2, 3, 8], [4, 5, 6, 7, 8]], np.int32))
     ali = dict(base, block_tables=np.array([[0, 1, 2, 3, 8], [0, 1, 2, 3, 8]], np.int32))
-    a, _, _ = gpu_decode(dup)
-    b, _, _ = gpu_decode(ali)
+    a, _, _ = gpu_decode(dup, engine=engine)
+    b, _, _ = gpu_decode(ali, engine=engine)
     np.testing.assert_array_equal(a, b)
     np.testing.assert_array_equal(a[0], a[1])
 
 
-def test_bad_block_and_length_are_reported():
+@pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])
+def test_bad_block_and_length_are_reported(engine):
     import paged_kv_cache_311_gb300 as pkv
     case = small_case(7, dtype="f16", B=3, H=4, Hk=2, D=128, bs=16, lens=(40, 40, 40))
-    good, _, _ = gpu_decode(case)
+    good, _, _ = gpu_decode(case, engine=engine)
     bad = dict(case)
     t = case["block_tables"].copy()
     t[1, 2] = case["k_cache"].shape[0] + 5
     bad["block_tables"] = t
     for P in (0, 32):
-        got, st, _ = gpu_decode(bad, partition_size=P)
+        got, st, _ = gpu_decode(bad, partition_size=P, engine=engine)
         assert st & pkv.DEV_BAD_BLOCK
         assert not got[1].any()
         np.testing.assert_array_equal(got[0], good[0])
@@ -118,7 +129,7 @@ def test_bad_block_and_length_are_reported():
     lens[2] = 41                                # beyond max_context_len passed below
     bl = dict(case, context_lens=lens)
     for P in (0, 32):
-        got, st, _ = gpu_decode(bl, partition_size=P, max_context_len=40)
+        got, st, _ = gpu_decode(bl, partition_size=P, max_context_len=40, engine=engine)
         assert st & pkv.DEV_BAD_CONTEXT_LEN
         assert not got[2].any()
         np.testing.assert_array_equal(got[0], good[0])
