@@ -74,7 +74,8 @@ def test_empty_and_single_token(dtype, engine):
         assert not got[0].any() and not got[3].any()
         for s in (1, 2):
             _, V = logical_kv(case, s)
-            np.testing.assert_array_equal(got[s], V[0])   # exactly v_0
+            # exactly v_0 of each query head's kv head (head h reads kv head h // 4)
+            np.testing.assert_array_equal(got[s], np.repeat(V[0], 4, axis=0))
 
 
 @pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])
