@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--config", default="llama7b_f16")
     ap.add_argument("--block-size", type=int, default=0)
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling cases)")
+    ap.add_argument("--pool-gb", type=float, default=0.0,
+                    help="cap the pool of byte-sized presets (profiling cases)")
     ap.add_argument("--partition-size", type=int, default=-1, help="-1: the preset's choice")
     ap.add_argument("--engine", default="auto", choices=["auto", "cuda_core", "tensor_core"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -162,7 +164,7 @@ def run_native(args):
     total = args.warmup + args.steps
     w = PagedDecodeWorkload(cfg, seed, total_steps=max(total, cfg.steps),
                             contiguous=args.identity_tables, num_seqs=args.num_seqs or None,
-                            pool_blocks=_pool_blocks(cfg, dev))
+                            pool_blocks=_pool_blocks(cfg, dev, args.pool_gb))
     P = cfg.partition_size if args.partition_size < 0 else args.partition_size
     out_dtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[cfg.dtype]
     state = DeviceState(cfg, w, seed, device=dev, out_dtype=out_dtype)
@@ -297,13 +299,16 @@ def _preroll():
         sleep(600_000)
 
 
-def _pool_blocks(cfg, dev):
+def _pool_blocks(cfg, dev, cap_gb=0.0):
     """Pools given in bytes (the long-context preset, ~60 GB) shrink to 80% of
-    the free device memory when the GPU has less room."""
+    the free device memory when the GPU has less room, or to cap_gb."""
     if cfg.pool != "bytes":
         return None
     free = torch.cuda.mem_get_info(dev)[0]
-    return int(min(cfg.pool_value, 0.8 * free) // (2 * cfg.block_bytes))
+    want = min(cfg.pool_value, 0.8 * free)
+    if cap_gb > 0:
+        want = min(want, cap_gb * 1e9)
+    return int(want // (2 * cfg.block_bytes))
 
 
 def _split_partition(P, max_len, launches):
