@@ -179,7 +179,7 @@ def run_native(args):
     pkv.set_decode_engine(args.engine)
     for s in steps:
         state.ensure_workspace(s.max_context_len, P)
-    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     out_bytes = torch.tensor([], dtype=out_dtype).element_size()
 
@@ -287,7 +287,7 @@ def _flush_l2(buf):
     """Evicts the decode step's data from L2 by reading a 256 MiB buffer (twice
     the L2).  A read leaves clean lines behind, so the timed kernels do not pay
     for writing flush data back to DRAM."""
-    torch.sum(buf, dtype=torch.int64)
+    torch.sum(buf)
 
 
 def _preroll():

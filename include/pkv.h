@@ -187,8 +187,8 @@ size_t pkv_static_workspace_capacity(void);
 
 /*
  * Engine of the decode kernel, process-wide (tests and benchmarks compare the
- * two): 0 = automatic (tensor cores for 16-bit caches when num_heads /
- * num_kv_heads >= 4, CUDA cores otherwise), 1 = CUDA cores, 2 = tensor cores
+ * two): 0 = automatic (tensor cores for 16-bit caches, CUDA cores for fp32
+ * caches), 1 = CUDA cores, 2 = tensor cores
  * (16-bit caches only; fp32 caches then return PKV_EUNSUPPORTED).
  * Returns PKV_EINVAL for other values.
  */

@@ -60,6 +60,11 @@ struct DecodeParams {
     int out_dtype;
     int split;           // nonzero: write partials to the workspace
     float qscale;        // softmax scale * log2(e)
+    // persistent split path with shared prefixes (null / 0 otherwise)
+    const int4 *items;         // explicit work items, two int4 each
+    const int *num_items;      // device count of `items`
+    const int32_t *seq_shared; // tokens each sequence shares with its run
+    int np_prefix;             // workspace slots reserved for shared-prefix partials
 };
 
 enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2 };
@@ -430,6 +435,62 @@ struct TcEngine {
                 ldsm_x4_trans(C::addr(vbase, t, 2 * mt + dq), a);
                 Mma<T>::run(o[mt], a, bh0, bh1);
                 Mma<T>::run(o[mt], a, bl0, bl1);
+            }
+        }
+    }
+
+    // Persistent split path: resets the state for a new work item whose query
+    // rows are r = 8 rb + g < nrows, row r being head (kvh G + r % G) of
+    // sequence seq0 + r / G (sequences that share the item's tokens).
+    __device__ void begin_item(const DecodeParams &p, int seq0, int nrows, int kvh, int rb, int lane)
+    {
+        g = lane >> 2;
+        c = lane & 3;
+        qscale = p.qscale;
+        const int r = 8 * rb + g;
+        const bool live = r < nrows;
+        const int64_t qrow = (int64_t)(seq0 + (live ? r / G : 0)) * p.num_heads + kvh * G + (live ? r % G : 0);
+        const uint32_t *qp = reinterpret_cast<const uint32_t *>(static_cast<const T *>(p.q) + qrow * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qf[ks][0] = live ? qp[(16 * ks + 2 * c) / 2] : 0u;
+            qf[ks][1] = live ? qp[(16 * ks + 2 * c + 8) / 2] : 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                o[ks][j] = 0.f;
+        }
+        m[0] = m[1] = -INFINITY;
+        lsum[0] = lsum[1] = 0.f;
+    }
+
+    // Persistent split path: writes this item's partial (max, sum,
+    // unnormalised acc) of every live row to workspace slot `slot` of its
+    // (sequence, head); `invalid` writes the (-inf, -1) marker instead.
+    __device__ void write_partial(const DecodeParams &p, int seq0, int nrows, int kvh, int rb,
+                                  int slot, bool invalid)
+    {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 4);
+            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 8);
+            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int r = 8 * rb + 2 * c + j;
+            if (r < nrows) {
+                const int64_t sh = (int64_t)(seq0 + r / G) * p.num_heads + kvh * G + r % G;
+                const int64_t base = sh * p.num_partitions + slot;
+                if (g == 0) {
+                    p.ws_ml[base * 2 + 0] = invalid ? -INFINITY : m[j];
+                    p.ws_ml[base * 2 + 1] = invalid ? -1.f : lsum[j];
+                }
+                float *acc = p.ws_acc + base * D;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    acc[16 * mt + g] = invalid ? 0.f : o[mt][j];
+                    acc[16 * mt + g + 8] = invalid ? 0.f : o[mt][2 + j];
+                }
             }
         }
     }

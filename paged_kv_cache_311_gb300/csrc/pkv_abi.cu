@@ -105,6 +105,23 @@ int encode_kv_map(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ECUDA;
 }
 
+int grid_for_occupancy(const void *func, int threads, int smem, int *cache_per_dev)
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return -1;
+    if (dev < 64 && cache_per_dev[dev] > 0)
+        return cache_per_dev[dev];
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, smem) != cudaSuccess ||
+        per_sm <= 0)
+        return -1;
+    const int blocks = per_sm * sm_count(dev);
+    if (dev < 64)
+        cache_per_dev[dev] = blocks;
+    return blocks;
+}
+
 int ensure_smem_attr(const void *func, int bytes, unsigned long long *done_mask)
 {
     const int dev = current_device();
@@ -248,6 +265,10 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     p.out_dtype = out_dtype;
     p.split = np > 1;
     p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax via exp2
+    p.items = nullptr;
+    p.num_items = nullptr;
+    p.seq_shared = nullptr;
+    p.np_prefix = 0;
     if (p.split) {
         const SplitLayout s = split_layout(num_seqs, num_heads, np, head_dim);
         if (!workspace || workspace_bytes < s.total || !aligned16(workspace))

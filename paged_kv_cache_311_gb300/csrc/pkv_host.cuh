@@ -5,7 +5,7 @@
 
 #include <cuda_runtime.h>
 
-#include "pa_decode.cuh"
+#include "pa_split.cuh"
 
 namespace pkv {
 
@@ -68,14 +68,58 @@ int run_decode(const DecodeLaunch &a)
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
-// Engine choice: tensor cores for 16-bit caches once G >= 4 query heads share
-// a kv head (the contraction is then dense enough that CUDA cores, not HBM,
-// bound the CUDA-core engine); CUDA cores otherwise.  `a.engine` overrides.
+// Persistent split path (tensor-core engine): one worker per warp over the
+// (sequence, kv head, partition) items, then the log-sum-exp merge.
+int grid_for_occupancy(const void *func, int threads, int smem, int *cache_per_dev);
+
+template <typename T, int D, int BS, int G, bool EXPLICIT>
+int run_split(const DecodeLaunch &a, long long max_items)
+{
+    using SC = SplitCfg<T, D, BS, G>;
+    const DecodeParams &p = a.p;
+    alignas(64) CUtensorMap tmk;
+    alignas(64) CUtensorMap tmv;
+    int rc = encode_kv_map(&tmk, a.k_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
+                           p.num_blocks, SC::C::BOX_ROWS);
+    if (rc)
+        return rc;
+    rc = encode_kv_map(&tmv, a.v_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
+                       p.num_blocks, SC::C::BOX_ROWS);
+    if (rc)
+        return rc;
+    static unsigned long long done = 0;
+    static int occ[64] = {};
+    auto kern = pa_split_kernel<T, D, BS, G, EXPLICIT>;
+    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), SC::SMEM_BYTES, &done);
+    if (rc)
+        return rc;
+    int blocks = grid_for_occupancy(reinterpret_cast<const void *>(kern), SC::NW * 32,
+                                    SC::SMEM_BYTES, occ);
+    if (blocks <= 0)
+        return PKV_ECUDA;
+    const long long need = (max_items + SC::NW - 1) / SC::NW;
+    if (need < blocks)
+        blocks = (int)(need > 0 ? need : 1);
+    kern<<<blocks, SC::NW * 32, SC::SMEM_BYTES, a.stream>>>(p, tmk, tmv);
+    pa_merge_kernel<D><<<(unsigned)((long long)p.num_seqs * p.num_heads), 128, 0, a.stream>>>(p);
+    if (a.engine_used)
+        *a.engine_used = kEngineTensorCore;
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+// Engine choice: tensor cores for every 16-bit cache (measured faster than the
+// CUDA-core engine at every G, and the only one that keeps up with HBM once
+// G >= 4 query heads share a kv head); CUDA cores for fp32 caches.
+// `a.engine` overrides.
 template <typename T, int D, int BS, int G>
 int run_engine(const DecodeLaunch &a)
 {
     if constexpr (Elem<T>::bytes == 2) {
-        const bool tc = a.engine == kEngineTensorCore || (a.engine == kEngineAuto && G >= 4);
+        const bool tc = a.engine != kEngineCudaCore;
+        if (tc && a.p.split &&
+            (a.p.partition_size + BS - 1) / BS <= SplitCfg<T, D, BS, G>::TABLE_W)
+            return run_split<T, D, BS, G, false>(
+                a, (long long)a.p.num_seqs * a.p.num_kv_heads * a.p.num_partitions);
         if (tc)
             return run_decode<T, D, BS, G, true>(a);
     } else {
