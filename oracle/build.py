@@ -18,10 +18,11 @@ def library_path() -> str:
 def build_oracle(extra_flags=(), out_path: str | None = None) -> str:
     out = out_path or library_path()
     os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = f"{out}.{os.getpid()}.tmp"   # parallel test workers may build at once
     cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra",
-           "-D_POSIX_C_SOURCE=200809L", *extra_flags, SRC, "-o", out + ".tmp", "-lm", "-lpthread"]
+           "-D_POSIX_C_SOURCE=200809L", *extra_flags, SRC, "-o", tmp, "-lm", "-lpthread"]
     subprocess.run(cmd, check=True)
-    os.replace(out + ".tmp", out)
+    os.replace(tmp, out)
     return out
 
 

@@ -53,7 +53,7 @@ def build(extra_flags=(), out_path: str | None = None, verbose_ptxas: bool = Fal
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = out + ".tmp"
+    tmp = f"{out}.{os.getpid()}.tmp"
     subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], check=True)
     os.replace(tmp, out)
     return out
