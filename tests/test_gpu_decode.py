@@ -116,7 +116,8 @@ def test_prefix_aliasing_is_bit_exact(engine):
 def test_bad_block_and_length_are_reported(engine):
     import paged_kv_cache_311_gb300 as pkv
     case = small_case(7, dtype="f16", B=3, H=4, Hk=2, D=128, bs=16, lens=(40, 40, 40))
-    good, _, _ = gpu_decode(case, engine=engine)
+    # the unaffected sequence must match the clean run on the same path bit for bit
+    good = {P: gpu_decode(case, partition_size=P, engine=engine)[0] for P in (0, 32)}
     bad = dict(case)
     t = case["block_tables"].copy()
     t[1, 2] = case["k_cache"].shape[0] + 5
@@ -125,7 +126,7 @@ def test_bad_block_and_length_are_reported(engine):
         got, st, _ = gpu_decode(bad, partition_size=P, engine=engine)
         assert st & pkv.DEV_BAD_BLOCK
         assert not got[1].any()
-        np.testing.assert_array_equal(got[0], good[0])
+        np.testing.assert_array_equal(got[0], good[P][0])
     lens = case["context_lens"].copy()
     lens[2] = 41                                # beyond max_context_len passed below
     bl = dict(case, context_lens=lens)
@@ -133,7 +134,7 @@ def test_bad_block_and_length_are_reported(engine):
         got, st, _ = gpu_decode(bl, partition_size=P, max_context_len=40, engine=engine)
         assert st & pkv.DEV_BAD_CONTEXT_LEN
         assert not got[2].any()
-        np.testing.assert_array_equal(got[0], good[0])
+        np.testing.assert_array_equal(got[0], good[P][0])
 
 
 def test_host_validation_rejects_bad_arguments():
