@@ -241,6 +241,8 @@ __global__ void __launch_bounds__(128) pa_merge_kernel(const __grid_constant__ D
     const int seq = (int)(sh / p.num_heads);
     const int L = p.context_lens[seq];
     const bool bad_len = L < 0 || L > p.max_context_len;
+    if (bad_len && threadIdx.x == 0 && sh % p.num_heads == 0)
+        report(p.status, PKV_DEV_BAD_CONTEXT_LEN);  // the item pass skipped it silently
     const int S = (!bad_len && p.seq_shared) ? p.seq_shared[seq] : 0;
     const int P = p.partition_size;
     const int na = S > 0 ? (S + P - 1) / P : 0;
