@@ -55,6 +55,8 @@ def parse_args():
                     help="cap the pool of byte-sized presets (profiling cases)")
     ap.add_argument("--partition-size", type=int, default=-1, help="-1: the preset's choice")
     ap.add_argument("--engine", default="auto", choices=["auto", "cuda_core", "tensor_core"])
+    ap.add_argument("--no-shared", action="store_true",
+                    help="shared-prefix workload: use the per-sequence entry point")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -177,15 +179,19 @@ def run_native(args):
     steps = [state.to_device(inp) for inp in host_inputs]
     import paged_kv_cache_311_gb300 as pkv
     pkv.set_decode_engine(args.engine)
+    shared = cfg.kind == "shared_prefix" and not args.no_shared
+    if shared and args.partition_size < 0:
+        P = 0   # the shared-prefix entry point's own default partition
+    decode_fn = pkv.paged_attention_decode_shared if shared else pkv.paged_attention_decode
     for s in steps:
-        state.ensure_workspace(s.max_context_len, P)
+        state.ensure_workspace(s.max_context_len, P, shared)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     out_bytes = torch.tensor([], dtype=out_dtype).element_size()
 
     # warm-up
     for s in steps[:args.warmup]:
-        state.run_step(s, partition_size=P)
+        state.run_step(s, partition_size=P, shared=shared)
     torch.cuda.synchronize()
     state.status.zero_()
 
@@ -211,10 +217,9 @@ def run_native(args):
                               device_status=state.status)
         launches += 1
         e1.record(stream)
-        pkv.paged_attention_decode(state.out, s.q, state.k_cache, state.v_cache, s.block_tables,
-                                   s.context_lens, cfg.softmax_scale,
-                                   max_context_len=s.max_context_len, partition_size=P,
-                                   workspace=state.workspace, device_status=state.status)
+        decode_fn(state.out, s.q, state.k_cache, state.v_cache, s.block_tables, s.context_lens,
+                  cfg.softmax_scale, max_context_len=s.max_context_len, partition_size=P,
+                  workspace=state.workspace, device_status=state.status)
         n = pkv.last_decode_launches()
         decode_launches.append(n)
         engine_used = pkv.last_decode_engine()
@@ -233,8 +238,12 @@ def run_native(args):
     tot_ms = sum(step_ms)
     bytes_step, bytes_dec, seqs = 0, 0, 0
     for s, n in zip(steps[args.warmup:], decode_launches):
-        Pp = _split_partition(P, s.max_context_len, n)
-        ab = algorithmic_bytes(cfg, s.host, w.num_seqs, split_partition=Pp, out_bytes=out_bytes)
+        if shared:
+            ab = algorithmic_bytes(cfg, s.host, w.num_seqs, out_bytes=out_bytes,
+                                   shared_partition=P or 256)
+        else:
+            Pp = _split_partition(P, s.max_context_len, n)
+            ab = algorithmic_bytes(cfg, s.host, w.num_seqs, split_partition=Pp, out_bytes=out_bytes)
         bytes_step += ab["total"]
         bytes_dec += ab["attention"]
         seqs += w.num_seqs
@@ -248,7 +257,8 @@ def run_native(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(state, steps[args.warmup:], host_inputs[args.warmup:], P, flush, bytes_step)
+        e2e = run_e2e(state, steps[args.warmup:], host_inputs[args.warmup:], P, flush, bytes_step,
+                      decode_fn)
 
     if rank == 0:
         line = {
@@ -267,7 +277,9 @@ def run_native(args):
                        "block_placement": "contiguous" if args.identity_tables else "random"},
             "seq_steps_per_s": round(seqs_all / t_max, 1),
             "pct_of_peak": round(100 * value / peak, 2),
-            "roofline": {"bound": "hbm", "kernel": "pa_decode_kernel" + ("+pa_reduce_kernel" if decode_launches[0] == 2 else ""),
+            "roofline": {"bound": "hbm",
+                         "kernel": ("pa_plan_kernel+pa_shared_kernel+pa_merge_kernel" if shared else
+                                    "pa_decode_kernel" + ("+pa_merge_kernel" if decode_launches[0] == 2 else "")),
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                          "traffic": traffic_for(cfg, bytes_dec / len(dec_ms)),
@@ -337,7 +349,7 @@ def traffic_for(cfg, algo_bytes):
     return int(e["traffic_per_algorithmic_byte"] * algo_bytes)
 
 
-def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
+def run_e2e(state, steps, host_inputs, P, flush, bytes_step, decode_fn):
     """Same step, inputs from pinned host memory, output read back, all timed."""
     import paged_kv_cache_311_gb300 as pkv
     cfg = state.cfg
@@ -377,10 +389,9 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
             cp.copy_(hp["cow_pairs"], non_blocking=True)
             pkv.copy_blocks([state.k_cache], [state.v_cache], cp, device_status=state.status)
         pkv.reshape_and_cache(key, val, state.k_cache, state.v_cache, sm, device_status=state.status)
-        pkv.paged_attention_decode(state.out, q, state.k_cache, state.v_cache, bt, cl,
-                                   cfg.softmax_scale, max_context_len=s.max_context_len,
-                                   partition_size=P, workspace=state.workspace,
-                                   device_status=state.status)
+        decode_fn(state.out, q, state.k_cache, state.v_cache, bt, cl, cfg.softmax_scale,
+                  max_context_len=s.max_context_len, partition_size=P,
+                  workspace=state.workspace, device_status=state.status)
         out_host.copy_(state.out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()

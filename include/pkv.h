@@ -114,6 +114,36 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
                                uint32_t *device_status, void *stream);
 
 /*
+ * paged_attention_decode_shared -- the same attention as
+ * pkv_paged_attention_decode, for batches in which runs of consecutive
+ * sequences share leading physical blocks (parallel sampling, beam search, a
+ * common system prompt: "Advanced Features", KV-Cache Sharing and Prefix
+ * Caching).  A planning kernel finds the runs by comparing block ids; the
+ * shared blocks of a group of up to 24 / (num_heads / num_kv_heads)
+ * sequences are then read once and feed every member's query heads, and each
+ * member's own tail is read separately.  Results equal the per-sequence path
+ * up to fp32 rounding order.
+ *
+ * Arguments as for pkv_paged_attention_decode, except: partition_size 0 means
+ * 256 tokens (a multiple of 32 and of block_size otherwise); the split path
+ * always runs, with pkv_paged_attention_shared_workspace_bytes(...) bytes of
+ * workspace; kv_dtype must be PKV_F16 or PKV_BF16 (fp32 caches:
+ * PKV_EUNSUPPORTED).  Enqueues three kernels (plan, attention, merge).
+ */
+int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, const void *k_cache,
+                                      const void *v_cache, int kv_dtype,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *context_lens, int num_seqs, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int64_t num_blocks, int max_context_len, float scale,
+                                      int partition_size, void *workspace, size_t workspace_bytes,
+                                      uint32_t *device_status, void *stream);
+
+/* Workspace bytes pkv_paged_attention_decode_shared needs for these sizes. */
+size_t pkv_paged_attention_shared_workspace_bytes(int num_seqs, int num_heads, int max_context_len,
+                                                  int head_dim, int partition_size);
+
+/*
  * reshape_and_cache -- write each new token's key/value rows into its slot
  * ("The PagedAttention Algorithm", Step 2: generated tokens fill the block).
  *

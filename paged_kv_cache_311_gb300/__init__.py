@@ -26,6 +26,7 @@ from .build import library_path
 __all__ = [
     "PkvError", "load_library", "paged_attention_decode", "reshape_and_cache", "copy_blocks",
     "paged_attention_workspace_bytes", "status_string", "last_decode_launches",
+    "paged_attention_decode_shared", "paged_attention_shared_workspace_bytes",
     "set_decode_engine", "last_decode_engine",
     "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "HEADER_PATH",
 ]
@@ -63,6 +64,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_paged_attention_decode.argtypes = [vp, i32, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
                                              i32, i32, i64, i32, f32, i32, vp, u64, vp, vp]
     L.pkv_paged_attention_decode.restype = i32
+    L.pkv_paged_attention_decode_shared.argtypes = list(L.pkv_paged_attention_decode.argtypes)
+    L.pkv_paged_attention_decode_shared.restype = i32
+    L.pkv_paged_attention_shared_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.pkv_paged_attention_shared_workspace_bytes.restype = u64
     L.pkv_reshape_and_cache.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, vp, vp]
     L.pkv_reshape_and_cache.restype = i32
     L.pkv_copy_blocks.argtypes = [vp, vp, i32, vp, i32, u64, i64, vp, vp]
@@ -177,6 +182,44 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(device_status), _stream(stream))
     _check(rc, "pkv_paged_attention_decode")
+    return out
+
+
+def paged_attention_shared_workspace_bytes(num_seqs: int, num_heads: int, max_context_len: int,
+                                           head_dim: int, partition_size: int = 0) -> int:
+    return int(load_library().pkv_paged_attention_shared_workspace_bytes(
+        num_seqs, num_heads, max_context_len, head_dim, partition_size))
+
+
+def paged_attention_decode_shared(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                  v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                  context_lens: torch.Tensor, scale: float, *,
+                                  max_context_len: Optional[int] = None, partition_size: int = 0,
+                                  workspace: Optional[torch.Tensor] = None,
+                                  device_status: Optional[torch.Tensor] = None,
+                                  stream=None) -> torch.Tensor:
+    """As paged_attention_decode, reading blocks that runs of consecutive
+    sequences share (same leading block ids) once for the whole run."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, workspace, device_status)
+    B, H, D = q.shape
+    NB, Hk, bs, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, H, D):
+        raise ValueError("shape mismatch")
+    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise ValueError("q, k_cache and v_cache must share a dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0
+    if workspace is None:
+        nbytes = paged_attention_shared_workspace_bytes(B, H, max_context_len, D, partition_size)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    rc = load_library().pkv_paged_attention_decode_shared(
+        _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[k_cache.dtype],
+        _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), B, H, Hk, D, bs, NB,
+        int(max_context_len), float(scale), int(partition_size), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(device_status), _stream(stream))
+    _check(rc, "pkv_paged_attention_decode_shared")
     return out
 
 

@@ -60,11 +60,10 @@ struct DecodeParams {
     int out_dtype;
     int split;           // nonzero: write partials to the workspace
     float qscale;        // softmax scale * log2(e)
-    // persistent split path with shared prefixes (null / 0 otherwise)
-    const int4 *items;         // explicit work items, two int4 each
-    const int *num_items;      // device count of `items`
-    const int32_t *seq_shared; // tokens each sequence shares with its run
-    int np_prefix;             // workspace slots reserved for shared-prefix partials
+    // shared-prefix path (null / 0 otherwise)
+    const int32_t *seq_shared;  // tokens each sequence shares with its group
+    const int32_t *seq_members; // group size for group leaders, else 0
+    int np_prefix;              // workspace slots reserved for shared-prefix partials
 };
 
 enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2 };
@@ -144,23 +143,36 @@ __device__ __forceinline__ void store_out(void *out, int dtype, int64_t i, float
         static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
 }
 
+// What one CTA computes: query rows r < nrows, row r being head
+// (kvh * G + r % G) of sequence seq0 + r / G, over the tokens [tok0, tok_end)
+// that the block table of `table_seq` addresses; split partials go to
+// workspace slot `slot`.
+struct CtaWork {
+    int seq0, nrows, kvh, tok0, tok_end, slot, table_seq;
+};
+
+__device__ __forceinline__ int64_t row_head(const DecodeParams &p, const CtaWork &w, int G, int r)
+{
+    return (int64_t)(w.seq0 + r / G) * p.num_heads + w.kvh * G + r % G;
+}
+
 // Writes the result of a CTA that cannot produce one (bad length / block):
 // zeros for the single pass, an "invalid" (max = -inf, sum = -1) marker for
 // the split path.
 template <int D, int G>
-__device__ void write_invalid(const DecodeParams &p, int seq, int kvh, int part)
+__device__ void write_invalid(const DecodeParams &p, const CtaWork &w)
 {
-    const int nthr = blockDim.x;
-    for (int idx = threadIdx.x; idx < G * D; idx += nthr) {
-        const int h = kvh * G + idx / D, d = idx % D;
-        const int64_t sh = (int64_t)seq * p.num_heads + h;
+    for (int idx = threadIdx.x; idx < w.nrows * D; idx += blockDim.x) {
+        const int r = idx / D, d = idx % D;
+        const int64_t sh = row_head(p, w, G, r);
         if (!p.split) {
             store_out(p.out, p.out_dtype, sh * D + d, 0.f);
         } else {
-            p.ws_acc[(sh * p.num_partitions + part) * D + d] = 0.f;
+            const int64_t slot = sh * p.num_partitions + w.slot;
+            p.ws_acc[slot * D + d] = 0.f;
             if (d == 0) {
-                p.ws_ml[(sh * p.num_partitions + part) * 2 + 0] = -INFINITY;
-                p.ws_ml[(sh * p.num_partitions + part) * 2 + 1] = -1.f;
+                p.ws_ml[slot * 2 + 0] = -INFINITY;
+                p.ws_ml[slot * 2 + 1] = -1.f;
             }
         }
     }
@@ -191,7 +203,7 @@ struct CcEngine {
         }
     }
 
-    __device__ void init(const DecodeParams &, uint8_t *smem, int, int, int warp, int lane)
+    __device__ void init(const DecodeParams &, uint8_t *smem, const CtaWork &, int warp, int lane)
     {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -307,8 +319,9 @@ struct CcEngine {
         }
     }
 
-    // Per-warp (max, sum, acc) of every head into the merge scratch.
-    __device__ void finish(float *mw, float *lw, float *aw, int warp, int lane)
+    // Per-warp (max, sum, acc) of every head into the merge scratch (rows
+    // are the G heads, row stride G).
+    __device__ void finish(float *mw, float *lw, float *aw, int warp, int lane, int)
     {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -333,42 +346,53 @@ struct CcEngine {
 };
 
 // ---------------------------------------------------------- tensor cores
-template <typename T, int D, int BS, int G>
+// NT n-tiles of 8 query rows each (NT = 1 for one sequence's G <= 8 heads).
+template <typename T, int D, int BS, int G, int NT = 1>
 struct TcEngine {
     using C = DecodeCfg<T, D, BS, G, true>;
     static constexpr int KS = D / 16;   // k-steps of QK = m-tiles of PV
+    static constexpr int RS = 8 * NT;   // row stride of the merge scratch
 
-    uint32_t qf[KS][2];   // q^T B-fragments: rows g (< G), dims 16 ks + 2c (+8)
-    float o[KS][4];       // O^T C-fragments: dims 16 mt + g (+8), rows 2c, 2c+1
-    float m[2], lsum[2];  // rows 2c, 2c+1
+    uint32_t qf[KS][NT][2];   // q^T B-fragments: row 8 nt + g, dims 16 ks + 2c (+8)
+    float o[KS][NT][4];       // O^T C-fragments: dims 16 mt + g (+8), rows 8 nt + 2c, +1
+    float m[NT][2], lsum[NT][2];
     float qscale;
-    int g, c;
+    int g, c, ntl;            // ntl: n-tiles that hold live rows
 
     __device__ static void stage_q(const DecodeParams &, uint8_t *, int, int) {}
 
-    __device__ void init(const DecodeParams &p, uint8_t *, int seq, int kvh, int, int lane)
+    __device__ void init(const DecodeParams &p, uint8_t *, const CtaWork &w, int, int lane)
     {
         g = lane >> 2;
         c = lane & 3;
         qscale = p.qscale;
-        const uint32_t *qp = reinterpret_cast<const uint32_t *>(
-            static_cast<const T *>(p.q) + ((int64_t)seq * p.num_heads + kvh * G + g) * D);
+        ntl = (w.nrows + 7) / 8;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qf[ks][0] = g < G ? qp[(16 * ks + 2 * c) / 2] : 0u;
-            qf[ks][1] = g < G ? qp[(16 * ks + 2 * c + 8) / 2] : 0u;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int r = 8 * nt + g;
+            const bool live = r < w.nrows;
+            const uint32_t *qp = reinterpret_cast<const uint32_t *>(
+                static_cast<const T *>(p.q) + row_head(p, w, G, live ? r : 0) * D);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                o[ks][j] = 0.f;
+            for (int ks = 0; ks < KS; ++ks) {
+                qf[ks][nt][0] = live ? qp[(16 * ks + 2 * c) / 2] : 0u;
+                qf[ks][nt][1] = live ? qp[(16 * ks + 2 * c + 8) / 2] : 0u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    o[ks][nt][j] = 0.f;
+            }
+            m[nt][0] = m[nt][1] = -INFINITY;
+            lsum[nt][0] = lsum[nt][1] = 0.f;
         }
-        m[0] = m[1] = -INFINITY;
-        lsum[0] = lsum[1] = 0.f;
     }
 
     __device__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, int lane)
     {
-        // ---- S^T (16 tokens x 8 query rows) = K q^T
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- S^T (16 tokens x 8 query rows per n-tile) = K q^T
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
         {
             const int t = (lane & 7) + ((lane >> 3) & 1) * 8;
             const int dq = lane >> 4;
@@ -376,31 +400,37 @@ struct TcEngine {
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a[4];
                 ldsm_x4(C::addr(kbase, t, 2 * ks + dq), a);
-                Mma<T>::run(s, a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    if (nt < ntl)
+                        Mma<T>::run(s[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
             }
         }
 
         // ---- online softmax: this lane holds tokens g, g + 8 of rows 2c, 2c+1
         const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
-        float p0[2], p1[2];
+        float p0[NT][2], p1[NT][2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float x0 = ok0 ? s[j] * qscale : -INFINITY;
-            const float x1 = ok1 ? s[2 + j] * qscale : -INFINITY;
-            float tm = fmaxf(x0, x1);
-            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
-            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
-            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
-            const float mn = fmaxf(m[j], tm);
-            const float alpha = exp2f(m[j] - mn);
-            p0[j] = exp2f(x0 - mn);
-            p1[j] = exp2f(x1 - mn);
-            lsum[j] = lsum[j] * alpha + p0[j] + p1[j];
-            m[j] = mn;
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                o[mt][j] *= alpha;
-                o[mt][2 + j] *= alpha;
+            for (int j = 0; j < 2; ++j) {
+                const float x0 = ok0 ? s[nt][j] * qscale : -INFINITY;
+                const float x1 = ok1 ? s[nt][2 + j] * qscale : -INFINITY;
+                float tm = fmaxf(x0, x1);
+                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+                const float mn = fmaxf(m[nt][j], tm);
+                const float alpha = exp2f(m[nt][j] - mn);
+                p0[nt][j] = exp2f(x0 - mn);
+                p1[nt][j] = exp2f(x1 - mn);
+                lsum[nt][j] = lsum[nt][j] * alpha + p0[nt][j] + p1[nt][j];
+                m[nt][j] = mn;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    o[mt][nt][j] *= alpha;
+                    o[mt][nt][2 + j] *= alpha;
+                }
             }
         }
 
@@ -417,15 +447,21 @@ struct TcEngine {
         }
 
         // ---- P^T B-fragments: P = hi + lo in the cache's 16-bit type
-        const uint32_t h0 = Mma<T>::pack(p0[0], p0[1]);  // tokens g,   rows 2c, 2c+1
-        const uint32_t h1 = Mma<T>::pack(p1[0], p1[1]);  // tokens g+8, rows 2c, 2c+1
-        const float2 f0 = Mma<T>::unpack(h0), f1 = Mma<T>::unpack(h1);
-        const uint32_t l0 = Mma<T>::pack(p0[0] - f0.x, p0[1] - f0.y);
-        const uint32_t l1 = Mma<T>::pack(p1[0] - f1.x, p1[1] - f1.y);
-        const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
-        const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
+        uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t h0 = Mma<T>::pack(p0[nt][0], p0[nt][1]);  // tokens g,   rows 2c, 2c+1
+            const uint32_t h1 = Mma<T>::pack(p1[nt][0], p1[nt][1]);  // tokens g+8, rows 2c, 2c+1
+            const float2 f0 = Mma<T>::unpack(h0), f1 = Mma<T>::unpack(h1);
+            const uint32_t l0 = Mma<T>::pack(p0[nt][0] - f0.x, p0[nt][1] - f0.y);
+            const uint32_t l1 = Mma<T>::pack(p1[nt][0] - f1.x, p1[nt][1] - f1.y);
+            bh[nt][0] = movmatrix_trans(h0);
+            bh[nt][1] = movmatrix_trans(h1);
+            bl[nt][0] = movmatrix_trans(l0);
+            bl[nt][1] = movmatrix_trans(l1);
+        }
 
-        // ---- O^T (D dims x 8 rows) += V^T P^T
+        // ---- O^T (D dims x 8 rows per n-tile) += V^T P^T
         {
             const int t = (lane & 7) + (lane >> 4) * 8;
             const int dq = (lane >> 3) & 1;
@@ -433,131 +469,67 @@ struct TcEngine {
             for (int mt = 0; mt < KS; ++mt) {
                 uint32_t a[4];
                 ldsm_x4_trans(C::addr(vbase, t, 2 * mt + dq), a);
-                Mma<T>::run(o[mt], a, bh0, bh1);
-                Mma<T>::run(o[mt], a, bl0, bl1);
-            }
-        }
-    }
-
-    // Persistent split path: resets the state for a new work item whose query
-    // rows are r = 8 rb + g < nrows, row r being head (kvh G + r % G) of
-    // sequence seq0 + r / G (sequences that share the item's tokens).
-    __device__ void begin_item(const DecodeParams &p, int seq0, int nrows, int kvh, int rb, int lane)
-    {
-        g = lane >> 2;
-        c = lane & 3;
-        qscale = p.qscale;
-        const int r = 8 * rb + g;
-        const bool live = r < nrows;
-        const int64_t qrow = (int64_t)(seq0 + (live ? r / G : 0)) * p.num_heads + kvh * G + (live ? r % G : 0);
-        const uint32_t *qp = reinterpret_cast<const uint32_t *>(static_cast<const T *>(p.q) + qrow * D);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qf[ks][0] = live ? qp[(16 * ks + 2 * c) / 2] : 0u;
-            qf[ks][1] = live ? qp[(16 * ks + 2 * c + 8) / 2] : 0u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                o[ks][j] = 0.f;
-        }
-        m[0] = m[1] = -INFINITY;
-        lsum[0] = lsum[1] = 0.f;
-    }
-
-    // Persistent split path: writes this item's partial (max, sum,
-    // unnormalised acc) of every live row to workspace slot `slot` of its
-    // (sequence, head); `invalid` writes the (-inf, -1) marker instead.
-    __device__ void write_partial(const DecodeParams &p, int seq0, int nrows, int kvh, int rb,
-                                  int slot, bool invalid)
-    {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 4);
-            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 8);
-            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 16);
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int r = 8 * rb + 2 * c + j;
-            if (r < nrows) {
-                const int64_t sh = (int64_t)(seq0 + r / G) * p.num_heads + kvh * G + r % G;
-                const int64_t base = sh * p.num_partitions + slot;
-                if (g == 0) {
-                    p.ws_ml[base * 2 + 0] = invalid ? -INFINITY : m[j];
-                    p.ws_ml[base * 2 + 1] = invalid ? -1.f : lsum[j];
-                }
-                float *acc = p.ws_acc + base * D;
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    acc[16 * mt + g] = invalid ? 0.f : o[mt][j];
-                    acc[16 * mt + g + 8] = invalid ? 0.f : o[mt][2 + j];
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (nt < ntl) {
+                        Mma<T>::run(o[mt][nt], a, bh[nt][0], bh[nt][1]);
+                        Mma<T>::run(o[mt][nt], a, bl[nt][0], bl[nt][1]);
+                    }
                 }
             }
         }
     }
 
-    __device__ void finish(float *mw, float *lw, float *aw, int warp, int lane)
+    // Per-warp (max, sum, acc) of live rows r < nrows into the merge scratch
+    // (row stride RS).
+    __device__ void finish(float *mw, float *lw, float *aw, int warp, int lane, int nrows)
     {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 4);
-            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 8);
-            lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 16);
-        }
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int row = 2 * c + j;
-            if (row < G) {
-                if (g == 0) {
-                    mw[warp * G + row] = m[j];
-                    lw[warp * G + row] = lsum[j];
-                }
+            for (int j = 0; j < 2; ++j) {
+                float l = lsum[nt][j];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                const int row = 8 * nt + 2 * c + j;
+                if (row < nrows) {
+                    if (g == 0) {
+                        mw[warp * RS + row] = m[nt][j];
+                        lw[warp * RS + row] = l;
+                    }
 #pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    aw[(warp * G + row) * D + 16 * mt + g] = o[mt][j];
-                    aw[(warp * G + row) * D + 16 * mt + g + 8] = o[mt][2 + j];
+                    for (int mt = 0; mt < KS; ++mt) {
+                        aw[(warp * RS + row) * D + 16 * mt + g] = o[mt][nt][j];
+                        aw[(warp * RS + row) * D + 16 * mt + g + 8] = o[mt][nt][2 + j];
+                    }
                 }
             }
         }
     }
 };
 
-// ------------------------------------------------------------ the kernel
-template <typename T, int D, int BS, int G, bool TC>
-__global__ void __launch_bounds__(DecodeCfg<T, D, BS, G, TC>::NW * 32)
-pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                 const __grid_constant__ CUtensorMap tmv)
+// ------------------------------------------------------------ CTA body
+// One CTA: stage the block-table slice, stream the tiles through the per-warp
+// rings, merge the warps and write the rows' output (single pass) or partials
+// (split).
+template <typename T, int D, int BS, int G, bool TC, int NT>
+__device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensorMap *tmk,
+                                           const CUtensorMap *tmv, uint8_t *smem, const CtaWork &w)
 {
     using C = DecodeCfg<T, D, BS, G, TC>;
-    using Eng = typename std::conditional<TC, TcEngine<T, D, BS, G>, CcEngine<T, D, BS, G>>::type;
+    using Eng = typename std::conditional<TC, TcEngine<T, D, BS, G, NT>, CcEngine<T, D, BS, G>>::type;
     constexpr int NW = C::NW, S = C::S, TILE = C::TILE;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-
-    const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+    constexpr int RS = TC ? 8 * NT : G;   // merge-scratch rows per warp
+    static_assert(NW * RS * (D + 2) * 4 <= C::STAGES_BYTES, "merge scratch fits in the ring");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    const int L = p.context_lens[seq];
-    if (L < 0 || L > p.max_context_len) {
-        if (part == 0 && kvh == 0 && tid == 0)
-            report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
-        if (!p.split)
-            write_invalid<D, G>(p, seq, kvh, part);
-        return;  // split path: the reduce kernel sees the bad length itself
-    }
-    const int tok0 = part * p.partition_size;
-    const int tok_end = min(tok0 + p.partition_size, L);
-    if (tok0 >= tok_end) {
-        if (!p.split && part == 0)
-            write_invalid<D, G>(p, seq, kvh, part);  // L == 0: zero output
-        return;
-    }
+    const int tok0 = w.tok0, tok_end = w.tok_end, kvh = w.kvh;
 
     // ---- stage the block-table slice (and, for the CUDA-core engine, q)
     const int j0 = tok0 / BS;
     const int nblk = (tok_end - tok0 + BS - 1) / BS;
     int32_t *table_s = reinterpret_cast<int32_t *>(smem + C::OFF_TABLE);
-    const int32_t *bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + j0;
+    const int32_t *bt = p.block_tables + (int64_t)w.table_seq * p.max_blocks_per_seq + j0;
     int bad = 0;
     for (int i = tid; i < nblk; i += NW * 32) {
         int b = bt[i];
@@ -567,7 +539,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
         }
         table_s[i] = b;
     }
-    Eng::stage_q(p, smem, seq, kvh);
+    Eng::stage_q(p, smem, w.seq0, kvh);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR) + warp * S;
     uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + C::OFF_FLAG);
     if (lane == 0) {
@@ -577,13 +549,13 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     }
     if (tid == 0) {
         *cta_flag = 0;
-        prefetch_tensormap(&tmk);
-        prefetch_tensormap(&tmv);
+        prefetch_tensormap(tmk);
+        prefetch_tensormap(tmv);
     }
     if (__syncthreads_or(bad)) {
         if (tid == 0)
             report(p.status, PKV_DEV_BAD_BLOCK);
-        write_invalid<D, G>(p, seq, kvh, part);
+        write_invalid<D, G>(p, w);
         return;
     }
 
@@ -603,8 +575,8 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
             const int tok = t0 + b * C::BOX_ROWS;
             const int phys = table_s[tok / BS - j0];
             const int row0 = tok % BS;
-            tma_load_5d(kd + b * C::BOX_BYTES, &tmk, &bars[st], 0, row0, 0, kvh, phys);
-            tma_load_5d(vd + b * C::BOX_BYTES, &tmv, &bars[st], 0, row0, 0, kvh, phys);
+            tma_load_5d(kd + b * C::BOX_BYTES, tmk, &bars[st], 0, row0, 0, kvh, phys);
+            tma_load_5d(vd + b * C::BOX_BYTES, tmv, &bars[st], 0, row0, 0, kvh, phys);
         }
     };
     if (lane == 0) {
@@ -614,7 +586,7 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     }
 
     Eng eng;
-    eng.init(p, smem, seq, kvh, warp, lane);
+    eng.init(p, smem, w, warp, lane);
 
     int failed_at = -1;
     for (int i = 0; i < my_n; ++i) {
@@ -649,32 +621,32 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     __syncthreads();  // every warp is done with its ring: reuse it as merge scratch
     const bool failed = *reinterpret_cast<volatile uint32_t *>(cta_flag) != 0;
     float *mw = reinterpret_cast<float *>(smem + C::OFF_STAGES);
-    float *lw = mw + NW * G;
-    float *aw = lw + NW * G;
-    eng.finish(mw, lw, aw, warp, lane);
+    float *lw = mw + NW * RS;
+    float *aw = lw + NW * RS;
+    eng.finish(mw, lw, aw, warp, lane, w.nrows);
     __syncthreads();
 
-    for (int idx = tid; idx < G * D; idx += NW * 32) {
-        const int h = idx / D, d = idx % D;
+    for (int idx = tid; idx < w.nrows * D; idx += NW * 32) {
+        const int r = idx / D, d = idx % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w)
-            M = fmaxf(M, mw[w * G + h]);
+        for (int k = 0; k < NW; ++k)
+            M = fmaxf(M, mw[k * RS + r]);
         float num = 0.f, den = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float mwh = mw[w * G + h];
-            if (mwh != -INFINITY) {
-                const float f = exp2f(mwh - M);
-                num += f * aw[(w * G + h) * D + d];
-                den += f * lw[w * G + h];
+        for (int k = 0; k < NW; ++k) {
+            const float mk = mw[k * RS + r];
+            if (mk != -INFINITY) {
+                const float f = exp2f(mk - M);
+                num += f * aw[(k * RS + r) * D + d];
+                den += f * lw[k * RS + r];
             }
         }
-        const int64_t sh = (int64_t)seq * p.num_heads + kvh * G + h;
+        const int64_t sh = row_head(p, w, G, r);
         if (!p.split) {
             store_out(p.out, p.out_dtype, sh * D + d, (failed || den == 0.f) ? 0.f : num / den);
         } else {
-            const int64_t slot = sh * p.num_partitions + part;
+            const int64_t slot = sh * p.num_partitions + w.slot;
             p.ws_acc[slot * D + d] = failed ? 0.f : num;
             if (d == 0) {
                 p.ws_ml[slot * 2 + 0] = failed ? -INFINITY : M;
@@ -684,64 +656,39 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     }
 }
 
-// Log-sum-exp merge of the split-context partials: one warp per (seq, head).
-template <int D>
-__global__ void __launch_bounds__(128) pa_reduce_kernel(const __grid_constant__ DecodeParams p)
+__device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw)
 {
-    constexpr int DPL = D / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
-    if (sh >= (int64_t)p.num_seqs * p.num_heads)
-        return;
-    const int seq = (int)(sh / p.num_heads);
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                       ~static_cast<uintptr_t>(1023));
+}
+
+// ------------------------------------------------------------ the kernel
+// Grid (partition, kv head, sequence); one partition = the whole context on
+// the single-pass path.
+template <typename T, int D, int BS, int G, bool TC>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, G, TC>::NW * 32)
+pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                 const __grid_constant__ CUtensorMap tmv)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = aligned_smem(smem_raw);
+    const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
     const int L = p.context_lens[seq];
-    const bool bad_len = L < 0 || L > p.max_context_len;
-    const int np = bad_len ? 0 : (L + p.partition_size - 1) / p.partition_size;
-    const float *ml = p.ws_ml + sh * p.num_partitions * 2;
-    const float *accp = p.ws_acc + sh * p.num_partitions * D;
-
-    float M = -INFINITY;
-    int invalid = 0;
-    for (int i = lane; i < np; i += 32) {
-        const float mi = ml[2 * i], li = ml[2 * i + 1];
-        invalid |= li < 0.f;
-        M = fmaxf(M, mi);
+    CtaWork w{seq, G, kvh, part * p.partition_size, 0, part, seq};
+    if (L < 0 || L > p.max_context_len) {
+        if (part == 0 && kvh == 0 && threadIdx.x == 0)
+            report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+        if (!p.split)
+            write_invalid<D, G>(p, w);
+        return;  // split path: the merge kernel sees the bad length itself
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    invalid = __any_sync(0xffffffffu, invalid);
-
-    float num[DPL];
-#pragma unroll
-    for (int k = 0; k < DPL; ++k)
-        num[k] = 0.f;
-    float den = 0.f;
-    if (!invalid) {
-        for (int i = 0; i < np; ++i) {
-            const float mi = ml[2 * i];
-            if (mi == -INFINITY)
-                continue;
-            const float f = exp2f(mi - M);
-            den += f * ml[2 * i + 1];
-            const float *a = accp + (int64_t)i * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(a);
-                num[0] += f * v.x;
-                num[1] += f * v.y;
-                num[2] += f * v.z;
-                num[3] += f * v.w;
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(a);
-                num[0] += f * v.x;
-                num[1] += f * v.y;
-            }
-        }
+    w.tok_end = min(w.tok0 + p.partition_size, L);
+    if (w.tok0 >= w.tok_end) {
+        if (!p.split && part == 0)
+            write_invalid<D, G>(p, w);  // L == 0: zero output
+        return;
     }
-    const bool zero = invalid || den == 0.f;
-#pragma unroll
-    for (int k = 0; k < DPL; ++k)
-        store_out(p.out, p.out_dtype, sh * D + lane * DPL + k, zero ? 0.f : num[k] / den);
+    decode_cta<T, D, BS, G, TC, 1>(p, &tmk, &tmv, smem, w);
 }
 
 }  // namespace pkv

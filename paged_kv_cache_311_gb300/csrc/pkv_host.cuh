@@ -5,7 +5,7 @@
 
 #include <cuda_runtime.h>
 
-#include "pa_split.cuh"
+#include "pa_shared.cuh"
 
 namespace pkv {
 
@@ -17,6 +17,7 @@ struct DecodeLaunch {
     int block_size;
     int group;
     int engine;          // Engine: kEngineAuto, kEngineCudaCore or kEngineTensorCore
+    bool shared;         // shared-prefix path (pa_shared_kernel)
     cudaStream_t stream;
     int *engine_used;    // out: the engine that ran
 };
@@ -59,48 +60,40 @@ int run_decode(const DecodeLaunch &a)
         return rc;
     dim3 grid(p.num_partitions, p.num_kv_heads, p.num_seqs);
     kern<<<grid, Sh::threads, Sh::smem, a.stream>>>(p, tmk, tmv);
-    if (p.split) {
-        const long long pairs = (long long)p.num_seqs * p.num_heads;
-        pa_reduce_kernel<D><<<(unsigned)((pairs + 3) / 4), 128, 0, a.stream>>>(p);
-    }
+    if (p.split)
+        pa_merge_kernel<D><<<(unsigned)((long long)p.num_seqs * p.num_heads), 128, 0, a.stream>>>(p);
     if (a.engine_used)
         *a.engine_used = TC ? kEngineTensorCore : kEngineCudaCore;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
-// Persistent split path (tensor-core engine): one worker per warp over the
-// (sequence, kv head, partition) items, then the log-sum-exp merge.
-int grid_for_occupancy(const void *func, int threads, int smem, int *cache_per_dev);
+// Shared-prefix path: up to 8 * kSharedNT query rows per CTA (all heads of the
+// members of one group), then the log-sum-exp merge.  pa_plan_kernel has run
+// on the same stream before this.
+constexpr int kSharedNT = 3;
 
-template <typename T, int D, int BS, int G, bool EXPLICIT>
-int run_split(const DecodeLaunch &a, long long max_items)
+template <typename T, int D, int BS, int G>
+int run_shared(const DecodeLaunch &a)
 {
-    using SC = SplitCfg<T, D, BS, G>;
+    using Sh = DecodeShape<T, D, BS, G, true>;
     const DecodeParams &p = a.p;
     alignas(64) CUtensorMap tmk;
     alignas(64) CUtensorMap tmv;
     int rc = encode_kv_map(&tmk, a.k_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
-                           p.num_blocks, SC::C::BOX_ROWS);
+                           p.num_blocks, Sh::box_rows);
     if (rc)
         return rc;
     rc = encode_kv_map(&tmv, a.v_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
-                       p.num_blocks, SC::C::BOX_ROWS);
+                       p.num_blocks, Sh::box_rows);
     if (rc)
         return rc;
     static unsigned long long done = 0;
-    static int occ[64] = {};
-    auto kern = pa_split_kernel<T, D, BS, G, EXPLICIT>;
-    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), SC::SMEM_BYTES, &done);
+    auto kern = pa_shared_kernel<T, D, BS, G, kSharedNT>;
+    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), Sh::smem, &done);
     if (rc)
         return rc;
-    int blocks = grid_for_occupancy(reinterpret_cast<const void *>(kern), SC::NW * 32,
-                                    SC::SMEM_BYTES, occ);
-    if (blocks <= 0)
-        return PKV_ECUDA;
-    const long long need = (max_items + SC::NW - 1) / SC::NW;
-    if (need < blocks)
-        blocks = (int)(need > 0 ? need : 1);
-    kern<<<blocks, SC::NW * 32, SC::SMEM_BYTES, a.stream>>>(p, tmk, tmv);
+    dim3 grid(p.num_partitions, p.num_kv_heads, p.num_seqs);
+    kern<<<grid, Sh::threads, Sh::smem, a.stream>>>(p, tmk, tmv);
     pa_merge_kernel<D><<<(unsigned)((long long)p.num_seqs * p.num_heads), 128, 0, a.stream>>>(p);
     if (a.engine_used)
         *a.engine_used = kEngineTensorCore;
@@ -115,15 +108,13 @@ template <typename T, int D, int BS, int G>
 int run_engine(const DecodeLaunch &a)
 {
     if constexpr (Elem<T>::bytes == 2) {
+        if (a.shared)
+            return run_shared<T, D, BS, G>(a);
         const bool tc = a.engine != kEngineCudaCore;
-        if (tc && a.p.split &&
-            (a.p.partition_size + BS - 1) / BS <= SplitCfg<T, D, BS, G>::TABLE_W)
-            return run_split<T, D, BS, G, false>(
-                a, (long long)a.p.num_seqs * a.p.num_kv_heads * a.p.num_partitions);
         if (tc)
             return run_decode<T, D, BS, G, true>(a);
     } else {
-        if (a.engine == kEngineTensorCore)
+        if (a.engine == kEngineTensorCore || a.shared)
             return PKV_EUNSUPPORTED;
     }
     return run_decode<T, D, BS, G, false>(a);

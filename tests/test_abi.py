@@ -105,3 +105,12 @@ def test_cache_ops_host_validation(lib):
 def test_package_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         pkv.load_library(str(tmp_path / "missing.so"))
+
+
+def test_shared_workspace_bytes(lib):
+    B, H, L, D = 192, 32, 1100, 128
+    np_ = -(-L // 256)
+    ints = ((4 * B * 4 + 255) // 256) * 256
+    ml = B * H * 2 * np_ * 2 * 4
+    expect = ints + ((ml + 255) // 256) * 256 + B * H * 2 * np_ * D * 4
+    assert pkv.paged_attention_shared_workspace_bytes(B, H, L, D, 0) == expect

@@ -1,0 +1,174 @@
+"""GPU parity of paged_attention_decode_shared (the shared-prefix path)
+against the CPU oracle, which knows nothing about sharing: it just follows
+every sequence's block table.
+
+Cases mix groups of sequences forked from one prompt (their tables start with
+the same block ids; the partially filled last prompt block is copied for all
+but one member, as copy-on-write does), singleton sequences, groups larger
+than one CTA can take (the planner cuts them), prefixes that are not a
+multiple of the alignment, empty contexts and bad block ids."""
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_support import TOL, max_err
+from tests.util import DT, raw_np
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def shared_case(seed, *, dtype="bf16", H=8, Hk=2, D=128, bs=16, groups=((300, (5, 40, 1, 70)),)):
+    """groups: (prompt length, tail lengths of its members); a member with
+    tail -1 is a singleton sequence of the given prompt length (no sharing)."""
+    rng = np.random.default_rng(seed)
+    seqs = []   # (logical K, V [L, Hk, D], table builder info)
+    tables, lens = [], []
+    next_block = [0]
+
+    def take(n):
+        b = list(range(next_block[0], next_block[0] + n))
+        next_block[0] += n
+        return b
+
+    plan = []
+    for prompt, tails in groups:
+        full, rem = divmod(prompt, bs)
+        shared_blocks = take(full + (1 if rem else 0))
+        for i, t in enumerate(tails):
+            if t < 0:
+                plan.append(("single", prompt, None, None))
+                continue
+            plan.append(("member", prompt, t, (shared_blocks, full, rem, i == len(tails) - 1)))
+    # assign blocks
+    for kind, prompt, t, info in plan:
+        if kind == "single":
+            L = prompt
+            tables.append(take(-(-L // bs)))
+        else:
+            shared_blocks, full, rem, keeps_partial = info
+            L = prompt + t
+            tb = list(shared_blocks[:full])
+            if rem:
+                tb.append(shared_blocks[full] if keeps_partial else take(1)[0])
+            need = -(-L // bs) - len(tb)
+            tb += take(max(need, 0))
+            tables.append(tb[: -(-L // bs)] if L else [])
+        lens.append(L)
+    NB = next_block[0] + 2
+    g = torch.Generator().manual_seed(seed)
+    kc = torch.randn(NB, Hk, bs, D, generator=g).to(DT[dtype])
+    vc = torch.randn(NB, Hk, bs, D, generator=g).to(DT[dtype])
+    # copy-on-write copies hold the prompt's rows of the shared partial block
+    for (kind, prompt, t, info), tb in zip(plan, tables):
+        if kind == "member":
+            shared_blocks, full, rem, keeps_partial = info
+            if rem and not keeps_partial and len(tb) > full:
+                kc[tb[full], :, :rem] = kc[shared_blocks[full], :, :rem]
+                vc[tb[full], :, :rem] = vc[shared_blocks[full], :, :rem]
+    MB = max(max(len(t) for t in tables), 1)
+    bt = np.full((len(tables), MB), -1, dtype=np.int32)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = t
+    q = torch.randn(len(tables), H, D, generator=g).to(DT[dtype])
+    return dict(q=q, k_cache=kc, v_cache=vc, block_tables=bt,
+                context_lens=np.array(lens, dtype=np.int32), dtype=dtype, bs=bs, Hk=Hk,
+                scale=float(np.float32(1.0 / np.sqrt(D))))
+
+
+def run_shared(case, P=0, out_dtype=torch.float32, tables=None):
+    import paged_kv_cache_311_gb300 as pkv
+    dev = "cuda"
+    q, kc, vc = case["q"].to(dev), case["k_cache"].to(dev), case["v_cache"].to(dev)
+    bt = torch.as_tensor(case["block_tables"] if tables is None else tables).to(dev)
+    cl = torch.as_tensor(case["context_lens"]).to(dev)
+    out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.paged_attention_decode_shared(out, q, kc, vc, bt, cl, case["scale"],
+                                      max_context_len=int(max(case["context_lens"].max(), 1)),
+                                      partition_size=P, device_status=st)
+    torch.cuda.synchronize()
+    assert pkv.last_decode_launches() == 3
+    return out.double().cpu().numpy(), int(st.item())
+
+
+def oracle_out(case, tables=None):
+    return oracle.paged_attention(raw_np(case["q"]), raw_np(case["k_cache"]), raw_np(case["v_cache"]),
+                                  case["dtype"],
+                                  case["block_tables"] if tables is None else tables,
+                                  case["context_lens"], case["Hk"], case["scale"])
+
+
+GROUPS = [
+    (300, (5, 40, 1, 70)),          # partial last prompt block, 4 members
+    (512, (0, 3, 17)),              # block-aligned prompt, a member with no tail
+    (40, (100, -1, 9)),             # short prompt; a singleton in the middle
+    (1000, (1, 2, 3, 4, 5, 6, 7)),  # more members than one CTA takes at G = 4
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_shared_prefix_matches_oracle(dtype, G, bs):
+    case = shared_case(10 * G + bs, dtype=dtype, H=2 * G, Hk=2, D=128, bs=bs, groups=GROUPS)
+    ref, st = oracle_out(case)
+    assert st == 0
+    for P in (0, 64, 512):
+        got, gst = run_shared(case, P=P)
+        assert gst == 0
+        err = max_err(got, ref)
+        assert err <= TOL[dtype], f"P={P} max err {err}"
+
+
+def test_shared_prefix_head_dim_64_and_half_output():
+    case = shared_case(3, dtype="bf16", H=8, Hk=1, D=64, bs=16, groups=GROUPS[:2])
+    ref, _ = oracle_out(case)
+    got, st = run_shared(case, out_dtype=torch.bfloat16)
+    assert st == 0
+    rne = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    from tests.gpu_support import ulp_bound
+    assert np.all(np.abs(got - rne) <= ulp_bound(ref, torch.bfloat16))
+
+
+def test_shared_prefix_equals_per_sequence_path():
+    from tests.gpu_support import gpu_decode
+    case = shared_case(5, dtype="bf16", H=16, Hk=4, D=128, bs=16, groups=GROUPS)
+    a, _ = run_shared(case)
+    b, _, _ = gpu_decode(case)
+    assert max_err(a, b) <= 1e-5
+
+
+def test_no_sharing_batch():
+    case = shared_case(6, dtype="f16", H=8, Hk=8, D=128, bs=16,
+                       groups=((100, (-1,)), (700, (-1,)), (33, (-1,))))
+    ref, _ = oracle_out(case)
+    got, st = run_shared(case)
+    assert st == 0 and max_err(got, ref) <= TOL["f16"]
+
+
+def test_empty_context_and_bad_block():
+    import paged_kv_cache_311_gb300 as pkv
+    case = shared_case(7, dtype="bf16", H=8, Hk=2, D=128, bs=16, groups=GROUPS[:1])
+    lens = case["context_lens"].copy()
+    lens[1] = 0
+    c0 = dict(case, context_lens=lens)
+    ref, _ = oracle_out(c0)
+    got, st = run_shared(c0)
+    assert st == 0 and not got[1].any() and max_err(got, ref) <= TOL["bf16"]
+    t = case["block_tables"].copy()
+    t[3, -1] = case["k_cache"].shape[0] + 3      # last member's own tail block
+    got, st = run_shared(case, tables=t)
+    assert st & pkv.DEV_BAD_BLOCK
+    assert not got[3].any()
+    ref, _ = oracle_out(case)
+    assert max_err(got[:3], ref[:3]) <= TOL["bf16"]
+
+
+def test_fp32_is_rejected():
+    import paged_kv_cache_311_gb300 as pkv
+    case = shared_case(8, dtype="f32", H=4, Hk=4, D=64, bs=16, groups=GROUPS[:1])
+    with pytest.raises(pkv.PkvError) as e:
+        run_shared(case)
+    assert e.value.status == -2

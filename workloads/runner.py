@@ -68,37 +68,77 @@ class DeviceState:
             context_lens=torch.as_tensor(inp.context_lens).to(dev),
             cow_pairs=pairs, max_context_len=inp.max_context_len, host=inp)
 
-    def ensure_workspace(self, max_context_len: int, partition_size: int) -> None:
+    def ensure_workspace(self, max_context_len: int, partition_size: int,
+                         shared: bool = False) -> None:
         import paged_kv_cache_311_gb300 as pkv
-        need = pkv.paged_attention_workspace_bytes(self.w.num_seqs, self.cfg.num_heads,
-                                                   max_context_len, self.cfg.head_dim,
-                                                   partition_size)
+        fn = pkv.paged_attention_shared_workspace_bytes if shared else pkv.paged_attention_workspace_bytes
+        need = fn(self.w.num_seqs, self.cfg.num_heads, max_context_len, self.cfg.head_dim,
+                  partition_size)
         if need and (self.workspace is None or self.workspace.numel() < need):
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
 
     def run_step(self, s: DeviceStep, partition_size: Optional[int] = None,
-                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                 out: Optional[torch.Tensor] = None, stream=None,
+                 shared: Optional[bool] = None) -> torch.Tensor:
         """copy_blocks (if the step has copy-on-write pairs), reshape_and_cache,
-        paged_attention_decode -- all on the current stream."""
+        then paged attention -- all on the current stream.  Attention takes the
+        shared-prefix entry point for workloads whose sequences are forked
+        from common prompts (``shared`` overrides)."""
         import paged_kv_cache_311_gb300 as pkv
         cfg = self.cfg
         P = cfg.partition_size if partition_size is None else partition_size
+        if shared is None:
+            shared = cfg.kind == "shared_prefix"
         out = self.out if out is None else out
         if s.cow_pairs is not None:
             pkv.copy_blocks([self.k_cache], [self.v_cache], s.cow_pairs,
                             device_status=self.status, stream=stream)
         pkv.reshape_and_cache(s.key, s.value, self.k_cache, self.v_cache, s.slot_mapping,
                               device_status=self.status, stream=stream)
-        self.ensure_workspace(s.max_context_len, P)
-        pkv.paged_attention_decode(out, s.q, self.k_cache, self.v_cache, s.block_tables,
-                                   s.context_lens, cfg.softmax_scale, max_context_len=s.max_context_len,
-                                   partition_size=P, workspace=self.workspace,
-                                   device_status=self.status, stream=stream)
+        self.ensure_workspace(s.max_context_len, P, shared)
+        fn = pkv.paged_attention_decode_shared if shared else pkv.paged_attention_decode
+        fn(out, s.q, self.k_cache, self.v_cache, s.block_tables, s.context_lens, cfg.softmax_scale,
+           max_context_len=s.max_context_len, partition_size=P, workspace=self.workspace,
+           device_status=self.status, stream=stream)
         return out
 
 
+def shared_lengths(inp: StepInputs, num_seqs: int, block_size: int, group: int,
+                   rows_per_cta: int = 24) -> np.ndarray:
+    """Host mirror of the library's grouping for the shared-prefix path (used
+    only to count that path's partials): runs of consecutive sequences whose
+    tables start with the same block ids, cut into groups of rows_per_cta /
+    group sequences; a group shares the shortest common prefix of its
+    members, rounded down to max(block_size, 32) tokens."""
+    align = max(block_size, 32)
+    lens = inp.context_lens[:num_seqs].astype(np.int64)
+    sp = np.zeros(num_seqs, dtype=np.int64)
+    for s in range(1, num_seqs):
+        la, lb = int(lens[s - 1]), int(lens[s])
+        if la <= 0 or lb <= 0:
+            continue
+        n = min(-(-la // block_size), -(-lb // block_size))
+        a, b = inp.block_tables[s - 1][:n], inp.block_tables[s][:n]
+        neq = np.nonzero(a != b)[0]
+        c = int(neq[0]) if neq.size else n
+        sp[s] = (min(c * block_size, la, lb) // align) * align
+    shared = np.zeros(num_seqs, dtype=np.int64)
+    mm = rows_per_cta // group
+    run = 0
+    for s in range(num_seqs):
+        if s == 0 or sp[s] == 0:
+            run = s
+        if (s - run) % mm == 0:
+            cnt, S = 1, None
+            while cnt < mm and s + cnt < num_seqs and sp[s + cnt] > 0 and (s + cnt - run) % mm != 0:
+                S = sp[s + cnt] if S is None else min(S, sp[s + cnt])
+                cnt += 1
+            shared[s:s + cnt] = S if (cnt >= 2 and S) else 0
+    return shared
+
+
 def algorithmic_bytes(cfg: DecodeConfig, inp: StepInputs, num_seqs: int, split_partition: int = 0,
-                      out_bytes: int = 4) -> dict:
+                      out_bytes: int = 4, shared_partition: int = 0) -> dict:
     """Bytes one decode step must move at minimum.
 
     attention: every distinct (physical block, kv head, row) slot that some
@@ -134,6 +174,12 @@ def algorithmic_bytes(cfg: DecodeConfig, inp: StepInputs, num_seqs: int, split_p
     ws = 0
     if split_partition:
         parts = sum(-(-int(L) // split_partition) for L in inp.context_lens[:num_seqs])
+        ws = 2 * cfg.num_heads * parts * (cfg.head_dim + 2) * 4
+    if shared_partition:
+        S = shared_lengths(inp, num_seqs, bs, cfg.group)
+        P = shared_partition
+        parts = sum(-(-int(sh) // P) + -(-(int(L) - int(sh)) // P)
+                    for sh, L in zip(S, inp.context_lens[:num_seqs]))
         ws = 2 * cfg.num_heads * parts * (cfg.head_dim + 2) * 4
     attn = kv + qo + meta + ws
     T = inp.num_tokens
