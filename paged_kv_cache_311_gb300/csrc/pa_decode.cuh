@@ -64,6 +64,8 @@ struct DecodeParams {
     const int32_t *seq_shared;  // tokens each sequence shares with its group
     const int32_t *seq_members; // group size for group leaders, else 0
     int np_prefix;              // workspace slots reserved for shared-prefix partials
+    const int2 *items;          // planned work: (sequence, slot)
+    const int *num_items;
 };
 
 enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2 };
@@ -510,12 +512,29 @@ struct TcEngine {
 };
 
 // ------------------------------------------------------------ CTA body
-// One CTA: stage the block-table slice, stream the tiles through the per-warp
-// rings, merge the warps and write the rows' output (single pass) or partials
-// (split).
+// Initialises the per-warp ring barriers (once per CTA).
+template <typename C>
+__device__ __forceinline__ void init_rings(uint8_t *smem)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR) + warp * C::S;
+        for (int s = 0; s < C::S; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+}
+
+// One CTA work unit: stage the block-table slice, stream the tiles through
+// the per-warp rings, merge the warps and write the rows' output (single
+// pass) or partials (split).  `ring` counts the tiles each warp has already
+// pushed through its ring (stage and phase of the next tile follow from it);
+// a CTA that runs several units passes the same counter to each.  Ends with
+// a CTA barrier, so the next unit may reuse all shared memory.
 template <typename T, int D, int BS, int G, bool TC, int NT>
 __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensorMap *tmk,
-                                           const CUtensorMap *tmv, uint8_t *smem, const CtaWork &w)
+                                           const CUtensorMap *tmv, uint8_t *smem, const CtaWork &w,
+                                           int &ring)
 {
     using C = DecodeCfg<T, D, BS, G, TC>;
     using Eng = typename std::conditional<TC, TcEngine<T, D, BS, G, NT>, CcEngine<T, D, BS, G>>::type;
@@ -542,11 +561,6 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
     Eng::stage_q(p, smem, w.seq0, kvh);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR) + warp * S;
     uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + C::OFF_FLAG);
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s)
-            mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
     if (tid == 0) {
         *cta_flag = 0;
         prefetch_tensormap(tmk);
@@ -556,6 +570,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
         if (tid == 0)
             report(p.status, PKV_DEV_BAD_BLOCK);
         write_invalid<D, G>(p, w);
+        __syncthreads();
         return;
     }
 
@@ -565,6 +580,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
     const int my_n = warp < ntiles ? (ntiles - 1 - warp) / NW + 1 : 0;
     uint8_t *stages = smem + C::OFF_STAGES + warp * S * C::STAGE_BYTES;
 
+    const int base = ring;
     auto issue = [&](int i, int st) {
         const int t0 = tok0 + (warp + i * NW) * TILE;
         uint8_t *kd = stages + st * C::STAGE_BYTES;
@@ -581,8 +597,10 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
     };
     if (lane == 0) {
         const int pre = my_n < S ? my_n : S;
+        if (pre > 0)
+            fence_proxy_async_smem();  // a previous unit's merge wrote into the rings
         for (int i = 0; i < pre; ++i)
-            issue(i, i);
+            issue(i, (base + i) % S);
     }
 
     Eng eng;
@@ -590,8 +608,8 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
 
     int failed_at = -1;
     for (int i = 0; i < my_n; ++i) {
-        const int st = i % S;
-        if (!mbar_wait_bounded(&bars[st], (uint32_t)((i / S) & 1))) {
+        const int st = (base + i) % S;
+        if (!mbar_wait_bounded(&bars[st], (uint32_t)(((base + i) / S) & 1))) {
             failed_at = i;
             break;
         }
@@ -611,13 +629,14 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
         // exit, then mark the CTA's result invalid.
         const int last = min(my_n, failed_at + S);
         for (int i = failed_at; i < last; ++i)
-            mbar_wait_bounded(&bars[i % S], (uint32_t)((i / S) & 1), 200000000ull);
+            mbar_wait_bounded(&bars[(base + i) % S], (uint32_t)(((base + i) / S) & 1), 200000000ull);
         if (lane == 0) {
             report(p.status, PKV_DEV_TIMEOUT);
             atomicOr(cta_flag, 1u);
         }
     }
 
+    ring = base + my_n;
     __syncthreads();  // every warp is done with its ring: reuse it as merge scratch
     const bool failed = *reinterpret_cast<volatile uint32_t *>(cta_flag) != 0;
     float *mw = reinterpret_cast<float *>(smem + C::OFF_STAGES);
@@ -654,6 +673,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
             }
         }
     }
+    __syncthreads();  // the merge scratch is read; the next unit may load into the rings
 }
 
 __device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw)
@@ -688,7 +708,9 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
             write_invalid<D, G>(p, w);  // L == 0: zero output
         return;
     }
-    decode_cta<T, D, BS, G, TC, 1>(p, &tmk, &tmv, smem, w);
+    init_rings<DecodeCfg<T, D, BS, G, TC>>(smem);
+    int ring = 0;
+    decode_cta<T, D, BS, G, TC, 1>(p, &tmk, &tmv, smem, w, ring);
 }
 
 }  // namespace pkv

@@ -88,16 +88,19 @@ SplitLayout split_layout(long long seqs, long long heads, long long np, long lon
 constexpr int kSharedPartition = 256;   // default partition of the shared-prefix path
 
 struct SharedLayout {
-    size_t ml_off, acc_off, total;
+    size_t items_off, count_off, ml_off, acc_off, total;
 };
 
 // Shared-prefix workspace: four int32 arrays of num_seqs (shared length, group
-// size, and two planning scratch arrays), then the split partials with
-// 2 * ceil(max_context_len / P) slots per (sequence, head).
+// size, two planning scratch arrays), the work list (one int2 per (sequence,
+// slot), at most num_seqs * slots) and its count, then the split partials
+// with slots = 2 * ceil(max_context_len / P) per (sequence, head).
 SharedLayout shared_layout(long long seqs, long long heads, long long slots, long long head_dim)
 {
     SharedLayout s;
-    s.ml_off = ((size_t)(4 * seqs) * sizeof(int32_t) + 255) & ~size_t(255);
+    s.items_off = ((size_t)(4 * seqs) * sizeof(int32_t) + 15) & ~size_t(15);
+    s.count_off = s.items_off + (size_t)(seqs * slots) * 2 * sizeof(int32_t);
+    s.ml_off = (s.count_off + sizeof(int32_t) + 255) & ~size_t(255);
     const size_t ml = (size_t)(seqs * heads * slots * 2) * sizeof(float);
     s.acc_off = s.ml_off + ((ml + 255) & ~size_t(255));
     s.total = s.acc_off + (size_t)(seqs * heads * slots * head_dim) * sizeof(float);
@@ -271,6 +274,8 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     p.seq_shared = nullptr;
     p.seq_members = nullptr;
     p.np_prefix = 0;
+    p.items = nullptr;
+    p.num_items = nullptr;
     if (p.split) {
         const SplitLayout s = split_layout(num_seqs, num_heads, np, head_dim);
         if (!workspace || workspace_bytes < s.total || !aligned16(workspace))
@@ -285,6 +290,7 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     a.group = group;
     a.engine = g_engine_override.load(std::memory_order_relaxed);
     a.shared = false;
+    a.sms = 0;
     a.stream = static_cast<cudaStream_t>(stream);
     int engine_used = 0;
     a.engine_used = &engine_used;
@@ -363,10 +369,12 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
             *run_start = ints + 3 * num_seqs;
     const int align = block_size > kTileAlign ? block_size : kTileAlign;
     const int max_members = 8 * kSharedNT / group;
+    int2 *items = reinterpret_cast<int2 *>(static_cast<char *>(workspace) + lay.items_off);
+    int *num_items = reinterpret_cast<int *>(static_cast<char *>(workspace) + lay.count_off);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     pa_plan_kernel<<<1, 1024, 0, st>>>(block_tables, context_lens, num_seqs, max_blocks_per_seq,
-                                       block_size, max_context_len, max_members, align, seq_shared,
-                                       members, sp, run_start);
+                                       block_size, max_context_len, max_members, align, P, (int)np,
+                                       seq_shared, members, sp, run_start, items, num_items);
     if (cudaGetLastError() != cudaSuccess)
         return PKV_ECUDA;
 
@@ -393,6 +401,8 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     p.seq_shared = seq_shared;
     p.seq_members = members;
     p.np_prefix = (int)np;
+    p.items = items;
+    p.num_items = num_items;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.head_dim = head_dim;
@@ -400,6 +410,7 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     a.group = group;
     a.engine = kEngineTensorCore;
     a.shared = true;
+    a.sms = sm_count(current_device());
     a.stream = st;
     int engine_used = 0;
     a.engine_used = &engine_used;

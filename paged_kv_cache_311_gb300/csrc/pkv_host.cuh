@@ -18,6 +18,7 @@ struct DecodeLaunch {
     int group;
     int engine;          // Engine: kEngineAuto, kEngineCudaCore or kEngineTensorCore
     bool shared;         // shared-prefix path (pa_shared_kernel)
+    int sms;             // SM count of the device (shared-prefix grid)
     cudaStream_t stream;
     int *engine_used;    // out: the engine that ran
 };
@@ -61,7 +62,7 @@ int run_decode(const DecodeLaunch &a)
     dim3 grid(p.num_partitions, p.num_kv_heads, p.num_seqs);
     kern<<<grid, Sh::threads, Sh::smem, a.stream>>>(p, tmk, tmv);
     if (p.split)
-        pa_merge_kernel<D><<<(unsigned)((long long)p.num_seqs * p.num_heads), 128, 0, a.stream>>>(p);
+        pa_merge_kernel<D><<<(unsigned)(((long long)p.num_seqs * p.num_heads + 3) / 4), 128, 0, a.stream>>>(p);
     if (a.engine_used)
         *a.engine_used = TC ? kEngineTensorCore : kEngineCudaCore;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
@@ -92,9 +93,15 @@ int run_shared(const DecodeLaunch &a)
     rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), Sh::smem, &done);
     if (rc)
         return rc;
-    dim3 grid(p.num_partitions, p.num_kv_heads, p.num_seqs);
+    // persistent: about two CTAs per SM over all kv heads, never more than
+    // the largest possible work list
+    long long gx = (2LL * (a.sms > 0 ? a.sms : 152) + p.num_kv_heads - 1) / p.num_kv_heads;
+    const long long max_items = (long long)p.num_seqs * p.num_partitions;
+    if (gx > max_items)
+        gx = max_items;
+    dim3 grid((unsigned)(gx > 0 ? gx : 1), p.num_kv_heads, 1);
     kern<<<grid, Sh::threads, Sh::smem, a.stream>>>(p, tmk, tmv);
-    pa_merge_kernel<D><<<(unsigned)((long long)p.num_seqs * p.num_heads), 128, 0, a.stream>>>(p);
+    pa_merge_kernel<D><<<(unsigned)(((long long)p.num_seqs * p.num_heads + 3) / 4), 128, 0, a.stream>>>(p);
     if (a.engine_used)
         *a.engine_used = kEngineTensorCore;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;

@@ -109,8 +109,10 @@ def test_package_fails_loudly_without_library(tmp_path):
 
 def test_shared_workspace_bytes(lib):
     B, H, L, D = 192, 32, 1100, 128
-    np_ = -(-L // 256)
-    ints = ((4 * B * 4 + 255) // 256) * 256
-    ml = B * H * 2 * np_ * 2 * 4
-    expect = ints + ((ml + 255) // 256) * 256 + B * H * 2 * np_ * D * 4
+    slots = 2 * -(-L // 256)
+    items_off = ((4 * B * 4 + 15) // 16) * 16
+    count_off = items_off + B * slots * 8
+    ml_off = ((count_off + 4 + 255) // 256) * 256
+    ml = B * H * slots * 2 * 4
+    expect = ml_off + ((ml + 255) // 256) * 256 + B * H * slots * D * 4
     assert pkv.paged_attention_shared_workspace_bytes(B, H, L, D, 0) == expect
