@@ -360,8 +360,18 @@ struct TcEngine {
     float m[NT][2], lsum[NT][2];
     float qscale;
     int g, c, ntl;            // ntl: n-tiles that hold live rows
+    // This lane's ldmatrix row offsets inside a tile (swizzle included): the
+    // K matrices of k-step ks and the V matrices of m-tile mt, for ks, mt < 8
+    // (the second 128-byte chunk adds a constant).
+    uint32_t koff[4], voff[4];
 
     __device__ static void stage_q(const DecodeParams &, uint8_t *, int, int) {}
+
+    // Chunk offset of k-step / m-tile k (its 16-byte pieces are 2k and 2k+1).
+    __device__ __forceinline__ static uint32_t chunk_off(int k)
+    {
+        return (uint32_t)((k >> 2) * C::BOX_ROWS * 128);
+    }
 
     __device__ void init(const DecodeParams &p, uint8_t *, const CtaWork &w, int, int lane)
     {
@@ -369,6 +379,15 @@ struct TcEngine {
         c = lane & 3;
         qscale = p.qscale;
         ntl = (w.nrows + 7) / 8;
+        {
+            const int tk = (lane & 7) + ((lane >> 3) & 1) * 8, dk = lane >> 4;
+            const int tv = (lane & 7) + (lane >> 4) * 8, dv = (lane >> 3) & 1;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                koff[k] = C::addr(0, tk, 2 * k + dk);
+                voff[k] = C::addr(0, tv, 2 * k + dv);
+            }
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int r = 8 * nt + g;
@@ -390,28 +409,37 @@ struct TcEngine {
 
     __device__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, int lane)
     {
-        // ---- S^T (16 tokens x 8 query rows per n-tile) = K q^T
-        float s[NT][4];
+        // ---- S^T (16 tokens x 8 query rows per n-tile) = K q^T, as two
+        // independent accumulation chains (even / odd k-steps)
+        float s[NT][4], s2[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-        {
-            const int t = (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int dq = lane >> 4;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(C::addr(kbase, t, 2 * ks + dq), a);
+            for (int j = 0; j < 4; ++j)
+                s[nt][j] = s2[nt][j] = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    if (nt < ntl)
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(kbase + chunk_off(ks) + koff[ks & 3], a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                if (nt < ntl) {
+                    if (ks & 1)
+                        Mma<T>::run(s2[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+                    else
                         Mma<T>::run(s[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
-            }
+                }
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                s[nt][j] += s2[nt][j];
 
         // ---- online softmax: this lane holds tokens g, g + 8 of rows 2c, 2c+1
         const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
-        float p0[NT][2], p1[NT][2];
+        float p0[NT][2], p1[NT][2], alpha[NT][2];
+        bool grew = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -423,17 +451,25 @@ struct TcEngine {
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
                 const float mn = fmaxf(m[nt][j], tm);
-                const float alpha = exp2f(m[nt][j] - mn);
+                alpha[nt][j] = exp2f(m[nt][j] - mn);
+                grew |= mn != m[nt][j];
                 p0[nt][j] = exp2f(x0 - mn);
                 p1[nt][j] = exp2f(x1 - mn);
-                lsum[nt][j] = lsum[nt][j] * alpha + p0[nt][j] + p1[nt][j];
+                lsum[nt][j] = lsum[nt][j] * alpha[nt][j] + p0[nt][j] + p1[nt][j];
                 m[nt][j] = mn;
+            }
+        }
+        // rescale the accumulators only when some row's running maximum moved
+        if (__any_sync(0xffffffffu, grew)) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
-                    o[mt][nt][j] *= alpha;
-                    o[mt][nt][2 + j] *= alpha;
+                    o[mt][nt][0] *= alpha[nt][0];
+                    o[mt][nt][1] *= alpha[nt][1];
+                    o[mt][nt][2] *= alpha[nt][0];
+                    o[mt][nt][3] *= alpha[nt][1];
                 }
-            }
         }
 
         // ---- rows of V past the valid tokens may hold anything (even NaN
@@ -465,12 +501,10 @@ struct TcEngine {
 
         // ---- O^T (D dims x 8 rows per n-tile) += V^T P^T
         {
-            const int t = (lane & 7) + (lane >> 4) * 8;
-            const int dq = (lane >> 3) & 1;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 uint32_t a[4];
-                ldsm_x4_trans(C::addr(vbase, t, 2 * mt + dq), a);
+                ldsm_x4_trans(vbase + chunk_off(mt) + voff[mt & 3], a);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     if (nt < ntl) {
