@@ -74,7 +74,7 @@ enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2 };
 #define PKV_DECODE_STAGE_BUDGET_CC 98304
 #endif
 #ifndef PKV_DECODE_STAGE_BUDGET_TC
-#define PKV_DECODE_STAGE_BUDGET_TC 98304
+#define PKV_DECODE_STAGE_BUDGET_TC 65536
 #endif
 
 template <typename T, int D, int BS, int G, bool TC>
