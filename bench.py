@@ -176,22 +176,21 @@ def run_native(args):
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(cfg, state, host_inputs, args.cpu_seconds, seed)
 
-    steps = [state.to_device(inp) for inp in host_inputs]
     import paged_kv_cache_311_gb300 as pkv
-    pkv.set_decode_engine(args.engine)
     shared = cfg.kind == "shared_prefix" and not args.no_shared
     if shared and args.partition_size < 0:
-        P = 0   # the shared-prefix entry point's own default partition
-    decode_fn = pkv.paged_attention_decode_shared if shared else pkv.paged_attention_decode
+        P = 0   # the shared-prefix planner's own default partition
+    steps = [state.to_device(inp, shared=shared, partition_size=P) for inp in host_inputs]
+    pkv.set_decode_engine(args.engine)
     for s in steps:
-        state.ensure_workspace(s.max_context_len, P, shared)
+        state.ensure_workspace(s.max_context_len, P, s.plan)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     out_bytes = torch.tensor([], dtype=out_dtype).element_size()
 
     # warm-up
     for s in steps[:args.warmup]:
-        state.run_step(s, partition_size=P, shared=shared)
+        state.run_step(s, partition_size=P)
     torch.cuda.synchronize()
     state.status.zero_()
 
@@ -217,9 +216,7 @@ def run_native(args):
                               device_status=state.status)
         launches += 1
         e1.record(stream)
-        decode_fn(state.out, s.q, state.k_cache, state.v_cache, s.block_tables, s.context_lens,
-                  cfg.softmax_scale, max_context_len=s.max_context_len, partition_size=P,
-                  workspace=state.workspace, device_status=state.status)
+        _decode(pkv, state, s, s.q, s.block_tables, s.context_lens, s.plan_device, P)
         n = pkv.last_decode_launches()
         decode_launches.append(n)
         engine_used = pkv.last_decode_engine()
@@ -239,8 +236,8 @@ def run_native(args):
     bytes_step, bytes_dec, seqs = 0, 0, 0
     for s, n in zip(steps[args.warmup:], decode_launches):
         if shared:
-            ab = algorithmic_bytes(cfg, s.host, w.num_seqs, out_bytes=out_bytes,
-                                   shared_partition=P or 256)
+            expected = s.plan.host[8:8 + w.num_seqs]
+            ab = algorithmic_bytes(cfg, s.host, w.num_seqs, out_bytes=out_bytes, partials=expected)
         else:
             Pp = _split_partition(P, s.max_context_len, n)
             ab = algorithmic_bytes(cfg, s.host, w.num_seqs, split_partition=Pp, out_bytes=out_bytes)
@@ -257,8 +254,7 @@ def run_native(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(state, steps[args.warmup:], host_inputs[args.warmup:], P, flush, bytes_step,
-                      decode_fn)
+        e2e = run_e2e(state, steps[args.warmup:], host_inputs[args.warmup:], P, flush, bytes_step)
 
     if rank == 0:
         line = {
@@ -278,7 +274,7 @@ def run_native(args):
             "seq_steps_per_s": round(seqs_all / t_max, 1),
             "pct_of_peak": round(100 * value / peak, 2),
             "roofline": {"bound": "hbm",
-                         "kernel": ("pa_plan_kernel+pa_shared_kernel+pa_merge_kernel" if shared else
+                         "kernel": ("pa_cascade_kernel" if shared else
                                     "pa_decode_kernel" + ("+pa_merge_kernel" if decode_launches[0] == 2 else "")),
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": peak_kind,
@@ -293,6 +289,22 @@ def run_native(args):
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def _decode(pkv, state, s, q, bt, cl, plan_dev, P):
+    """The step's attention call: the shared-prefix entry point when the step
+    carries a plan, the per-sequence one otherwise."""
+    cfg = state.cfg
+    if s.plan is not None:
+        pkv.paged_attention_decode_shared(state.out, q, state.k_cache, state.v_cache, bt, cl,
+                                          cfg.softmax_scale, s.plan, plan_dev,
+                                          max_context_len=s.max_context_len,
+                                          workspace=state.workspace, device_status=state.status)
+    else:
+        pkv.paged_attention_decode(state.out, q, state.k_cache, state.v_cache, bt, cl,
+                                   cfg.softmax_scale, max_context_len=s.max_context_len,
+                                   partition_size=P, workspace=state.workspace,
+                                   device_status=state.status)
 
 
 def _flush_l2(buf):
@@ -349,7 +361,7 @@ def traffic_for(cfg, algo_bytes):
     return int(e["traffic_per_algorithmic_byte"] * algo_bytes)
 
 
-def run_e2e(state, steps, host_inputs, P, flush, bytes_step, decode_fn):
+def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
     """Same step, inputs from pinned host memory, output read back, all timed."""
     import paged_kv_cache_311_gb300 as pkv
     cfg = state.cfg
@@ -361,6 +373,8 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step, decode_fn):
              ("q", "key", "value", "slot_mapping", "block_tables", "context_lens")}
         if s.cow_pairs is not None:
             d["cow_pairs"] = s.cow_pairs.cpu().pin_memory()
+        if s.plan is not None:
+            d["plan"] = torch.from_numpy(s.plan.host).pin_memory()
         pinned.append(d)
     dev_bufs = {k: torch.empty_like(getattr(steps[0], k)) for k in
                 ("q", "slot_mapping", "context_lens")}
@@ -388,10 +402,12 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step, decode_fn):
             cp = torch.empty(hp["cow_pairs"].shape, dtype=torch.int64, device=dev)
             cp.copy_(hp["cow_pairs"], non_blocking=True)
             pkv.copy_blocks([state.k_cache], [state.v_cache], cp, device_status=state.status)
+        plan_dev = None
+        if "plan" in hp:
+            plan_dev = torch.empty(hp["plan"].shape, dtype=torch.int32, device=dev)
+            plan_dev.copy_(hp["plan"], non_blocking=True)
         pkv.reshape_and_cache(key, val, state.k_cache, state.v_cache, sm, device_status=state.status)
-        decode_fn(state.out, q, state.k_cache, state.v_cache, bt, cl, cfg.softmax_scale,
-                  max_context_len=s.max_context_len, partition_size=P,
-                  workspace=state.workspace, device_status=state.status)
+        _decode(pkv, state, s, q, bt, cl, plan_dev, P)
         out_host.copy_(state.out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()

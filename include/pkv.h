@@ -114,21 +114,58 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
                                uint32_t *device_status, void *stream);
 
 /*
- * paged_attention_decode_shared -- the same attention as
- * pkv_paged_attention_decode, for batches in which runs of consecutive
- * sequences share leading physical blocks (parallel sampling, beam search, a
- * common system prompt: "Advanced Features", KV-Cache Sharing and Prefix
- * Caching).  A planning kernel finds the runs by comparing block ids; the
- * shared blocks of a group of up to 24 / (num_heads / num_kv_heads)
- * sequences are then read once and feed every member's query heads, and each
- * member's own tail is read separately.  Results equal the per-sequence path
- * up to fp32 rounding order.
+ * plan_shared_prefix -- HOST planner of the shared-prefix (cascade) decode:
+ * sequences forked from one prompt (parallel sampling, beam search, a common
+ * system prompt; "Advanced Features", KV-Cache Sharing and Prefix Caching)
+ * point their tables at the same physical blocks for the shared part.  The
+ * planner finds runs of consecutive sequences whose block tables start with
+ * the same block ids, groups them (at most 24 / G sequences per group, G =
+ * num_heads / num_kv_heads) and cuts the attention into work items: each
+ * partition of a group's shared prefix once for all members' query heads,
+ * and every member's own tail.
  *
- * Arguments as for pkv_paged_attention_decode, except: partition_size 0 means
- * 256 tokens (a multiple of 32 and of block_size otherwise); the split path
- * always runs, with pkv_paged_attention_shared_workspace_bytes(...) bytes of
- * workspace; kv_dtype must be PKV_F16 or PKV_BF16 (fp32 caches:
- * PKV_EUNSUPPORTED).  Enqueues three kernels (plan, attention, merge).
+ *   block_tables, context_lens  HOST copies of the arrays the decode call
+ *              will get on the device (same layout as for decode)
+ *   partition_size  tokens per work item (0 = 256; a multiple of 32 and of
+ *              block_size)
+ *   plan       HOST int32 buffer of plan_capacity_ints entries; receives the
+ *              plan (opaque apart from plan[0] = number of items and plan[1] =
+ *              partial slots per (sequence, head)); copy it to the device and
+ *              pass it to pkv_paged_attention_decode_shared
+ *   plan_ints  out: entries the plan needs
+ *   workspace_bytes  out: workspace the decode call needs for this plan
+ * Returns PKV_EWORKSPACE (after filling both outputs) when plan is NULL or
+ * too small; pkv_shared_plan_max_ints bounds the size in advance.
+ */
+int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                           int max_blocks_per_seq, int block_size, int num_heads,
+                           int num_kv_heads, int head_dim, int max_context_len,
+                           int partition_size, int32_t *plan, size_t plan_capacity_ints,
+                           size_t *plan_ints, size_t *workspace_bytes);
+
+/* Upper bound of plan_ints for these sizes. */
+size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, int max_context_len,
+                                int partition_size);
+
+/*
+ * paged_attention_decode_shared -- the same attention as
+ * pkv_paged_attention_decode, following a plan from pkv_plan_shared_prefix:
+ * one CTA per (kv head, work item) reads each shared block once for all the
+ * query heads of its group; the CTA that completes a sequence merges its
+ * partials (log-sum-exp) and writes its output.  Results equal the
+ * per-sequence path up to fp32 rounding order.
+ *
+ * Arguments as for pkv_paged_attention_decode, plus:
+ *   plan       DEVICE copy of the plan (4-byte aligned, writable: the call
+ *              counts arrivals in it and leaves those counters at zero again,
+ *              so the same device plan serves any number of calls with the
+ *              same tables and lengths, e.g. every layer of a step)
+ *   num_items, slots  plan[0] and plan[1]
+ *   workspace  at least the planner's workspace_bytes
+ * The device checks that the members of every group hold the same block ids
+ * over the shared part (PKV_DEV_BAD_BLOCK and zero rows otherwise).
+ * kv_dtype must be PKV_F16 or PKV_BF16 (fp32 caches: PKV_EUNSUPPORTED).
+ * Enqueues one kernel.
  */
 int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, const void *k_cache,
                                       const void *v_cache, int kv_dtype,
@@ -136,12 +173,9 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
                                       const int32_t *context_lens, int num_seqs, int num_heads,
                                       int num_kv_heads, int head_dim, int block_size,
                                       int64_t num_blocks, int max_context_len, float scale,
-                                      int partition_size, void *workspace, size_t workspace_bytes,
-                                      uint32_t *device_status, void *stream);
-
-/* Workspace bytes pkv_paged_attention_decode_shared needs for these sizes. */
-size_t pkv_paged_attention_shared_workspace_bytes(int num_seqs, int num_heads, int max_context_len,
-                                                  int head_dim, int partition_size);
+                                      int32_t *plan, int num_items, int slots, void *workspace,
+                                      size_t workspace_bytes, uint32_t *device_status,
+                                      void *stream);
 
 /*
  * reshape_and_cache -- write each new token's key/value rows into its slot

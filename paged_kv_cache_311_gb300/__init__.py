@@ -26,7 +26,7 @@ from .build import library_path
 __all__ = [
     "PkvError", "load_library", "paged_attention_decode", "reshape_and_cache", "copy_blocks",
     "paged_attention_workspace_bytes", "status_string", "last_decode_launches",
-    "paged_attention_decode_shared", "paged_attention_shared_workspace_bytes",
+    "paged_attention_decode_shared", "plan_shared_prefix", "SharedPrefixPlan",
     "set_decode_engine", "last_decode_engine",
     "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "HEADER_PATH",
 ]
@@ -64,10 +64,16 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_paged_attention_decode.argtypes = [vp, i32, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
                                              i32, i32, i64, i32, f32, i32, vp, u64, vp, vp]
     L.pkv_paged_attention_decode.restype = i32
-    L.pkv_paged_attention_decode_shared.argtypes = list(L.pkv_paged_attention_decode.argtypes)
+    L.pkv_paged_attention_decode_shared.argtypes = [vp, i32, vp, vp, vp, i32, vp, i32, vp, i32,
+                                                    i32, i32, i32, i32, i64, i32, f32, vp, i32,
+                                                    i32, vp, u64, vp, vp]
     L.pkv_paged_attention_decode_shared.restype = i32
-    L.pkv_paged_attention_shared_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
-    L.pkv_paged_attention_shared_workspace_bytes.restype = u64
+    L.pkv_plan_shared_prefix.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, u64,
+                                         ctypes.POINTER(ctypes.c_size_t),
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    L.pkv_plan_shared_prefix.restype = i32
+    L.pkv_shared_plan_max_ints.argtypes = [i32, i32, i32, i32, i32]
+    L.pkv_shared_plan_max_ints.restype = u64
     L.pkv_reshape_and_cache.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, vp, vp]
     L.pkv_reshape_and_cache.restype = i32
     L.pkv_copy_blocks.argtypes = [vp, vp, i32, vp, i32, u64, i64, vp, vp]
@@ -185,40 +191,80 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     return out
 
 
-def paged_attention_shared_workspace_bytes(num_seqs: int, num_heads: int, max_context_len: int,
-                                           head_dim: int, partition_size: int = 0) -> int:
-    return int(load_library().pkv_paged_attention_shared_workspace_bytes(
-        num_seqs, num_heads, max_context_len, head_dim, partition_size))
+class SharedPrefixPlan:
+    """A host-made plan of the shared-prefix decode (see plan_shared_prefix).
+
+    host: the int32 plan; num_items, slots, workspace_bytes: its sizes.
+    to(device) gives the device copy the decode call takes (its arrival
+    counters return to zero after every call, so one device copy serves every
+    call with the same tables and lengths)."""
+
+    def __init__(self, host, num_items: int, slots: int, workspace_bytes: int):
+        self.host = host
+        self.num_items = int(num_items)
+        self.slots = int(slots)
+        self.workspace_bytes = int(workspace_bytes)
+
+    def to(self, device) -> torch.Tensor:
+        return torch.from_numpy(self.host).to(device)
+
+
+def plan_shared_prefix(block_tables, context_lens, num_heads: int, num_kv_heads: int,
+                       head_dim: int, block_size: int, max_context_len: Optional[int] = None,
+                       partition_size: int = 0) -> SharedPrefixPlan:
+    """Host planner: groups consecutive sequences whose block tables start
+    with the same block ids and cuts the attention into work items.
+    block_tables, context_lens: host int32 arrays (numpy or CPU tensors)."""
+    import numpy as np
+    bt = np.ascontiguousarray(np.asarray(block_tables), dtype=np.int32)
+    cl = np.ascontiguousarray(np.asarray(context_lens), dtype=np.int32)
+    B, MB = bt.shape
+    if max_context_len is None:
+        max_context_len = int(cl.max()) if B else 0
+    L = load_library()
+    cap = int(L.pkv_shared_plan_max_ints(B, num_heads, num_kv_heads, max_context_len,
+                                          partition_size))
+    plan = np.zeros(max(cap, 16), dtype=np.int32)
+    n_ints, ws = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    rc = L.pkv_plan_shared_prefix(bt.ctypes.data, cl.ctypes.data, B, MB, block_size, num_heads,
+                                  num_kv_heads, head_dim, max_context_len, partition_size,
+                                  plan.ctypes.data, plan.size, ctypes.byref(n_ints), ctypes.byref(ws))
+    _check(rc, "pkv_plan_shared_prefix")
+    plan = plan[: n_ints.value].copy()
+    return SharedPrefixPlan(plan, plan[0], plan[1], ws.value)
 
 
 def paged_attention_decode_shared(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                                   v_cache: torch.Tensor, block_tables: torch.Tensor,
-                                  context_lens: torch.Tensor, scale: float, *,
-                                  max_context_len: Optional[int] = None, partition_size: int = 0,
+                                  context_lens: torch.Tensor, scale: float, plan: SharedPrefixPlan,
+                                  plan_device: torch.Tensor, *,
+                                  max_context_len: Optional[int] = None,
                                   workspace: Optional[torch.Tensor] = None,
                                   device_status: Optional[torch.Tensor] = None,
-                                  stream=None) -> torch.Tensor:
-    """As paged_attention_decode, reading blocks that runs of consecutive
-    sequences share (same leading block ids) once for the whole run."""
-    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, workspace, device_status)
+                                  stream=None, **_unused) -> torch.Tensor:
+    """As paged_attention_decode, reading the blocks that a plan's groups
+    share once for all their members' query heads."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, plan_device, workspace,
+               device_status)
     B, H, D = q.shape
     NB, Hk, bs, D2 = k_cache.shape
     if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, H, D):
         raise ValueError("shape mismatch")
     if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
         raise ValueError("q, k_cache and v_cache must share a dtype")
-    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
-        raise ValueError("block_tables and context_lens must be int32")
+    if (block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or
+            plan_device.dtype != torch.int32):
+        raise ValueError("block_tables, context_lens and the plan must be int32")
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0
     if workspace is None:
-        nbytes = paged_attention_shared_workspace_bytes(B, H, max_context_len, D, partition_size)
-        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(plan.workspace_bytes, 16), dtype=torch.uint8, device=q.device)
     rc = load_library().pkv_paged_attention_decode_shared(
         _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[k_cache.dtype],
         _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), B, H, Hk, D, bs, NB,
-        int(max_context_len), float(scale), int(partition_size), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(device_status), _stream(stream))
+        int(max_context_len), float(scale), _ptr(plan_device), plan.num_items, plan.slots,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_status),
+        _stream(stream))
     _check(rc, "pkv_paged_attention_decode_shared")
     return out
 

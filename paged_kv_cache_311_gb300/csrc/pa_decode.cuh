@@ -60,12 +60,6 @@ struct DecodeParams {
     int out_dtype;
     int split;           // nonzero: write partials to the workspace
     float qscale;        // softmax scale * log2(e)
-    // shared-prefix path (null / 0 otherwise)
-    const int32_t *seq_shared;  // tokens each sequence shares with its group
-    const int32_t *seq_members; // group size for group leaders, else 0
-    int np_prefix;              // workspace slots reserved for shared-prefix partials
-    const int2 *items;          // planned work: (sequence, slot)
-    const int *num_items;
 };
 
 enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2 };
@@ -407,7 +401,9 @@ struct TcEngine {
         }
     }
 
-    __device__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, int lane)
+    // Rows outside [row_lo, row_hi) ignore the tile (their state is unchanged).
+    __device__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, int lane, int row_lo = 0,
+                         int row_hi = 1 << 30)
     {
         // ---- S^T (16 tokens x 8 query rows per n-tile) = K q^T, as two
         // independent accumulation chains (even / odd k-steps)
@@ -444,17 +440,21 @@ struct TcEngine {
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const float x0 = ok0 ? s[nt][j] * qscale : -INFINITY;
-                const float x1 = ok1 ? s[nt][2 + j] * qscale : -INFINITY;
+                const int row = 8 * nt + 2 * c + j;
+                const bool live = row >= row_lo && row < row_hi;
+                const float x0 = (ok0 && live) ? s[nt][j] * qscale : -INFINITY;
+                const float x1 = (ok1 && live) ? s[nt][2 + j] * qscale : -INFINITY;
                 float tm = fmaxf(x0, x1);
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
                 tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
                 const float mn = fmaxf(m[nt][j], tm);
-                alpha[nt][j] = exp2f(m[nt][j] - mn);
+                // a row with no token yet keeps max -inf: nothing to rescale or add
+                const bool none = mn == -INFINITY;
+                alpha[nt][j] = none ? 1.f : exp2f(m[nt][j] - mn);
                 grew |= mn != m[nt][j];
-                p0[nt][j] = exp2f(x0 - mn);
-                p1[nt][j] = exp2f(x1 - mn);
+                p0[nt][j] = none ? 0.f : exp2f(x0 - mn);
+                p1[nt][j] = none ? 0.f : exp2f(x1 - mn);
                 lsum[nt][j] = lsum[nt][j] * alpha[nt][j] + p0[nt][j] + p1[nt][j];
                 m[nt][j] = mn;
             }

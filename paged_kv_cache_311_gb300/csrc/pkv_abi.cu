@@ -9,7 +9,7 @@
 
 #include "../../include/pkv.h"
 #include "cache_ops.cuh"
-#include "pa_plan.cuh"
+#include "cascade_plan.h"
 #include "pkv_host.cuh"
 
 namespace pkv {
@@ -82,28 +82,6 @@ SplitLayout split_layout(long long seqs, long long heads, long long np, long lon
     s.ml_bytes = (size_t)(seqs * heads * np * 2) * sizeof(float);
     s.acc_off = (s.ml_bytes + 255) & ~size_t(255);
     s.total = s.acc_off + (size_t)(seqs * heads * np * head_dim) * sizeof(float);
-    return s;
-}
-
-constexpr int kSharedPartition = 256;   // default partition of the shared-prefix path
-
-struct SharedLayout {
-    size_t items_off, count_off, ml_off, acc_off, total;
-};
-
-// Shared-prefix workspace: four int32 arrays of num_seqs (shared length, group
-// size, two planning scratch arrays), the work list (one int2 per (sequence,
-// slot), at most num_seqs * slots) and its count, then the split partials
-// with slots = 2 * ceil(max_context_len / P) per (sequence, head).
-SharedLayout shared_layout(long long seqs, long long heads, long long slots, long long head_dim)
-{
-    SharedLayout s;
-    s.items_off = ((size_t)(4 * seqs) * sizeof(int32_t) + 15) & ~size_t(15);
-    s.count_off = s.items_off + (size_t)(seqs * slots) * 2 * sizeof(int32_t);
-    s.ml_off = (s.count_off + sizeof(int32_t) + 255) & ~size_t(255);
-    const size_t ml = (size_t)(seqs * heads * slots * 2) * sizeof(float);
-    s.acc_off = s.ml_off + ((ml + 255) & ~size_t(255));
-    s.total = s.acc_off + (size_t)(seqs * heads * slots * head_dim) * sizeof(float);
     return s;
 }
 
@@ -271,11 +249,6 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     p.out_dtype = out_dtype;
     p.split = np > 1;
     p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax via exp2
-    p.seq_shared = nullptr;
-    p.seq_members = nullptr;
-    p.np_prefix = 0;
-    p.items = nullptr;
-    p.num_items = nullptr;
     if (p.split) {
         const SplitLayout s = split_layout(num_seqs, num_heads, np, head_dim);
         if (!workspace || workspace_bytes < s.total || !aligned16(workspace))
@@ -290,7 +263,8 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     a.group = group;
     a.engine = g_engine_override.load(std::memory_order_relaxed);
     a.shared = false;
-    a.sms = 0;
+    a.plan = nullptr;
+    a.num_items = 0;
     a.stream = static_cast<cudaStream_t>(stream);
     int engine_used = 0;
     a.engine_used = &engine_used;
@@ -308,26 +282,15 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     return rc;
 }
 
-size_t pkv_paged_attention_shared_workspace_bytes(int num_seqs, int num_heads, int max_context_len,
-                                                  int head_dim, int partition_size)
-{
-    if (num_seqs <= 0 || num_heads <= 0 || max_context_len < 0 || head_dim <= 0 ||
-        partition_size < 0)
-        return 0;
-    const int P = partition_size > 0 ? partition_size : kSharedPartition;
-    const long long maxL = max_context_len > 0 ? max_context_len : 1;
-    const long long np = (maxL + P - 1) / P;
-    return shared_layout(num_seqs, num_heads, 2 * np, head_dim).total;
-}
-
 int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, const void *k_cache,
                                       const void *v_cache, int kv_dtype,
                                       const int32_t *block_tables, int max_blocks_per_seq,
                                       const int32_t *context_lens, int num_seqs, int num_heads,
                                       int num_kv_heads, int head_dim, int block_size,
                                       int64_t num_blocks, int max_context_len, float scale,
-                                      int partition_size, void *workspace, size_t workspace_bytes,
-                                      uint32_t *device_status, void *stream)
+                                      int32_t *plan, int num_items, int slots, void *workspace,
+                                      size_t workspace_bytes, uint32_t *device_status,
+                                      void *stream)
 {
     g_last_decode_launches = 0;
     g_last_decode_engine = 0;
@@ -336,47 +299,29 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     if (!valid_dtype(out_dtype) || !valid_dtype(kv_dtype))
         return PKV_EINVAL;
     if (num_blocks <= 0 || num_blocks > INT32_MAX || max_blocks_per_seq <= 0 || block_size <= 0 ||
-        max_context_len < 0 || partition_size < 0 || !std::isfinite(scale))
+        max_context_len < 0 || !std::isfinite(scale))
         return PKV_EINVAL;
     if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size)
         return PKV_EINVAL;
     if (num_seqs == 0)
         return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !plan)
         return PKV_EINVAL;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(plan) & 3u))
+        return PKV_EINVAL;
+    if (num_items <= 0 || num_items > 65535 || slots <= 0)
         return PKV_EINVAL;
     const int group = num_heads / num_kv_heads;
     if (kv_dtype == PKV_F32 || (head_dim != 64 && head_dim != 128) ||
         (block_size != 8 && block_size != 16 && block_size != 32) ||
         (group != 1 && group != 2 && group != 4 && group != 8))
         return PKV_EUNSUPPORTED;
-    if (num_kv_heads > 65535 || num_seqs > 65535)
+    if (num_kv_heads > 65535)
         return PKV_EUNSUPPORTED;
-    const int P = partition_size > 0 ? partition_size : kSharedPartition;
-    if (P % kTileAlign || P % block_size || P / block_size > kTableCap)
-        return PKV_EINVAL;
-    const int maxL = max_context_len > 0 ? max_context_len : 1;
-    const long long np = (maxL + (long long)P - 1) / P;
-    if (2 * np > 65535)
-        return PKV_EUNSUPPORTED;
-    const SharedLayout lay = shared_layout(num_seqs, num_heads, 2 * np, head_dim);
+    const SplitLayout lay = split_layout(num_seqs, num_heads, slots, head_dim);
     if (!workspace || workspace_bytes < lay.total || !aligned16(workspace))
         return PKV_EWORKSPACE;
-
-    int32_t *ints = static_cast<int32_t *>(workspace);
-    int32_t *seq_shared = ints, *members = ints + num_seqs, *sp = ints + 2 * num_seqs,
-            *run_start = ints + 3 * num_seqs;
-    const int align = block_size > kTileAlign ? block_size : kTileAlign;
-    const int max_members = 8 * kSharedNT / group;
-    int2 *items = reinterpret_cast<int2 *>(static_cast<char *>(workspace) + lay.items_off);
-    int *num_items = reinterpret_cast<int *>(static_cast<char *>(workspace) + lay.count_off);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    pa_plan_kernel<<<1, 1024, 0, st>>>(block_tables, context_lens, num_seqs, max_blocks_per_seq,
-                                       block_size, max_context_len, max_members, align, P, (int)np,
-                                       seq_shared, members, sp, run_start, items, num_items);
-    if (cudaGetLastError() != cudaSuccess)
-        return PKV_ECUDA;
 
     DecodeLaunch a;
     DecodeParams &p = a.p;
@@ -384,7 +329,7 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     p.q = q;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
-    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.ml_off);
+    p.ws_ml = static_cast<float *>(workspace);
     p.ws_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.acc_off);
     p.status = device_status;
     p.num_blocks = num_blocks;
@@ -393,16 +338,11 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     p.num_kv_heads = num_kv_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.max_context_len = max_context_len;
-    p.partition_size = P;
-    p.num_partitions = (int)(2 * np);
+    p.partition_size = 0;
+    p.num_partitions = slots;
     p.out_dtype = out_dtype;
     p.split = 1;
     p.qscale = scale * 1.4426950408889634f;
-    p.seq_shared = seq_shared;
-    p.seq_members = members;
-    p.np_prefix = (int)np;
-    p.items = items;
-    p.num_items = num_items;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.head_dim = head_dim;
@@ -410,13 +350,14 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     a.group = group;
     a.engine = kEngineTensorCore;
     a.shared = true;
-    a.sms = sm_count(current_device());
-    a.stream = st;
+    a.plan = plan;
+    a.num_items = num_items;
+    a.stream = static_cast<cudaStream_t>(stream);
     int engine_used = 0;
     a.engine_used = &engine_used;
     const int rc = kv_dtype == PKV_F16 ? launch_decode_f16(a) : launch_decode_bf16(a);
     if (rc == PKV_OK) {
-        g_last_decode_launches = 3;
+        g_last_decode_launches = 1;
         g_last_decode_engine = engine_used;
     }
     return rc;

@@ -5,7 +5,8 @@
 
 #include <cuda_runtime.h>
 
-#include "pa_shared.cuh"
+#include "pa_cascade.cuh"
+#include "pa_merge.cuh"
 
 namespace pkv {
 
@@ -17,8 +18,9 @@ struct DecodeLaunch {
     int block_size;
     int group;
     int engine;          // Engine: kEngineAuto, kEngineCudaCore or kEngineTensorCore
-    bool shared;         // shared-prefix path (pa_shared_kernel)
-    int sms;             // SM count of the device (shared-prefix grid)
+    bool shared;         // shared-prefix (cascade) path
+    int32_t *plan;       // device copy of the cascade plan
+    int num_items;
     cudaStream_t stream;
     int *engine_used;    // out: the engine that ran
 };
@@ -68,40 +70,29 @@ int run_decode(const DecodeLaunch &a)
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
-// Shared-prefix path: up to 8 * kSharedNT query rows per CTA (all heads of the
-// members of one group), then the log-sum-exp merge.  pa_plan_kernel has run
-// on the same stream before this.
-constexpr int kSharedNT = 3;
-
+// Shared-prefix (cascade) path: one CTA per (kv head, planned item).
 template <typename T, int D, int BS, int G>
-int run_shared(const DecodeLaunch &a)
+int run_cascade(const DecodeLaunch &a)
 {
-    using Sh = DecodeShape<T, D, BS, G, true>;
+    using CC = CascadeCfg<T, D, BS, G>;
     const DecodeParams &p = a.p;
     alignas(64) CUtensorMap tmk;
     alignas(64) CUtensorMap tmv;
     int rc = encode_kv_map(&tmk, a.k_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
-                           p.num_blocks, Sh::box_rows);
+                           p.num_blocks, CC::C::BOX_ROWS);
     if (rc)
         return rc;
     rc = encode_kv_map(&tmv, a.v_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
-                       p.num_blocks, Sh::box_rows);
+                       p.num_blocks, CC::C::BOX_ROWS);
     if (rc)
         return rc;
     static unsigned long long done = 0;
-    auto kern = pa_shared_kernel<T, D, BS, G, kSharedNT>;
-    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), Sh::smem, &done);
+    auto kern = pa_cascade_kernel<T, D, BS, G>;
+    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), CC::SMEM_BYTES, &done);
     if (rc)
         return rc;
-    // persistent: about two CTAs per SM over all kv heads, never more than
-    // the largest possible work list
-    long long gx = (2LL * (a.sms > 0 ? a.sms : 152) + p.num_kv_heads - 1) / p.num_kv_heads;
-    const long long max_items = (long long)p.num_seqs * p.num_partitions;
-    if (gx > max_items)
-        gx = max_items;
-    dim3 grid((unsigned)(gx > 0 ? gx : 1), p.num_kv_heads, 1);
-    kern<<<grid, Sh::threads, Sh::smem, a.stream>>>(p, tmk, tmv);
-    pa_merge_kernel<D><<<(unsigned)(((long long)p.num_seqs * p.num_heads + 3) / 4), 128, 0, a.stream>>>(p);
+    dim3 grid(p.num_kv_heads, a.num_items, 1);
+    kern<<<grid, CC::C::NW * 32, CC::SMEM_BYTES, a.stream>>>(p, tmk, tmv, a.plan);
     if (a.engine_used)
         *a.engine_used = kEngineTensorCore;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
@@ -116,7 +107,7 @@ int run_engine(const DecodeLaunch &a)
 {
     if constexpr (Elem<T>::bytes == 2) {
         if (a.shared)
-            return run_shared<T, D, BS, G>(a);
+            return run_cascade<T, D, BS, G>(a);
         const bool tc = a.engine != kEngineCudaCore;
         if (tc)
             return run_decode<T, D, BS, G, true>(a);

@@ -77,19 +77,30 @@ def shared_case(seed, *, dtype="bf16", H=8, Hk=2, D=128, bs=16, groups=((300, (5
                 scale=float(np.float32(1.0 / np.sqrt(D))))
 
 
-def run_shared(case, P=0, out_dtype=torch.float32, tables=None):
+def run_shared(case, P=0, out_dtype=torch.float32, tables=None, plan_tables=None, calls=1):
+    """Plans on the host from plan_tables (default: the tables given to the
+    device), then runs the shared-prefix decode `calls` times with the same
+    device plan; returns the last output and the OR of the status words."""
     import paged_kv_cache_311_gb300 as pkv
     dev = "cuda"
     q, kc, vc = case["q"].to(dev), case["k_cache"].to(dev), case["v_cache"].to(dev)
-    bt = torch.as_tensor(case["block_tables"] if tables is None else tables).to(dev)
+    dev_tables = case["block_tables"] if tables is None else tables
+    bt = torch.as_tensor(dev_tables).to(dev)
     cl = torch.as_tensor(case["context_lens"]).to(dev)
-    out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=dev)
+    B, H, D = q.shape
+    mcl = int(max(case["context_lens"].max(), 1))
+    plan = pkv.plan_shared_prefix(dev_tables if plan_tables is None else plan_tables,
+                                  case["context_lens"], H, case["Hk"], D, case["bs"], mcl, P)
+    plan_dev = plan.to(dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    pkv.paged_attention_decode_shared(out, q, kc, vc, bt, cl, case["scale"],
-                                      max_context_len=int(max(case["context_lens"].max(), 1)),
-                                      partition_size=P, device_status=st)
-    torch.cuda.synchronize()
-    assert pkv.last_decode_launches() == 3
+    out = None
+    for _ in range(calls):
+        out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=dev)
+        pkv.paged_attention_decode_shared(out, q, kc, vc, bt, cl, case["scale"], plan, plan_dev,
+                                          max_context_len=mcl, device_status=st)
+        torch.cuda.synchronize()
+        assert pkv.last_decode_launches() == 1
+    assert int(plan_dev[8 + B:8 + B + B * case["Hk"]].abs().sum().item()) == 0  # counters reset
     return out.double().cpu().numpy(), int(st.item())
 
 
@@ -120,6 +131,29 @@ def test_shared_prefix_matches_oracle(dtype, G, bs):
         assert gst == 0
         err = max_err(got, ref)
         assert err <= TOL[dtype], f"P={P} max err {err}"
+
+
+def test_same_device_plan_serves_repeated_calls():
+    case = shared_case(11, dtype="bf16", H=16, Hk=4, D=128, bs=16, groups=GROUPS)
+    once, _ = run_shared(case, calls=1)
+    thrice, st = run_shared(case, calls=3)
+    assert st == 0
+    np.testing.assert_array_equal(once, thrice)
+
+
+def test_group_whose_tables_disagree_is_rejected_on_the_device():
+    """The plan says the first group shares its prompt, but on the device one
+    member's table points elsewhere in the shared part: that group's rows are
+    zeroed and PKV_DEV_BAD_BLOCK is raised; the other groups are unaffected."""
+    import paged_kv_cache_311_gb300 as pkv
+    case = shared_case(12, dtype="bf16", H=8, Hk=2, D=128, bs=16, groups=GROUPS[:2])
+    t = case["block_tables"].copy()
+    t[2, 0] = case["k_cache"].shape[0] - 1          # member 2 of group 0, first prompt block
+    got, st = run_shared(case, tables=t, plan_tables=case["block_tables"])
+    assert st & pkv.DEV_BAD_BLOCK
+    assert not got[:4].any()
+    ref, _ = oracle_out(case)
+    assert max_err(got[4:], ref[4:]) <= TOL["bf16"]
 
 
 def test_shared_prefix_head_dim_64_and_half_output():

@@ -87,18 +87,3 @@ def test_long_context_pool_is_about_60_gb():
         pool_bytes = w.num_blocks * 2 * cfg.with_(block_size=bs).block_bytes
         assert 59e9 < pool_bytes <= 60e9
         assert w.init_lens.min() >= 16384 and w.init_lens.max() <= 32768
-
-
-def test_shared_lengths_mirror_on_forked_prompts():
-    """Forked samples share their prompt's full blocks (rounded down to 32
-    tokens); the partial last prompt block is copied, so it is not shared."""
-    from workloads.runner import shared_lengths
-    cfg = get("shared_prefix_bf16")
-    w = PagedDecodeWorkload(cfg, 31103, total_steps=2)
-    inp = w.next_step()
-    S = shared_lengths(inp, w.num_seqs, cfg.block_size, cfg.group)
-    for p, lp in enumerate(w.prompt_lens):
-        want = ((int(lp) // cfg.block_size) * cfg.block_size // 32) * 32
-        np.testing.assert_array_equal(S[p * 6:(p + 1) * 6], want)
-    plain = PagedDecodeWorkload(get("llama7b_f16"), 1, total_steps=1).next_step()
-    assert not shared_lengths(plain, 64, 16, 1).any()

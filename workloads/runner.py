@@ -32,6 +32,8 @@ class DeviceStep:
     cow_pairs: Optional[torch.Tensor]
     max_context_len: int
     host: StepInputs
+    plan: object = None                     # SharedPrefixPlan (shared-prefix workloads)
+    plan_device: Optional[torch.Tensor] = None
 
 
 class DeviceState:
@@ -54,98 +56,81 @@ class DeviceState:
                                device=self.device)
         self.workspace: Optional[torch.Tensor] = None
 
-    def to_device(self, inp: StepInputs, value_device=None) -> DeviceStep:
+    def to_device(self, inp: StepInputs, value_device=None, shared: Optional[bool] = None,
+                  partition_size: int = 0) -> DeviceStep:
         cfg, dev = self.cfg, self.device
+        if shared is None:
+            shared = cfg.kind == "shared_prefix"
         q, k, v = step_values(cfg, self.seed, inp, self.w.num_seqs,
                               device=value_device if value_device is not None else dev)
         pairs = None
         if inp.cow_pairs.shape[0]:
             pairs = torch.as_tensor(inp.cow_pairs, dtype=torch.int64).to(dev)
+        plan = plan_dev = None
+        if shared:
+            import paged_kv_cache_311_gb300 as pkv
+            plan = pkv.plan_shared_prefix(inp.block_tables, inp.context_lens, cfg.num_heads,
+                                          cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
+                                          inp.max_context_len, partition_size)
+            plan_dev = plan.to(dev)
         return DeviceStep(
             step=inp.step, q=q.to(dev), key=k.to(dev), value=v.to(dev),
             slot_mapping=torch.as_tensor(inp.slot_mapping).to(dev),
             block_tables=torch.as_tensor(inp.block_tables).to(dev),
             context_lens=torch.as_tensor(inp.context_lens).to(dev),
-            cow_pairs=pairs, max_context_len=inp.max_context_len, host=inp)
+            cow_pairs=pairs, max_context_len=inp.max_context_len, host=inp,
+            plan=plan, plan_device=plan_dev)
 
     def ensure_workspace(self, max_context_len: int, partition_size: int,
-                         shared: bool = False) -> None:
+                         plan=None) -> None:
         import paged_kv_cache_311_gb300 as pkv
-        fn = pkv.paged_attention_shared_workspace_bytes if shared else pkv.paged_attention_workspace_bytes
-        need = fn(self.w.num_seqs, self.cfg.num_heads, max_context_len, self.cfg.head_dim,
-                  partition_size)
+        if plan is not None:
+            need = plan.workspace_bytes
+        else:
+            need = pkv.paged_attention_workspace_bytes(self.w.num_seqs, self.cfg.num_heads,
+                                                       max_context_len, self.cfg.head_dim,
+                                                       partition_size)
         if need and (self.workspace is None or self.workspace.numel() < need):
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
 
     def run_step(self, s: DeviceStep, partition_size: Optional[int] = None,
-                 out: Optional[torch.Tensor] = None, stream=None,
-                 shared: Optional[bool] = None) -> torch.Tensor:
+                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         """copy_blocks (if the step has copy-on-write pairs), reshape_and_cache,
-        then paged attention -- all on the current stream.  Attention takes the
-        shared-prefix entry point for workloads whose sequences are forked
-        from common prompts (``shared`` overrides)."""
+        then paged attention -- all on the current stream.  A step that
+        carries a shared-prefix plan takes the shared-prefix entry point."""
         import paged_kv_cache_311_gb300 as pkv
         cfg = self.cfg
         P = cfg.partition_size if partition_size is None else partition_size
-        if shared is None:
-            shared = cfg.kind == "shared_prefix"
         out = self.out if out is None else out
         if s.cow_pairs is not None:
             pkv.copy_blocks([self.k_cache], [self.v_cache], s.cow_pairs,
                             device_status=self.status, stream=stream)
         pkv.reshape_and_cache(s.key, s.value, self.k_cache, self.v_cache, s.slot_mapping,
                               device_status=self.status, stream=stream)
-        self.ensure_workspace(s.max_context_len, P, shared)
-        fn = pkv.paged_attention_decode_shared if shared else pkv.paged_attention_decode
-        fn(out, s.q, self.k_cache, self.v_cache, s.block_tables, s.context_lens, cfg.softmax_scale,
-           max_context_len=s.max_context_len, partition_size=P, workspace=self.workspace,
-           device_status=self.status, stream=stream)
+        self.ensure_workspace(s.max_context_len, P, s.plan)
+        if s.plan is not None:
+            pkv.paged_attention_decode_shared(
+                out, s.q, self.k_cache, self.v_cache, s.block_tables, s.context_lens,
+                cfg.softmax_scale, s.plan, s.plan_device, max_context_len=s.max_context_len,
+                workspace=self.workspace, device_status=self.status, stream=stream)
+        else:
+            pkv.paged_attention_decode(
+                out, s.q, self.k_cache, self.v_cache, s.block_tables, s.context_lens,
+                cfg.softmax_scale, max_context_len=s.max_context_len, partition_size=P,
+                workspace=self.workspace, device_status=self.status, stream=stream)
         return out
 
 
-def shared_lengths(inp: StepInputs, num_seqs: int, block_size: int, group: int,
-                   rows_per_cta: int = 24) -> np.ndarray:
-    """Host mirror of the library's grouping for the shared-prefix path (used
-    only to count that path's partials): runs of consecutive sequences whose
-    tables start with the same block ids, cut into groups of rows_per_cta /
-    group sequences; a group shares the shortest common prefix of its
-    members, rounded down to max(block_size, 32) tokens."""
-    align = max(block_size, 32)
-    lens = inp.context_lens[:num_seqs].astype(np.int64)
-    sp = np.zeros(num_seqs, dtype=np.int64)
-    for s in range(1, num_seqs):
-        la, lb = int(lens[s - 1]), int(lens[s])
-        if la <= 0 or lb <= 0:
-            continue
-        n = min(-(-la // block_size), -(-lb // block_size))
-        a, b = inp.block_tables[s - 1][:n], inp.block_tables[s][:n]
-        neq = np.nonzero(a != b)[0]
-        c = int(neq[0]) if neq.size else n
-        sp[s] = (min(c * block_size, la, lb) // align) * align
-    shared = np.zeros(num_seqs, dtype=np.int64)
-    mm = rows_per_cta // group
-    run = 0
-    for s in range(num_seqs):
-        if s == 0 or sp[s] == 0:
-            run = s
-        if (s - run) % mm == 0:
-            cnt, S = 1, None
-            while cnt < mm and s + cnt < num_seqs and sp[s + cnt] > 0 and (s + cnt - run) % mm != 0:
-                S = sp[s + cnt] if S is None else min(S, sp[s + cnt])
-                cnt += 1
-            shared[s:s + cnt] = S if (cnt >= 2 and S) else 0
-    return shared
-
-
 def algorithmic_bytes(cfg: DecodeConfig, inp: StepInputs, num_seqs: int, split_partition: int = 0,
-                      out_bytes: int = 4, shared_partition: int = 0) -> dict:
+                      out_bytes: int = 4, partials=None) -> dict:
     """Bytes one decode step must move at minimum.
 
     attention: every distinct (physical block, kv head, row) slot that some
     sequence reads (logical position < its context length), K and V, once;
     plus q, the output, the block-table entries and context lengths; plus the
     split path's workspace round trip when it runs (one partial per head and
-    non-empty partition of split_partition tokens).  Shared prefix blocks
+    non-empty partition of split_partition tokens, or `partials[s]` per head
+    of sequence s for a shared-prefix plan).  Shared prefix blocks
     count once.  scatter: the new tokens' K/V read once and written once.
     copy: each copied block read once and written once."""
     bs, e = cfg.block_size, cfg.elem_bytes
@@ -175,12 +160,8 @@ def algorithmic_bytes(cfg: DecodeConfig, inp: StepInputs, num_seqs: int, split_p
     if split_partition:
         parts = sum(-(-int(L) // split_partition) for L in inp.context_lens[:num_seqs])
         ws = 2 * cfg.num_heads * parts * (cfg.head_dim + 2) * 4
-    if shared_partition:
-        S = shared_lengths(inp, num_seqs, bs, cfg.group)
-        P = shared_partition
-        parts = sum(-(-int(sh) // P) + -(-(int(L) - int(sh)) // P)
-                    for sh, L in zip(S, inp.context_lens[:num_seqs]))
-        ws = 2 * cfg.num_heads * parts * (cfg.head_dim + 2) * 4
+    if partials is not None:
+        ws = 2 * cfg.num_heads * int(np.sum(partials)) * (cfg.head_dim + 2) * 4
     attn = kv + qo + meta + ws
     T = inp.num_tokens
     scatter = 2 * 2 * T * cfg.num_kv_heads * row + T * 8
