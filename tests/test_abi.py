@@ -105,14 +105,3 @@ def test_cache_ops_host_validation(lib):
 def test_package_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         pkv.load_library(str(tmp_path / "missing.so"))
-
-
-def test_shared_workspace_bytes(lib):
-    B, H, L, D = 192, 32, 1100, 128
-    slots = 2 * -(-L // 256)
-    items_off = ((4 * B * 4 + 15) // 16) * 16
-    count_off = items_off + B * slots * 8
-    ml_off = ((count_off + 4 + 255) // 256) * 256
-    ml = B * H * slots * 2 * 4
-    expect = ml_off + ((ml + 255) // 256) * 256 + B * H * slots * D * 4
-    assert pkv.paged_attention_shared_workspace_bytes(B, H, L, D, 0) == expect
