@@ -127,7 +127,7 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
  *   block_tables, context_lens  HOST copies of the arrays the decode call
  *              will get on the device (same layout as for decode)
  *   partition_size  tokens per work item (0 = 256; a multiple of 32 and of
- *              block_size)
+ *              block_size, at most 128 * block_size; PKV_EINVAL otherwise)
  *   plan       HOST int32 buffer of plan_capacity_ints entries; receives the
  *              plan (opaque apart from plan[0] = number of items and plan[1] =
  *              partial slots per (sequence, head)); copy it to the device and

@@ -33,6 +33,9 @@ constexpr int kTag = 0x43564b50;    // "PKVC"
 constexpr int kNT = 3;              // n-tiles of 8 query rows per item
 constexpr int kMaxRows = 8 * kNT;   // query rows per item
 constexpr int kItemHead = 4;
+// Block-table entries one item may address (all segments together): the
+// planner keeps items within it and the kernel stages that many.
+constexpr int kTableCap = 256;
 constexpr int kSegInts = 5;
 
 constexpr int max_segments(int group) { return 1 + kMaxRows / group; }

@@ -18,23 +18,37 @@
 
 #include "cascade_plan.h"
 #include "pa_decode.cuh"
+#include "pa_merge.cuh"
 
 namespace pkv {
 
 template <typename T, int D, int BS, int G>
 struct CascadeCfg {
     using C = DecodeCfg<T, D, BS, G, true>;
+    using Engine = TcEngine<T, D, BS, G, plan::kNT, true>;
+    static constexpr int NW = C::NW, S = C::S;
     static constexpr int MAXSEG = plan::max_segments(G);
     static constexpr int ITEM_INTS = plan::item_ints(G);
-    static constexpr int OFF_EXTRA = (C::SMEM_USED + 15) / 16 * 16;
-    // item copy, first tile / table offset / bad flag per segment, merge flags
+    static constexpr int TABLE_CAP = plan::kTableCap;
+    // ring | barriers | flag | q rows | block table | item copy, first tile /
+    // table offset / bad flag per segment, merge flags | per-row warp weights
+    static constexpr int OFF_STAGES = 0;
+    static constexpr int OFF_BAR = C::STAGES_BYTES;
+    static constexpr int OFF_FLAG = OFF_BAR + NW * S * 8;
+    static constexpr int OFF_Q = OFF_FLAG + 16;
+    static constexpr int OFF_TABLE = OFF_Q + Engine::q_smem_bytes;
+    static constexpr int OFF_EXTRA = OFF_TABLE + TABLE_CAP * 4;
     static constexpr int EXTRA_INTS = ITEM_INTS + 3 * (MAXSEG + 1) + plan::kMaxRows;
-    static constexpr int SMEM_BYTES = OFF_EXTRA + EXTRA_INTS * 4 + 1024;
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static constexpr int OFF_WTS = (OFF_EXTRA + EXTRA_INTS * 4 + 15) / 16 * 16;
+    static constexpr int SMEM_USED = OFF_WTS + plan::kMaxRows * NW * 4;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
+    // three CTAs (12 warps) per SM: 228 KB of shared memory, 1 KB per CTA reserved
+    static_assert(3 * (SMEM_BYTES + 1024) <= 228 * 1024, "three CTAs per SM");
+    static_assert(OFF_Q % 16 == 0 && Engine::QROWB % 16 == 0, "q rows: 16-byte pieces");
 };
 
 template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 3)
 pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int32_t *plan_buf)
 {
@@ -61,7 +75,7 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     int32_t *flag = segbad + CC::MAXSEG + 1; // merge flags per member
     for (int i = tid; i < CC::ITEM_INTS; i += blockDim.x)
         it[i] = src[i];
-    init_rings<C>(smem);
+    init_rings<CC>(smem);
     __syncthreads();
 
     const int seq0 = it[0], nrows = it[1], slot = it[2], nseg = it[3];
@@ -93,11 +107,11 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
 
     // ---- stage every segment's block-table slice; the members of a shared
     // prefix must hold the same block ids there (checked)
-    int32_t *table_s = reinterpret_cast<int32_t *>(smem + C::OFF_TABLE);
-    uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + C::OFF_FLAG);
+    int32_t *table_s = reinterpret_cast<int32_t *>(smem + CC::OFF_TABLE);
+    uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + CC::OFF_FLAG);
     // A bad block id (or a member whose shared blocks differ) invalidates the
     // rows of its segment only; block 0 is loaded in its place.
-    const bool invalid_item = tab[nseg] > C::TABLE_CAP;
+    const bool invalid_item = tab[nseg] > CC::TABLE_CAP;
     for (int k = 0; k < nseg && !invalid_item; ++k) {
         const int tseq = seg[5 * k], j0 = seg[5 * k + 1] / BS;
         const int nb = tab[k + 1] - tab[k];
@@ -116,6 +130,7 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             table_s[tab[k] + i] = (b < 0 || (int64_t)b >= p.num_blocks) ? 0 : b;
         }
     }
+    CC::Engine::stage_q_rows(p, smem + CC::OFF_Q, w);
     if (tid == 0) {
         *cta_flag = 0;
         prefetch_tensormap(&tmk);
@@ -137,8 +152,10 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     };
 
     const int total = first[nseg];
-    auto seg_of = [&](int tile) {
-        int k = 0;
+    // Segment of a tile.  Each warp asks for its tiles in increasing order,
+    // separately for issuing and for consuming, so each keeps a cursor that
+    // only moves forward.
+    auto seg_of = [&](int tile, int &k) {
         while (k + 1 < nseg && first[k + 1] <= tile)
             ++k;
         return k;
@@ -150,9 +167,10 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     if (!invalid_item) {
         const int my_n = warp < total ? (total - 1 - warp) / NW + 1 : 0;
         uint8_t *stages = smem + C::OFF_STAGES + warp * S * C::STAGE_BYTES;
-        uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR) + warp * S;
+        uint64_t *bars = reinterpret_cast<uint64_t *>(smem + CC::OFF_BAR) + warp * S;
+        int k_issue = 0, k_use = 0;
         auto issue = [&](int i, int st) {
-            const int tile = warp + i * NW, k = seg_of(tile);
+            const int tile = warp + i * NW, k = seg_of(tile, k_issue);
             const int tb = seg[5 * k + 1], te = seg[5 * k + 2], j0 = tb / BS;
             const int t0 = tb + (tile - first[k]) * TILE;
             uint8_t *kd = stages + st * C::STAGE_BYTES;
@@ -170,8 +188,8 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             for (int i = 0; i < (my_n < S ? my_n : S); ++i)
                 issue(i, i);
 
-        TcEngine<T, D, BS, G, NT> eng;
-        eng.init(p, smem, w, warp, lane);
+        typename CC::Engine eng;
+        eng.init(p, smem + CC::OFF_Q, w, warp, lane);
         int failed_at = -1;
         for (int i = 0; i < my_n; ++i) {
             const int st = i % S;
@@ -179,7 +197,7 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                 failed_at = i;
                 break;
             }
-            const int tile = warp + i * NW, k = seg_of(tile);
+            const int tile = warp + i * NW, k = seg_of(tile, k_use);
             const int t0 = seg[5 * k + 1] + (tile - first[k]) * TILE;
             const int nvalid = min(TILE, seg[5 * k + 2] - t0);
             const uint32_t kbase = smem_u32(stages + st * C::STAGE_BYTES);
@@ -204,75 +222,73 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     }
     __syncthreads();
 
-    // ---- this item's partial of every row
+    // ---- this item's partial of every row (other CTAs read it through L2):
+    // one thread per row folds the warps' (max, sum) and keeps the warps'
+    // weights in shared memory; then float4 pieces of the accumulators.
+    float *wts = reinterpret_cast<float *>(smem + CC::OFF_WTS);   // [RS][NW]
     const bool failed_all = invalid_item || *reinterpret_cast<volatile uint32_t *>(cta_flag) != 0;
-    for (int idx = tid; idx < nrows * D; idx += blockDim.x) {
-        const int r = idx / D, d = idx % D;
+    if (tid < nrows) {
+        const int r = tid;
         const bool failed = failed_all || row_bad(r);
-        float M = -INFINITY, num = 0.f, den = 0.f;
-        if (!failed) {
+        float M = -INFINITY, den = 0.f, f[NW];
 #pragma unroll
-            for (int k = 0; k < NW; ++k)
-                M = fmaxf(M, mw[k * RS + r]);
+        for (int k = 0; k < NW; ++k)
+            M = fmaxf(M, failed ? -INFINITY : mw[k * RS + r]);
 #pragma unroll
-            for (int k = 0; k < NW; ++k) {
-                const float mk = mw[k * RS + r];
-                if (mk != -INFINITY) {
-                    const float f = exp2f(mk - M);
-                    num += f * aw[(k * RS + r) * D + d];
-                    den += f * lw[k * RS + r];
-                }
-            }
+        for (int k = 0; k < NW; ++k) {
+            const float mk = failed ? -INFINITY : mw[k * RS + r];
+            f[k] = mk == -INFINITY ? 0.f : exp2f(mk - M);
+            den += f[k] * lw[k * RS + r];
+            wts[r * NW + k] = f[k];
         }
         const int64_t base = row_head(p, w, G, r) * slots + slot;
-        p.ws_acc[base * D + d] = num;
-        if (d == 0) {
-            p.ws_ml[base * 2 + 0] = failed ? -INFINITY : M;
-            p.ws_ml[base * 2 + 1] = failed ? -1.f : den;
+        __stcg(reinterpret_cast<float2 *>(p.ws_ml) + base,
+               make_float2(failed ? -INFINITY : M, failed ? -1.f : den));
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nrows * (D / 4); idx += blockDim.x) {
+        const int r = idx / (D / 4), d4 = idx % (D / 4);
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const float f = wts[r * NW + k];
+            const float4 a = reinterpret_cast<const float4 *>(aw + (k * RS + r) * D)[d4];
+            num.x += f * a.x;
+            num.y += f * a.y;
+            num.z += f * a.z;
+            num.w += f * a.w;
         }
+        const int64_t base = row_head(p, w, G, r) * slots + slot;
+        __stcg(reinterpret_cast<float4 *>(p.ws_acc + base * D) + d4, num);
     }
 
-    // ---- arrivals: the CTA that completes a sequence merges it
+    // ---- arrivals: the CTA that delivers a sequence's last partial merges
+    // it.  One thread per member: release this CTA's partials, count, and
+    // acquire the others' before the merge reads them.
     __threadfence();
     __syncthreads();
-    if (tid == 0) {
+    if (tid < nmem) {
+        const int seq = seq0 + tid;
+        int32_t *ctr = &counters[(int64_t)seq * Hk + kvh];
         __threadfence();
-        for (int m = 0; m < nmem; ++m) {
-            const int seq = seq0 + m;
-            const int old = atomicAdd(&counters[(int64_t)seq * Hk + kvh], 1);
-            flag[m] = old == expected[seq] - 1;
-        }
+        const int old = atomicAdd(ctr, 1);
+        const bool last = old == expected[seq] - 1;
+        flag[tid] = last;
+        if (last)
+            *ctr = 0;  // every arrival is in: ready for the next call
         __threadfence();
     }
     __syncthreads();
+    // the (member, head) rows of the completed members, spread over the warps
+    int pr = 0;
     for (int m = 0; m < nmem; ++m) {
         if (!flag[m])
             continue;
-        const int seq = seq0 + m, n = expected[seq];
-        for (int idx = tid; idx < G * D; idx += blockDim.x) {
-            const int h = idx / D, d = idx % D;
-            const int64_t sh = (int64_t)seq * p.num_heads + kvh * G + h;
-            const float *ml = p.ws_ml + sh * slots * 2;
-            const float *acc = p.ws_acc + sh * slots * D + d;
-            float M = -INFINITY;
-            bool inval = false;
-            for (int k = 0; k < n; ++k) {
-                M = fmaxf(M, __ldcg(ml + 2 * k));
-                inval |= __ldcg(ml + 2 * k + 1) < 0.f;
-            }
-            float num = 0.f, den = 0.f;
-            for (int k = 0; k < n && !inval; ++k) {
-                const float mk = __ldcg(ml + 2 * k);
-                if (mk != -INFINITY) {
-                    const float f = exp2f(mk - M);
-                    den += f * __ldcg(ml + 2 * k + 1);
-                    num += f * __ldcg(acc + (int64_t)k * D);
-                }
-            }
-            store_out(p.out, p.out_dtype, sh * D + d, (inval || den == 0.f) ? 0.f : num / den);
-        }
-        if (tid == 0)
-            counters[(int64_t)seq * Hk + kvh] = 0;  // ready for the next call
+        const int seq = seq0 + m;
+        for (int h = 0; h < G; ++h, ++pr)
+            if (pr % NW == warp)
+                merge_partials<D>(p, (int64_t)seq * p.num_heads + kvh * G + h, expected[seq], slots,
+                                  false, lane);
     }
 }
 

@@ -343,13 +343,22 @@ struct CcEngine {
 
 // ---------------------------------------------------------- tensor cores
 // NT n-tiles of 8 query rows each (NT = 1 for one sequence's G <= 8 heads).
-template <typename T, int D, int BS, int G, int NT = 1>
+// QS: the q^T B-fragments are read from a shared-memory copy of the rows
+// (q_smem_bytes, staged by the caller before init) with ldmatrix at every
+// tile instead of being held in registers -- 16 * NT registers fewer, for
+// the multi-row (shared-prefix) CTAs.
+template <typename T, int D, int BS, int G, int NT = 1, bool QS = false>
 struct TcEngine {
     using C = DecodeCfg<T, D, BS, G, true>;
     static constexpr int KS = D / 16;   // k-steps of QK = m-tiles of PV
     static constexpr int RS = 8 * NT;   // row stride of the merge scratch
+    // shared-memory q rows: D 16-bit values padded by 16 bytes, so the 8
+    // row addresses of one ldmatrix fall in distinct bank groups
+    static constexpr int QROWB = D * 2 + 16;
+    static constexpr int q_smem_bytes = RS * QROWB;
 
-    uint32_t qf[KS][NT][2];   // q^T B-fragments: row 8 nt + g, dims 16 ks + 2c (+8)
+    uint32_t qf[QS ? 1 : KS][NT][2];   // q^T B-fragments: row 8 nt + g, dims 16 ks + 2c (+8)
+    uint32_t qaddr;                    // QS: this lane's ldmatrix row address
     float o[KS][NT][4];       // O^T C-fragments: dims 16 mt + g (+8), rows 8 nt + 2c, +1
     float m[NT][2], lsum[NT][2];
     float qscale;
@@ -367,12 +376,30 @@ struct TcEngine {
         return (uint32_t)((k >> 2) * C::BOX_ROWS * 128);
     }
 
-    __device__ void init(const DecodeParams &p, uint8_t *, const CtaWork &w, int, int lane)
+    // Copies the CTA's query rows (rows >= nrows zero) into shared memory at
+    // `qs` for QS engines; all threads of the CTA take part, and a barrier
+    // must follow before init.
+    __device__ static void stage_q_rows(const DecodeParams &p, uint8_t *qs, const CtaWork &w)
+    {
+        constexpr int PCS = D * 2 / 16;   // 16-byte pieces per row
+        for (int i = threadIdx.x; i < RS * PCS; i += blockDim.x) {
+            const int r = i / PCS, pc = i % PCS;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < w.nrows)
+                v = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.q) +
+                                                    row_head(p, w, G, r) * D)[pc];
+            *reinterpret_cast<uint4 *>(qs + r * QROWB + pc * 16) = v;
+        }
+    }
+
+    __device__ void init(const DecodeParams &p, uint8_t *qs, const CtaWork &w, int, int lane)
     {
         g = lane >> 2;
         c = lane & 3;
         qscale = p.qscale;
         ntl = (w.nrows + 7) / 8;
+        if constexpr (QS)
+            qaddr = smem_u32(qs) + (lane & 7) * QROWB + (lane >> 3) * 16;
         {
             const int tk = (lane & 7) + ((lane >> 3) & 1) * 8, dk = lane >> 4;
             const int tv = (lane & 7) + (lane >> 4) * 8, dv = (lane >> 3) & 1;
@@ -390,8 +417,10 @@ struct TcEngine {
                 static_cast<const T *>(p.q) + row_head(p, w, G, live ? r : 0) * D);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                qf[ks][nt][0] = live ? qp[(16 * ks + 2 * c) / 2] : 0u;
-                qf[ks][nt][1] = live ? qp[(16 * ks + 2 * c + 8) / 2] : 0u;
+                if constexpr (!QS) {
+                    qf[ks][nt][0] = live ? qp[(16 * ks + 2 * c) / 2] : 0u;
+                    qf[ks][nt][1] = live ? qp[(16 * ks + 2 * c + 8) / 2] : 0u;
+                }
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     o[ks][nt][j] = 0.f;
@@ -401,10 +430,12 @@ struct TcEngine {
         }
     }
 
-    // Rows outside [row_lo, row_hi) ignore the tile (their state is unchanged).
+    // Rows outside [row_lo, row_hi) ignore the tile (their state is unchanged);
+    // n-tiles without such a row issue no MMA.
     __device__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, int lane, int row_lo = 0,
                          int row_hi = 1 << 30)
     {
+        const int nlo = row_lo >> 3, nhi = min(ntl, (row_hi + 7) >> 3);
         // ---- S^T (16 tokens x 8 query rows per n-tile) = K q^T, as two
         // independent accumulation chains (even / odd k-steps)
         float s[NT][4], s2[NT][4];
@@ -413,18 +444,37 @@ struct TcEngine {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 s[nt][j] = s2[nt][j] = 0.f;
+        if constexpr (QS) {
+            // one ldmatrix.x4 of q gives the fragments of k-steps 2 kp, 2 kp + 1;
+            // with several n-tiles, their chains are the independent ones
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a[4];
-            ldsm_x4(kbase + chunk_off(ks) + koff[ks & 3], a);
+            for (int kp = 0; kp < KS / 2; ++kp) {
+                uint32_t a0[4], a1[4];
+                ldsm_x4(kbase + chunk_off(2 * kp) + koff[(2 * kp) & 3], a0);
+                ldsm_x4(kbase + chunk_off(2 * kp + 1) + koff[(2 * kp + 1) & 3], a1);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                if (nt < ntl) {
-                    if (ks & 1)
-                        Mma<T>::run(s2[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
-                    else
-                        Mma<T>::run(s[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
-                }
+                for (int nt = 0; nt < NT; ++nt)
+                    if (nt >= nlo && nt < nhi) {
+                        uint32_t b[4];
+                        ldsm_x4(qaddr + nt * 8 * QROWB + kp * 64, b);
+                        Mma<T>::run(s[nt], a0, b[0], b[1]);
+                        Mma<T>::run(NT > 1 ? s[nt] : s2[nt], a1, b[2], b[3]);
+                    }
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(kbase + chunk_off(ks) + koff[ks & 3], a);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    if (nt >= nlo && nt < nhi) {
+                        if (ks & 1)
+                            Mma<T>::run(s2[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+                        else
+                            Mma<T>::run(s[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+                    }
+            }
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -507,7 +557,7 @@ struct TcEngine {
                 ldsm_x4_trans(vbase + chunk_off(mt) + voff[mt & 3], a);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    if (nt < ntl) {
+                    if (nt >= nlo && nt < nhi) {
                         Mma<T>::run(o[mt][nt], a, bh[nt][0], bh[nt][1]);
                         Mma<T>::run(o[mt][nt], a, bl[nt][0], bl[nt][1]);
                     }

@@ -16,7 +16,6 @@
 namespace {
 
 constexpr int kDefaultPartition = 256;
-constexpr int kTableCap = 1024;  // block-table entries one CTA stages
 
 struct Seg {
     int table_seq, tok_begin, tok_end, row_lo, row_hi;
