@@ -341,6 +341,20 @@ def _split_partition(P, max_len, launches):
     return P if P > 0 else 512
 
 
+KERNEL_SOURCES = ("pa_decode.cuh", "pa_cascade.cuh", "pa_merge.cuh", "pkv_device.cuh", "cascade_plan.h")
+
+
+def kernel_source_sha():
+    """sha256 prefix over the decode kernels' sources: a traffic figure taken
+    on other sources is stale."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_311_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(cfg, algo_bytes):
     """Per-launch DRAM traffic (read + write) of the decode kernel, from the
     committed ncu capture's traffic / algorithmic-bytes ratio scaled to this
@@ -352,10 +366,8 @@ def traffic_for(cfg, algo_bytes):
             d = json.load(f)
     except Exception:
         return None
-    import hashlib
-    src = os.path.join(ROOT, "paged_kv_cache_311_gb300", "csrc", "pa_decode.cuh")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     e = d.get(cfg.name)
+    h = kernel_source_sha()
     if not e or e.get("source_sha") != h:
         return None
     return int(e["traffic_per_algorithmic_byte"] * algo_bytes)

@@ -126,8 +126,13 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
  *
  *   block_tables, context_lens  HOST copies of the arrays the decode call
  *              will get on the device (same layout as for decode)
- *   partition_size  tokens per work item (0 = 256; a multiple of 32 and of
- *              block_size, at most 128 * block_size; PKV_EINVAL otherwise)
+ *   partition_size  target tokens per work item: a multiple of 32 and of
+ *              block_size, at most 64 * block_size (PKV_EINVAL otherwise); 0 =
+ *              automatic: about one item per resident CTA slot of the current
+ *              GPU (three per SM) over all kv heads, at least 64 tokens.
+ *              Each group's shared prefix is cut into nearly equal pieces;
+ *              members' short tails join the group's last piece, longer ones
+ *              become items of their own.
  *   plan       HOST int32 buffer of plan_capacity_ints entries; receives the
  *              plan (opaque apart from plan[0] = number of items and plan[1] =
  *              partial slots per (sequence, head)); copy it to the device and
@@ -162,8 +167,11 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
  *              same tables and lengths, e.g. every layer of a step)
  *   num_items, slots  plan[0] and plan[1]
  *   workspace  at least the planner's workspace_bytes
- * The device checks that the members of every group hold the same block ids
- * over the shared part (PKV_DEV_BAD_BLOCK and zero rows otherwise).
+ * The device checks the plan against the device arrays: every table the
+ * plan reads must hold the block ids the plan was made with (PKV_DEV_BAD_BLOCK
+ * and zero rows for the rows they serve otherwise), and every sequence's
+ * context length must be the one it was made for (PKV_DEV_BAD_CONTEXT_LEN and
+ * zero rows otherwise).
  * kv_dtype must be PKV_F16 or PKV_BF16 (fp32 caches: PKV_EUNSUPPORTED).
  * Enqueues one kernel.
  */

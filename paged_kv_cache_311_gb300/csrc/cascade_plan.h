@@ -5,13 +5,20 @@
 //   header[kHeader]            see the H_* indices
 //   expected[num_seqs]         partials each sequence receives (one per item
 //                              that holds its rows)
+//   lens[num_seqs]             the context lengths the plan was made for (the
+//                              kernel rejects a sequence whose device length
+//                              differs)
 //   counters[num_seqs * Hk]    arrivals per (sequence, kv head); zero between
 //                              calls (the kernel that merges resets them)
 //   items[num_items][item_ints]
-// An item is {seq0, nrows, slot, nseg, then nseg segments of {table_seq,
-// tok_begin, tok_end, row_lo, row_hi}}: query rows r < nrows are head
-// r % G of sequence seq0 + r / G; segment k covers tokens [tok_begin,
-// tok_end) addressed by table_seq's block table, for rows [row_lo, row_hi).
+// An item is {seq0, nrows, slot, nseg, then max_segments segments of
+// {table_seq, tok_begin, tok_end, row_lo, row_hi}, then kTableCap block ids}:
+// query rows r < nrows are head r % G of sequence seq0 + r / G; segment k
+// covers tokens [tok_begin, tok_end) addressed by table_seq's block table,
+// for rows [row_lo, row_hi).  The block ids are the physical blocks of the
+// segments' logical blocks [tok_begin / bs, ceil(tok_end / bs)), segment
+// after segment, as the host tables held them when the plan was made (the
+// kernel starts its loads from them and checks the device tables meanwhile).
 // nseg == 0 marks a sequence with an empty or invalid context (zero output).
 #pragma once
 
@@ -26,7 +33,7 @@ enum : int {
     H_NUM_KV_HEADS = 3,
     H_ITEM_INTS = 4,
     H_MAX_SEG = 5,
-    H_PARTITION = 6,
+    H_PARTITION = 6,     // target tokens per item the plan was cut with
     H_TAG = 7,
 };
 constexpr int kTag = 0x43564b50;    // "PKVC"
@@ -39,7 +46,8 @@ constexpr int kTableCap = 256;
 constexpr int kSegInts = 5;
 
 constexpr int max_segments(int group) { return 1 + kMaxRows / group; }
-constexpr int item_ints(int group) { return kItemHead + kSegInts * max_segments(group); }
+constexpr int item_ids_offset(int group) { return kItemHead + kSegInts * max_segments(group); }
+constexpr int item_ints(int group) { return item_ids_offset(group) + kTableCap; }
 
 }  // namespace plan
 }  // namespace pkv

@@ -182,6 +182,7 @@ struct CcEngine {
     static constexpr int PCL = 8 / LPT;        // pieces per 128-byte chunk per lane
     static constexpr int DPL = D / 32;         // PV dims per lane
     static constexpr int VBYTES = DPL * C::E;  // PV bytes per lane per row
+    static constexpr int AWS = D;              // accumulator row stride of the merge scratch
 
     float m[G], lsum[G];
     float2 acc[G][DPL / 2];
@@ -352,6 +353,9 @@ struct TcEngine {
     using C = DecodeCfg<T, D, BS, G, true>;
     static constexpr int KS = D / 16;   // k-steps of QK = m-tiles of PV
     static constexpr int RS = 8 * NT;   // row stride of the merge scratch
+    // accumulator row stride of the merge scratch, in floats: padded so that
+    // the rows 2c, 2c + 1 of one store fall in distinct banks
+    static constexpr int AWS = D + 4;
     // shared-memory q rows: D 16-bit values padded by 16 bytes, so the 8
     // row addresses of one ldmatrix fall in distinct bank groups
     static constexpr int QROWB = D * 2 + 16;
@@ -377,18 +381,28 @@ struct TcEngine {
     }
 
     // Copies the CTA's query rows (rows >= nrows zero) into shared memory at
-    // `qs` for QS engines; all threads of the CTA take part, and a barrier
-    // must follow before init.
+    // `qs` for QS engines; all C::NW * 32 threads of the CTA take part, and a
+    // barrier must follow before init.
     __device__ static void stage_q_rows(const DecodeParams &p, uint8_t *qs, const CtaWork &w)
     {
+        // all loads first, then all stores: a store between two loads would
+        // keep the second load from issuing before the first returns
         constexpr int PCS = D * 2 / 16;   // 16-byte pieces per row
-        for (int i = threadIdx.x; i < RS * PCS; i += blockDim.x) {
-            const int r = i / PCS, pc = i % PCS;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < w.nrows)
-                v = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.q) +
-                                                    row_head(p, w, G, r) * D)[pc];
-            *reinterpret_cast<uint4 *>(qs + r * QROWB + pc * 16) = v;
+        constexpr int PER = (RS * PCS + C::NW * 32 - 1) / (C::NW * 32);
+        uint4 v[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int i = threadIdx.x + u * C::NW * 32, r = i / PCS;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < RS * PCS && r < w.nrows)
+                v[u] = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.q) +
+                                                       row_head(p, w, G, r) * D)[i % PCS];
+        }
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int i = threadIdx.x + u * C::NW * 32;
+            if (i < RS * PCS)
+                *reinterpret_cast<uint4 *>(qs + (i / PCS) * QROWB + (i % PCS) * 16) = v[u];
         }
     }
 
@@ -586,8 +600,8 @@ struct TcEngine {
                     }
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
-                        aw[(warp * RS + row) * D + 16 * mt + g] = o[mt][nt][j];
-                        aw[(warp * RS + row) * D + 16 * mt + g + 8] = o[mt][nt][2 + j];
+                        aw[(warp * RS + row) * AWS + 16 * mt + g] = o[mt][nt][j];
+                        aw[(warp * RS + row) * AWS + 16 * mt + g + 8] = o[mt][nt][2 + j];
                     }
                 }
             }
@@ -624,7 +638,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
     using Eng = typename std::conditional<TC, TcEngine<T, D, BS, G, NT>, CcEngine<T, D, BS, G>>::type;
     constexpr int NW = C::NW, S = C::S, TILE = C::TILE;
     constexpr int RS = TC ? 8 * NT : G;   // merge-scratch rows per warp
-    static_assert(NW * RS * (D + 2) * 4 <= C::STAGES_BYTES, "merge scratch fits in the ring");
+    static_assert(NW * RS * (Eng::AWS + 2) * 4 <= C::STAGES_BYTES, "merge scratch fits in the ring");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tok0 = w.tok0, tok_end = w.tok_end, kvh = w.kvh;
 
@@ -741,7 +755,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
             const float mk = mw[k * RS + r];
             if (mk != -INFINITY) {
                 const float f = exp2f(mk - M);
-                num += f * aw[(k * RS + r) * D + d];
+                num += f * aw[(k * RS + r) * Eng::AWS + d];
                 den += f * lw[k * RS + r];
             }
         }

@@ -64,7 +64,7 @@ int run_decode(const DecodeLaunch &a)
     dim3 grid(p.num_partitions, p.num_kv_heads, p.num_seqs);
     kern<<<grid, Sh::threads, Sh::smem, a.stream>>>(p, tmk, tmv);
     if (p.split)
-        pa_merge_kernel<D><<<(unsigned)(((long long)p.num_seqs * p.num_heads + 3) / 4), 128, 0, a.stream>>>(p);
+        pa_merge_kernel<D><<<(unsigned)(((long long)p.num_seqs * p.num_heads + 7) / 8), 128, 0, a.stream>>>(p);
     if (a.engine_used)
         *a.engine_used = TC ? kEngineTensorCore : kEngineCudaCore;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;

@@ -7,6 +7,7 @@
 // side re-checks on the device that the members of a group really share the
 // blocks it was told about.
 #include <algorithm>
+#include <cuda_runtime.h>
 #include <cstring>
 #include <vector>
 
@@ -15,7 +16,21 @@
 
 namespace {
 
-constexpr int kDefaultPartition = 256;
+// Smallest automatic item (tokens): below it the per-item fixed costs win.
+constexpr int kMinAutoTokens = 64;
+
+// SMs of the current device (the automatic cut targets three resident CTAs
+// per SM); 152, a GB300's count, when no device answers.
+int gpu_sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();   // leave no error behind for the next launch check
+        return 152;
+    }
+    return n;
+}
 
 struct Seg {
     int table_seq, tok_begin, tok_end, row_lo, row_hi;
@@ -50,9 +65,11 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
     const int G = num_heads / num_kv_heads;
     if (G > pkv::plan::kMaxRows)
         return 0;
-    const int P = partition_size > 0 ? partition_size : kDefaultPartition;
-    const long long per_seq = (max_context_len + P - 1) / P + 1;
-    return (size_t)pkv::plan::kHeader + (size_t)num_seqs + (size_t)num_seqs * num_kv_heads +
+    // items per sequence: its partitions of at least P (or kMinAutoTokens)
+    // tokens, one more for the rounding of a cut, one for a group's last item
+    const int P = partition_size > 0 ? partition_size : kMinAutoTokens;
+    const long long per_seq = (max_context_len + P - 1) / P + 2;
+    return (size_t)pkv::plan::kHeader + 2 * (size_t)num_seqs + (size_t)num_seqs * num_kv_heads +
            (size_t)(num_seqs * per_seq) * pkv::plan::item_ints(G);
 }
 
@@ -72,8 +89,8 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     const int G = num_heads / num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8)
         return PKV_EUNSUPPORTED;
-    const int P = partition_size > 0 ? partition_size : kDefaultPartition;
-    if (P % 32 || P % block_size || P / block_size > kTableCap / 2)
+    if (partition_size > 0 &&
+        (partition_size % 32 || partition_size % block_size || partition_size / block_size > kTableCap / 4))
         return PKV_EINVAL;
     const int B = num_seqs, MB = max_blocks_per_seq, bs = block_size;
     const int align = bs > 32 ? bs : 32;
@@ -98,59 +115,161 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         sp[s] = std::min(c * bs, std::min(la, lb)) / align * align;
     }
 
-    std::vector<Item> items;
-    std::vector<int> expected(B, 0);
-    auto add_partitions = [&](int seq, int tb, int te, int first_slot) {
-        int k = 0;
-        for (int t = tb; t < te; t += P, ++k) {
-            const int e = std::min(t + P, te);
-            items.push_back(Item{seq, G, first_slot + k, {Seg{seq, t, e, 0, G}}, (long long)(e - t),
-                                 blocks_between(t, e, bs)});
-        }
-        return k;
+    // groups: runs of up to max_members consecutive sequences that share S
+    // leading tokens (cnt == 1: a sequence on its own)
+    struct Group {
+        int s, cnt, S;
     };
-
+    std::vector<Group> groups;
+    long long total = 0;   // tokens to stream per kv head, shared ones once
     for (int s = 0; s < B;) {
         int cnt = 1, S = 0x7fffffff;
         while (cnt < max_members && s + cnt < B && sp[s + cnt] > 0) {
             S = std::min(S, sp[s + cnt]);
             ++cnt;
         }
-        if (cnt < 2) {                       // a sequence on its own
-            if (!len_ok(s)) {
-                items.push_back(Item{s, G, 0, {}, 0, 0});   // zero output
-            } else {
-                expected[s] = add_partitions(s, 0, context_lens[s], 0);
-            }
-            s += 1;
-            continue;
-        }
-        // a group [s, s + cnt) sharing S tokens
-        const int rows = cnt * G;
-        const int first_item = (int)items.size();
-        const int n_pre = (S + P - 1) / P;
-        for (int x = 0; x < n_pre; ++x) {
-            const int t = x * P, e = std::min(t + P, S);
-            items.push_back(Item{s, rows, x, {Seg{s, t, e, 0, rows}}, (long long)(e - t) * 3,
-                                 blocks_between(t, e, bs)});
-        }
-        for (int m = 0; m < cnt; ++m) {
-            const int seq = s + m, L = context_lens[seq];
-            int n_tail = 0;
-            if (L > S) {
-                Item &last = items[first_item + n_pre - 1];
-                const int need = blocks_between(S, L, bs);
-                if (L - S <= P && last.entries + need <= kTableCap) {
-                    last.segs.push_back(Seg{seq, S, L, m * G, (m + 1) * G});
-                    last.weight += L - S;
-                    last.entries += need;
-                } else {
-                    n_tail = add_partitions(seq, S, L, n_pre);
-                }
-            }
-            expected[seq] = n_pre + n_tail;
+        if (cnt < 2) {
+            groups.push_back(Group{s, 1, 0});
+            total += len_ok(s) ? context_lens[s] : 0;
+        } else {
+            groups.push_back(Group{s, cnt, S});
+            total += S;
+            for (int m = 0; m < cnt; ++m)
+                total += context_lens[s + m] - S;
         }
         s += cnt;
+    }
+
+    // A member's own tail costs whole 16-row loads; it joins its group's
+    // last item while that item stays within T tokens (and within half the
+    // block-id capacity), longer tails become items of their own.
+    auto tail_cost = [](int t) { return (t + 15) / 16 * 16; };
+    auto fold_tails = [&](const Group &g, int T, std::vector<char> *folded) {
+        long long F = 0;
+        int entries = 0;
+        for (int m = 0; m < g.cnt; ++m) {
+            const int t = context_lens[g.s + m] - g.S, need = blocks_between(g.S, g.S + t, bs);
+            const bool f = t > 0 && F + tail_cost(t) <= T && entries + need <= kTableCap / 2;
+            if (f) {
+                F += tail_cost(t);
+                entries += need;
+            }
+            if (folded)
+                (*folded)[m] = f;
+        }
+        return F;
+    };
+    // items per kv head that target T gives
+    auto count_items = [&](int T) {
+        long long n = 0;
+        for (const Group &g : groups) {
+            if (g.cnt == 1) {
+                n += len_ok(g.s) ? (context_lens[g.s] + T - 1) / T : 1;
+                continue;
+            }
+            std::vector<char> folded(g.cnt, 0);
+            const long long F = fold_tails(g, T, &folded);
+            n += std::max(1LL, (g.S + F + T - 1) / T);
+            for (int m = 0; m < g.cnt; ++m) {
+                const int t = context_lens[g.s + m] - g.S;
+                if (t > 0 && !folded[m])
+                    n += (t + T - 1) / T;
+            }
+        }
+        return n;
+    };
+
+    // Target tokens per item.  Automatic: the smallest T (a multiple of
+    // `align`, between kMinAutoTokens or 4 blocks and 64 blocks) whose items
+    // fit one CTA per resident slot of the GPU (three per SM) over all kv
+    // heads, so that the launch runs as one wave of items of at most T tokens.
+    int T = partition_size;
+    if (T == 0) {
+        const long long per_head = std::max(1LL, 3LL * gpu_sm_count() / num_kv_heads);
+        const int lo = (std::max(4 * bs, kMinAutoTokens) + align - 1) / align;
+        const int hi = (kTableCap / 4) * bs / align;
+        int a = lo, b = hi;                       // in units of align
+        while (a < b) {
+            const int mid = (a + b) / 2;
+            if (count_items(mid * align) <= per_head)
+                b = mid;
+            else
+                a = mid + 1;
+        }
+        T = a * align;
+    }
+
+    std::vector<Item> items;
+    std::vector<int> expected(B, 0);
+    // [tb, te) cut into n nearly equal pieces at multiples of `align`
+    auto cut = [&](int tb, int te, int n) {
+        std::vector<int> b{tb};
+        for (int i = 1; i < n; ++i) {
+            const int x = (int)((tb + (long long)(te - tb) * i / n) / align * align);
+            if (x > b.back() && x < te)
+                b.push_back(x);
+        }
+        b.push_back(te);
+        return b;
+    };
+    auto add_partitions = [&](int seq, int tb, int te, int first_slot) {
+        const std::vector<int> b = cut(tb, te, (te - tb + T - 1) / T);
+        for (size_t k = 0; k + 1 < b.size(); ++k)
+            items.push_back(Item{seq, G, first_slot + (int)k, {Seg{seq, b[k], b[k + 1], 0, G}},
+                                 (long long)(b[k + 1] - b[k]), blocks_between(b[k], b[k + 1], bs)});
+        return (int)b.size() - 1;
+    };
+
+    for (const Group &g : groups) {
+        const int s = g.s, cnt = g.cnt, S = g.S;
+        if (cnt == 1) {
+            if (!len_ok(s))
+                items.push_back(Item{s, G, 0, {}, 0, 0});   // zero output
+            else
+                expected[s] = add_partitions(s, 0, context_lens[s], 0);
+            continue;
+        }
+        // n_g items of at most about T tokens: the prefix cut into n_g - 1
+        // equal pieces plus the part that goes with the folded tails
+        const int rows = cnt * G;
+        std::vector<char> folded(cnt, 0);
+        const long long F = fold_tails(g, T, &folded);
+        int n_g = (int)std::max(1LL, (S + F + T - 1) / T);
+        int Sp = 0;
+        if (n_g > 1) {
+            const long long per = (S + F + n_g - 1) / n_g;
+            const long long Pl = std::min<long long>(S, std::max(0LL, per - F));
+            Sp = (int)((S - Pl) / align * align);
+            if (Sp <= 0)
+                n_g = 1, Sp = 0;
+        }
+        int n_pre = 0;
+        if (n_g > 1) {
+            const std::vector<int> b = cut(0, Sp, n_g - 1);
+            for (size_t k = 0; k + 1 < b.size(); ++k, ++n_pre)
+                items.push_back(Item{s, rows, n_pre, {Seg{s, b[k], b[k + 1], 0, rows}},
+                                     (long long)(b[k + 1] - b[k]), blocks_between(b[k], b[k + 1], bs)});
+        }
+        Item last{s, rows, n_pre, {}, 0, 0};
+        if (Sp < S) {
+            last.segs.push_back(Seg{s, Sp, S, 0, rows});
+            last.weight += S - Sp;
+            last.entries += blocks_between(Sp, S, bs);
+        }
+        for (int m = 0; m < cnt; ++m)
+            if (folded[m]) {
+                const int seq = s + m, L = context_lens[seq];
+                last.segs.push_back(Seg{seq, S, L, m * G, (m + 1) * G});
+                last.weight += L - S;
+                last.entries += blocks_between(S, L, bs);
+            }
+        items.push_back(last);
+        const int n_items = n_pre + 1;
+        for (int m = 0; m < cnt; ++m) {
+            const int seq = s + m, L = context_lens[seq];
+            const int n_tail = (L > S && !folded[m]) ? add_partitions(seq, S, L, n_items) : 0;
+            expected[seq] = n_items + n_tail;
+        }
     }
 
     std::stable_sort(items.begin(), items.end(),
@@ -159,7 +278,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     for (int s = 0; s < B; ++s)
         slots = std::max(slots, expected[s]);
     const int iints = item_ints(G);
-    const size_t need = (size_t)kHeader + B + (size_t)B * num_kv_heads + items.size() * iints;
+    const size_t need = (size_t)kHeader + 2 * (size_t)B + (size_t)B * num_kv_heads + items.size() * iints;
     if (plan_ints)
         *plan_ints = need;
     if (workspace_bytes)
@@ -169,6 +288,9 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     if (!plan || plan_capacity_ints < need)
         return PKV_EWORKSPACE;
 
+    for (const Item &it : items)
+        if (it.entries > kTableCap)   // cannot happen: items are cut to fit
+            return PKV_EUNSUPPORTED;
     std::memset(plan, 0, need * sizeof(int32_t));
     plan[H_NUM_ITEMS] = (int)items.size();
     plan[H_SLOTS] = slots;
@@ -176,15 +298,17 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     plan[H_NUM_KV_HEADS] = num_kv_heads;
     plan[H_ITEM_INTS] = iints;
     plan[H_MAX_SEG] = max_segments(G);
-    plan[H_PARTITION] = P;
+    plan[H_PARTITION] = T;
     plan[H_TAG] = kTag;
     std::copy(expected.begin(), expected.end(), plan + kHeader);
-    int32_t *dst = plan + kHeader + B + (size_t)B * num_kv_heads;
+    std::copy(context_lens, context_lens + B, plan + kHeader + B);
+    int32_t *dst = plan + kHeader + 2 * (size_t)B + (size_t)B * num_kv_heads;
     for (const Item &it : items) {
         dst[0] = it.seq0;
         dst[1] = it.nrows;
         dst[2] = it.slot;
         dst[3] = (int)it.segs.size();
+        int32_t *ids = dst + item_ids_offset(G);
         for (size_t k = 0; k < it.segs.size(); ++k) {
             const Seg &g = it.segs[k];
             int32_t *q = dst + kItemHead + kSegInts * k;
@@ -193,6 +317,9 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
             q[2] = g.tok_end;
             q[3] = g.row_lo;
             q[4] = g.row_hi;
+            const int32_t *row = block_tables + (long long)g.table_seq * MB;
+            for (int j = g.tok_begin / bs; j < (g.tok_end + bs - 1) / bs; ++j)
+                *ids++ = row[j];
         }
         dst += iints;
     }

@@ -77,10 +77,12 @@ def shared_case(seed, *, dtype="bf16", H=8, Hk=2, D=128, bs=16, groups=((300, (5
                 scale=float(np.float32(1.0 / np.sqrt(D))))
 
 
-def run_shared(case, P=0, out_dtype=torch.float32, tables=None, plan_tables=None, calls=1):
-    """Plans on the host from plan_tables (default: the tables given to the
-    device), then runs the shared-prefix decode `calls` times with the same
-    device plan; returns the last output and the OR of the status words."""
+def run_shared(case, P=0, out_dtype=torch.float32, tables=None, plan_tables=None, calls=1,
+               plan_lens=None):
+    """Plans on the host from plan_tables and plan_lens (default: the tables
+    and lengths given to the device), then runs the shared-prefix decode
+    `calls` times with the same device plan; returns the last output and the
+    OR of the status words."""
     import paged_kv_cache_311_gb300 as pkv
     dev = "cuda"
     q, kc, vc = case["q"].to(dev), case["k_cache"].to(dev), case["v_cache"].to(dev)
@@ -90,7 +92,8 @@ def run_shared(case, P=0, out_dtype=torch.float32, tables=None, plan_tables=None
     B, H, D = q.shape
     mcl = int(max(case["context_lens"].max(), 1))
     plan = pkv.plan_shared_prefix(dev_tables if plan_tables is None else plan_tables,
-                                  case["context_lens"], H, case["Hk"], D, case["bs"], mcl, P)
+                                  case["context_lens"] if plan_lens is None else plan_lens,
+                                  H, case["Hk"], D, case["bs"], mcl, P)
     plan_dev = plan.to(dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     out = None
@@ -100,7 +103,7 @@ def run_shared(case, P=0, out_dtype=torch.float32, tables=None, plan_tables=None
                                           max_context_len=mcl, device_status=st)
         torch.cuda.synchronize()
         assert pkv.last_decode_launches() == 1
-    assert int(plan_dev[8 + B:8 + B + B * case["Hk"]].abs().sum().item()) == 0  # counters reset
+    assert int(plan_dev[8 + 2 * B:8 + 2 * B + B * case["Hk"]].abs().sum().item()) == 0  # counters reset
     return out.double().cpu().numpy(), int(st.item())
 
 
@@ -156,14 +159,38 @@ def test_group_whose_tables_disagree_is_rejected_on_the_device():
     assert max_err(got[4:], ref[4:]) <= TOL["bf16"]
 
 
+def test_plan_made_for_other_lengths_is_rejected_on_the_device():
+    """The device holds one token fewer for sequence 1 than the plan was made
+    for: its rows are zeroed and PKV_DEV_BAD_CONTEXT_LEN is raised; every
+    other sequence is unaffected."""
+    import paged_kv_cache_311_gb300 as pkv
+    case = shared_case(13, dtype="bf16", H=8, Hk=2, D=128, bs=16, groups=GROUPS[:2])
+    planned = case["context_lens"].copy()
+    lens = planned.copy()
+    lens[1] -= 1
+    dev = dict(case, context_lens=lens)
+    got, st = run_shared(dev, plan_lens=planned)
+    assert st & pkv.DEV_BAD_CONTEXT_LEN
+    assert not st & pkv.DEV_BAD_BLOCK
+    assert not got[1].any()
+    ref, _ = oracle_out(dev)
+    keep = [i for i in range(len(lens)) if i != 1]
+    assert max_err(got[keep], ref[keep]) <= TOL["bf16"]
+
+
 def test_shared_prefix_head_dim_64_and_half_output():
+    """bf16 output within one bf16 unit in the last place of the oracle's
+    value rounded to bf16, plus the fp32 path's own absolute error (1e-6:
+    the rounding of outputs below ~1e-4 can hinge on it); also for the plan
+    cut into many 64-token items (one kv head fills the GPU with them)."""
     case = shared_case(3, dtype="bf16", H=8, Hk=1, D=64, bs=16, groups=GROUPS[:2])
     ref, _ = oracle_out(case)
-    got, st = run_shared(case, out_dtype=torch.bfloat16)
-    assert st == 0
-    rne = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
     from tests.gpu_support import ulp_bound
-    assert np.all(np.abs(got - rne) <= ulp_bound(ref, torch.bfloat16))
+    rne = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    for P in (0, 512):
+        got, st = run_shared(case, P=P, out_dtype=torch.bfloat16)
+        assert st == 0
+        assert np.all(np.abs(got - rne) <= ulp_bound(ref, torch.bfloat16) + 1e-6), f"P={P}"
 
 
 def test_shared_prefix_equals_per_sequence_path():

@@ -23,28 +23,34 @@ def decode_plan(plan, B, Hk, G):
     n_items, slots, nseq, nkv, iints, maxseg = (int(x) for x in h[:6])
     assert (nseq, nkv) == (B, Hk)
     expected = h[8:8 + B]
-    counters = h[8 + B:8 + B + B * Hk]
+    counters = h[8 + 2 * B:8 + 2 * B + B * Hk]
     assert not counters.any()
     items = []
-    base = 8 + B + B * Hk
+    base = 8 + 2 * B + B * Hk
     for i in range(n_items):
         it = h[base + i * iints: base + (i + 1) * iints]
         seq0, nrows, slot, nseg = (int(x) for x in it[:4])
         segs = [tuple(int(x) for x in it[4 + 5 * k: 9 + 5 * k]) for k in range(nseg)]
-        items.append((seq0, nrows, slot, segs))
+        ids = it[4 + 5 * maxseg:]
+        items.append((seq0, nrows, slot, segs, ids))
     return items, expected, slots
 
 
 def check_coverage(plan, tables, lens, G, Hk, bs=16):
     B = len(lens)
     items, expected, slots = decode_plan(plan, B, Hk, G)
+    np.testing.assert_array_equal(plan.host[8 + B:8 + 2 * B], lens)   # the lengths it was made for
     covered = [np.zeros(max(int(L), 0), dtype=int) for L in lens]
     slots_seen = [set() for _ in range(B)]
-    for seq0, nrows, slot, segs in items:
+    for seq0, nrows, slot, segs, ids in items:
         assert nrows % G == 0 and nrows <= 24
         if not segs:
             assert lens[seq0] <= 0
             continue
+        # the item carries its segments' physical block ids, in segment order
+        want = np.concatenate([tables[tseq][tb // bs: -(-te // bs)] for tseq, tb, te, _, _ in segs])
+        assert want.size <= ids.size
+        np.testing.assert_array_equal(ids[:want.size], want)
         for tseq, tb, te, rlo, rhi in segs:
             assert rlo % G == 0 and rhi % G == 0
             for m in range(rlo // G, rhi // G):
@@ -80,10 +86,31 @@ def test_forked_prompts_share_their_full_blocks():
         shared = (int(lp) // 16 * 16) // 32 * 32
         mine = [it for it in prefix_items if it[0] == 6 * p]
         assert sum(seg[2] - seg[1] for it in mine for seg in it[3] if seg[3] == 0 and seg[4] == 24) == shared
-    # the heavy (prefix) items come first
-    weights = [sum((s[2] - s[1]) * (3 if (s[3] == 0 and s[4] == it[1] and it[1] > cfg.group) else 1)
-                   for s in it[3]) for it in items]
-    assert weights[0] == max(weights)
+    # the items come heaviest first (tokens streamed)
+    weights = [sum(s[2] - s[1] for s in it[3]) for it in items]
+    assert all(a >= b for a, b in zip(weights, weights[1:]))
+
+
+def test_automatic_plan_is_one_balanced_wave():
+    """partition_size 0: the smallest target T whose items fit one CTA per
+    resident slot (3 per SM; 152 SMs when no GPU answers) over the kv heads;
+    every item then streams at most T tokens (plus one alignment step)."""
+    cfg = get("shared_prefix_bf16")
+    w = PagedDecodeWorkload(cfg, 31103, total_steps=8)
+    for _ in range(6):
+        inp = w.next_step()
+    plan = pkv.plan_shared_prefix(inp.block_tables, inp.context_lens, cfg.num_heads, cfg.num_kv_heads,
+                                  cfg.head_dim, cfg.block_size, inp.max_context_len)
+    items, _ = check_coverage(plan, inp.block_tables, inp.context_lens, cfg.group, cfg.num_kv_heads)
+    T = int(plan.host[6])
+    tokens = [sum(s[2] - s[1] for s in it[3]) for it in items]
+    assert max(tokens) <= T + 32
+    assert len(items) * cfg.num_kv_heads <= 3 * 152
+    # one step below T would not fit: T is the smallest that does
+    smaller = pkv.plan_shared_prefix(inp.block_tables, inp.context_lens, cfg.num_heads,
+                                     cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
+                                     inp.max_context_len, T - 32)
+    assert int(smaller.host[0]) * cfg.num_kv_heads > 3 * 152
 
 
 def test_no_sharing_gives_plain_partitions():
@@ -118,7 +145,9 @@ def test_groups_are_cut_at_24_rows_and_long_tails_split():
     items, expected = check_coverage(plan, bt, lens, G, 4)
     groups = sorted({(it[0], it[1]) for it in items if it[1] > G})
     assert groups == [(0, 24), (6, 8)]
-    assert expected[1] == 1 + 3                  # one prefix item + three 256-token tail items
+    # 192 shared tokens plus five folded 13-token tails (a 16-row load each)
+    # exceed one 256-token item: the group takes two; the long tail three more
+    assert expected[1] == 2 + 3
 
 
 def test_empty_context_gets_a_zero_item_and_plan_size_is_bounded():
