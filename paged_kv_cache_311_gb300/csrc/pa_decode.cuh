@@ -496,44 +496,79 @@ struct TcEngine {
             for (int j = 0; j < 4; ++j)
                 s[nt][j] += s2[nt][j];
 
-        // ---- online softmax: this lane holds tokens g, g + 8 of rows 2c, 2c+1
+        // ---- online softmax in the log2 domain: this lane holds tokens g,
+        // g + 8 of rows 2c, 2c + 1.  Each row keeps a reference maximum m.
+        // While every new score of the warp stays within kSlack of its row's
+        // reference -- the common case once a row has seen a tile -- the
+        // probabilities 2^(x - m) <= 2^kSlack are taken against the unchanged
+        // reference: no cross-lane maximum, no rescale (fp32 sums and the
+        // hi/lo 16-bit split of P lose nothing at that size).  Otherwise every
+        // row moves to its exact running maximum and the accumulators are
+        // rescaled.  (m, lsum, o) always share one reference, which is all the
+        // merges need.
+        constexpr float kSlack = 8.f;
         const bool ok0 = g < nvalid, ok1 = g + 8 < nvalid;
-        float p0[NT][2], p1[NT][2], alpha[NT][2];
-        bool grew = false;
+        float x0[NT][2], x1[NT][2], p0[NT][2], p1[NT][2];
+        bool over = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int row = 8 * nt + 2 * c + j;
                 const bool live = row >= row_lo && row < row_hi;
-                const float x0 = (ok0 && live) ? s[nt][j] * qscale : -INFINITY;
-                const float x1 = (ok1 && live) ? s[nt][2 + j] * qscale : -INFINITY;
-                float tm = fmaxf(x0, x1);
-                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
-                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
-                tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
-                const float mn = fmaxf(m[nt][j], tm);
-                // a row with no token yet keeps max -inf: nothing to rescale or add
-                const bool none = mn == -INFINITY;
-                alpha[nt][j] = none ? 1.f : exp2f(m[nt][j] - mn);
-                grew |= mn != m[nt][j];
-                p0[nt][j] = none ? 0.f : exp2f(x0 - mn);
-                p1[nt][j] = none ? 0.f : exp2f(x1 - mn);
-                lsum[nt][j] = lsum[nt][j] * alpha[nt][j] + p0[nt][j] + p1[nt][j];
-                m[nt][j] = mn;
+                x0[nt][j] = (ok0 && live) ? s[nt][j] * qscale : -INFINITY;
+                x1[nt][j] = (ok1 && live) ? s[nt][2 + j] * qscale : -INFINITY;
+                // a row with no token yet (m = -inf) is over for any live score
+                over |= fmaxf(x0[nt][j], x1[nt][j]) > m[nt][j] + kSlack;
             }
         }
-        // rescale the accumulators only when some row's running maximum moved
-        if (__any_sync(0xffffffffu, grew)) {
+        if (!__any_sync(0xffffffffu, over)) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    o[mt][nt][0] *= alpha[nt][0];
-                    o[mt][nt][1] *= alpha[nt][1];
-                    o[mt][nt][2] *= alpha[nt][0];
-                    o[mt][nt][3] *= alpha[nt][1];
+                for (int j = 0; j < 2; ++j) {
+                    // rows still without a token have no live score here: the
+                    // finite stand-in keeps 2^(-inf - m) at 0 instead of NaN
+                    const float mr = fmaxf(m[nt][j], -1e30f);
+                    p0[nt][j] = exp2f(x0[nt][j] - mr);
+                    p1[nt][j] = exp2f(x1[nt][j] - mr);
+                    lsum[nt][j] += p0[nt][j] + p1[nt][j];
                 }
+            }
+        } else {
+            float alpha[NT][2];
+            bool grew = false;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float tm = fmaxf(x0[nt][j], x1[nt][j]);
+                    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+                    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+                    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+                    const float mn = fmaxf(m[nt][j], tm);
+                    // a row with no token yet keeps max -inf: nothing to rescale or add
+                    const bool none = mn == -INFINITY;
+                    alpha[nt][j] = none ? 1.f : exp2f(m[nt][j] - mn);
+                    grew |= mn != m[nt][j];
+                    p0[nt][j] = none ? 0.f : exp2f(x0[nt][j] - mn);
+                    p1[nt][j] = none ? 0.f : exp2f(x1[nt][j] - mn);
+                    lsum[nt][j] = lsum[nt][j] * alpha[nt][j] + p0[nt][j] + p1[nt][j];
+                    m[nt][j] = mn;
+                }
+            }
+            // rescale the accumulators only when some row's running maximum moved
+            if (__any_sync(0xffffffffu, grew)) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        o[mt][nt][0] *= alpha[nt][0];
+                        o[mt][nt][1] *= alpha[nt][1];
+                        o[mt][nt][2] *= alpha[nt][0];
+                        o[mt][nt][3] *= alpha[nt][1];
+                    }
+            }
         }
 
         // ---- rows of V past the valid tokens may hold anything (even NaN

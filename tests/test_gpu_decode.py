@@ -43,14 +43,20 @@ def test_decode_matrix(dtype, engine, D, bs, G):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])
 def test_half_output_within_one_ulp(dtype, engine):
+    """16-bit output is the fp32 result rounded to nearest even (bit-exact
+    against the same call with fp32 output), so it lies within one 16-bit ulp
+    of the oracle rounded to that type, plus the fp32 result's own error."""
     case = small_case(3, dtype=dtype, B=4, H=8, Hk=2, D=128, bs=16, lens=(7, 300, 64, 1000))
     ref, _ = oracle_decode(case)
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    rne = torch.from_numpy(ref).to(tdt).to(torch.float64).numpy()
     for P in (0, 64):
         got, st, _ = gpu_decode(case, partition_size=P, out_dtype=tdt, engine=engine)
-        assert st == 0
-        rne = torch.from_numpy(ref).to(tdt).to(torch.float64).numpy()
-        assert np.all(np.abs(got - rne) <= ulp_bound(ref, tdt))
+        got32, st32, _ = gpu_decode(case, partition_size=P, engine=engine)
+        assert st == 0 and st32 == 0
+        np.testing.assert_array_equal(got, torch.from_numpy(got32).to(tdt).double().numpy())
+        assert max_err(got32, ref) <= TOL[dtype]
+        assert np.all(np.abs(got - rne) <= ulp_bound(ref, tdt) + np.abs(got32 - ref))
 
 
 @pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])

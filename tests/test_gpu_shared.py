@@ -179,18 +179,21 @@ def test_plan_made_for_other_lengths_is_rejected_on_the_device():
 
 
 def test_shared_prefix_head_dim_64_and_half_output():
-    """bf16 output within one bf16 unit in the last place of the oracle's
-    value rounded to bf16, plus the fp32 path's own absolute error (1e-6:
-    the rounding of outputs below ~1e-4 can hinge on it); also for the plan
-    cut into many 64-token items (one kv head fills the GPU with them)."""
+    """bf16 output is the fp32 result rounded to nearest even (bit-exact
+    against the same plan with fp32 output), so it lies within one bf16 ulp
+    of the oracle rounded to bf16, plus the fp32 result's own error; also
+    for the plan cut into many 64-token items (one kv head fills the GPU)."""
     case = shared_case(3, dtype="bf16", H=8, Hk=1, D=64, bs=16, groups=GROUPS[:2])
     ref, _ = oracle_out(case)
     from tests.gpu_support import ulp_bound
     rne = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
     for P in (0, 512):
         got, st = run_shared(case, P=P, out_dtype=torch.bfloat16)
-        assert st == 0
-        assert np.all(np.abs(got - rne) <= ulp_bound(ref, torch.bfloat16) + 1e-6), f"P={P}"
+        got32, st32 = run_shared(case, P=P)
+        assert st == 0 and st32 == 0
+        np.testing.assert_array_equal(got, torch.from_numpy(got32).to(torch.bfloat16).double().numpy())
+        assert max_err(got32, ref) <= TOL["bf16"]
+        assert np.all(np.abs(got - rne) <= ulp_bound(ref, torch.bfloat16) + np.abs(got32 - ref)), f"P={P}"
 
 
 def test_shared_prefix_equals_per_sequence_path():
