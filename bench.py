@@ -274,7 +274,7 @@ def run_native(args):
             "seq_steps_per_s": round(seqs_all / t_max, 1),
             "pct_of_peak": round(100 * value / peak, 2),
             "roofline": {"bound": "hbm",
-                         "kernel": ("pa_cascade_kernel" if shared else
+                         "kernel": ("pa_cascade_kernel+pa_cascade_merge_kernel" if shared else
                                     "pa_decode_kernel" + ("+pa_merge_kernel" if decode_launches[0] == 2 else "")),
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": peak_kind,

@@ -156,15 +156,15 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
  * paged_attention_decode_shared -- the same attention as
  * pkv_paged_attention_decode, following a plan from pkv_plan_shared_prefix:
  * one CTA per (kv head, work item) reads each shared block once for all the
- * query heads of its group; the CTA that completes a sequence merges its
- * partials (log-sum-exp) and writes its output.  Results equal the
- * per-sequence path up to fp32 rounding order.
+ * query heads of its group and writes the output of a sequence it holds
+ * entirely, or else one partial per row; a second kernel, queued as a
+ * programmatic dependent of the first, merges the partials (log-sum-exp).
+ * Results equal the per-sequence path up to fp32 rounding order.
  *
  * Arguments as for pkv_paged_attention_decode, plus:
- *   plan       DEVICE copy of the plan (4-byte aligned, writable: the call
- *              counts arrivals in it and leaves those counters at zero again,
- *              so the same device plan serves any number of calls with the
- *              same tables and lengths, e.g. every layer of a step)
+ *   plan       DEVICE copy of the plan (4-byte aligned; read only, so the
+ *              same device plan serves any number of calls with the same
+ *              tables and lengths, e.g. every layer of a step)
  *   num_items, slots  plan[0] and plan[1]
  *   workspace  at least the planner's workspace_bytes
  * The device checks the plan against the device arrays: every table the
@@ -173,7 +173,7 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
  * context length must be the one it was made for (PKV_DEV_BAD_CONTEXT_LEN and
  * zero rows otherwise).
  * kv_dtype must be PKV_F16 or PKV_BF16 (fp32 caches: PKV_EUNSUPPORTED).
- * Enqueues one kernel.
+ * Enqueues two kernels.
  */
 int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, const void *k_cache,
                                       const void *v_cache, int kv_dtype,
@@ -181,7 +181,7 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
                                       const int32_t *context_lens, int num_seqs, int num_heads,
                                       int num_kv_heads, int head_dim, int block_size,
                                       int64_t num_blocks, int max_context_len, float scale,
-                                      int32_t *plan, int num_items, int slots, void *workspace,
+                                      const int32_t *plan, int num_items, int slots, void *workspace,
                                       size_t workspace_bytes, uint32_t *device_status,
                                       void *stream);
 

@@ -195,9 +195,9 @@ class SharedPrefixPlan:
     """A host-made plan of the shared-prefix decode (see plan_shared_prefix).
 
     host: the int32 plan; num_items, slots, workspace_bytes: its sizes.
-    to(device) gives the device copy the decode call takes (its arrival
-    counters return to zero after every call, so one device copy serves every
-    call with the same tables and lengths)."""
+    to(device) gives the device copy the decode call takes (read only by the
+    device, so one device copy serves every call with the same tables and
+    lengths)."""
 
     def __init__(self, host, num_items: int, slots: int, workspace_bytes: int):
         self.host = host

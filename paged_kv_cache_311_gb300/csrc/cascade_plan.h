@@ -1,21 +1,25 @@
 // cascade_plan.h -- layout of the shared-prefix work plan that
-// pkv_plan_shared_prefix writes (host) and pa_cascade_kernel reads (device).
+// pkv_plan_shared_prefix writes (host) and pa_cascade_kernel and
+// pa_cascade_merge_kernel read (device).
 //
-// The plan is one int32 array:
+// The plan is one int32 array, read-only for the device:
 //   header[kHeader]            see the H_* indices
 //   expected[num_seqs]         partials each sequence receives (one per item
-//                              that holds its rows)
+//                              that holds its rows; 1: the item writes the
+//                              output itself; 0: empty or invalid context)
 //   lens[num_seqs]             the context lengths the plan was made for (the
 //                              kernel rejects a sequence whose device length
 //                              differs)
-//   counters[num_seqs * Hk]    arrivals per (sequence, kv head); zero between
-//                              calls (the kernel that merges resets them)
 //   items[num_items][item_ints]
-// An item is {seq0, nrows, slot, nseg, then max_segments segments of
-// {table_seq, tok_begin, tok_end, row_lo, row_hi}, then kTableCap block ids}:
-// query rows r < nrows are head r % G of sequence seq0 + r / G; segment k
-// covers tokens [tok_begin, tok_end) addressed by table_seq's block table,
-// for rows [row_lo, row_hi).  The block ids are the physical blocks of the
+// An item is {seq0, nrows, slot, nseg, tiles, ids, checks, 0}, then
+// max_segments segments of {table_seq, tok_begin, tok_end, row_lo, row_hi,
+// first_tile, id_off, check_off}, then kTableCap block ids: query rows
+// r < nrows are head r % G of sequence seq0 + r / G; segment k covers tokens
+// [tok_begin, tok_end) addressed by table_seq's block table, for rows
+// [row_lo, row_hi); its 16-token tiles are the item's tiles [first_tile, ...),
+// its block ids start at id_off, and its device-table checks (one per block,
+// per member for a shared-prefix segment) at check_off; tiles, ids and
+// checks are the item's totals.  The block ids are the physical blocks of the
 // segments' logical blocks [tok_begin / bs, ceil(tok_end / bs)), segment
 // after segment, as the host tables held them when the plan was made (the
 // kernel starts its loads from them and checks the device tables meanwhile).
@@ -39,11 +43,14 @@ enum : int {
 constexpr int kTag = 0x43564b50;    // "PKVC"
 constexpr int kNT = 3;              // n-tiles of 8 query rows per item
 constexpr int kMaxRows = 8 * kNT;   // query rows per item
-constexpr int kItemHead = 4;
+constexpr int kItemHead = 8;
+enum : int { I_SEQ0 = 0, I_NROWS, I_SLOT, I_NSEG, I_TILES, I_IDS, I_CHECKS };
+enum : int { S_TABLE_SEQ = 0, S_BEGIN, S_END, S_ROW_LO, S_ROW_HI, S_FIRST_TILE, S_ID_OFF, S_CHECK_OFF };
 // Block-table entries one item may address (all segments together): the
 // planner keeps items within it and the kernel stages that many.
 constexpr int kTableCap = 256;
-constexpr int kSegInts = 5;
+constexpr int kSegInts = 8;
+constexpr int kTileTokens = 16;     // tokens per warp tile of the kernel
 
 constexpr int max_segments(int group) { return 1 + kMaxRows / group; }
 constexpr int item_ids_offset(int group) { return kItemHead + kSegInts * max_segments(group); }

@@ -139,6 +139,23 @@ __device__ __forceinline__ void store_out(void *out, int dtype, int64_t i, float
         static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
 }
 
+// Four consecutive outputs from element i (a multiple of 4; the output is
+// 16-byte aligned): one 16- or 8-byte store.
+__device__ __forceinline__ void store_out4(void *out, int dtype, int64_t i, float4 v)
+{
+    if (dtype == PKV_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + i) = v;
+    } else if (dtype == PKV_F16) {
+        const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        *reinterpret_cast<uint2 *>(static_cast<__half *>(out) + i) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+    } else {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(out) + i) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+    }
+}
+
 // What one CTA computes: query rows r < nrows, row r being head
 // (kvh * G + r % G) of sequence seq0 + r / G, over the tokens [tok0, tok_end)
 // that the block table of `table_seq` addresses; split partials go to

@@ -1,6 +1,6 @@
 // pa_merge.cuh -- the log-sum-exp merge of split-context partials: the
-// half-warp routine merge_partials (also called by the shared-prefix kernel
-// in pa_cascade.cuh) and pa_merge_kernel, which runs it for every (sequence,
+// half-warp routine merge_partials (also used by pa_cascade_merge_kernel in
+// pa_cascade.cuh) and pa_merge_kernel, which runs it for every (sequence,
 // head) after the split-context pass.
 #pragma once
 
@@ -8,50 +8,64 @@
 
 namespace pkv {
 
-// Sixteen lanes (a half-warp; hl = lane within it) merge the n partials of
+// Sixteen lanes (a half-warp; hl = lane within it) merge the partials of
 // (sequence, head) `sh`, held in slots [0, n) of the split workspace (row
 // stride `slots`), and write the output row:
 //   out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k,  M = max_k m_k.
-// A partial with l < 0 marks a failed pass and zeroes the row, as does
-// `zero_row`.  Slots are read eight at a time, all loads of a chunk in
-// flight together, with a running maximum (the sums are rescaled when a
-// chunk raises it), so n <= 8 costs one round trip to L2.  Each lane owns
-// D / 16 dims; every lane reads the same (m, l) pairs, so no lane exchange
-// is needed.  Loads bypass L1 (ld.global.cg): partials written by other CTAs
-// of the same launch are seen once their writers have released them.
-template <int D>
-__device__ __forceinline__ void merge_partials(const DecodeParams &p, int64_t sh, int n, int slots,
-                                               bool zero_row, int hl)
+// get_n() gives n: a count >= 0, kMergeZero to write a zero row, or
+// kMergeSkip to leave the row untouched.  It is called after the first U
+// slots' loads are issued -- they lie inside the row whatever n turns out to
+// be, and slots >= n are ignored -- so a merge of up to U partials costs one
+// round trip to L2 including the load behind n.  Later chunks of U rescale
+// the running sums when they raise the maximum.  A partial with
+// l < 0 marks a failed pass and zeroes the row.  Each lane owns D / 16
+// dims; every lane reads the same (m, l) pairs, so no lane exchange is
+// needed.  Loads bypass L1 (ld.global.cg).
+constexpr int kMergeZero = -1, kMergeSkip = -2;
+
+template <int D, int U, typename GetN>
+__device__ __forceinline__ void merge_partials(const DecodeParams &p, int64_t sh, int slots, int hl,
+                                               GetN get_n)
 {
     constexpr int DPL = D / 16;   // dims per lane
     constexpr int V4 = DPL / 4;   // float4 pieces per lane
-    constexpr int U = 8;          // slots per chunk
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sh * slots;
     const float4 *acc = reinterpret_cast<const float4 *>(p.ws_acc + sh * slots * D + hl * DPL);
 
-    float M = -INFINITY, den = 0.f, num[DPL];
-#pragma unroll
-    for (int d = 0; d < DPL; ++d)
-        num[d] = 0.f;
-    bool invalid = zero_row;
-    for (int k0 = 0; k0 < n && !invalid; k0 += U) {
-        float2 t[U];
-        float4 a[U][V4];
+    float2 t[U];
+    float4 a[U][V4];
+    auto load_chunk = [&](int k0, int lim) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             t[u] = make_float2(-INFINITY, 0.f);
-            if (k0 + u < n) {
+            if (k0 + u < lim) {
                 t[u] = __ldcg(ml + k0 + u);
 #pragma unroll
                 for (int v = 0; v < V4; ++v)
                     a[u][v] = __ldcg(acc + (int64_t)(k0 + u) * (D / 4) + v);
             }
         }
+    };
+    load_chunk(0, slots < U ? slots : U);   // speculative: n is not known yet
+    const int n = get_n();
+    if (n == kMergeSkip)
+        return;
+
+    float M = -INFINITY, den = 0.f, num[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d)
+        num[d] = 0.f;
+    bool invalid = n < 0;
+    for (int k0 = 0; k0 < n && !invalid; k0 += U) {
+        if (k0 > 0)
+            load_chunk(k0, n);
         float Mc = M;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            Mc = fmaxf(Mc, t[u].x);
-            invalid |= t[u].y < 0.f;
+            if (k0 + u < n) {
+                Mc = fmaxf(Mc, t[u].x);
+                invalid |= t[u].y < 0.f;
+            }
         }
         if (Mc == -INFINITY)
             continue;   // nothing attended so far
@@ -62,7 +76,7 @@ __device__ __forceinline__ void merge_partials(const DecodeParams &p, int64_t sh
             num[d] *= s;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            if (t[u].x != -INFINITY) {
+            if (k0 + u < n && t[u].x != -INFINITY) {
                 const float f = exp2f(t[u].x - Mc);
                 den += f * t[u].y;
 #pragma unroll
@@ -79,13 +93,15 @@ __device__ __forceinline__ void merge_partials(const DecodeParams &p, int64_t sh
     const bool zero = invalid || den == 0.f;
     const float inv = zero ? 0.f : 1.f / den;
 #pragma unroll
-    for (int d = 0; d < DPL; ++d)
-        store_out(p.out, p.out_dtype, sh * D + hl * DPL + d, zero ? 0.f : num[d] * inv);
+    for (int v = 0; v < V4; ++v)
+        store_out4(p.out, p.out_dtype, sh * D + hl * DPL + 4 * v,
+                   make_float4(num[4 * v] * inv, num[4 * v + 1] * inv, num[4 * v + 2] * inv,
+                               num[4 * v + 3] * inv));
 }
 
 // Merge after the split-context pass: one half-warp per (sequence, head),
 // eight per CTA; the valid slots are the ceil(L / P) partitions of the
-// context.
+// context (up to 64 and more for long contexts: chunks of eight slots).
 template <int D>
 __global__ void __launch_bounds__(128) pa_merge_kernel(const __grid_constant__ DecodeParams p)
 {
@@ -94,13 +110,15 @@ __global__ void __launch_bounds__(128) pa_merge_kernel(const __grid_constant__ D
     if (sh >= (int64_t)p.num_seqs * p.num_heads)
         return;
     const int seq = (int)(sh / p.num_heads);
-    const int L = p.context_lens[seq];
-    const bool bad_len = L < 0 || L > p.max_context_len;
-    if (bad_len && hl == 0 && sh % p.num_heads == 0)
-        report(p.status, PKV_DEV_BAD_CONTEXT_LEN);  // the partition pass skipped it silently
-    const int P = p.partition_size;
-    const int n = bad_len ? 0 : (L + P - 1) / P;
-    merge_partials<D>(p, sh, n, p.num_partitions, bad_len, hl);
+    merge_partials<D, 8>(p, sh, p.num_partitions, hl, [&]() {
+        const int L = p.context_lens[seq];
+        if (L < 0 || L > p.max_context_len) {
+            if (hl == 0 && sh % p.num_heads == 0)
+                report(p.status, PKV_DEV_BAD_CONTEXT_LEN);  // the partition pass skipped it silently
+            return kMergeZero;
+        }
+        return (L + p.partition_size - 1) / p.partition_size;
+    });
 }
 
 }  // namespace pkv

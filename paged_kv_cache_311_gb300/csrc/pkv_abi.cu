@@ -117,6 +117,12 @@ int ensure_smem_attr(const void *func, int bytes, unsigned long long *done_mask)
     if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
         return PKV_ECUDA;
+    // every library kernel asks for the largest shared-memory carveout, so
+    // that consecutive launches of them never wait for an L1 / shared
+    // memory reconfiguration of the SMs
+    if (cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return PKV_ECUDA;
     if (bit)
         __atomic_fetch_or(done_mask, bit, __ATOMIC_RELEASE);
     return PKV_OK;
@@ -288,7 +294,7 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
                                       const int32_t *context_lens, int num_seqs, int num_heads,
                                       int num_kv_heads, int head_dim, int block_size,
                                       int64_t num_blocks, int max_context_len, float scale,
-                                      int32_t *plan, int num_items, int slots, void *workspace,
+                                      const int32_t *plan, int num_items, int slots, void *workspace,
                                       size_t workspace_bytes, uint32_t *device_status,
                                       void *stream)
 {
@@ -357,7 +363,7 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     a.engine_used = &engine_used;
     const int rc = kv_dtype == PKV_F16 ? launch_decode_f16(a) : launch_decode_bf16(a);
     if (rc == PKV_OK) {
-        g_last_decode_launches = 1;
+        g_last_decode_launches = 2;
         g_last_decode_engine = engine_used;
     }
     return rc;
@@ -380,6 +386,9 @@ int pkv_reshape_and_cache(const void *key, const void *value, void *k_cache, voi
         return PKV_EINVAL;
     if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
         return PKV_EINVAL;
+    static unsigned long long scatter_attr = 0;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(reshape_and_cache_kernel), 0, &scatter_attr))
+        return PKV_ECUDA;
     reshape_and_cache_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_kv_heads,
@@ -408,6 +417,9 @@ int pkv_copy_blocks(void *const *k_caches, void *const *v_caches, int num_layers
             ptrs.v[l] = static_cast<uint4 *>(v_caches[l0 + l]);
         }
         dim3 grid(num_pairs, nl, 2);
+        static unsigned long long copy_attr = 0;
+        if (ensure_smem_attr(reinterpret_cast<const void *>(copy_blocks_kernel), 0, &copy_attr))
+            return PKV_ECUDA;
         copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
             ptrs, src_dst_pairs, (int64_t)(block_bytes / 16), num_blocks, device_status);
         if (cudaGetLastError() != cudaSuccess)

@@ -69,7 +69,7 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
     // tokens, one more for the rounding of a cut, one for a group's last item
     const int P = partition_size > 0 ? partition_size : kMinAutoTokens;
     const long long per_seq = (max_context_len + P - 1) / P + 2;
-    return (size_t)pkv::plan::kHeader + 2 * (size_t)num_seqs + (size_t)num_seqs * num_kv_heads +
+    return (size_t)pkv::plan::kHeader + 2 * (size_t)num_seqs +
            (size_t)(num_seqs * per_seq) * pkv::plan::item_ints(G);
 }
 
@@ -278,7 +278,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     for (int s = 0; s < B; ++s)
         slots = std::max(slots, expected[s]);
     const int iints = item_ints(G);
-    const size_t need = (size_t)kHeader + 2 * (size_t)B + (size_t)B * num_kv_heads + items.size() * iints;
+    const size_t need = (size_t)kHeader + 2 * (size_t)B + items.size() * iints;
     if (plan_ints)
         *plan_ints = need;
     if (workspace_bytes)
@@ -302,25 +302,38 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     plan[H_TAG] = kTag;
     std::copy(expected.begin(), expected.end(), plan + kHeader);
     std::copy(context_lens, context_lens + B, plan + kHeader + B);
-    int32_t *dst = plan + kHeader + 2 * (size_t)B + (size_t)B * num_kv_heads;
+    int32_t *dst = plan + kHeader + 2 * (size_t)B;
     for (const Item &it : items) {
-        dst[0] = it.seq0;
-        dst[1] = it.nrows;
-        dst[2] = it.slot;
-        dst[3] = (int)it.segs.size();
+        const int nmem = it.nrows / G;
+        int tiles = 0, nids = 0, checks = 0;
+        dst[I_SEQ0] = it.seq0;
+        dst[I_NROWS] = it.nrows;
+        dst[I_SLOT] = it.slot;
+        dst[I_NSEG] = (int)it.segs.size();
         int32_t *ids = dst + item_ids_offset(G);
         for (size_t k = 0; k < it.segs.size(); ++k) {
             const Seg &g = it.segs[k];
+            const int nb = blocks_between(g.tok_begin, g.tok_end, bs);
+            const bool shared = g.row_lo == 0 && g.row_hi == it.nrows && nmem > 1;
             int32_t *q = dst + kItemHead + kSegInts * k;
-            q[0] = g.table_seq;
-            q[1] = g.tok_begin;
-            q[2] = g.tok_end;
-            q[3] = g.row_lo;
-            q[4] = g.row_hi;
+            q[S_TABLE_SEQ] = g.table_seq;
+            q[S_BEGIN] = g.tok_begin;
+            q[S_END] = g.tok_end;
+            q[S_ROW_LO] = g.row_lo;
+            q[S_ROW_HI] = g.row_hi;
+            q[S_FIRST_TILE] = tiles;
+            q[S_ID_OFF] = nids;
+            q[S_CHECK_OFF] = checks;
+            tiles += (g.tok_end - g.tok_begin + kTileTokens - 1) / kTileTokens;
+            nids += nb;
+            checks += (shared ? nmem : 1) * nb;
             const int32_t *row = block_tables + (long long)g.table_seq * MB;
             for (int j = g.tok_begin / bs; j < (g.tok_end + bs - 1) / bs; ++j)
                 *ids++ = row[j];
         }
+        dst[I_TILES] = tiles;
+        dst[I_IDS] = nids;
+        dst[I_CHECKS] = checks;
         dst += iints;
     }
     return PKV_OK;

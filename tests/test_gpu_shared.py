@@ -102,8 +102,9 @@ def run_shared(case, P=0, out_dtype=torch.float32, tables=None, plan_tables=None
         pkv.paged_attention_decode_shared(out, q, kc, vc, bt, cl, case["scale"], plan, plan_dev,
                                           max_context_len=mcl, device_status=st)
         torch.cuda.synchronize()
-        assert pkv.last_decode_launches() == 1
-    assert int(plan_dev[8 + 2 * B:8 + 2 * B + B * case["Hk"]].abs().sum().item()) == 0  # counters reset
+        assert pkv.last_decode_launches() == 2
+    # the device only reads the plan
+    np.testing.assert_array_equal(plan_dev.cpu().numpy(), plan.host)
     return out.double().cpu().numpy(), int(st.item())
 
 

@@ -23,16 +23,15 @@ def decode_plan(plan, B, Hk, G):
     n_items, slots, nseq, nkv, iints, maxseg = (int(x) for x in h[:6])
     assert (nseq, nkv) == (B, Hk)
     expected = h[8:8 + B]
-    counters = h[8 + 2 * B:8 + 2 * B + B * Hk]
-    assert not counters.any()
     items = []
-    base = 8 + 2 * B + B * Hk
+    base = 8 + 2 * B
     for i in range(n_items):
         it = h[base + i * iints: base + (i + 1) * iints]
-        seq0, nrows, slot, nseg = (int(x) for x in it[:4])
-        segs = [tuple(int(x) for x in it[4 + 5 * k: 9 + 5 * k]) for k in range(nseg)]
-        ids = it[4 + 5 * maxseg:]
-        items.append((seq0, nrows, slot, segs, ids))
+        seq0, nrows, slot, nseg, tiles, nids, checks = (int(x) for x in it[:7])
+        raw = [[int(x) for x in it[8 + 8 * k: 16 + 8 * k]] for k in range(nseg)]
+        segs = [tuple(r[:5]) for r in raw]
+        ids = it[8 + 8 * maxseg:]
+        items.append((seq0, nrows, slot, segs, ids, (tiles, nids, checks), raw))
     return items, expected, slots
 
 
@@ -42,11 +41,23 @@ def check_coverage(plan, tables, lens, G, Hk, bs=16):
     np.testing.assert_array_equal(plan.host[8 + B:8 + 2 * B], lens)   # the lengths it was made for
     covered = [np.zeros(max(int(L), 0), dtype=int) for L in lens]
     slots_seen = [set() for _ in range(B)]
-    for seq0, nrows, slot, segs, ids in items:
+    for seq0, nrows, slot, segs, ids, totals, raw in items:
         assert nrows % G == 0 and nrows <= 24
         if not segs:
             assert lens[seq0] <= 0
             continue
+        # the per-segment offsets the kernel reads: 16-token tiles, block ids
+        # and device-table checks (every member's table for a shared prefix
+        # segment), in segment order, and the item's totals
+        t = n = c = 0
+        for tseq, tb, te, rlo, rhi, first_tile, id_off, check_off in raw:
+            assert (first_tile, id_off, check_off) == (t, n, c)
+            nb = -(-te // bs) - tb // bs
+            shared = rlo == 0 and rhi == nrows and nrows > G
+            t += -(-(te - tb) // 16)
+            n += nb
+            c += (nrows // G if shared else 1) * nb
+        assert totals == (t, n, c)
         # the item carries its segments' physical block ids, in segment order
         want = np.concatenate([tables[tseq][tb // bs: -(-te // bs)] for tseq, tb, te, _, _ in segs])
         assert want.size <= ids.size

@@ -130,8 +130,9 @@ def algorithmic_bytes(cfg: DecodeConfig, inp: StepInputs, num_seqs: int, split_p
     plus q, the output, the block-table entries and context lengths; plus the
     split path's workspace round trip when it runs (one partial per head and
     non-empty partition of split_partition tokens, or `partials[s]` per head
-    of sequence s for a shared-prefix plan).  Shared prefix blocks
-    count once.  scatter: the new tokens' K/V read once and written once.
+    of sequence s for a shared-prefix plan; none when partials[s] is 1, since
+    the one item that holds such a sequence writes its output directly).
+    Shared prefix blocks count once.  scatter: the new tokens' K/V read once and written once.
     copy: each copied block read once and written once."""
     bs, e = cfg.block_size, cfg.elem_bytes
     row = cfg.head_dim * e
@@ -161,7 +162,8 @@ def algorithmic_bytes(cfg: DecodeConfig, inp: StepInputs, num_seqs: int, split_p
         parts = sum(-(-int(L) // split_partition) for L in inp.context_lens[:num_seqs])
         ws = 2 * cfg.num_heads * parts * (cfg.head_dim + 2) * 4
     if partials is not None:
-        ws = 2 * cfg.num_heads * int(np.sum(partials)) * (cfg.head_dim + 2) * 4
+        merged = np.asarray(partials)
+        ws = 2 * cfg.num_heads * int(np.sum(merged[merged > 1])) * (cfg.head_dim + 2) * 4
     attn = kv + qo + meta + ws
     T = inp.num_tokens
     scatter = 2 * 2 * T * cfg.num_kv_heads * row + T * 8
