@@ -255,6 +255,12 @@ def run_native(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(state, steps[args.warmup:], host_inputs[args.warmup:], P, flush, bytes_step)
+    # memory accounting of the paged cache at the first timed step
+    first = host_inputs[args.warmup]
+    use = pkv.kv_cache_usage(first.block_tables, first.context_lens, cfg.block_size, w.num_blocks)
+    kv_memory = {"block_size": cfg.block_size, "tokens": use.tokens, "blocks": use.blocks,
+                 "paged_waste": round(use.paged_waste, 4),
+                 "reserve_longest_waste": round(use.reserved_waste(int(first.context_lens.max())), 4)}
 
     if rank == 0:
         line = {
@@ -285,6 +291,7 @@ def run_native(args):
             "gpu_launches": launches,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "kv_memory": kv_memory,
         }
         print(json.dumps(line))
     if dist is not None:

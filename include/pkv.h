@@ -186,6 +186,27 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
                                       void *stream);
 
 /*
+ * kv_cache_usage -- HOST accounting of the paged cache ("Memory Efficiency":
+ * blocks are taken on demand, so only the tail of a sequence's last block is
+ * unused; "Advanced Features": sharers of a prefix hold its blocks once).
+ *
+ *   block_tables, context_lens  HOST arrays, layout as for decode
+ *   num_blocks      size of the physical pool (block ids must lie in it)
+ *   tokens          out: sum of the context lengths (tokens cached)
+ *   blocks          out: distinct physical blocks the tables reference for
+ *                   those tokens
+ *   occupied_slots  out: token slots of those blocks that hold a token (a
+ *                   shared block counts its longest sharer's rows)
+ * The paged waste is 1 - occupied_slots / (blocks * block_size); reserving
+ * R tokens per sequence instead wastes 1 - tokens / (num_seqs * R).  Returns
+ * PKV_EINVAL for a negative length, a length beyond the table or a block id
+ * outside [0, num_blocks).
+ */
+int pkv_kv_cache_usage(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                       int max_blocks_per_seq, int block_size, int64_t num_blocks, int64_t *tokens,
+                       int64_t *blocks, int64_t *occupied_slots);
+
+/*
  * reshape_and_cache -- write each new token's key/value rows into its slot
  * ("The PagedAttention Algorithm", Step 2: generated tokens fill the block).
  *

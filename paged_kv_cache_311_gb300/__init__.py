@@ -27,7 +27,7 @@ __all__ = [
     "PkvError", "load_library", "paged_attention_decode", "reshape_and_cache", "copy_blocks",
     "paged_attention_workspace_bytes", "status_string", "last_decode_launches",
     "paged_attention_decode_shared", "plan_shared_prefix", "SharedPrefixPlan",
-    "set_decode_engine", "last_decode_engine",
+    "set_decode_engine", "last_decode_engine", "kv_cache_usage", "KvCacheUsage",
     "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "HEADER_PATH",
 ]
 
@@ -74,6 +74,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_plan_shared_prefix.restype = i32
     L.pkv_shared_plan_max_ints.argtypes = [i32, i32, i32, i32, i32]
     L.pkv_shared_plan_max_ints.restype = u64
+    L.pkv_kv_cache_usage.argtypes = [vp, vp, i32, i32, i32, i64, ctypes.POINTER(i64),
+                                     ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.pkv_kv_cache_usage.restype = i32
     L.pkv_reshape_and_cache.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, vp, vp]
     L.pkv_reshape_and_cache.restype = i32
     L.pkv_copy_blocks.argtypes = [vp, vp, i32, vp, i32, u64, i64, vp, vp]
@@ -207,6 +210,44 @@ class SharedPrefixPlan:
 
     def to(self, device) -> torch.Tensor:
         return torch.from_numpy(self.host).to(device)
+
+
+class KvCacheUsage:
+    """What kv_cache_usage counted: cached tokens, distinct blocks and the
+    token slots of those blocks that hold a token, for one block size."""
+
+    def __init__(self, tokens: int, blocks: int, occupied_slots: int, block_size: int, num_seqs: int):
+        self.tokens = tokens
+        self.blocks = blocks
+        self.occupied_slots = occupied_slots
+        self.block_size = block_size
+        self.num_seqs = num_seqs
+
+    @property
+    def paged_waste(self) -> float:
+        """Share of the allocated slots that hold no token."""
+        slots = self.blocks * self.block_size
+        return 1.0 - self.occupied_slots / slots if slots else 0.0
+
+    def reserved_waste(self, reserve_tokens: int) -> float:
+        """Share unused if every sequence reserved reserve_tokens slots."""
+        total = self.num_seqs * reserve_tokens
+        return 1.0 - self.tokens / total if total else 0.0
+
+
+def kv_cache_usage(block_tables, context_lens, block_size: int, num_blocks: int) -> KvCacheUsage:
+    """Memory accounting of a paged cache from its host block tables and
+    lengths (the C function pkv_kv_cache_usage)."""
+    import numpy as np
+    bt = np.ascontiguousarray(np.asarray(block_tables), dtype=np.int32)
+    cl = np.ascontiguousarray(np.asarray(context_lens), dtype=np.int32)
+    B, MB = bt.shape
+    t, b, o = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = load_library().pkv_kv_cache_usage(bt.ctypes.data, cl.ctypes.data, B, MB, block_size,
+                                           int(num_blocks), ctypes.byref(t), ctypes.byref(b),
+                                           ctypes.byref(o))
+    _check(rc, "pkv_kv_cache_usage")
+    return KvCacheUsage(t.value, b.value, o.value, block_size, B)
 
 
 def plan_shared_prefix(block_tables, context_lens, num_heads: int, num_kv_heads: int,
