@@ -56,6 +56,8 @@ def lib():
         L.pkv_oracle_reshape_and_cache.restype = u32
         L.pkv_oracle_copy_blocks.argtypes = [P, P, i32, P, i32, sz, i64]
         L.pkv_oracle_copy_blocks.restype = u32
+        L.pkv_oracle_swap_blocks.argtypes = [P, P, P, P, i32, P, i32, sz, i64, i64, i32]
+        L.pkv_oracle_swap_blocks.restype = u32
         _lib = L
     return _lib
 
@@ -142,3 +144,17 @@ def copy_blocks(k_caches, v_caches, src_dst_pairs):
     block_bytes = k_caches[0][0].nbytes
     return int(lib().pkv_oracle_copy_blocks(kp, vp, nl, _ptr(pairs), pairs.shape[0],
                                             block_bytes, NB))
+
+
+
+def swap_blocks(gpu_k, gpu_v, host_k, host_v, pairs, direction):
+    """Block swap between two pools of every layer: pairs of (gpu block,
+    host block); direction 0 copies gpu -> host, 1 host -> gpu."""
+    nl = len(gpu_k)
+    for c in list(gpu_k) + list(gpu_v) + list(host_k) + list(host_v):
+        assert c.flags.c_contiguous
+    arr = lambda cs: (ctypes.c_void_p * nl)(*[c.ctypes.data for c in cs])
+    pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    return int(lib().pkv_oracle_swap_blocks(arr(gpu_k), arr(gpu_v), arr(host_k), arr(host_v), nl,
+                                            _ptr(pr), pr.shape[0], gpu_k[0][0].nbytes,
+                                            gpu_k[0].shape[0], host_k[0].shape[0], int(direction)))

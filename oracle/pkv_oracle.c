@@ -380,3 +380,37 @@ uint32_t pkv_oracle_copy_blocks(void *const *k_caches, void *const *v_caches, in
     }
     return st;
 }
+
+/* Swapping blocks out to host memory and back in ("Advanced Features": a
+ * preempted sequence's blocks can be moved to CPU memory and restored).
+ * Pair p = (gpu block, host block); direction 0 copies every layer's K and V
+ * gpu block -> host block, direction 1 host block -> gpu block.  A pair with
+ * an id outside its pool is skipped and flags ORC_BAD_BLOCK. */
+uint32_t pkv_oracle_swap_blocks(void *const *gpu_k, void *const *gpu_v, void *const *host_k,
+                                void *const *host_v, int num_layers, const int64_t *pairs,
+                                int num_pairs, size_t block_bytes, int64_t gpu_blocks,
+                                int64_t host_blocks, int direction)
+{
+    uint32_t st = 0;
+    for (int p = 0; p < num_pairs; ++p) {
+        int64_t g = pairs[2 * p], h = pairs[2 * p + 1];
+        if (g < 0 || g >= gpu_blocks || h < 0 || h >= host_blocks) {
+            st |= ORC_BAD_BLOCK;
+            continue;
+        }
+        for (int l = 0; l < num_layers; ++l) {
+            char *gk = (char *)gpu_k[l] + (size_t)g * block_bytes;
+            char *gv = (char *)gpu_v[l] + (size_t)g * block_bytes;
+            char *hk = (char *)host_k[l] + (size_t)h * block_bytes;
+            char *hv = (char *)host_v[l] + (size_t)h * block_bytes;
+            if (direction == 0) {
+                memcpy(hk, gk, block_bytes);
+                memcpy(hv, gv, block_bytes);
+            } else {
+                memcpy(gk, hk, block_bytes);
+                memcpy(gv, hv, block_bytes);
+            }
+        }
+    }
+    return st;
+}

@@ -32,6 +32,10 @@ MUTANTS = {
                                      "size_t dst = (size_t)(((o * num_kv_heads + h) * block_size + b)) * row;"),
     "copy_direction_swapped": ("memcpy((char *)k_caches[l] + (size_t)dst * block_bytes,\n                   (const char *)k_caches[l] + (size_t)src * block_bytes",
                                "memcpy((char *)k_caches[l] + (size_t)src * block_bytes,\n                   (const char *)k_caches[l] + (size_t)dst * block_bytes"),
+    "swap_direction_inverted": ("            if (direction == 0) {\n                memcpy(hk, gk, block_bytes);",
+                                "            if (direction != 0) {\n                memcpy(hk, gk, block_bytes);"),
+    "swap_host_index_is_gpu_index": ("char *hk = (char *)host_k[l] + (size_t)h * block_bytes;",
+                                     "char *hk = (char *)host_k[l] + (size_t)(g % host_blocks) * block_bytes;"),
 }
 
 

@@ -359,6 +359,36 @@ def test_copy_blocks_matches_slices(oracle_lib):
     assert oracle_lib.copy_blocks(ks, vs, np.array([[0, NB]])) == oracle_lib.BAD_BLOCK
 
 
+def test_swap_blocks_matches_slices_and_round_trips(oracle_lib):
+    """Swap-out copies each pair's gpu block into its host block for every
+    layer's K and V (numpy fancy indexing is the definition); swap-in of the
+    same pairs after the gpu blocks were overwritten restores them; an id
+    outside either pool is skipped and flagged."""
+    rng = np.random.default_rng(29)
+    layers, NB, NH = 2, 12, 5
+    gk = [rng.standard_normal((NB, 2, 16, 64)).astype(np.float32) for _ in range(layers)]
+    gv = [rng.standard_normal((NB, 2, 16, 64)).astype(np.float32) for _ in range(layers)]
+    hk = [np.zeros((NH, 2, 16, 64), np.float32) for _ in range(layers)]
+    hv = [np.zeros((NH, 2, 16, 64), np.float32) for _ in range(layers)]
+    pairs = np.array([[3, 0], [11, 4], [5, 2]], dtype=np.int64)
+    saved_k = [k.copy() for k in gk]; saved_v = [v.copy() for v in gv]
+    assert oracle_lib.swap_blocks(gk, gv, hk, hv, pairs, 0) == 0
+    for l in range(layers):
+        np.testing.assert_array_equal(hk[l][pairs[:, 1]], gk[l][pairs[:, 0]])
+        np.testing.assert_array_equal(hv[l][pairs[:, 1]], gv[l][pairs[:, 0]])
+        untouched = np.setdiff1d(np.arange(NH), pairs[:, 1])
+        assert not hk[l][untouched].any() and not hv[l][untouched].any()
+        gk[l][pairs[:, 0]] = -1.0; gv[l][pairs[:, 0]] = -2.0     # the blocks are reused meanwhile
+    assert oracle_lib.swap_blocks(gk, gv, hk, hv, pairs, 1) == 0
+    for l in range(layers):
+        np.testing.assert_array_equal(gk[l], saved_k[l])
+        np.testing.assert_array_equal(gv[l], saved_v[l])
+    assert oracle_lib.swap_blocks(gk, gv, hk, hv, np.array([[NB, 0]]), 0) == oracle_lib.BAD_BLOCK
+    assert oracle_lib.swap_blocks(gk, gv, hk, hv, np.array([[0, NH]]), 1) == oracle_lib.BAD_BLOCK
+    for l in range(layers):
+        np.testing.assert_array_equal(gk[l], saved_k[l])
+
+
 # --------------------------------------------------------- copy-on-write
 def test_copy_on_write_rule():
     """Six samples fork a 37-token prompt (partial last block of 16): samples
