@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=95)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--op", default="decode", choices=["decode", "swap_blocks"],
+                    help="swap_blocks: time the block swap of a preempted tenth of the batch")
     ap.add_argument("--config", default="llama7b_f16")
     ap.add_argument("--block-size", type=int, default=0)
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling cases)")
@@ -621,10 +623,97 @@ def run_reference(args):
         dist.destroy_process_group()
 
 
+def run_swap(args):
+    """Swap-out and swap-in of every block of about a tenth of the workload's
+    sequences (preemption), against the host link's own copy bandwidth
+    measured in the same run (one pinned cudaMemcpyAsync of the same bytes
+    each way) and against one copy per block (the many small transfers the
+    pages name as the cost of swapping small blocks)."""
+    import paged_kv_cache_311_gb300 as pkv
+    dev = local_device()
+    cfg = get(args.config)
+    if args.block_size:
+        cfg = cfg.with_(block_size=args.block_size)
+    seed = SEED_BASE + CONFIGS.index(get(args.config))
+    w = PagedDecodeWorkload(cfg, seed, total_steps=max(args.warmup + args.steps, 1),
+                            pool_blocks=_pool_blocks(cfg, dev, args.pool_gb))
+    state = DeviceState(cfg, w, seed, device=dev)
+    inp = w.next_step()
+    n_out = max(1, w.num_seqs // 10)
+    blocks = []
+    for s in range(n_out):
+        nb = -(-int(inp.context_lens[s]) // cfg.block_size)
+        blocks += [int(b) for b in inp.block_tables[s][:nb]]
+    blocks = sorted(set(blocks))
+    n = len(blocks)
+    pairs = torch.tensor([[b, i] for i, b in enumerate(blocks)], dtype=torch.int64, device=dev)
+    shape = (n,) + tuple(state.k_cache.shape[1:])
+    hk = torch.empty(shape, dtype=state.k_cache.dtype).pin_memory()
+    hv = torch.empty(shape, dtype=state.k_cache.dtype).pin_memory()
+    nbytes = 2 * n * cfg.block_bytes
+    stream = torch.cuda.current_stream()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def timed(fn, reps):
+        ms = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return sorted(ms)[len(ms) // 2]
+
+    out = lambda: pkv.swap_blocks([state.k_cache], [state.v_cache], [hk], [hv], pairs, pkv.SWAP_OUT,
+                                  device_status=st)
+    inn = lambda: pkv.swap_blocks([state.k_cache], [state.v_cache], [hk], [hv], pairs, pkv.SWAP_IN,
+                                  device_status=st)
+    for _ in range(args.warmup):
+        out(); inn()
+    torch.cuda.synchronize()
+    reps = max(args.steps, 3)
+    t_out, t_in = timed(out, reps), timed(inn, reps)
+    # the link: one contiguous copy of the same bytes each way
+    hbuf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    t_d2h = timed(lambda: hbuf.copy_(dbuf, non_blocking=True), reps)
+    t_h2d = timed(lambda: dbuf.copy_(hbuf, non_blocking=True), reps)
+    # one copy per block and cache (copy engines, no gather kernel)
+    idx = pairs[:, 0].tolist()
+    def per_block():
+        for i, b in enumerate(idx):
+            hk[i].copy_(state.k_cache[b], non_blocking=True)
+            hv[i].copy_(state.v_cache[b], non_blocking=True)
+    t_small = timed(per_block, max(3, reps // 3))
+    if st.item() != 0:
+        raise RuntimeError(f"device status {st.item()} during the swaps")
+    gbs = lambda t: nbytes / (t / 1e3) / 1e9
+    line = {"metric": "swap_blocks: block bytes moved per second between the GPU pool and pinned host memory",
+            "value": round(gbs(t_out), 2), "unit": "GB/s", "n_gpus": 1, "steps": reps,
+            "warmup": args.warmup, "ms_per_step": round(t_out, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": cfg.name, "block_size": cfg.block_size, "blocks": n,
+                       "sequences_swapped": n_out, "bytes": nbytes, "block_bytes": cfg.block_bytes},
+            "swap_in": {"value": round(gbs(t_in), 2), "unit": "GB/s", "ms": round(t_in, 5)},
+            "roofline": {"bound": "host link", "unit": "GB/s",
+                         "out": {"achieved": round(gbs(t_out), 2), "peak": round(gbs(t_d2h), 2),
+                                 "frac": round(t_d2h / t_out, 4)},
+                         "in": {"achieved": round(gbs(t_in), 2), "peak": round(gbs(t_h2d), 2),
+                                "frac": round(t_h2d / t_in, 4)},
+                         "peak_source": "one pinned cudaMemcpyAsync of the same bytes, same run"},
+            "one_copy_per_block": {"value": round(gbs(t_small), 2), "unit": "GB/s",
+                                   "ms": round(t_small, 5)},
+            "gpu_launches": 1}
+    print(json.dumps(line))
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "swap_blocks":
+        run_swap(args)
     else:
         run_native(args)
 

@@ -242,6 +242,34 @@ int pkv_copy_blocks(void *const *k_caches, void *const *v_caches, int num_layers
                     int64_t num_blocks, uint32_t *device_status, void *stream);
 
 /*
+ * swap_blocks -- move whole blocks between the GPU pool and a host pool (a
+ * preempted request's KV cache goes to CPU memory when the GPU is full and
+ * comes back when it resumes: "vLLM: The Serving Engine", smart scheduling;
+ * the paper's section 7.3 compares swapping with recomputation).  One
+ * kernel moves all pairs of all layers, reading and writing the host pool
+ * over the host link.
+ *
+ *   gpu_k, gpu_v    HOST arrays of num_layers DEVICE pointers to the caches
+ *                   [gpu_blocks, Hk, bs, D], 16-byte aligned
+ *   host_k, host_v  HOST arrays of num_layers pointers to HOST pools of
+ *                   host_blocks blocks of the same size, pinned and mapped for
+ *                   the device (cudaHostAlloc, or torch's pin_memory);
+ *                   PKV_EINVAL otherwise
+ *   pairs           int64 [num_pairs, 2] (device): (gpu block, host block)
+ *   block_bytes     bytes of one block of one cache, a multiple of 16
+ *   direction       PKV_SWAP_OUT (gpu block -> host block) or PKV_SWAP_IN
+ *                   (host block -> gpu block)
+ * Pairs with an id outside its pool: skipped, PKV_DEV_BAD_BLOCK.  Bit-exact
+ * copy.  Caller contract: the destination blocks are distinct; the host
+ * pools stay allocated until the stream has passed the call.
+ */
+enum { PKV_SWAP_OUT = 0, PKV_SWAP_IN = 1 };
+int pkv_swap_blocks(void *const *gpu_k, void *const *gpu_v, void *const *host_k,
+                    void *const *host_v, int num_layers, const int64_t *pairs, int num_pairs,
+                    size_t block_bytes, int64_t gpu_blocks, int64_t host_blocks, int direction,
+                    uint32_t *device_status, void *stream);
+
+/*
  * paged_attention_decode_static -- the same attention as
  * pkv_paged_attention_decode, for callers that cannot allocate device
  * memory.  (The pages have no counterpart; this is a convenience of this

@@ -381,9 +381,11 @@ uint32_t pkv_oracle_copy_blocks(void *const *k_caches, void *const *v_caches, in
     return st;
 }
 
-/* Swapping blocks out to host memory and back in ("Advanced Features": a
- * preempted sequence's blocks can be moved to CPU memory and restored).
- * Pair p = (gpu block, host block); direction 0 copies every layer's K and V
+/* Swapping blocks out to host memory and back in (PagedAttention: Efficient
+ * LLM Serving with vLLM, "vLLM: The Serving Engine": a preempted request's
+ * KV cache goes to CPU memory when the GPU is full and comes back when it
+ * resumes; the paper's section 7.3 compares this with recomputation). */
+/* Pair p = (gpu block, host block); direction 0 copies every layer's K and V
  * gpu block -> host block, direction 1 host block -> gpu block.  A pair with
  * an id outside its pool is skipped and flags ORC_BAD_BLOCK. */
 uint32_t pkv_oracle_swap_blocks(void *const *gpu_k, void *const *gpu_v, void *const *host_k,

@@ -27,7 +27,8 @@ __all__ = [
     "PkvError", "load_library", "paged_attention_decode", "reshape_and_cache", "copy_blocks",
     "paged_attention_workspace_bytes", "status_string", "last_decode_launches",
     "paged_attention_decode_shared", "plan_shared_prefix", "SharedPrefixPlan",
-    "set_decode_engine", "last_decode_engine", "kv_cache_usage", "KvCacheUsage",
+    "set_decode_engine", "last_decode_engine", "kv_cache_usage", "KvCacheUsage", "swap_blocks",
+    "SWAP_OUT", "SWAP_IN",
     "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "HEADER_PATH",
 ]
 
@@ -81,6 +82,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_reshape_and_cache.restype = i32
     L.pkv_copy_blocks.argtypes = [vp, vp, i32, vp, i32, u64, i64, vp, vp]
     L.pkv_copy_blocks.restype = i32
+    L.pkv_swap_blocks.argtypes = [vp, vp, vp, vp, i32, vp, i32, u64, i64, i64, i32, vp, vp]
+    L.pkv_swap_blocks.restype = i32
     L.pkv_status_string.argtypes = [i32]
     L.pkv_status_string.restype = ctypes.c_char_p
     L.pkv_last_decode_launches.argtypes = []
@@ -350,3 +353,37 @@ def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tenso
                                         int(src_dst_pairs.numel() // 2), block_bytes, shape[0],
                                         _ptr(device_status), _stream(stream))
     _check(rc, "pkv_copy_blocks")
+
+
+SWAP_OUT, SWAP_IN = 0, 1
+
+
+def swap_blocks(gpu_k: Sequence[torch.Tensor], gpu_v: Sequence[torch.Tensor],
+                host_k: Sequence[torch.Tensor], host_v: Sequence[torch.Tensor],
+                pairs: torch.Tensor, direction: int, *,
+                device_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Moves whole blocks between every layer's GPU caches and pinned host
+    pools: pairs (gpu block, host block), SWAP_OUT copies gpu -> host,
+    SWAP_IN host -> gpu."""
+    if not (len(gpu_k) == len(gpu_v) == len(host_k) == len(host_v)) or not gpu_k:
+        raise ValueError("need one K and one V pool per layer on each side")
+    _need_cuda(*gpu_k, *gpu_v, pairs, device_status)
+    if pairs.dtype != torch.int64:
+        raise ValueError("pairs must be int64")
+    gshape, hshape = tuple(gpu_k[0].shape), tuple(host_k[0].shape)
+    for c in list(gpu_k) + list(gpu_v):
+        if tuple(c.shape) != gshape or c.dtype != gpu_k[0].dtype:
+            raise ValueError("all GPU caches must share shape and dtype")
+    for c in list(host_k) + list(host_v):
+        if tuple(c.shape[1:]) != gshape[1:] or c.shape[0] != hshape[0] or c.dtype != gpu_k[0].dtype:
+            raise ValueError("host pools must hold blocks of the GPU caches' shape and dtype")
+        if c.is_cuda or not c.is_pinned():
+            raise ValueError("host pools must be pinned CPU tensors")
+    nl = len(gpu_k)
+    arr = lambda cs: (ctypes.c_void_p * nl)(*[c.data_ptr() for c in cs])
+    block_bytes = gpu_k[0][0].numel() * gpu_k[0].element_size()
+    rc = load_library().pkv_swap_blocks(arr(gpu_k), arr(gpu_v), arr(host_k), arr(host_v), nl,
+                                        _ptr(pairs), int(pairs.numel() // 2), block_bytes,
+                                        gshape[0], hshape[0], int(direction),
+                                        _ptr(device_status), _stream(stream))
+    _check(rc, "pkv_swap_blocks")

@@ -65,4 +65,53 @@ copy_blocks_kernel(const __grid_constant__ CopyBlocksParams ptrs, const int64_t 
         d[i] = s[i];
 }
 
+// swap_blocks (a preempted request's blocks go to CPU memory when the GPU is
+// full and come back when it resumes: PagedAttention: Efficient LLM Serving
+// with vLLM, "vLLM: The Serving Engine"): grid (pair, layer, K/V), one CTA
+// moves one block between the GPU pool and a pinned, device-mapped host pool
+// over the host link.  One launch moves any number of blocks, so small blocks
+// cost no transfer each.  Each thread keeps four 16-byte loads in flight.
+constexpr int kSwapMaxLayers = 64;
+
+struct SwapBlocksParams {
+    uint4 *gpu_k[kSwapMaxLayers];
+    uint4 *gpu_v[kSwapMaxLayers];
+    uint4 *host_k[kSwapMaxLayers];
+    uint4 *host_v[kSwapMaxLayers];
+};
+
+__global__ void __launch_bounds__(256)
+swap_blocks_kernel(const __grid_constant__ SwapBlocksParams ptrs, const int64_t *__restrict__ pairs,
+                   int64_t block_vecs, int64_t gpu_blocks, int64_t host_blocks, int to_host,
+                   uint32_t *status)
+{
+    const int pr = blockIdx.x, layer = blockIdx.y, which = blockIdx.z;
+    const int64_t g = pairs[2 * pr], h = pairs[2 * pr + 1];
+    if (g < 0 || g >= gpu_blocks || h < 0 || h >= host_blocks) {
+        if (threadIdx.x == 0 && layer == 0 && which == 0)
+            report(status, PKV_DEV_BAD_BLOCK);
+        return;
+    }
+    uint4 *gb = (which == 0 ? ptrs.gpu_k[layer] : ptrs.gpu_v[layer]) + g * block_vecs;
+    uint4 *hb = (which == 0 ? ptrs.host_k[layer] : ptrs.host_v[layer]) + h * block_vecs;
+    const uint4 *src = to_host ? gb : hb;
+    uint4 *dst = to_host ? hb : gb;
+    constexpr int U = 4;
+    for (int64_t i0 = threadIdx.x; i0 < block_vecs; i0 += U * blockDim.x) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + (int64_t)u * blockDim.x;
+            if (i < block_vecs)
+                v[u] = src[i];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + (int64_t)u * blockDim.x;
+            if (i < block_vecs)
+                dst[i] = v[u];
+        }
+    }
+}
+
 }  // namespace pkv

@@ -428,4 +428,52 @@ int pkv_copy_blocks(void *const *k_caches, void *const *v_caches, int num_layers
     return PKV_OK;
 }
 
+int pkv_swap_blocks(void *const *gpu_k, void *const *gpu_v, void *const *host_k,
+                    void *const *host_v, int num_layers, const int64_t *pairs, int num_pairs,
+                    size_t block_bytes, int64_t gpu_blocks, int64_t host_blocks, int direction,
+                    uint32_t *device_status, void *stream)
+{
+    if (num_layers < 0 || num_pairs < 0 || block_bytes == 0 || block_bytes % 16 ||
+        gpu_blocks <= 0 || host_blocks <= 0 ||
+        (direction != PKV_SWAP_OUT && direction != PKV_SWAP_IN))
+        return PKV_EINVAL;
+    if (num_layers == 0 || num_pairs == 0)
+        return PKV_OK;
+    if (!gpu_k || !gpu_v || !host_k || !host_v || !pairs)
+        return PKV_EINVAL;
+    for (int l0 = 0; l0 < num_layers; l0 += kSwapMaxLayers) {
+        const int nl = num_layers - l0 < kSwapMaxLayers ? num_layers - l0 : kSwapMaxLayers;
+        SwapBlocksParams ptrs;
+        for (int l = 0; l < nl; ++l) {
+            void *hk = nullptr, *hv = nullptr;
+            if (!gpu_k[l0 + l] || !gpu_v[l0 + l] || !aligned16(gpu_k[l0 + l]) ||
+                !aligned16(gpu_v[l0 + l]))
+                return PKV_EINVAL;
+            // the host pools must be pinned and mapped into the device's
+            // address space (cudaHostAlloc / torch pin_memory)
+            if (!host_k[l0 + l] || !host_v[l0 + l] ||
+                cudaHostGetDevicePointer(&hk, host_k[l0 + l], 0) != cudaSuccess ||
+                cudaHostGetDevicePointer(&hv, host_v[l0 + l], 0) != cudaSuccess ||
+                !aligned16(hk) || !aligned16(hv)) {
+                (void)cudaGetLastError();
+                return PKV_EINVAL;
+            }
+            ptrs.gpu_k[l] = static_cast<uint4 *>(gpu_k[l0 + l]);
+            ptrs.gpu_v[l] = static_cast<uint4 *>(gpu_v[l0 + l]);
+            ptrs.host_k[l] = static_cast<uint4 *>(hk);
+            ptrs.host_v[l] = static_cast<uint4 *>(hv);
+        }
+        static unsigned long long swap_attr = 0;
+        if (ensure_smem_attr(reinterpret_cast<const void *>(swap_blocks_kernel), 0, &swap_attr))
+            return PKV_ECUDA;
+        dim3 grid(num_pairs, nl, 2);
+        swap_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+            ptrs, pairs, (int64_t)(block_bytes / 16), gpu_blocks, host_blocks,
+            direction == PKV_SWAP_OUT ? 1 : 0, device_status);
+        if (cudaGetLastError() != cudaSuccess)
+            return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
+
 }  // extern "C"

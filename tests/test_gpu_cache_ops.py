@@ -88,3 +88,80 @@ def test_copy_blocks_bad_pair_is_skipped_and_reported():
     torch.cuda.synchronize()
     assert st.item() == pkv.DEV_BAD_BLOCK
     assert torch.equal(kc[2], before[1]) and torch.equal(kc[0], before[0]) and torch.equal(kc[3], before[3])
+
+
+def _swap_case(seed, layers, NB, NH, Hk, bs, D, dtype):
+    g = torch.Generator().manual_seed(seed)
+    gk = [torch.randn(NB, Hk, bs, D, generator=g).to(DT[dtype]) for _ in range(layers)]
+    gv = [torch.randn(NB, Hk, bs, D, generator=g).to(DT[dtype]) for _ in range(layers)]
+    hk = [torch.zeros(NH, Hk, bs, D, dtype=DT[dtype]).pin_memory() for _ in range(layers)]
+    hv = [torch.zeros(NH, Hk, bs, D, dtype=DT[dtype]).pin_memory() for _ in range(layers)]
+    return gk, gv, hk, hv
+
+
+def _bytes(t):
+    return raw_np(t.cpu()).view(np.uint8)
+
+
+@pytest.mark.parametrize("dtype,Hk,bs,D,layers", [("bf16", 8, 16, 128, 3), ("f16", 4, 8, 64, 1),
+                                                  ("f32", 2, 32, 64, 2)])
+def test_swap_blocks_round_trip_bit_exact(dtype, Hk, bs, D, layers):
+    """Swap-out writes each pair's GPU block into its host block, bit for bit
+    as the oracle's copy; after the GPU blocks were reused, swap-in puts them
+    back."""
+    import paged_kv_cache_311_gb300 as pkv
+    NB, NH = 64, 40
+    gk, gv, hk, hv = _swap_case(7 + Hk, layers, NB, NH, Hk, bs, D, dtype)
+    rng = np.random.default_rng(Hk)
+    pairs = np.stack([rng.permutation(NB)[:30], rng.permutation(NH)[:30]], axis=1).astype(np.int64)
+    ref_hk = [raw_np(h).copy() for h in hk]; ref_hv = [raw_np(h).copy() for h in hv]
+    ref_gk = [raw_np(x).copy() for x in gk]; ref_gv = [raw_np(x).copy() for x in gv]
+    assert oracle.swap_blocks(ref_gk, ref_gv, ref_hk, ref_hv, pairs, 0) == 0
+    dk = [x.cuda() for x in gk]; dv = [x.cuda() for x in gv]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dp = torch.from_numpy(pairs).cuda()
+    pkv.swap_blocks(dk, dv, hk, hv, dp, pkv.SWAP_OUT, device_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for l in range(layers):
+        assert np.array_equal(_bytes(hk[l]), ref_hk[l].view(np.uint8))
+        assert np.array_equal(_bytes(hv[l]), ref_hv[l].view(np.uint8))
+        dk[l][dp[:, 0]] = 0      # the blocks are reused while the sequence is out
+        dv[l][dp[:, 0]] = 0
+    pkv.swap_blocks(dk, dv, hk, hv, dp, pkv.SWAP_IN, device_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for l in range(layers):
+        assert np.array_equal(_bytes(dk[l]), raw_np(gk[l]).view(np.uint8))
+        assert np.array_equal(_bytes(dv[l]), raw_np(gv[l]).view(np.uint8))
+
+
+def test_swap_blocks_many_small_blocks_in_one_launch():
+    """The small-block case the pages call costly for swapping (many small
+    transfers): 2,000 blocks of 8 rows move in one launch, bit-exact."""
+    import paged_kv_cache_311_gb300 as pkv
+    NB, NH = 4096, 2048
+    gk, gv, hk, hv = _swap_case(3, 1, NB, NH, 8, 8, 64, "bf16")
+    pairs = np.stack([np.random.default_rng(1).permutation(NB)[:2000], np.arange(2000)], 1)
+    dp = torch.from_numpy(pairs.astype(np.int64)).cuda()
+    dk, dv = [gk[0].cuda()], [gv[0].cuda()]
+    pkv.swap_blocks(dk, dv, hk, hv, dp, pkv.SWAP_OUT)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bytes(hk[0])[:2000], raw_np(gk[0]).view(np.uint8)[pairs[:, 0]])
+    assert np.array_equal(_bytes(hv[0])[:2000], raw_np(gv[0]).view(np.uint8)[pairs[:, 0]])
+
+
+def test_swap_blocks_bad_pair_and_unpinned_host():
+    import paged_kv_cache_311_gb300 as pkv
+    gk, gv, hk, hv = _swap_case(5, 1, 8, 4, 2, 16, 64, "f16")
+    dk, dv = [gk[0].cuda()], [gv[0].cuda()]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dp = torch.tensor([[1, 0], [8, 1], [2, 4], [3, 2]], dtype=torch.int64, device="cuda")
+    pkv.swap_blocks(dk, dv, hk, hv, dp, pkv.SWAP_OUT, device_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & pkv.DEV_BAD_BLOCK
+    assert np.array_equal(_bytes(hk[0])[0], raw_np(gk[0]).view(np.uint8)[1])
+    assert np.array_equal(_bytes(hk[0])[2], raw_np(gk[0]).view(np.uint8)[3])
+    assert not _bytes(hk[0])[1].any()                    # the (8, 1) pair was skipped
+    with pytest.raises(ValueError):
+        pkv.swap_blocks(dk, dv, [torch.zeros_like(hk[0])], hv, dp, pkv.SWAP_OUT)
