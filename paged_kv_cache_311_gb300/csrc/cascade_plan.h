@@ -12,9 +12,11 @@
 //                              differs)
 //   items[num_items][item_ints]
 // An item is {seq0, nrows, slot, nseg, tiles, ids, checks, 0}, then
-// max_segments segments of {table_seq, tok_begin, tok_end, row_lo, row_hi,
-// first_tile, id_off, check_off}, then kTableCap block ids: query rows
-// r < nrows are head r % G of sequence seq0 + r / G; segment k covers tokens
+// kMaxRows member sequence ids, then max_segments segments of {table_seq,
+// tok_begin, tok_end, row_lo, row_hi, first_tile, id_off, check_off}, then
+// kTableCap block ids: query rows r < nrows are head r % G of sequence
+// members[r / G] (a group's members need not be neighbours in the batch;
+// seq0 is the first member); segment k covers tokens
 // [tok_begin, tok_end) addressed by table_seq's block table, for rows
 // [row_lo, row_hi); its 16-token tiles are the item's tiles [first_tile, ...),
 // its block ids start at id_off, and its device-table checks (one per block,
@@ -53,7 +55,8 @@ constexpr int kSegInts = 8;
 constexpr int kTileTokens = 16;     // tokens per warp tile of the kernel
 
 constexpr int max_segments(int group) { return 1 + kMaxRows / group; }
-constexpr int item_ids_offset(int group) { return kItemHead + kSegInts * max_segments(group); }
+constexpr int item_segments_offset() { return kItemHead + kMaxRows; }
+constexpr int item_ids_offset(int group) { return item_segments_offset() + kSegInts * max_segments(group); }
 constexpr int item_ints(int group) { return item_ids_offset(group) + kTableCap; }
 
 }  // namespace plan

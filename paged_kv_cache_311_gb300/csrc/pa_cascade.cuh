@@ -36,6 +36,7 @@ struct CascadeCfg {
     static constexpr int MAXSEG = plan::max_segments(G);
     static constexpr int ITEM_INTS = plan::item_ints(G);
     static constexpr int IDS = plan::item_ids_offset(G);
+    static constexpr int SEGS = plan::item_segments_offset();
     static constexpr int TABLE_CAP = plan::kTableCap;
     // ring | barriers | flag | q rows | item copy (with its block ids) | bad
     // flag per segment, members' expected partial counts, bad-row and
@@ -119,7 +120,8 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     const int seq0 = it[plan::I_SEQ0], nrows = it[plan::I_NROWS], slot = it[plan::I_SLOT];
     const int nseg = it[plan::I_NSEG], total = it[plan::I_TILES];
     const int nmem = nrows / G;
-    const CtaWork w{seq0, nrows, kvh, 0, 0, slot, seq0};
+    const int32_t *members = it + plan::kItemHead;   // the item's sequences, member m = rows mG..
+    const CtaWork w{seq0, nrows, kvh, 0, 0, slot, seq0, members};
     if (nseg == 0) {  // empty or invalid context: zero rows, nothing to merge
         const int L = p.context_lens[seq0];
         if ((L < 0 || L > p.max_context_len) && tid == 0 && kvh == 0)
@@ -129,7 +131,7 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         return;
     }
     // segment k: seg(k)[plan::S_*]; its block ids start at ids + S_ID_OFF
-    auto seg = [&](int k) { return it + plan::kItemHead + plan::kSegInts * k; };
+    auto seg = [&](int k) { return it + CC::SEGS + plan::kSegInts * k; };
     int32_t *ids = it + CC::IDS;
     const bool invalid_item = it[plan::I_IDS] > CC::TABLE_CAP;
 
@@ -195,7 +197,7 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                     const int local = x - g[plan::S_CHECK_OFF];
                     const int m = local / nb, i = local % nb;
                     const bool shared = g[plan::S_ROW_LO] == 0 && g[plan::S_ROW_HI] == nrows && nmem > 1;
-                    const int s = shared ? seq0 + m : g[plan::S_TABLE_SEQ];
+                    const int s = shared ? members[m] : g[plan::S_TABLE_SEQ];
                     got[u] = p.block_tables[(int64_t)s * p.max_blocks_per_seq + g[plan::S_BEGIN] / BS + i];
                     want[u] = ids[g[plan::S_ID_OFF] + i];
                     kk[u] = k;
@@ -209,8 +211,9 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     }
     CC::Engine::stage_q_rows(p, smem + CC::OFF_Q, w);
     if (tid < nmem) {
-        exp_s[tid] = expected[seq0 + tid];
-        if (plan_lens[seq0 + tid] != p.context_lens[seq0 + tid])
+        const int sq = members[tid];
+        exp_s[tid] = expected[sq];
+        if (plan_lens[sq] != p.context_lens[sq])
             atomicOr(lenbad, 1u << tid);
     }
     __syncthreads();

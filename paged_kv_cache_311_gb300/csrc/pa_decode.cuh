@@ -160,13 +160,18 @@ __device__ __forceinline__ void store_out4(void *out, int dtype, int64_t i, floa
 // (kvh * G + r % G) of sequence seq0 + r / G, over the tokens [tok0, tok_end)
 // that the block table of `table_seq` addresses; split partials go to
 // workspace slot `slot`.
+// Query rows r < nrows of a CTA are head r % G (of its kv head's group) of
+// sequence seq0 + r / G, or of members[r / G] when the CTA serves an explicit
+// list of sequences (a shared-prefix item).
 struct CtaWork {
     int seq0, nrows, kvh, tok0, tok_end, slot, table_seq;
+    const int32_t *members = nullptr;
 };
 
 __device__ __forceinline__ int64_t row_head(const DecodeParams &p, const CtaWork &w, int G, int r)
 {
-    return (int64_t)(w.seq0 + r / G) * p.num_heads + w.kvh * G + r % G;
+    const int seq = w.members ? w.members[r / G] : w.seq0 + r / G;
+    return (int64_t)seq * p.num_heads + w.kvh * G + r % G;
 }
 
 // Writes the result of a CTA that cannot produce one (bad length / block):

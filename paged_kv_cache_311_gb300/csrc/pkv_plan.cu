@@ -39,8 +39,9 @@ struct Seg {
 struct Item {
     int seq0, nrows, slot;
     std::vector<Seg> segs;
-    long long weight;  // tokens x row n-tiles, for the heavy-first order
+    long long weight;  // tokens streamed, for the heavy-first order
     int entries;       // block-table entries of all segments
+    std::vector<int> members;  // the sequences whose rows the item serves
 };
 
 int blocks_between(int tb, int te, int bs) { return (te + bs - 1) / bs - tb / bs; }
@@ -100,44 +101,65 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         return L > 0 && L <= max_context_len;
     };
 
-    // tokens sequence s shares with s - 1
+    // Sequences that share leading blocks are grouped wherever they sit in
+    // the batch (forked samples are neighbours, requests that reuse a cached
+    // system prompt need not be): order them by the block ids of their
+    // tables, valid contexts first and batch order among equal prefixes.
+    auto nblk = [&](int s) { return len_ok(s) ? (context_lens[s] + bs - 1) / bs : 0; };
+    std::vector<int> order(B);
+    for (int s = 0; s < B; ++s)
+        order[s] = s;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        const int na = nblk(a), nb = nblk(b);
+        if ((na > 0) != (nb > 0))
+            return na > 0;
+        const int32_t *ta = block_tables + (long long)a * MB, *tb = block_tables + (long long)b * MB;
+        for (int j = 0, n = std::min(na, nb); j < n; ++j)
+            if (ta[j] != tb[j])
+                return ta[j] < tb[j];
+        return false;
+    });
+
+    // tokens that order[k] shares with order[k - 1]
     std::vector<int> sp(B, 0);
-    for (int s = 1; s < B; ++s) {
-        if (!len_ok(s - 1) || !len_ok(s))
+    for (int k = 1; k < B; ++k) {
+        const int sa = order[k - 1], sb = order[k];
+        if (!len_ok(sa) || !len_ok(sb))
             continue;
-        const int la = context_lens[s - 1], lb = context_lens[s];
-        const int n = std::min((la + bs - 1) / bs, (lb + bs - 1) / bs);
-        const int32_t *a = block_tables + (long long)(s - 1) * MB;
-        const int32_t *b = block_tables + (long long)s * MB;
+        const int la = context_lens[sa], lb = context_lens[sb];
+        const int n = std::min(nblk(sa), nblk(sb));
+        const int32_t *a = block_tables + (long long)sa * MB;
+        const int32_t *b = block_tables + (long long)sb * MB;
         int c = 0;
         while (c < n && a[c] == b[c])
             ++c;
-        sp[s] = std::min(c * bs, std::min(la, lb)) / align * align;
+        sp[k] = std::min(c * bs, std::min(la, lb)) / align * align;
     }
 
-    // groups: runs of up to max_members consecutive sequences that share S
-    // leading tokens (cnt == 1: a sequence on its own)
+    // groups: runs of up to max_members neighbours in that order that share
+    // S leading tokens (cnt == 1: a sequence on its own); member m of a
+    // group is sequence order[first + m]
     struct Group {
-        int s, cnt, S;
+        int first, cnt, S;
     };
     std::vector<Group> groups;
     long long total = 0;   // tokens to stream per kv head, shared ones once
-    for (int s = 0; s < B;) {
+    for (int k = 0; k < B;) {
         int cnt = 1, S = 0x7fffffff;
-        while (cnt < max_members && s + cnt < B && sp[s + cnt] > 0) {
-            S = std::min(S, sp[s + cnt]);
+        while (cnt < max_members && k + cnt < B && sp[k + cnt] > 0) {
+            S = std::min(S, sp[k + cnt]);
             ++cnt;
         }
         if (cnt < 2) {
-            groups.push_back(Group{s, 1, 0});
-            total += len_ok(s) ? context_lens[s] : 0;
+            groups.push_back(Group{k, 1, 0});
+            total += len_ok(order[k]) ? context_lens[order[k]] : 0;
         } else {
-            groups.push_back(Group{s, cnt, S});
+            groups.push_back(Group{k, cnt, S});
             total += S;
             for (int m = 0; m < cnt; ++m)
-                total += context_lens[s + m] - S;
+                total += context_lens[order[k + m]] - S;
         }
-        s += cnt;
+        k += cnt;
     }
 
     // A member's own tail costs whole 16-row loads; it joins its group's
@@ -148,7 +170,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         long long F = 0;
         int entries = 0;
         for (int m = 0; m < g.cnt; ++m) {
-            const int t = context_lens[g.s + m] - g.S, need = blocks_between(g.S, g.S + t, bs);
+            const int t = context_lens[order[g.first + m]] - g.S, need = blocks_between(g.S, g.S + t, bs);
             const bool f = t > 0 && F + tail_cost(t) <= T && entries + need <= kTableCap / 2;
             if (f) {
                 F += tail_cost(t);
@@ -164,14 +186,14 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         long long n = 0;
         for (const Group &g : groups) {
             if (g.cnt == 1) {
-                n += len_ok(g.s) ? (context_lens[g.s] + T - 1) / T : 1;
+                n += len_ok(order[g.first]) ? (context_lens[order[g.first]] + T - 1) / T : 1;
                 continue;
             }
             std::vector<char> folded(g.cnt, 0);
             const long long F = fold_tails(g, T, &folded);
             n += std::max(1LL, (g.S + F + T - 1) / T);
             for (int m = 0; m < g.cnt; ++m) {
-                const int t = context_lens[g.s + m] - g.S;
+                const int t = context_lens[order[g.first + m]] - g.S;
                 if (t > 0 && !folded[m])
                     n += (t + T - 1) / T;
             }
@@ -216,15 +238,17 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         const std::vector<int> b = cut(tb, te, (te - tb + T - 1) / T);
         for (size_t k = 0; k + 1 < b.size(); ++k)
             items.push_back(Item{seq, G, first_slot + (int)k, {Seg{seq, b[k], b[k + 1], 0, G}},
-                                 (long long)(b[k + 1] - b[k]), blocks_between(b[k], b[k + 1], bs)});
+                                 (long long)(b[k + 1] - b[k]), blocks_between(b[k], b[k + 1], bs),
+                                 {seq}});
         return (int)b.size() - 1;
     };
 
     for (const Group &g : groups) {
-        const int s = g.s, cnt = g.cnt, S = g.S;
+        const int s = order[g.first], cnt = g.cnt, S = g.S;
+        std::vector<int> mem(order.begin() + g.first, order.begin() + g.first + cnt);
         if (cnt == 1) {
             if (!len_ok(s))
-                items.push_back(Item{s, G, 0, {}, 0, 0});   // zero output
+                items.push_back(Item{s, G, 0, {}, 0, 0, {s}});   // zero output
             else
                 expected[s] = add_partitions(s, 0, context_lens[s], 0);
             continue;
@@ -248,9 +272,10 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
             const std::vector<int> b = cut(0, Sp, n_g - 1);
             for (size_t k = 0; k + 1 < b.size(); ++k, ++n_pre)
                 items.push_back(Item{s, rows, n_pre, {Seg{s, b[k], b[k + 1], 0, rows}},
-                                     (long long)(b[k + 1] - b[k]), blocks_between(b[k], b[k + 1], bs)});
+                                     (long long)(b[k + 1] - b[k]), blocks_between(b[k], b[k + 1], bs),
+                                     mem});
         }
-        Item last{s, rows, n_pre, {}, 0, 0};
+        Item last{s, rows, n_pre, {}, 0, 0, mem};
         if (Sp < S) {
             last.segs.push_back(Seg{s, Sp, S, 0, rows});
             last.weight += S - Sp;
@@ -258,7 +283,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         }
         for (int m = 0; m < cnt; ++m)
             if (folded[m]) {
-                const int seq = s + m, L = context_lens[seq];
+                const int seq = mem[m], L = context_lens[seq];
                 last.segs.push_back(Seg{seq, S, L, m * G, (m + 1) * G});
                 last.weight += L - S;
                 last.entries += blocks_between(S, L, bs);
@@ -266,7 +291,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         items.push_back(last);
         const int n_items = n_pre + 1;
         for (int m = 0; m < cnt; ++m) {
-            const int seq = s + m, L = context_lens[seq];
+            const int seq = mem[m], L = context_lens[seq];
             const int n_tail = (L > S && !folded[m]) ? add_partitions(seq, S, L, n_items) : 0;
             expected[seq] = n_items + n_tail;
         }
@@ -307,6 +332,8 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         const int nmem = it.nrows / G;
         int tiles = 0, nids = 0, checks = 0;
         dst[I_SEQ0] = it.seq0;
+        for (int m = 0; m < kMaxRows; ++m)
+            dst[kItemHead + m] = m < (int)it.members.size() ? it.members[m] : -1;
         dst[I_NROWS] = it.nrows;
         dst[I_SLOT] = it.slot;
         dst[I_NSEG] = (int)it.segs.size();
@@ -315,7 +342,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
             const Seg &g = it.segs[k];
             const int nb = blocks_between(g.tok_begin, g.tok_end, bs);
             const bool shared = g.row_lo == 0 && g.row_hi == it.nrows && nmem > 1;
-            int32_t *q = dst + kItemHead + kSegInts * k;
+            int32_t *q = dst + item_segments_offset() + kSegInts * k;
             q[S_TABLE_SEQ] = g.table_seq;
             q[S_BEGIN] = g.tok_begin;
             q[S_END] = g.tok_end;

@@ -237,3 +237,25 @@ def test_fp32_is_rejected():
     with pytest.raises(pkv.PkvError) as e:
         run_shared(case)
     assert e.value.status == -2
+
+
+def test_sharers_scattered_through_the_batch():
+    """The batch order is shuffled, so each group's members are scattered
+    (requests reusing a cached prompt arrive in any order): the planner still
+    groups them and every output matches the oracle."""
+    case = shared_case(14, dtype="bf16", H=16, Hk=4, D=128, bs=16, groups=GROUPS)
+    perm = np.random.default_rng(14).permutation(len(case["context_lens"]))
+    shuffled = dict(case, q=case["q"][torch.from_numpy(perm)],
+                    block_tables=np.ascontiguousarray(case["block_tables"][perm]),
+                    context_lens=np.ascontiguousarray(case["context_lens"][perm]))
+    import paged_kv_cache_311_gb300 as pkv
+    plan = pkv.plan_shared_prefix(shuffled["block_tables"], shuffled["context_lens"], 16, 4, 128, 16)
+    h, B = plan.host, len(perm)
+    base, iints = 8 + 2 * B, int(h[4])
+    nrows = [int(h[base + i * iints + 1]) for i in range(int(h[0]))]
+    assert max(nrows) > 4                    # groups formed: an item serves several sequences
+    ref, _ = oracle_out(shuffled)
+    for P in (0, 64):
+        got, st = run_shared(shuffled, P=P)
+        assert st == 0
+        assert max_err(got, ref) <= TOL["bf16"], f"P={P}"

@@ -28,10 +28,12 @@ def decode_plan(plan, B, Hk, G):
     for i in range(n_items):
         it = h[base + i * iints: base + (i + 1) * iints]
         seq0, nrows, slot, nseg, tiles, nids, checks = (int(x) for x in it[:7])
-        raw = [[int(x) for x in it[8 + 8 * k: 16 + 8 * k]] for k in range(nseg)]
+        members = [int(x) for x in it[8:8 + nrows // G]]
+        assert members[0] == seq0 and all(x == -1 for x in it[8 + nrows // G:32])
+        raw = [[int(x) for x in it[32 + 8 * k: 40 + 8 * k]] for k in range(nseg)]
         segs = [tuple(r[:5]) for r in raw]
-        ids = it[8 + 8 * maxseg:]
-        items.append((seq0, nrows, slot, segs, ids, (tiles, nids, checks), raw))
+        ids = it[32 + 8 * maxseg:]
+        items.append((seq0, nrows, slot, segs, ids, (tiles, nids, checks), raw, members))
     return items, expected, slots
 
 
@@ -41,7 +43,8 @@ def check_coverage(plan, tables, lens, G, Hk, bs=16):
     np.testing.assert_array_equal(plan.host[8 + B:8 + 2 * B], lens)   # the lengths it was made for
     covered = [np.zeros(max(int(L), 0), dtype=int) for L in lens]
     slots_seen = [set() for _ in range(B)]
-    for seq0, nrows, slot, segs, ids, totals, raw in items:
+    for seq0, nrows, slot, segs, ids, totals, raw, members in items:
+        assert len(set(members)) == len(members)
         assert nrows % G == 0 and nrows <= 24
         if not segs:
             assert lens[seq0] <= 0
@@ -65,7 +68,7 @@ def check_coverage(plan, tables, lens, G, Hk, bs=16):
         for tseq, tb, te, rlo, rhi in segs:
             assert rlo % G == 0 and rhi % G == 0
             for m in range(rlo // G, rhi // G):
-                s = seq0 + m
+                s = members[m]
                 assert 0 <= tb < te <= lens[s]
                 # the tokens come from table_seq's blocks: they must be s's blocks too
                 j = np.arange(tb // bs, -(-te // bs))
@@ -95,7 +98,7 @@ def test_forked_prompts_share_their_full_blocks():
     prefix_items = [it for it in items if it[1] == 24]
     for p, lp in enumerate(w.prompt_lens):
         shared = (int(lp) // 16 * 16) // 32 * 32
-        mine = [it for it in prefix_items if it[0] == 6 * p]
+        mine = [it for it in prefix_items if set(it[7]) == set(range(6 * p, 6 * p + 6))]
         assert sum(seg[2] - seg[1] for it in mine for seg in it[3] if seg[3] == 0 and seg[4] == 24) == shared
     # the items come heaviest first (tokens streamed)
     weights = [sum(s[2] - s[1] for s in it[3]) for it in items]
@@ -154,7 +157,7 @@ def test_groups_are_cut_at_24_rows_and_long_tails_split():
     lens = np.array(lens, np.int32)
     plan = pkv.plan_shared_prefix(bt, lens, 16, 4, 128, bs, int(lens.max()), 256)
     items, expected = check_coverage(plan, bt, lens, G, 4)
-    groups = sorted({(it[0], it[1]) for it in items if it[1] > G})
+    groups = sorted({(min(it[7]), it[1]) for it in items if it[1] > G})
     assert groups == [(0, 24), (6, 8)]
     # 192 shared tokens plus five folded 13-token tails (a 16-row load each)
     # exceed one 256-token item: the group takes two; the long tail three more
@@ -172,3 +175,31 @@ def test_empty_context_gets_a_zero_item_and_plan_size_is_bounded():
     assert expected[2] == 0
     # sequences 0 and 1 share block 0 and 1 but only 20 tokens -> below 32: no group
     assert all(it[1] == 4 for it in items)
+
+
+def test_sharers_are_grouped_wherever_they_sit_in_the_batch():
+    """Requests that reuse two cached prompts alternate in the batch with
+    singletons: each prompt's requests form one group (its members listed in
+    the items), and every token is still covered once."""
+    bs, G = 16, 4
+    rng = np.random.default_rng(3)
+    prompt = {0: list(range(0, 20)), 1: list(range(20, 40))}      # 320 tokens each
+    which = [0, 1, None, 0, 1, 0, None, 1, 0]
+    next_block, rows, lens = 100, [], []
+    for w_ in which:
+        own_len = int(rng.integers(1, 60))
+        base = prompt[w_] if w_ is not None else []
+        L = len(base) * bs + own_len
+        nb_own = -(-L // bs) - len(base)
+        rows.append(base + list(range(next_block, next_block + nb_own)))
+        next_block += nb_own
+        lens.append(L)
+    MB = max(len(r) for r in rows)
+    bt = np.full((len(rows), MB), -1, np.int32)
+    for i, r in enumerate(rows):
+        bt[i, :len(r)] = r
+    lens = np.array(lens, np.int32)
+    plan = pkv.plan_shared_prefix(bt, lens, 16, 4, 128, bs, int(lens.max()), 256)
+    items, expected = check_coverage(plan, bt, lens, G, 4)
+    groups = {frozenset(it[7]) for it in items if it[1] > G}
+    assert groups == {frozenset(i for i, w_ in enumerate(which) if w_ == p) for p in (0, 1)}
