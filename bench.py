@@ -179,7 +179,7 @@ def run_native(args):
         cpu = cpu_baseline(cfg, state, host_inputs, args.cpu_seconds, seed)
 
     import paged_kv_cache_311_gb300 as pkv
-    shared = cfg.kind == "shared_prefix" and not args.no_shared
+    shared = cfg.kind in ("shared_prefix", "system_prompt") and not args.no_shared
     if shared and args.partition_size < 0:
         P = 0   # the shared-prefix planner's own default partition
     steps = [state.to_device(inp, shared=shared, partition_size=P) for inp in host_inputs]

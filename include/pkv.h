@@ -207,6 +207,69 @@ int pkv_kv_cache_usage(const int32_t *block_tables, const int32_t *context_lens,
                        int64_t *blocks, int64_t *occupied_slots);
 
 /*
+ * block pool -- HOST allocator of the physical blocks of one paged cache,
+ * with prefix caching (page "PagedAttention: Efficient LLM Serving with
+ * vLLM": blocks are taken on demand, "The PagedAttention Algorithm" Steps
+ * 1-3; sharers hold a block by reference count and a write into a shared
+ * block copies it first, "Advanced Features", KV-Cache Sharing; the blocks of
+ * a common prompt prefix stay cached for later requests, "Advanced
+ * Features", Prefix Caching).  A full prompt block is cached under a key
+ * chained over its own tokens and every token before it; entries keep their
+ * tokens, so a hit is exact.  A cached block nobody holds stays reusable
+ * until the pool needs a block and has no free one: then the least recently
+ * released goes.  Not thread-safe: one caller at a time per pool.
+ */
+typedef struct pkv_block_pool pkv_block_pool;
+
+/* A pool of num_blocks blocks of block_size tokens; NULL on bad sizes or
+ * when memory for it cannot be had.  Block 0 is handed out first. */
+pkv_block_pool *pkv_block_pool_create(int64_t num_blocks, int block_size);
+void pkv_block_pool_destroy(pkv_block_pool *pool);
+
+/* Blocks for a new request's prompt: table[0 .. ceil(num_tokens /
+ * block_size)) receives the longest run of leading full blocks the cache
+ * holds for exactly these tokens (each now held once more), then fresh
+ * blocks.  *cached_tokens = the tokens whose K/V those reused blocks already
+ * hold (a multiple of block_size).  PKV_EWORKSPACE, with nothing taken, if
+ * the pool cannot supply the rest; PKV_EINVAL if table_capacity is short. */
+int pkv_block_pool_allocate_prompt(pkv_block_pool *pool, const int32_t *tokens, int num_tokens,
+                                   int32_t *table, int table_capacity, int *cached_tokens);
+
+/* Once the K/V of a prompt's tokens is in its blocks: caches its full
+ * blocks that no entry holds yet, so later prompts with the same prefix
+ * reuse them.  table must hold blocks the caller holds. */
+int pkv_block_pool_commit_prompt(pkv_block_pool *pool, const int32_t *tokens, int num_tokens,
+                                 const int32_t *table);
+
+/* n fresh blocks (a growing sequence's next block): PKV_EWORKSPACE, with
+ * nothing taken, if the pool has fewer. */
+int pkv_block_pool_allocate(pkv_block_pool *pool, int n, int32_t *out);
+
+/* A forked sequence holds every block of table once more. */
+int pkv_block_pool_fork(pkv_block_pool *pool, const int32_t *table, int num_blocks);
+
+/* The sequence lets go of its blocks: one holder fewer each; a block nobody
+ * holds returns to the free list, or stays cached (reusable, evictable). */
+int pkv_block_pool_release(pkv_block_pool *pool, const int32_t *table, int num_blocks);
+
+/* Before writing into table[logical_block]: if another sequence holds that
+ * block too, or it is a prefix-cache entry, the sequence gets a fresh block
+ * in its place (table updated, one holder fewer on the old one) and
+ * copy_pair = {old, new} for pkv_copy_blocks; returns 1 then, 0 when the
+ * block can be written in place, PKV_EWORKSPACE when no block is left. */
+int pkv_block_pool_prepare_write(pkv_block_pool *pool, int32_t *table, int logical_block,
+                                 int64_t *copy_pair);
+
+/* Blocks a new holder can get (free + cached ones nobody holds), -1 for a
+ * NULL pool; holders of a block; whether it is a cache entry (-1 if out of
+ * range); and counters (any pointer may be NULL). */
+int64_t pkv_block_pool_available(const pkv_block_pool *pool);
+int pkv_block_pool_refcount(const pkv_block_pool *pool, int32_t block);
+int pkv_block_pool_is_cached(const pkv_block_pool *pool, int32_t block);
+int pkv_block_pool_stats(const pkv_block_pool *pool, int64_t *free_blocks, int64_t *cached_blocks,
+                         int64_t *evictable_blocks, uint64_t *lookups, uint64_t *hits);
+
+/*
  * reshape_and_cache -- write each new token's key/value rows into its slot
  * ("The PagedAttention Algorithm", Step 2: generated tokens fill the block).
  *

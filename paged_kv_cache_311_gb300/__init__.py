@@ -28,7 +28,7 @@ __all__ = [
     "paged_attention_workspace_bytes", "status_string", "last_decode_launches",
     "paged_attention_decode_shared", "plan_shared_prefix", "SharedPrefixPlan",
     "set_decode_engine", "last_decode_engine", "kv_cache_usage", "KvCacheUsage", "swap_blocks",
-    "SWAP_OUT", "SWAP_IN",
+    "SWAP_OUT", "SWAP_IN", "BlockPool",
     "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "HEADER_PATH",
 ]
 
@@ -78,6 +78,31 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_kv_cache_usage.argtypes = [vp, vp, i32, i32, i32, i64, ctypes.POINTER(i64),
                                      ctypes.POINTER(i64), ctypes.POINTER(i64)]
     L.pkv_kv_cache_usage.restype = i32
+    L.pkv_block_pool_create.argtypes = [i64, i32]
+    L.pkv_block_pool_create.restype = vp
+    L.pkv_block_pool_destroy.argtypes = [vp]
+    L.pkv_block_pool_destroy.restype = None
+    L.pkv_block_pool_allocate_prompt.argtypes = [vp, vp, i32, vp, i32, ctypes.POINTER(i32)]
+    L.pkv_block_pool_allocate_prompt.restype = i32
+    L.pkv_block_pool_commit_prompt.argtypes = [vp, vp, i32, vp]
+    L.pkv_block_pool_commit_prompt.restype = i32
+    L.pkv_block_pool_allocate.argtypes = [vp, i32, vp]
+    L.pkv_block_pool_allocate.restype = i32
+    L.pkv_block_pool_fork.argtypes = [vp, vp, i32]
+    L.pkv_block_pool_fork.restype = i32
+    L.pkv_block_pool_release.argtypes = [vp, vp, i32]
+    L.pkv_block_pool_release.restype = i32
+    L.pkv_block_pool_prepare_write.argtypes = [vp, vp, i32, vp]
+    L.pkv_block_pool_prepare_write.restype = i32
+    L.pkv_block_pool_available.argtypes = [vp]
+    L.pkv_block_pool_available.restype = i64
+    L.pkv_block_pool_refcount.argtypes = [vp, i32]
+    L.pkv_block_pool_refcount.restype = i32
+    L.pkv_block_pool_is_cached.argtypes = [vp, i32]
+    L.pkv_block_pool_is_cached.restype = i32
+    L.pkv_block_pool_stats.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                       ctypes.POINTER(i64), ctypes.POINTER(u64), ctypes.POINTER(u64)]
+    L.pkv_block_pool_stats.restype = i32
     L.pkv_reshape_and_cache.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, vp, vp]
     L.pkv_reshape_and_cache.restype = i32
     L.pkv_copy_blocks.argtypes = [vp, vp, i32, vp, i32, u64, i64, vp, vp]
@@ -213,6 +238,90 @@ class SharedPrefixPlan:
 
     def to(self, device) -> torch.Tensor:
         return torch.from_numpy(self.host).to(device)
+
+
+class BlockPool:
+    """Host allocator of one paged cache's blocks with prefix caching (the C
+    pkv_block_pool_*).  Tables are numpy int32 arrays of block ids."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._L = load_library()
+        self._p = self._L.pkv_block_pool_create(int(num_blocks), int(block_size))
+        if not self._p:
+            raise PkvError(-1, "pkv_block_pool_create")
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def __del__(self):
+        p, self._p = getattr(self, "_p", None), None
+        if p:
+            self._L.pkv_block_pool_destroy(p)
+
+    @staticmethod
+    def _i32(a):
+        import numpy as np
+        return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+
+    def allocate_prompt(self, tokens):
+        """-> (table, cached_tokens) for a new request's prompt tokens."""
+        import numpy as np
+        t = self._i32(tokens)
+        table = np.empty(max(1, -(-t.size // self.block_size)), np.int32)
+        cached = ctypes.c_int32(0)
+        rc = self._L.pkv_block_pool_allocate_prompt(self._p, t.ctypes.data, t.size,
+                                                    table.ctypes.data, table.size,
+                                                    ctypes.byref(cached))
+        _check(rc, "pkv_block_pool_allocate_prompt")
+        return table[: -(-t.size // self.block_size)].copy(), cached.value
+
+    def commit_prompt(self, tokens, table) -> None:
+        t, tb = self._i32(tokens), self._i32(table)
+        _check(self._L.pkv_block_pool_commit_prompt(self._p, t.ctypes.data, t.size, tb.ctypes.data),
+               "pkv_block_pool_commit_prompt")
+
+    def allocate(self, n: int):
+        import numpy as np
+        out = np.empty(max(n, 1), np.int32)
+        _check(self._L.pkv_block_pool_allocate(self._p, int(n), out.ctypes.data),
+               "pkv_block_pool_allocate")
+        return out[:n].copy()
+
+    def fork(self, table) -> None:
+        tb = self._i32(table)
+        _check(self._L.pkv_block_pool_fork(self._p, tb.ctypes.data, tb.size), "pkv_block_pool_fork")
+
+    def release(self, table) -> None:
+        tb = self._i32(table)
+        _check(self._L.pkv_block_pool_release(self._p, tb.ctypes.data, tb.size),
+               "pkv_block_pool_release")
+
+    def prepare_write(self, table, logical_block: int):
+        """-> (src, dst) copy pair if the block had to be copied first (the
+        table, a numpy int32 array, is updated in place), else None."""
+        import numpy as np
+        assert table.dtype == np.int32 and table.flags.c_contiguous
+        pair = np.zeros(2, np.int64)
+        rc = self._L.pkv_block_pool_prepare_write(self._p, table.ctypes.data, int(logical_block),
+                                                  pair.ctypes.data)
+        if rc < 0:
+            _check(rc, "pkv_block_pool_prepare_write")
+        return (int(pair[0]), int(pair[1])) if rc == 1 else None
+
+    def available(self) -> int:
+        return int(self._L.pkv_block_pool_available(self._p))
+
+    def refcount(self, block: int) -> int:
+        return int(self._L.pkv_block_pool_refcount(self._p, int(block)))
+
+    def is_cached(self, block: int) -> bool:
+        return bool(self._L.pkv_block_pool_is_cached(self._p, int(block)) == 1)
+
+    def stats(self) -> dict:
+        f, c, e = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        lk, h = ctypes.c_uint64(0), ctypes.c_uint64(0)
+        _check(self._L.pkv_block_pool_stats(self._p, ctypes.byref(f), ctypes.byref(c), ctypes.byref(e),
+                                            ctypes.byref(lk), ctypes.byref(h)), "pkv_block_pool_stats")
+        return {"free": f.value, "cached": c.value, "evictable": e.value, "lookups": lk.value,
+                "hits": h.value}
 
 
 class KvCacheUsage:

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB_DIR = os.path.join(HERE, "_lib")
 SOURCES = ["pkv_abi.cu", "pa_decode_f32.cu", "pa_decode_f16.cu", "pa_decode_bf16.cu",
-           "pkv_static_ws.cu", "pkv_plan.cu", "pkv_usage.cu"]
+           "pkv_static_ws.cu", "pkv_plan.cu", "pkv_usage.cu", "pkv_block_pool.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

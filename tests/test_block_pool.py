@@ -1,0 +1,295 @@
+"""The host block pool with prefix caching (pkv_block_pool_*), on the CPU.
+
+Without prefix caching the pool must hand out exactly the blocks the
+oracle's block manager does (on-demand allocation, forks, copy-on-write and
+frees on the page "PagedAttention: Efficient LLM Serving with vLLM", "The
+PagedAttention Algorithm" and "Advanced Features"); with it, a request whose
+prompt starts with the tokens of committed full blocks reuses exactly those
+blocks ("Advanced Features", Prefix Caching)."""
+import os
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_311_gb300 as pkv
+from oracle.block_manager import OracleBlockManager
+from paged_kv_cache_311_gb300.build import build, library_path
+from tests.util import read_golden
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not os.path.exists(library_path()):
+        build()
+    return pkv.load_library()
+
+
+def test_blocks_on_demand_worked_example():
+    _, rows = read_golden("worked_example_blocks.txt")
+    for tokens, bs, blocks, slots, unused in rows:
+        pool = pkv.BlockPool(64, bs)
+        table, cached = pool.allocate_prompt(np.arange(tokens))
+        assert (len(table), cached) == (blocks, 0)
+        np.testing.assert_array_equal(table, np.arange(blocks))    # block 0 first
+        assert pool.available() == 64 - blocks
+
+
+def test_same_blocks_as_the_oracle_block_manager_without_caching():
+    """Random adds, token appends (a new block when the last is full, a
+    copy when it is shared), forks and frees: tables, copy pairs and
+    refcounts follow the oracle's block manager step for step."""
+    rng = np.random.default_rng(8)
+    bs, NB = 16, 400
+    pool, ref = pkv.BlockPool(NB, bs), OracleBlockManager(NB, bs)
+    tables, lens, nxt = {}, {}, 0
+    for step in range(600):
+        op = rng.random()
+        live = sorted(tables)
+        if op < 0.15 or not live:
+            n = int(rng.integers(1, 70))
+            if pool.available() < -(-n // bs) + 8:
+                continue
+            tb, cached = pool.allocate_prompt(rng.integers(0, 1000, n))
+            assert cached == 0
+            assert list(tb) == ref.add_sequence(nxt, n)
+            tables[nxt], lens[nxt] = tb, n
+            nxt += 1
+        elif op < 0.25:
+            s = int(rng.choice(live))
+            pool.fork(tables[s])
+            ref.fork(s, nxt)
+            tables[nxt], lens[nxt] = tables[s].copy(), lens[s]
+            nxt += 1
+        elif op < 0.35:
+            s = int(rng.choice(live))
+            pool.release(tables.pop(s))
+            lens.pop(s)
+            ref.free_sequence(s)
+        else:
+            s = int(rng.choice(live))
+            if pool.available() < 2:
+                continue
+            slot, ref_pair = ref.append_token(s)
+            j, off = divmod(lens[s], bs)
+            if off == 0:
+                tables[s] = np.append(tables[s], pool.allocate(1)).astype(np.int32)
+                pair = None
+            else:
+                pair = pool.prepare_write(tables[s], j)
+            lens[s] += 1
+            assert pair == ref_pair
+            assert tables[s][j] * bs + off == slot
+        for s in tables:
+            assert list(tables[s]) == ref.tables[s]
+    for b in range(NB):
+        assert pool.refcount(b) == ref.refcount[b]
+    assert pool.available() == len(ref.free)
+
+
+def test_prefix_reuse_is_exact_and_chained():
+    bs = 16
+    pool = pkv.BlockPool(64, bs)
+    rng = np.random.default_rng(2)
+    sys_prompt = rng.integers(0, 32000, 3 * bs + 5)          # 3 full blocks + 5 tokens
+    a = np.concatenate([sys_prompt, rng.integers(0, 32000, 20)])
+    ta, ca = pool.allocate_prompt(a)
+    assert ca == 0
+    pool.commit_prompt(a, ta)
+    assert all(pool.is_cached(b) for b in ta[:len(a) // bs]) and not pool.is_cached(ta[-1])
+    # same system prompt, another question: its 3 full blocks are reused;
+    # block 4 of a held the prompt's 5 last tokens plus a's own: no match
+    b = np.concatenate([sys_prompt, rng.integers(0, 32000, 30)])
+    tb, cb = pool.allocate_prompt(b)
+    assert cb == 3 * bs
+    np.testing.assert_array_equal(tb[:3], ta[:3])
+    assert len(set(tb[3:]) & set(ta)) == 0
+    assert [pool.refcount(x) for x in ta[:3]] == [2, 2, 2]
+    # the same tokens for block 2 after a different block 1: only block 0 matches
+    c = a.copy()
+    c[bs + 3] += 1
+    tc, cc = pool.allocate_prompt(c)
+    assert cc == bs and tc[0] == ta[0] and tc[2] != ta[2]
+    # a prompt ending inside a cached block reuses only the full blocks before
+    td, cd = pool.allocate_prompt(a[:2 * bs + 7])
+    assert cd == 2 * bs and list(td[:2]) == list(ta[:2]) and td[2] != ta[2]
+    st = pool.stats()
+    assert st["hits"] == 3 + 1 + 2
+
+
+def test_released_prefix_stays_cached_until_evicted_least_recent_first():
+    bs, NB = 8, 12
+    pool = pkv.BlockPool(NB, bs)
+    p1, p2 = np.arange(2 * bs), np.arange(100, 100 + 2 * bs)
+    t1, _ = pool.allocate_prompt(p1); pool.commit_prompt(p1, t1)
+    t2, _ = pool.allocate_prompt(p2); pool.commit_prompt(p2, t2)
+    pool.release(t1)                      # released first: evicted first
+    pool.release(t2)
+    assert pool.available() == NB
+    assert pool.stats()["evictable"] == 4
+    again, cached = pool.allocate_prompt(p1)   # still reusable
+    assert cached == 2 * bs and list(again) == list(t1)
+    pool.release(again)                   # now p1 is the most recently released
+    filler = pool.allocate(8)              # the 8 free blocks
+    assert not set(filler) & set(t1) | set(filler) & set(t2)
+    more = pool.allocate(2)                # evicts p2's blocks (least recently released)
+    assert set(more) == set(t2)
+    _, c2 = pool.allocate_prompt(p1)       # p1 survived
+    assert c2 == 2 * bs
+
+
+def test_out_of_blocks_takes_nothing():
+    pool = pkv.BlockPool(6, 16)
+    t, _ = pool.allocate_prompt(np.arange(70))          # 5 blocks
+    pool.commit_prompt(np.arange(70), t)
+    with pytest.raises(pkv.PkvError):
+        pool.allocate_prompt(np.concatenate([np.arange(64), np.arange(900, 950)]))  # 4 reused + 4 new
+    assert pool.available() == 1
+    assert [pool.refcount(b) for b in t] == [1] * 5
+    with pytest.raises(pkv.PkvError):
+        pool.allocate(2)
+    assert pool.available() == 1
+
+
+def test_writing_into_a_cached_block_copies_it():
+    """A cached block is shared with every later request that reuses it, so
+    a write into it (its sole holder included) goes to a copy."""
+    bs = 8
+    pool = pkv.BlockPool(16, bs)
+    p = np.arange(3 * bs)
+    t, _ = pool.allocate_prompt(p)
+    pool.commit_prompt(p, t)
+    pair = pool.prepare_write(t, 2)
+    assert pair is not None and pair[0] == 2 and t[2] == pair[1]
+    assert pool.refcount(2) == 0 and pool.is_cached(2)   # the entry stays reusable
+    assert pool.prepare_write(t, 2) is None               # the copy is private
+
+
+class PoolModel:
+    """Plain reference of the prefix cache for the random test below: the
+    cache maps a prompt's token prefix up to a block boundary to its block."""
+
+    def __init__(self, nb, bs):
+        self.bs, self.free = bs, list(range(nb))[::-1]
+        self.refs = [0] * nb
+        self.entry = {}          # tuple(tokens[:k * bs]) -> block
+        self.key_of = {}         # block -> key
+        self.lru = []            # cached blocks nobody holds, least recent first
+
+    def available(self):
+        return len(self.free) + len(self.lru)
+
+    def take(self):
+        if self.free:
+            b = self.free.pop()
+        else:
+            b = self.lru.pop(0)
+            del self.entry[self.key_of.pop(b)]
+        self.refs[b] = 1
+        return b
+
+    def hold(self, b):
+        if self.refs[b] == 0 and b in self.key_of:
+            self.lru.remove(b)
+        self.refs[b] += 1
+
+    def drop(self, b):
+        self.refs[b] -= 1
+        if self.refs[b] == 0:
+            (self.lru if b in self.key_of else self.free).append(b)
+
+    def allocate_prompt(self, toks):
+        bs, n = self.bs, len(toks)
+        table = []
+        for k in range(n // bs):
+            b = self.entry.get(tuple(toks[:(k + 1) * bs]))
+            if b is None:
+                break
+            table.append(b)
+        for b in table:
+            self.hold(b)
+        need = -(-n // bs) - len(table)
+        if self.available() < need:
+            for b in table:
+                self.drop(b)
+            return None
+        reused = len(table)
+        table += [self.take() for _ in range(need)]
+        return table, reused * bs
+
+    def commit(self, toks, table):
+        for k in range(len(toks) // self.bs):
+            key = tuple(toks[:(k + 1) * self.bs])
+            b = table[k]
+            if b not in self.key_of and key not in self.entry:
+                self.entry[key], self.key_of[b] = b, key
+
+
+def test_prefix_cache_against_a_reference_model():
+    rng = np.random.default_rng(21)
+    bs, NB = 8, 60
+    pool, model = pkv.BlockPool(NB, bs), PoolModel(NB, bs)
+    prefixes = [rng.integers(0, 50, int(rng.integers(4, 40))) for _ in range(5)]
+    live = []
+    for step in range(800):
+        if live and (rng.random() < 0.45 or model.available() < 12):
+            i = int(rng.integers(0, len(live)))
+            toks, table = live.pop(i)
+            pool.release(table)
+            for b in table:
+                model.drop(b)
+        else:
+            pre = prefixes[int(rng.integers(0, len(prefixes)))]
+            toks = np.concatenate([pre[:int(rng.integers(0, len(pre) + 1))],
+                                   rng.integers(0, 50, int(rng.integers(0, 20)))]).astype(np.int32)
+            if toks.size == 0:
+                continue
+            want = model.allocate_prompt(list(toks))
+            if want is None:
+                with pytest.raises(pkv.PkvError):
+                    pool.allocate_prompt(toks)
+                continue
+            table, cached = pool.allocate_prompt(toks)
+            assert (list(table), cached) == (want[0], want[1])
+            if rng.random() < 0.8:
+                pool.commit_prompt(toks, table)
+                model.commit(list(toks), list(table))
+            live.append((toks, table))
+        assert pool.available() == model.available()
+    for b in range(NB):
+        assert pool.refcount(b) == model.refs[b]
+        assert pool.is_cached(b) == (b in model.key_of)
+    assert pool.stats()["hits"] > 100          # the walk reused cached prefixes often
+
+
+def test_system_prompt_requests_share_cached_blocks_and_group():
+    """Requests for 3 system prompts arrive interleaved; each prompt's first
+    request computes and commits it, every later one reuses its full blocks
+    (cached_tokens = those blocks' tokens).  The planner then groups each
+    prompt's requests across their batch positions."""
+    bs, G = 16, 4
+    rng = np.random.default_rng(12)
+    prompts = [rng.integers(0, 32000, int(n)) for n in (200, 333, 128)]
+    pool = pkv.BlockPool(400, bs)
+    tables, lens, which = [], [], []
+    for i in range(18):
+        p = i % 3
+        toks = np.concatenate([prompts[p], rng.integers(0, 32000, int(rng.integers(5, 40)))])
+        t, cached = pool.allocate_prompt(toks)
+        assert cached == (0 if i < 3 else len(prompts[p]) // bs * bs)
+        pool.commit_prompt(toks, t)
+        tables.append(t); lens.append(len(toks)); which.append(p)
+    for p in range(3):
+        full = len(prompts[p]) // bs
+        first = tables[p][:full]
+        for i in range(p, 18, 3):
+            np.testing.assert_array_equal(tables[i][:full], first)
+            assert pool.refcount(int(first[0])) == 6
+    MB = max(len(t) for t in tables)
+    bt = np.full((18, MB), -1, np.int32)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = t
+    from tests.test_planner import check_coverage
+    plan = pkv.plan_shared_prefix(bt, np.array(lens, np.int32), 16, 4, 128, bs, max(lens), 256)
+    items, _ = check_coverage(plan, bt, np.array(lens, np.int32), G, 4)
+    groups = {frozenset(it[7]) for it in items if it[1] > G}
+    assert groups == {frozenset(range(p, 18, 3)) for p in range(3)}

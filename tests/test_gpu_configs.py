@@ -41,7 +41,7 @@ def test_tiny_f32_every_sequence():
     run_config(cfg, SEED_BASE + 0, steps=cfg.steps, samples=cfg.num_seqs)
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3])
+@pytest.mark.parametrize("idx", [1, 2, 3, 5])
 def test_preset_sampled(idx):
     cfg = CONFIGS[idx]
     run_config(cfg, SEED_BASE + idx, steps=3, samples=6)

@@ -30,7 +30,8 @@ def _check_tables(w, inp):
         assert len(owners[b]) == 1, "write into a block that is still shared"
 
 
-@pytest.mark.parametrize("cfg", CONFIGS[:4], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [c for c in CONFIGS if c.name != "long_context_bf16"],
+                         ids=lambda c: c.name)
 def test_generator_tables_follow_block_rules(cfg):
     w = PagedDecodeWorkload(cfg, 1234, total_steps=4)
     prev = w.context_lens().copy()

@@ -25,6 +25,12 @@ with vLLM, "The PagedAttention Algorithm" and "Advanced Features"):
                       lengths U{16384..32768}, block size 8/16/32, blocks
                       scattered over a ~60 GB pool, split-context partitions of
                       512 tokens.
+  system_prompt_bf16  Prefix caching: 256 requests, each one of 4 system
+                      prompts of U{1024..2048} tokens (request i takes prompt
+                      i % 4, so sharers are spread through the batch) followed
+                      by U{32..256} tokens of its own; the prompts' full blocks
+                      are held once (a prefix cache's state), GQA 32 q / 8 kv
+                      heads, 64 steps.
 
 This module holds sizes only; the random draws live in ``workloads.gen``.
 """
@@ -51,7 +57,7 @@ class DecodeConfig:
     len_hi: int             # upper bound of the initial cached length
     pool: str               # "fixed" | "factor" | "bytes"
     pool_value: float       # blocks, factor over need, or bytes
-    kind: str = "plain"     # "plain" | "continuous" | "shared_prefix"
+    kind: str = "plain"     # "plain" | "continuous" | "shared_prefix" | "system_prompt"
     lognormal_median: float = 600.0
     lognormal_sigma: float = 0.8
     replace_fraction: float = 0.0   # continuous batching: share finishing per step
@@ -115,7 +121,14 @@ LONG_CONTEXT_BF16 = DecodeConfig(
     num_kv_heads=8, head_dim=128, block_size=16, steps=10, lengths="uniform",
     len_lo=16384, len_hi=32768, pool="bytes", pool_value=60e9, partition_size=512)
 
-CONFIGS = [TINY_F32, LLAMA7B_F16, LLAMA13B_CB_BF16, SHARED_PREFIX_BF16, LONG_CONTEXT_BF16]
+SYSTEM_PROMPT_BF16 = DecodeConfig(
+    name="system_prompt_bf16", dtype="bf16", num_seqs=256, num_heads=32, num_kv_heads=8,
+    head_dim=128, block_size=16, steps=64, lengths="uniform", len_lo=1024, len_hi=2048,
+    pool="factor", pool_value=1.25, kind="system_prompt", num_prompts=4, new_len_lo=32,
+    new_len_hi=256)
+
+CONFIGS = [TINY_F32, LLAMA7B_F16, LLAMA13B_CB_BF16, SHARED_PREFIX_BF16, LONG_CONTEXT_BF16,
+           SYSTEM_PROMPT_BF16]
 BY_NAME = {c.name: c for c in CONFIGS}
 LONG_CONTEXT_BLOCK_SIZES = (8, 16, 32)
 

@@ -120,6 +120,12 @@ class PagedDecodeWorkload:
             self.prompt_lens = self.rng.integers(cfg.len_lo, cfg.len_hi + 1, size=P)
             init_lens = np.repeat(self.prompt_lens, cfg.samples_per_prompt)
             B = int(init_lens.shape[0])
+        elif cfg.kind == "system_prompt":
+            # request i starts with system prompt i % P, then its own tokens
+            self.prompt_lens = self.rng.integers(cfg.len_lo, cfg.len_hi + 1, size=cfg.num_prompts)
+            self.own_lens = self.rng.integers(cfg.new_len_lo, cfg.new_len_hi + 1, size=B)
+            self.prompt_of = np.arange(B) % cfg.num_prompts
+            init_lens = self.prompt_lens[self.prompt_of] + self.own_lens
         else:
             init_lens = self._draw_lengths(B, cfg.len_lo, cfg.len_hi)
         self.num_seqs = B
@@ -174,6 +180,20 @@ class PagedDecodeWorkload:
                     self.refcount[b] = S
                 for _ in range(S):
                     self.seqs.append(_Seq(table=list(table), length=int(lp)))
+        elif cfg.kind == "system_prompt":
+            # A prefix cache holds the full blocks of each system prompt once;
+            # a request's own blocks hold the prompt's partial last block (if
+            # any) and its own tokens.
+            self.refcount = np.zeros(nb, dtype=np.int32)
+            shared = [[self.free.pop() for _ in range(int(lp) // self.bs)] for lp in self.prompt_lens]
+            for i, L in enumerate(self.init_lens):
+                base = shared[self.prompt_of[i]]
+                own = [self.free.pop() for _ in range(_blocks_for(int(L), self.bs) - len(base))]
+                for b in base:
+                    self.refcount[b] += 1
+                for b in own:
+                    self.refcount[b] = 1
+                self.seqs.append(_Seq(table=list(base) + own, length=int(L)))
         else:
             for L in self.init_lens:
                 table = [self.free.pop() for _ in range(_blocks_for(int(L), self.bs))]
@@ -204,6 +224,12 @@ class PagedDecodeWorkload:
                     own = S * (_blocks_for(int(lp) + self.total_steps, self.bs) - (int(lp) // self.bs))
                     total += shared + own
                 return total
+            if cfg.kind == "system_prompt":
+                shared = sum(int(lp) // self.bs for lp in self.prompt_lens)
+                own = sum(_blocks_for(int(L) + self.total_steps, self.bs) -
+                          int(self.prompt_lens[self.prompt_of[i]]) // self.bs
+                          for i, L in enumerate(self.init_lens))
+                return shared + own
             if cfg.kind == "continuous":
                 lens = self.init_lens.copy()
                 in_use = int(sum(_blocks_for(int(L), self.bs) for L in lens))

@@ -60,7 +60,7 @@ class DeviceState:
                   partition_size: int = 0) -> DeviceStep:
         cfg, dev = self.cfg, self.device
         if shared is None:
-            shared = cfg.kind == "shared_prefix"
+            shared = cfg.kind in ("shared_prefix", "system_prompt")
         q, k, v = step_values(cfg, self.seed, inp, self.w.num_seqs,
                               device=value_device if value_device is not None else dev)
         pairs = None
