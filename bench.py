@@ -236,6 +236,7 @@ def run_native(args):
     dec_ms = [b.elapsed_time(c) for _, b, c in ev]
     tot_ms = sum(step_ms)
     bytes_step, bytes_dec, seqs = 0, 0, 0
+    dec_bytes = []
     for s, n in zip(steps[args.warmup:], decode_launches):
         if shared:
             expected = s.plan.host[8:8 + w.num_seqs]
@@ -245,6 +246,7 @@ def run_native(args):
             ab = algorithmic_bytes(cfg, s.host, w.num_seqs, split_partition=Pp, out_bytes=out_bytes)
         bytes_step += ab["total"]
         bytes_dec += ab["attention"]
+        dec_bytes.append(ab["attention"])
         seqs += w.num_seqs
     t_max = max_over_ranks(dist, tot_ms / 1e3)
     bytes_all = sum_over_ranks(dist, bytes_step)
@@ -253,6 +255,8 @@ def run_native(args):
     dec_mean_ms = sum(dec_ms) / len(dec_ms)
     achieved = bytes_dec / len(dec_ms) / (dec_mean_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
+
+    unflushed = _unflushed_decode(pkv, state, steps[-1], P, dec_bytes[-1], peak)
 
     e2e = None
     if not args.no_e2e:
@@ -280,6 +284,9 @@ def run_native(args):
                        "l2": "flushed (256 MiB read) before every timed step, outside the events",
                        "block_placement": "contiguous" if args.identity_tables else "random"},
             "seq_steps_per_s": round(seqs_all / t_max, 1),
+            "step_ms": _spread(step_ms),
+            "decode_ms": _spread(dec_ms),
+            "unflushed": unflushed,
             "pct_of_peak": round(100 * value / peak, 2),
             "roofline": {"bound": "hbm",
                          "kernel": ("pa_cascade_kernel+pa_cascade_merge_kernel" if shared else
@@ -314,6 +321,33 @@ def _decode(pkv, state, s, q, bt, cl, plan_dev, P):
                                    cfg.softmax_scale, max_context_len=s.max_context_len,
                                    partition_size=P, workspace=state.workspace,
                                    device_status=state.status)
+
+
+def _spread(ms):
+    """p10 / median / p90 of per-step times (ms)."""
+    a = np.sort(np.asarray(ms, dtype=np.float64))
+    return {"p10": round(float(np.percentile(a, 10)), 5), "median": round(float(np.median(a)), 5),
+            "p90": round(float(np.percentile(a, 90)), 5)}
+
+
+def _unflushed_decode(pkv, state, s, P, algo_bytes, peak, reps=5):
+    """The last timed step's attention again, `reps` times back to back with
+    no L2 flush in between (it only reads the cache and rewrites its output):
+    what L2 reuse across launches adds when nothing else runs between them."""
+    stream = torch.cuda.current_stream()
+    _decode(pkv, state, s, s.q, s.block_tables, s.context_lens, s.plan_device, P)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    _preroll()
+    for a, b in evs:
+        a.record(stream)
+        _decode(pkv, state, s, s.q, s.block_tables, s.context_lens, s.plan_device, P)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
+    gbs = algo_bytes / (ms / 1e3) / 1e9
+    return {"decode_ms_median": round(ms, 5), "achieved": round(gbs, 2), "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "launches": reps}
 
 
 def _flush_l2(buf):

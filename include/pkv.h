@@ -126,17 +126,22 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
  *
  *   block_tables, context_lens  HOST copies of the arrays the decode call
  *              will get on the device (same layout as for decode)
- *   partition_size  target tokens per work item: a multiple of 32 and of
- *              block_size, at most 64 * block_size (PKV_EINVAL otherwise); 0 =
- *              automatic: about one item per resident CTA slot of the current
- *              GPU (three per SM) over all kv heads, at least 64 tokens.
- *              Each group's shared prefix is cut into nearly equal pieces;
- *              members' short tails join the group's last piece, longer ones
- *              become items of their own.
+ *   partition_size  target tokens per work list (one CTA per kv head and
+ *              list): a multiple of 32 and of block_size, at most 64 *
+ *              block_size (PKV_EINVAL otherwise); 0 = automatic: one list per
+ *              resident CTA slot of the current GPU (three per SM) over all kv
+ *              heads, at least 64 tokens each.
+ *              Per kv head the work is one stream of 16-token tiles: each
+ *              group's shared prefix (once for all members' query heads), then
+ *              each member's own tail, then the next group or ungrouped
+ *              sequence.  The stream is cut into lists of nearly equal tiles;
+ *              a list holds the pieces of the groups and sequences its range
+ *              covers (work items), and each piece writes one partial per row.
  *   plan       HOST int32 buffer of plan_capacity_ints entries; receives the
- *              plan (opaque apart from plan[0] = number of items and plan[1] =
- *              partial slots per (sequence, head)); copy it to the device and
- *              pass it to pkv_paged_attention_decode_shared
+ *              plan (opaque apart from plan[0] = number of lists, plan[1] =
+ *              partial slots per (sequence, head) and plan[7] = number of
+ *              items); copy it to the device and pass it to
+ *              pkv_paged_attention_decode_shared
  *   plan_ints  out: entries the plan needs
  *   workspace_bytes  out: workspace the decode call needs for this plan
  * Returns PKV_EWORKSPACE (after filling both outputs) when plan is NULL or
@@ -155,17 +160,18 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
 /*
  * paged_attention_decode_shared -- the same attention as
  * pkv_paged_attention_decode, following a plan from pkv_plan_shared_prefix:
- * one CTA per (kv head, work item) reads each shared block once for all the
- * query heads of its group and writes the output of a sequence it holds
- * entirely, or else one partial per row; a second kernel, queued as a
- * programmatic dependent of the first, merges the partials (log-sum-exp).
+ * one CTA per (kv head, work list) takes the list's items in turn, reads each
+ * shared block once for all the query heads of its group and writes the
+ * output of a sequence an item holds entirely, or else one partial per row; a
+ * second kernel, queued as a programmatic dependent of the first, merges the
+ * partials (log-sum-exp).
  * Results equal the per-sequence path up to fp32 rounding order.
  *
  * Arguments as for pkv_paged_attention_decode, plus:
  *   plan       DEVICE copy of the plan (4-byte aligned; read only, so the
  *              same device plan serves any number of calls with the same
  *              tables and lengths, e.g. every layer of a step)
- *   num_items, slots  plan[0] and plan[1]
+ *   num_lists, num_items, slots  plan[0], plan[7] and plan[1]
  *   workspace  at least the planner's workspace_bytes
  * The device checks the plan against the device arrays: every table the
  * plan reads must hold the block ids the plan was made with (PKV_DEV_BAD_BLOCK
@@ -181,9 +187,9 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
                                       const int32_t *context_lens, int num_seqs, int num_heads,
                                       int num_kv_heads, int head_dim, int block_size,
                                       int64_t num_blocks, int max_context_len, float scale,
-                                      const int32_t *plan, int num_items, int slots, void *workspace,
-                                      size_t workspace_bytes, uint32_t *device_status,
-                                      void *stream);
+                                      const int32_t *plan, int num_lists, int num_items, int slots,
+                                      void *workspace, size_t workspace_bytes,
+                                      uint32_t *device_status, void *stream);
 
 /*
  * kv_cache_usage -- HOST accounting of the paged cache ("Memory Efficiency":

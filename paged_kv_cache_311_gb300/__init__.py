@@ -67,7 +67,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_paged_attention_decode.restype = i32
     L.pkv_paged_attention_decode_shared.argtypes = [vp, i32, vp, vp, vp, i32, vp, i32, vp, i32,
                                                     i32, i32, i32, i32, i64, i32, f32, vp, i32,
-                                                    i32, vp, u64, vp, vp]
+                                                    i32, i32, vp, u64, vp, vp]
     L.pkv_paged_attention_decode_shared.restype = i32
     L.pkv_plan_shared_prefix.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, u64,
                                          ctypes.POINTER(ctypes.c_size_t),
@@ -225,13 +225,14 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
 class SharedPrefixPlan:
     """A host-made plan of the shared-prefix decode (see plan_shared_prefix).
 
-    host: the int32 plan; num_items, slots, workspace_bytes: its sizes.
-    to(device) gives the device copy the decode call takes (read only by the
-    device, so one device copy serves every call with the same tables and
-    lengths)."""
+    host: the int32 plan; num_lists (CTAs per kv head), num_items, slots,
+    workspace_bytes: its sizes.  to(device) gives the device copy the decode
+    call takes (read only by the device, so one device copy serves every call
+    with the same tables and lengths)."""
 
-    def __init__(self, host, num_items: int, slots: int, workspace_bytes: int):
+    def __init__(self, host, num_lists: int, num_items: int, slots: int, workspace_bytes: int):
         self.host = host
+        self.num_lists = int(num_lists)
         self.num_items = int(num_items)
         self.slots = int(slots)
         self.workspace_bytes = int(workspace_bytes)
@@ -384,7 +385,7 @@ def plan_shared_prefix(block_tables, context_lens, num_heads: int, num_kv_heads:
                                   plan.ctypes.data, plan.size, ctypes.byref(n_ints), ctypes.byref(ws))
     _check(rc, "pkv_plan_shared_prefix")
     plan = plan[: n_ints.value].copy()
-    return SharedPrefixPlan(plan, plan[0], plan[1], ws.value)
+    return SharedPrefixPlan(plan, plan[0], plan[7], plan[1], ws.value)
 
 
 def paged_attention_decode_shared(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
@@ -415,7 +416,8 @@ def paged_attention_decode_shared(out: torch.Tensor, q: torch.Tensor, k_cache: t
     rc = load_library().pkv_paged_attention_decode_shared(
         _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[k_cache.dtype],
         _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), B, H, Hk, D, bs, NB,
-        int(max_context_len), float(scale), _ptr(plan_device), plan.num_items, plan.slots,
+        int(max_context_len), float(scale), _ptr(plan_device), plan.num_lists, plan.num_items,
+        plan.slots,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_status),
         _stream(stream))
     _check(rc, "pkv_paged_attention_decode_shared")

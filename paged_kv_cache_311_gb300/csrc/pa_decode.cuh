@@ -60,6 +60,7 @@ struct DecodeParams {
     int out_dtype;
     int split;           // nonzero: write partials to the workspace
     float qscale;        // softmax scale * log2(e)
+    int num_items;       // shared-prefix plans: work items in the plan
 };
 
 enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2 };
@@ -402,30 +403,46 @@ struct TcEngine {
         return (uint32_t)((k >> 2) * C::BOX_ROWS * 128);
     }
 
-    // Copies the CTA's query rows (rows >= nrows zero) into shared memory at
-    // `qs` for QS engines; all C::NW * 32 threads of the CTA take part, and a
-    // barrier must follow before init.
+    // The CTA's query rows (rows >= nrows zero) on their way to shared memory
+    // for QS engines, in two halves so that a caller can put other loads in
+    // flight between them: load() issues every global load, store() writes
+    // the rows at `qs`.  All C::NW * 32 threads of the CTA take part, and a
+    // barrier must follow the stores before init.
+    struct QRows {
+        static constexpr int PCS = D * 2 / 16;   // 16-byte pieces per row
+        static constexpr int PER = (RS * PCS + C::NW * 32 - 1) / (C::NW * 32);
+        uint4 v[PER];
+
+        __device__ __forceinline__ void load(const DecodeParams &p, const CtaWork &w)
+        {
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int i = threadIdx.x + u * C::NW * 32, r = i / PCS;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < RS * PCS && r < w.nrows)
+                    v[u] = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.q) +
+                                                           row_head(p, w, G, r) * D)[i % PCS];
+            }
+        }
+        __device__ __forceinline__ void store(uint8_t *qs) const
+        {
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int i = threadIdx.x + u * C::NW * 32;
+                if (i < RS * PCS)
+                    *reinterpret_cast<uint4 *>(qs + (i / PCS) * QROWB + (i % PCS) * 16) = v[u];
+            }
+        }
+    };
+
+    // Both halves back to back: all loads first, then all stores (a store
+    // between two loads would keep the second load from issuing before the
+    // first returns).
     __device__ static void stage_q_rows(const DecodeParams &p, uint8_t *qs, const CtaWork &w)
     {
-        // all loads first, then all stores: a store between two loads would
-        // keep the second load from issuing before the first returns
-        constexpr int PCS = D * 2 / 16;   // 16-byte pieces per row
-        constexpr int PER = (RS * PCS + C::NW * 32 - 1) / (C::NW * 32);
-        uint4 v[PER];
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int i = threadIdx.x + u * C::NW * 32, r = i / PCS;
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < RS * PCS && r < w.nrows)
-                v[u] = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.q) +
-                                                       row_head(p, w, G, r) * D)[i % PCS];
-        }
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int i = threadIdx.x + u * C::NW * 32;
-            if (i < RS * PCS)
-                *reinterpret_cast<uint4 *>(qs + (i / PCS) * QROWB + (i % PCS) * 16) = v[u];
-        }
+        QRows q;
+        q.load(p, w);
+        q.store(qs);
     }
 
     __device__ void init(const DecodeParams &p, uint8_t *qs, const CtaWork &w, int, int lane)

@@ -270,7 +270,8 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     a.engine = g_engine_override.load(std::memory_order_relaxed);
     a.shared = false;
     a.plan = nullptr;
-    a.num_items = 0;
+    a.num_lists = 0;
+    a.p.num_items = 0;
     a.stream = static_cast<cudaStream_t>(stream);
     int engine_used = 0;
     a.engine_used = &engine_used;
@@ -294,9 +295,9 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
                                       const int32_t *context_lens, int num_seqs, int num_heads,
                                       int num_kv_heads, int head_dim, int block_size,
                                       int64_t num_blocks, int max_context_len, float scale,
-                                      const int32_t *plan, int num_items, int slots, void *workspace,
-                                      size_t workspace_bytes, uint32_t *device_status,
-                                      void *stream)
+                                      const int32_t *plan, int num_lists, int num_items, int slots,
+                                      void *workspace, size_t workspace_bytes,
+                                      uint32_t *device_status, void *stream)
 {
     g_last_decode_launches = 0;
     g_last_decode_engine = 0;
@@ -316,7 +317,7 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
         (reinterpret_cast<uintptr_t>(plan) & 3u))
         return PKV_EINVAL;
-    if (num_items <= 0 || num_items > 65535 || slots <= 0)
+    if (num_lists <= 0 || num_lists > 65535 || num_items < num_lists || slots <= 0)
         return PKV_EINVAL;
     const int group = num_heads / num_kv_heads;
     if (kv_dtype == PKV_F32 || (head_dim != 64 && head_dim != 128) ||
@@ -357,7 +358,8 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     a.engine = kEngineTensorCore;
     a.shared = true;
     a.plan = plan;
-    a.num_items = num_items;
+    a.num_lists = num_lists;
+    p.num_items = num_items;
     a.stream = static_cast<cudaStream_t>(stream);
     int engine_used = 0;
     a.engine_used = &engine_used;

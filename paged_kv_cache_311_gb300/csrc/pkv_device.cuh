@@ -95,6 +95,19 @@ __device__ __forceinline__ void tma_load_5d(void *dst_smem, const CUtensorMap *m
         : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (no register staging); complete
+// the thread's copies with cp_async_wait_all before reading them.
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

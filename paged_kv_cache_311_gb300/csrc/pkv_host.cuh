@@ -22,7 +22,7 @@ struct DecodeLaunch {
     int engine;          // Engine: kEngineAuto, kEngineCudaCore or kEngineTensorCore
     bool shared;         // shared-prefix (cascade) path
     const int32_t *plan; // device copy of the cascade plan
-    int num_items;
+    int num_lists;     // shared-prefix plans: CTAs per kv head
     cudaStream_t stream;
     int *engine_used;    // out: the engine that ran
 };
@@ -127,7 +127,7 @@ int run_cascade(const DecodeLaunch &a)
     rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), CC::SMEM_BYTES, &done);
     if (rc)
         return rc;
-    dim3 grid(p.num_kv_heads, a.num_items, 1);
+    dim3 grid(p.num_kv_heads, a.num_lists, 1);
     rc = launch_pdl(kern, grid, dim3(CC::C::NW * 32), CC::SMEM_BYTES, a.stream, p, tmk, tmv, a.plan);
     if (rc)
         return rc;

@@ -7,6 +7,7 @@
 // side re-checks on the device that the members of a group really share the
 // blocks it was told about.
 #include <algorithm>
+#include <cstdint>
 #include <cuda_runtime.h>
 #include <cstring>
 #include <vector>
@@ -16,8 +17,14 @@
 
 namespace {
 
-// Smallest automatic item (tokens): below it the per-item fixed costs win.
+// Smallest automatic list (tokens): below it the per-CTA fixed costs win.
 constexpr int kMinAutoTokens = 64;
+// What a CTA's switch from one item to the next costs, in 16-token tiles
+// streamed: the epilogue of one item and the start of the next (about 6 us
+// on a GB300, against about 0.6 us per tile while all CTAs stream).
+constexpr long long kItemCostTiles = 10;
+// Fewest tiles a list starts another unit with.
+constexpr long long kMinPieceTiles = 4;
 
 // SMs of the current device (the automatic cut targets three resident CTAs
 // per SM); 152, a GB300's count, when no device answers.
@@ -39,7 +46,7 @@ struct Seg {
 struct Item {
     int seq0, nrows, slot;
     std::vector<Seg> segs;
-    long long weight;  // tokens streamed, for the heavy-first order
+    long long weight;  // tokens streamed
     int entries;       // block-table entries of all segments
     std::vector<int> members;  // the sequences whose rows the item serves
 };
@@ -66,12 +73,20 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
     const int G = num_heads / num_kv_heads;
     if (G > pkv::plan::kMaxRows)
         return 0;
-    // items per sequence: its partitions of at least P (or kMinAutoTokens)
-    // tokens, one more for the rounding of a cut, one for a group's last item
-    const int P = partition_size > 0 ? partition_size : kMinAutoTokens;
-    const long long per_seq = (max_context_len + P - 1) / P + 2;
-    return (size_t)pkv::plan::kHeader + 2 * (size_t)num_seqs +
-           (size_t)(num_seqs * per_seq) * pkv::plan::item_ints(G);
+    // lists: at most the automatic count (one per resident CTA slot) or the
+    // stream over the explicit target, or the stream over the smallest list
+    // the table capacity allows (block size 8); items: every unit's first
+    // piece (at most one per sequence) plus one more per list boundary
+    using namespace pkv::plan;
+    const long long W = (long long)num_seqs * ((max_context_len + kTileTokens - 1) / kTileTokens);
+    const long long q_cap = (long long)(kTableCap - 2 * max_segments(G)) * 8 / kTileTokens;
+    long long lists = (W + q_cap - 1) / q_cap + 1;
+    if (partition_size > 0)
+        lists = std::max(lists, W / std::max(1, partition_size / kTileTokens) + 1);
+    else
+        lists = std::max(lists, 3LL * gpu_sm_count() / num_kv_heads + 1);
+    return (size_t)kHeader + 2 * (size_t)num_seqs +
+           (size_t)(num_seqs + lists) * item_ints(G);
 }
 
 int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
@@ -94,7 +109,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         (partition_size % 32 || partition_size % block_size || partition_size / block_size > kTableCap / 4))
         return PKV_EINVAL;
     const int B = num_seqs, MB = max_blocks_per_seq, bs = block_size;
-    const int align = bs > 32 ? bs : 32;
+    const int align = std::max(bs, kTileTokens);   // shared prefixes end on a tile and a block
     const int max_members = kMaxRows / G;
     auto len_ok = [&](int s) {
         const int L = context_lens[s];
@@ -143,162 +158,179 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         int first, cnt, S;
     };
     std::vector<Group> groups;
-    long long total = 0;   // tokens to stream per kv head, shared ones once
     for (int k = 0; k < B;) {
         int cnt = 1, S = 0x7fffffff;
         while (cnt < max_members && k + cnt < B && sp[k + cnt] > 0) {
             S = std::min(S, sp[k + cnt]);
             ++cnt;
         }
-        if (cnt < 2) {
-            groups.push_back(Group{k, 1, 0});
-            total += len_ok(order[k]) ? context_lens[order[k]] : 0;
-        } else {
-            groups.push_back(Group{k, cnt, S});
-            total += S;
-            for (int m = 0; m < cnt; ++m)
-                total += context_lens[order[k + m]] - S;
-        }
+        groups.push_back(cnt < 2 ? Group{k, 1, 0} : Group{k, cnt, S});
         k += cnt;
     }
+    std::vector<int> expected(B, 0);
 
-    // A member's own tail costs whole 16-row loads; it joins its group's
-    // last item while that item stays within T tokens (and within half the
-    // block-id capacity), longer tails become items of their own.
-    auto tail_cost = [](int t) { return (t + 15) / 16 * 16; };
-    auto fold_tails = [&](const Group &g, int T, std::vector<char> *folded) {
-        long long F = 0;
-        int entries = 0;
-        for (int m = 0; m < g.cnt; ++m) {
-            const int t = context_lens[order[g.first + m]] - g.S, need = blocks_between(g.S, g.S + t, bs);
-            const bool f = t > 0 && F + tail_cost(t) <= T && entries + need <= kTableCap / 2;
-            if (f) {
-                F += tail_cost(t);
-                entries += need;
-            }
-            if (folded)
-                (*folded)[m] = f;
-        }
-        return F;
+    // ---- the tile stream of one kv head: unit after unit, a unit being a
+    // group (its shared prefix once for all members' rows, then each
+    // member's own tail for that member's rows) or an ungrouped sequence
+    // (whole).  Costs count 16-token tiles, the kernel's unit of load.
+    struct Part {
+        int table_seq, tb, te, row_lo, row_hi;
+        long long t0, tiles;   // place in the unit's stream
     };
-    // items per kv head that target T gives
-    auto count_items = [&](int T) {
-        long long n = 0;
-        for (const Group &g : groups) {
-            if (g.cnt == 1) {
-                n += len_ok(order[g.first]) ? (context_lens[order[g.first]] + T - 1) / T : 1;
+    struct Unit {
+        int seq0, nrows;
+        std::vector<int> members;
+        std::vector<Part> parts;
+        long long t0 = 0, tiles = 0;   // place in the kv head's stream
+        int pieces = 0;
+    };
+    auto tiles_of = [](int tb, int te) { return (long long)((te - tb + kTileTokens - 1) / kTileTokens); };
+    std::vector<Unit> units;
+    std::vector<int> empty;   // sequences with an empty or invalid context
+    long long W = 0;
+    for (const Group &g : groups) {
+        const int s = order[g.first];
+        Unit u;
+        u.seq0 = s;
+        u.members.assign(order.begin() + g.first, order.begin() + g.first + g.cnt);
+        u.nrows = g.cnt * G;
+        auto add = [&](int seq, int tb, int te, int lo, int hi) {
+            const long long t = tiles_of(tb, te);
+            u.parts.push_back(Part{seq, tb, te, lo, hi, u.tiles, t});
+            u.tiles += t;
+        };
+        if (g.cnt == 1) {
+            if (!len_ok(s)) {
+                empty.push_back(s);
                 continue;
             }
-            std::vector<char> folded(g.cnt, 0);
-            const long long F = fold_tails(g, T, &folded);
-            n += std::max(1LL, (g.S + F + T - 1) / T);
+            add(s, 0, context_lens[s], 0, G);
+        } else {
+            add(s, 0, g.S, 0, u.nrows);
             for (int m = 0; m < g.cnt; ++m) {
-                const int t = context_lens[order[g.first + m]] - g.S;
-                if (t > 0 && !folded[m])
-                    n += (t + T - 1) / T;
+                const int L = context_lens[u.members[m]];
+                if (L > g.S)
+                    add(u.members[m], g.S, L, m * G, (m + 1) * G);
             }
+        }
+        u.t0 = W;
+        W += u.tiles;
+        units.push_back(std::move(u));
+    }
+
+    // ---- lists: the stream cut into consecutive ranges, one CTA each (per
+    // kv head), of nearly equal cost whatever the units' sizes.  A list's
+    // cost is its tiles plus kItemCostTiles for every item after its first
+    // (the CTA's epilogue of one item and start of the next stream nothing);
+    // a list does not start another unit with less than kMinPieceTiles of
+    // budget left (no sliver items).  Greedy filling under a budget gives the
+    // fewest lists for that budget; the budget is the smallest whose lists
+    // fit one per resident CTA slot of the GPU (three per SM) over the kv
+    // heads (automatic), or the explicit target.  An item's block ids stay
+    // within the kernel's table capacity whatever the segments' alignment.
+    const long long q_cap = (long long)(kTableCap - 2 * max_segments(G)) * bs / kTileTokens;
+    auto walk = [&](long long budget, std::vector<long long> *cuts) {
+        long long pos = 0, n = 0;
+        size_t u = 0;
+        if (cuts)
+            cuts->assign(1, 0);
+        while (pos < W) {
+            ++n;
+            long long cost = 0;
+            for (bool first = true; pos < W; first = false) {
+                while (units[u].t0 + units[u].tiles <= pos)
+                    ++u;
+                const long long avail = units[u].t0 + units[u].tiles - pos;
+                const long long extra = first ? 0 : kItemCostTiles;
+                const long long room = budget - cost - extra;
+                if (avail <= room) {
+                    cost += extra + avail;
+                    pos += avail;
+                    continue;
+                }
+                if (!first && room < kMinPieceTiles)
+                    break;
+                pos += std::max(1LL, room);
+                break;
+            }
+            if (cuts)
+                cuts->push_back(pos);
         }
         return n;
     };
-
-    // Target tokens per item.  Automatic: the smallest T (a multiple of
-    // `align`, between kMinAutoTokens or 4 blocks and 64 blocks) whose items
-    // fit one CTA per resident slot of the GPU (three per SM) over all kv
-    // heads, so that the launch runs as one wave of items of at most T tokens.
-    int T = partition_size;
-    if (T == 0) {
-        const long long per_head = std::max(1LL, 3LL * gpu_sm_count() / num_kv_heads);
-        const int lo = (std::max(4 * bs, kMinAutoTokens) + align - 1) / align;
-        const int hi = (kTableCap / 4) * bs / align;
-        int a = lo, b = hi;                       // in units of align
-        while (a < b) {
-            const int mid = (a + b) / 2;
-            if (count_items(mid * align) <= per_head)
-                b = mid;
+    long long Q;
+    if (partition_size > 0) {
+        Q = std::min<long long>(partition_size / kTileTokens, q_cap);
+    } else {
+        const long long N = std::max(1LL, 3LL * gpu_sm_count() / num_kv_heads);
+        long long lo = std::min(q_cap, std::max<long long>(kMinAutoTokens / kTileTokens, (W + N - 1) / N));
+        long long hi = lo;
+        while (hi < q_cap && walk(hi, nullptr) > N)
+            hi = std::min(q_cap, 2 * hi);
+        while (lo < hi) {
+            const long long mid = (lo + hi) / 2;
+            if (walk(mid, nullptr) <= N)
+                hi = mid;
             else
-                a = mid + 1;
+                lo = mid + 1;
         }
-        T = a * align;
+        Q = hi;
     }
+    std::vector<long long> cuts;
+    const long long nl = walk(Q, &cuts);
 
-    std::vector<Item> items;
-    std::vector<int> expected(B, 0);
-    // [tb, te) cut into n nearly equal pieces at multiples of `align`
-    auto cut = [&](int tb, int te, int n) {
-        std::vector<int> b{tb};
-        for (int i = 1; i < n; ++i) {
-            const int x = (int)((tb + (long long)(te - tb) * i / n) / align * align);
-            if (x > b.back() && x < te)
-                b.push_back(x);
-        }
-        b.push_back(te);
-        return b;
-    };
-    auto add_partitions = [&](int seq, int tb, int te, int first_slot) {
-        const std::vector<int> b = cut(tb, te, (te - tb + T - 1) / T);
-        for (size_t k = 0; k + 1 < b.size(); ++k)
-            items.push_back(Item{seq, G, first_slot + (int)k, {Seg{seq, b[k], b[k + 1], 0, G}},
-                                 (long long)(b[k + 1] - b[k]), blocks_between(b[k], b[k + 1], bs),
-                                 {seq}});
-        return (int)b.size() - 1;
-    };
-
-    for (const Group &g : groups) {
-        const int s = order[g.first], cnt = g.cnt, S = g.S;
-        std::vector<int> mem(order.begin() + g.first, order.begin() + g.first + cnt);
-        if (cnt == 1) {
-            if (!len_ok(s))
-                items.push_back(Item{s, G, 0, {}, 0, 0, {s}});   // zero output
-            else
-                expected[s] = add_partitions(s, 0, context_lens[s], 0);
-            continue;
-        }
-        // n_g items of at most about T tokens: the prefix cut into n_g - 1
-        // equal pieces plus the part that goes with the folded tails
-        const int rows = cnt * G;
-        std::vector<char> folded(cnt, 0);
-        const long long F = fold_tails(g, T, &folded);
-        int n_g = (int)std::max(1LL, (S + F + T - 1) / T);
-        int Sp = 0;
-        if (n_g > 1) {
-            const long long per = (S + F + n_g - 1) / n_g;
-            const long long Pl = std::min<long long>(S, std::max(0LL, per - F));
-            Sp = (int)((S - Pl) / align * align);
-            if (Sp <= 0)
-                n_g = 1, Sp = 0;
-        }
-        int n_pre = 0;
-        if (n_g > 1) {
-            const std::vector<int> b = cut(0, Sp, n_g - 1);
-            for (size_t k = 0; k + 1 < b.size(); ++k, ++n_pre)
-                items.push_back(Item{s, rows, n_pre, {Seg{s, b[k], b[k + 1], 0, rows}},
-                                     (long long)(b[k + 1] - b[k]), blocks_between(b[k], b[k + 1], bs),
-                                     mem});
-        }
-        Item last{s, rows, n_pre, {}, 0, 0, mem};
-        if (Sp < S) {
-            last.segs.push_back(Seg{s, Sp, S, 0, rows});
-            last.weight += S - Sp;
-            last.entries += blocks_between(Sp, S, bs);
-        }
-        for (int m = 0; m < cnt; ++m)
-            if (folded[m]) {
-                const int seq = mem[m], L = context_lens[seq];
-                last.segs.push_back(Seg{seq, S, L, m * G, (m + 1) * G});
-                last.weight += L - S;
-                last.entries += blocks_between(S, L, bs);
+    // items: the pieces of units that each list's range covers, in stream
+    // order; a piece serves all its unit's rows, with the unit's parts (or
+    // pieces of them) inside its range as segments
+    std::vector<std::vector<Item>> lists((size_t)std::max(1LL, nl));
+    {
+        size_t u = 0;
+        for (long long k = 0; k < nl; ++k) {
+            while (u < units.size() && units[u].t0 + units[u].tiles <= cuts[k])
+                ++u;
+            for (size_t v = u; v < units.size() && units[v].t0 < cuts[k + 1]; ++v) {
+                Unit &un = units[v];
+                const long long a0 = std::max(cuts[k], un.t0) - un.t0;
+                const long long b0 = std::min(cuts[k + 1], un.t0 + un.tiles) - un.t0;
+                if (a0 >= b0)
+                    continue;
+                Item it{un.seq0, un.nrows, un.pieces++, {}, 0, 0, un.members};
+                for (const Part &pt : un.parts) {
+                    const long long x = std::max(a0, pt.t0), y = std::min(b0, pt.t0 + pt.tiles);
+                    if (x >= y)
+                        continue;
+                    const int tb = pt.tb + (int)((x - pt.t0) * kTileTokens);
+                    const int te = std::min(pt.te, pt.tb + (int)((y - pt.t0) * kTileTokens));
+                    it.segs.push_back(Seg{pt.table_seq, tb, te, pt.row_lo, pt.row_hi});
+                    it.weight += te - tb;
+                    it.entries += blocks_between(tb, te, bs);
+                }
+                lists[(size_t)k].push_back(std::move(it));
             }
-        items.push_back(last);
-        const int n_items = n_pre + 1;
-        for (int m = 0; m < cnt; ++m) {
-            const int seq = mem[m], L = context_lens[seq];
-            const int n_tail = (L > S && !folded[m]) ? add_partitions(seq, S, L, n_items) : 0;
-            expected[seq] = n_items + n_tail;
         }
     }
+    for (size_t e = 0; e < empty.size(); ++e)   // zero output, no loads: any list
+        lists[e % lists.size()].push_back(Item{empty[e], G, 0, {}, 0, 0, {empty[e]}});
+    for (const Unit &un : units)
+        for (int m : un.members)
+            expected[m] = un.pieces;
 
-    std::stable_sort(items.begin(), items.end(),
-                     [](const Item &a, const Item &b) { return a.weight > b.weight; });
+    // list k starts at item k; the rest follow, each list's items chained
+    std::vector<Item> items;
+    std::vector<int> next;
+    for (auto &l : lists)
+        items.push_back(l[0]);
+    next.assign(items.size(), -1);
+    for (size_t k = 0; k < lists.size(); ++k) {
+        int prev = (int)k;
+        for (size_t j = 1; j < lists[k].size(); ++j) {
+            items.push_back(lists[k][j]);
+            next.push_back(-1);
+            next[(size_t)prev] = (int)items.size() - 1;
+            prev = (int)items.size() - 1;
+        }
+    }
+    const int T = (int)(Q * kTileTokens);
     int slots = 1;
     for (int s = 0; s < B; ++s)
         slots = std::max(slots, expected[s]);
@@ -308,7 +340,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         *plan_ints = need;
     if (workspace_bytes)
         *workspace_bytes = split_total(B, num_heads, slots, head_dim);
-    if (items.size() > 65535)
+    if (items.size() > INT32_MAX / 2 || lists.size() > 65535)
         return PKV_EUNSUPPORTED;
     if (!plan || plan_capacity_ints < need)
         return PKV_EWORKSPACE;
@@ -317,18 +349,20 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         if (it.entries > kTableCap)   // cannot happen: items are cut to fit
             return PKV_EUNSUPPORTED;
     std::memset(plan, 0, need * sizeof(int32_t));
-    plan[H_NUM_ITEMS] = (int)items.size();
+    plan[H_NUM_LISTS] = (int)lists.size();
     plan[H_SLOTS] = slots;
     plan[H_NUM_SEQS] = B;
     plan[H_NUM_KV_HEADS] = num_kv_heads;
     plan[H_ITEM_INTS] = iints;
     plan[H_MAX_SEG] = max_segments(G);
-    plan[H_PARTITION] = T;
-    plan[H_TAG] = kTag;
+    plan[H_TARGET] = T;
+    plan[H_NUM_ITEMS] = (int)items.size();
     std::copy(expected.begin(), expected.end(), plan + kHeader);
     std::copy(context_lens, context_lens + B, plan + kHeader + B);
     int32_t *dst = plan + kHeader + 2 * (size_t)B;
-    for (const Item &it : items) {
+    for (size_t i = 0; i < items.size(); ++i) {
+        const Item &it = items[i];
+        dst[I_NEXT] = next[i];
         const int nmem = it.nrows / G;
         int tiles = 0, nids = 0, checks = 0;
         dst[I_SEQ0] = it.seq0;

@@ -252,7 +252,7 @@ def test_sharers_scattered_through_the_batch():
     plan = pkv.plan_shared_prefix(shuffled["block_tables"], shuffled["context_lens"], 16, 4, 128, 16)
     h, B = plan.host, len(perm)
     base, iints = 8 + 2 * B, int(h[4])
-    nrows = [int(h[base + i * iints + 1]) for i in range(int(h[0]))]
+    nrows = [int(h[base + i * iints + 1]) for i in range(plan.num_items)]
     assert max(nrows) > 4                    # groups formed: an item serves several sequences
     ref, _ = oracle_out(shuffled)
     for P in (0, 64):

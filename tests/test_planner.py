@@ -18,10 +18,63 @@ def lib():
     return pkv.load_library()
 
 
+def plan_lists(plan, B):
+    """The plan's work lists: list k starts at item k and follows the
+    items' next links, which only point further down; every item belongs to
+    exactly one list."""
+    h = plan.host
+    n_lists, iints, n_items = int(h[0]), int(h[4]), int(h[7])
+    assert (plan.num_lists, plan.num_items) == (n_lists, n_items)
+    assert 1 <= n_lists <= n_items
+    base = 8 + 2 * B
+    seen, lists = set(), []
+    for k in range(n_lists):
+        chain, i = [], k
+        while i >= 0:
+            assert i not in seen
+            seen.add(i)
+            chain.append(i)
+            nxt = int(h[base + i * iints + 7])
+            assert nxt == -1 or i < nxt < n_items
+            i = nxt
+        lists.append(chain)
+    assert seen == set(range(n_items))
+    return lists
+
+
+def list_tiles(plan, B):
+    h, iints = plan.host, int(plan.host[4])
+    return [sum(int(h[8 + 2 * B + i * iints + 4]) for i in chain) for chain in plan_lists(plan, B)]
+
+
+ITEM_COST = 10       # tiles a CTA's switch to its list's next item costs the planner
+MIN_PIECE = 4        # fewest tiles a list starts another unit with
+
+
+def list_costs(plan, B):
+    """A list's cost as the planner balances it: its tiles plus ITEM_COST
+    for every item after the first."""
+    lists = plan_lists(plan, B)
+    return [t + ITEM_COST * (len(c) - 1) for t, c in zip(list_tiles(plan, B), lists)]
+
+
+def check_budget(plan, B):
+    """Every list costs at most the plan's budget, and the greedy fill leaves
+    no list but the last one far below it (a list ends only when the next
+    unit would start with less than MIN_PIECE tiles after its item cost, or
+    at the budget itself inside a unit)."""
+    budget = int(plan.host[6]) // 16
+    costs = list_costs(plan, B)
+    assert max(costs) <= budget
+    assert min(costs[:-1], default=budget) >= budget - ITEM_COST - MIN_PIECE
+    return budget, costs
+
+
 def decode_plan(plan, B, Hk, G):
     h = plan.host
-    n_items, slots, nseq, nkv, iints, maxseg = (int(x) for x in h[:6])
+    n_lists, slots, nseq, nkv, iints, maxseg, target, n_items = (int(x) for x in h[:8])
     assert (nseq, nkv) == (B, Hk)
+    plan_lists(plan, B)
     expected = h[8:8 + B]
     items = []
     base = 8 + 2 * B
@@ -42,13 +95,18 @@ def check_coverage(plan, tables, lens, G, Hk, bs=16):
     items, expected, slots = decode_plan(plan, B, Hk, G)
     np.testing.assert_array_equal(plan.host[8 + B:8 + 2 * B], lens)   # the lengths it was made for
     covered = [np.zeros(max(int(L), 0), dtype=int) for L in lens]
-    slots_seen = [set() for _ in range(B)]
+    # an item writes one partial per row of every member it lists (an empty
+    # one for a member none of its segments serve), in its slot: each
+    # (sequence, slot) exactly once, slots 0 .. expected - 1
+    slots_seen = [[] for _ in range(B)]
     for seq0, nrows, slot, segs, ids, totals, raw, members in items:
         assert len(set(members)) == len(members)
-        assert nrows % G == 0 and nrows <= 24
+        assert nrows % G == 0 and nrows <= 24 and len(members) == nrows // G
         if not segs:
             assert lens[seq0] <= 0
             continue
+        for s in members:
+            slots_seen[s].append(slot)
         # the per-segment offsets the kernel reads: 16-token tiles, block ids
         # and device-table checks (every member's table for a shared prefix
         # segment), in segment order, and the item's totals
@@ -74,11 +132,10 @@ def check_coverage(plan, tables, lens, G, Hk, bs=16):
                 j = np.arange(tb // bs, -(-te // bs))
                 np.testing.assert_array_equal(tables[tseq][j], tables[s][j])
                 covered[s][tb:te] += 1
-                slots_seen[s].add(slot)
     for s in range(B):
         if lens[s] > 0:
             assert (covered[s] == 1).all(), f"sequence {s} not covered exactly once"
-            assert slots_seen[s] == set(range(int(expected[s])))
+            assert sorted(slots_seen[s]) == list(range(int(expected[s])))
         else:
             assert expected[s] == 0
     assert slots == max(1, int(expected.max()))
@@ -97,44 +154,57 @@ def test_forked_prompts_share_their_full_blocks():
     # read the prompt's full blocks once
     prefix_items = [it for it in items if it[1] == 24]
     for p, lp in enumerate(w.prompt_lens):
-        shared = (int(lp) // 16 * 16) // 32 * 32
+        shared = int(lp) // 16 * 16           # the prompt's full blocks
         mine = [it for it in prefix_items if set(it[7]) == set(range(6 * p, 6 * p + 6))]
         assert sum(seg[2] - seg[1] for it in mine for seg in it[3] if seg[3] == 0 and seg[4] == 24) == shared
-    # the items come heaviest first (tokens streamed)
-    weights = [sum(s[2] - s[1] for s in it[3]) for it in items]
-    assert all(a >= b for a, b in zip(weights, weights[1:]))
 
 
-def test_automatic_plan_is_one_balanced_wave():
-    """partition_size 0: the smallest target T whose items fit one CTA per
-    resident slot (3 per SM; 152 SMs when no GPU answers) over the kv heads;
-    every item then streams at most T tokens (plus one alignment step)."""
-    cfg = get("shared_prefix_bf16")
-    w = PagedDecodeWorkload(cfg, 31103, total_steps=8)
-    for _ in range(6):
+def stream_tiles(items):
+    """Tiles of the per-kv-head stream: every item's segments, 16 tokens a tile."""
+    return sum(-(-(te - tb) // 16) for it in items for _, tb, te, _, _ in it[3])
+
+
+@pytest.mark.parametrize("name,step", [("shared_prefix_bf16", 6), ("shared_prefix_bf16", 120),
+                                       ("system_prompt_bf16", 30)])
+def test_automatic_plan_is_one_balanced_wave(name, step):
+    """partition_size 0: one list per resident CTA slot (3 per SM; 152 SMs
+    when no GPU answers) over the kv heads, each list within a snap (at most
+    8 tiles) of an equal share of the stream, whatever the groups' sizes."""
+    cfg = get(name)
+    w = PagedDecodeWorkload(cfg, 31103, total_steps=step + 2)
+    for _ in range(step + 1):
         inp = w.next_step()
     plan = pkv.plan_shared_prefix(inp.block_tables, inp.context_lens, cfg.num_heads, cfg.num_kv_heads,
                                   cfg.head_dim, cfg.block_size, inp.max_context_len)
-    items, _ = check_coverage(plan, inp.block_tables, inp.context_lens, cfg.group, cfg.num_kv_heads)
-    T = int(plan.host[6])
-    tokens = [sum(s[2] - s[1] for s in it[3]) for it in items]
-    assert max(tokens) <= T + 32
-    assert len(items) * cfg.num_kv_heads <= 3 * 152
-    # one step below T would not fit: T is the smallest that does
-    smaller = pkv.plan_shared_prefix(inp.block_tables, inp.context_lens, cfg.num_heads,
-                                     cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
-                                     inp.max_context_len, T - 32)
-    assert int(smaller.host[0]) * cfg.num_kv_heads > 3 * 152
+    items, expected = check_coverage(plan, inp.block_tables, inp.context_lens, cfg.group,
+                                     cfg.num_kv_heads)
+    B = len(inp.context_lens)
+    tiles = list_tiles(plan, B)
+    W = stream_tiles(items)
+    assert sum(tiles) == W
+    n, N = len(tiles), 3 * 152 // cfg.num_kv_heads
+    assert N - 2 <= n <= N
+    budget, costs = check_budget(plan, B)
+    # the budget pays for the item switches the cuts need, not much more
+    assert -(-W // N) <= budget <= -(-W // N) + ITEM_COST + MIN_PIECE
+    # a piece per list boundary at most: items <= units + lists - 1
+    assert len(items) <= len({frozenset(it[7]) for it in items}) + n - 1
 
 
-def test_no_sharing_gives_plain_partitions():
+def test_no_sharing_gives_equal_lists_of_whole_sequences():
     cfg = get("llama7b_f16")
     inp = PagedDecodeWorkload(cfg, 1, total_steps=1).next_step()
     plan = pkv.plan_shared_prefix(inp.block_tables, inp.context_lens, 32, 32, 128, 16,
                                   inp.max_context_len, 512)
     items, expected = check_coverage(plan, inp.block_tables, inp.context_lens, 1, 32)
     assert all(it[1] == 1 and len(it[3]) == 1 for it in items)
-    np.testing.assert_array_equal(expected, -(-inp.context_lens // 512))
+    # lists of a 512-token (32-tile) budget over the stream of all sequences
+    tiles = list_tiles(plan, len(inp.context_lens))
+    W = int((-(-inp.context_lens // 16)).sum())
+    assert sum(tiles) == W
+    budget, _ = check_budget(plan, len(inp.context_lens))
+    assert budget == 32
+    assert expected.sum() == len(items)
 
 
 def test_groups_are_cut_at_24_rows_and_long_tails_split():
@@ -159,9 +229,11 @@ def test_groups_are_cut_at_24_rows_and_long_tails_split():
     items, expected = check_coverage(plan, bt, lens, G, 4)
     groups = sorted({(min(it[7]), it[1]) for it in items if it[1] > G})
     assert groups == [(0, 24), (6, 8)]
-    # 192 shared tokens plus five folded 13-token tails (a 16-row load each)
-    # exceed one 256-token item: the group takes two; the long tail three more
-    assert expected[1] == 2 + 3
+    # the first group streams 192 shared tokens, five 13-token tails (a tile
+    # each) and one 708-token tail: 12 + 5 + 45 = 62 tiles over 16-tile
+    # lists, so its members take at least four partials each
+    assert all(expected[m] >= 4 for m in range(6))
+    assert check_budget(plan, 8)[0] == 16
 
 
 def test_empty_context_gets_a_zero_item_and_plan_size_is_bounded():
@@ -173,8 +245,10 @@ def test_empty_context_gets_a_zero_item_and_plan_size_is_bounded():
     items, expected = check_coverage(plan, bt, lens, 4, 2)
     assert any(it[0] == 2 and not it[3] for it in items)
     assert expected[2] == 0
-    # sequences 0 and 1 share block 0 and 1 but only 20 tokens -> below 32: no group
-    assert all(it[1] == 4 for it in items)
+    # sequences 0 and 1 share blocks 0 and 1, but sequence 0 holds only 20
+    # tokens: their shared prefix is its first full 16-token tile
+    pre = [seg for it in items for seg in it[3] if it[1] == 8 and seg[3] == 0 and seg[4] == 8]
+    assert sum(te - tb for _, tb, te, _, _ in pre) == 16
 
 
 def test_sharers_are_grouped_wherever_they_sit_in_the_batch():
