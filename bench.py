@@ -56,7 +56,7 @@ def parse_args():
     ap.add_argument("--pool-gb", type=float, default=0.0,
                     help="cap the pool of byte-sized presets (profiling cases)")
     ap.add_argument("--partition-size", type=int, default=-1, help="-1: the preset's choice")
-    ap.add_argument("--engine", default="auto", choices=["auto", "cuda_core", "tensor_core"])
+    ap.add_argument("--engine", default="auto", choices=["auto", "cuda_core", "tensor_core", "tcgen05"])
     ap.add_argument("--no-shared", action="store_true",
                     help="shared-prefix workload: use the per-sequence entry point")
     ap.add_argument("--no-e2e", action="store_true")
@@ -289,7 +289,8 @@ def run_native(args):
             "unflushed": unflushed,
             "pct_of_peak": round(100 * value / peak, 2),
             "roofline": {"bound": "hbm",
-                         "kernel": ("pa_cascade_kernel+pa_cascade_merge_kernel" if shared else
+                         "kernel": ((("pa_cascade_tc05_kernel" if engine_used == "tcgen05" else "pa_cascade_kernel")
+                                     + "+pa_cascade_merge_kernel") if shared else
                                     "pa_decode_kernel" + ("+pa_merge_kernel" if decode_launches[0] == 2 else "")),
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": peak_kind,
@@ -384,7 +385,8 @@ def _split_partition(P, max_len, launches):
     return P if P > 0 else 512
 
 
-KERNEL_SOURCES = ("pa_decode.cuh", "pa_cascade.cuh", "pa_merge.cuh", "pkv_device.cuh", "cascade_plan.h")
+KERNEL_SOURCES = ("pa_decode.cuh", "pa_cascade.cuh", "pa_cascade_tc05.cuh", "pa_merge.cuh",
+                  "pkv_device.cuh", "cascade_plan.h")
 
 
 def kernel_source_sha():

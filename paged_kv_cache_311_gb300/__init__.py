@@ -137,17 +137,19 @@ def last_decode_launches() -> int:
     return int(load_library().pkv_last_decode_launches())
 
 
-ENGINES = {"auto": 0, "cuda_core": 1, "tensor_core": 2}
+ENGINES = {"auto": 0, "cuda_core": 1, "tensor_core": 2, "tcgen05": 3}
 
 
 def set_decode_engine(engine: str) -> None:
-    """Process-wide engine of the decode kernel: "auto", "cuda_core" or "tensor_core"."""
+    """Process-wide engine of the decode kernels: "auto", "cuda_core", "tensor_core"
+    (warp-level MMA) or "tcgen05" (the shared-prefix kernel on tcgen05 MMAs with
+    TMEM accumulators; the per-sequence kernel keeps the warp-level MMA)."""
     _check(load_library().pkv_decode_set_engine(ENGINES[engine]), "pkv_decode_set_engine")
 
 
 def last_decode_engine() -> str:
     code = int(load_library().pkv_last_decode_engine())
-    return {1: "cuda_core", 2: "tensor_core"}.get(code, "none")
+    return {1: "cuda_core", 2: "tensor_core", 3: "tcgen05"}.get(code, "none")
 
 
 def _ptr(t: Optional[torch.Tensor]):

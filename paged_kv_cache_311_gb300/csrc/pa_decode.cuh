@@ -63,7 +63,7 @@ struct DecodeParams {
     int num_items;       // shared-prefix plans: work items in the plan
 };
 
-enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2 };
+enum Engine { kEngineAuto = 0, kEngineCudaCore = 1, kEngineTensorCore = 2, kEngineTcgen05 = 3 };
 
 #ifndef PKV_DECODE_STAGE_BUDGET_CC
 #define PKV_DECODE_STAGE_BUDGET_CC 98304

@@ -88,7 +88,8 @@ SplitLayout split_layout(long long seqs, long long heads, long long np, long lon
 }  // namespace
 
 int encode_kv_map(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int eb,
-                  int head_dim, int block_size, int num_kv_heads, int64_t num_blocks, int box_rows)
+                  int head_dim, int block_size, int num_kv_heads, int64_t num_blocks, int box_rows,
+                  int box_chunks)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -97,8 +98,8 @@ int encode_kv_map(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
     const cuuint64_t dims[5] = {(cuuint64_t)(128 / eb), (cuuint64_t)block_size, row / 128,
                                 (cuuint64_t)num_kv_heads, (cuuint64_t)num_blocks};
     const cuuint64_t strides[4] = {row, 128, row * block_size, row * block_size * num_kv_heads};
-    const cuuint32_t box[5] = {(cuuint32_t)(128 / eb), (cuuint32_t)box_rows, (cuuint32_t)(row / 128),
-                               1, 1};
+    const cuuint32_t box[5] = {(cuuint32_t)(128 / eb), (cuuint32_t)box_rows,
+                               (cuuint32_t)(box_chunks > 0 ? box_chunks : row / 128), 1, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(map, dtype, 5, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -152,7 +153,7 @@ int pkv_last_decode_engine(void) { return g_last_decode_engine; }
 
 int pkv_decode_set_engine(int engine)
 {
-    if (engine < kEngineAuto || engine > kEngineTensorCore)
+    if (engine < kEngineAuto || engine > kEngineTcgen05)
         return PKV_EINVAL;
     g_engine_override.store(engine, std::memory_order_relaxed);
     return PKV_OK;
@@ -355,7 +356,7 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
     a.head_dim = head_dim;
     a.block_size = block_size;
     a.group = group;
-    a.engine = kEngineTensorCore;
+    a.engine = g_engine_override.load(std::memory_order_relaxed);
     a.shared = true;
     a.plan = plan;
     a.num_lists = num_lists;

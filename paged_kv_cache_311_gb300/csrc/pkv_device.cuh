@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "../../include/pkv.h"
 
 namespace pkv {
@@ -271,4 +273,95 @@ template <> struct Mma<__half> {
     __device__ __forceinline__ static float2 unpack(uint32_t w) { return Unpack<__half>::pair(w); }
 };
 
+}  // namespace pkv
+
+namespace pkv {
+namespace tc05 {
+
+// ------------------------------------------- 5th-generation tensor cores
+// Shared-memory matrix descriptor with 128-byte swizzling (the layout the
+// TMA's 128-byte swizzle writes: 8-row atoms of 128-byte rows, 16-byte
+// pieces of row r at piece ^ (r % 8); atoms 1024-byte aligned).  K-major
+// operands: sbo = byte stride between 8-row groups, lbo unused; MN-major
+// operands: lbo = byte stride between 64-element chunks along M (or N), sbo
+// = byte stride between 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((addr >> 4) & 0x3fffu) | (uint64_t)((lbo >> 4) & 0x3fffu) << 16 |
+           (uint64_t)((sbo >> 4) & 0x3fffu) << 32 | (uint64_t)1 << 46 | (uint64_t)2 << 61;
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulation: A and B of
+// the cache's 16-bit type, M x N, each operand K-major or MN-major.
+template <typename T>
+__device__ __forceinline__ uint32_t idesc(int M, int N, bool a_mn, bool b_mn)
+{
+    constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    return 1u << 4 | fmt << 7 | fmt << 10 | (a_mn ? 1u : 0u) << 15 | (b_mn ? 1u : 0u) << 16 |
+           (uint32_t)(N >> 3) << 17 | (uint32_t)(M >> 4) << 24;
+}
+
+// D (TMEM) = A * B (+ D when acc), issued by one thread.
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, bool acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a), "l"(b), "r"(id), "r"(acc ? 1u : 0u)
+                 : "memory");
+}
+
+// The barrier's next phase completes when every MMA this thread issued so
+// far has completed.
+__device__ __forceinline__ void commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// Warp-collective TMEM allocation of `ncols` columns (a power of two >= 32);
+// the address is written to *slot.
+__device__ __forceinline__ void alloc(uint32_t *slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Ordering of tensor-core operations across a thread barrier.
+__device__ __forceinline__ void fence_before_sync()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Warp-collective: this warp's 32 TMEM lanes (lane quarter warp % 4), 8
+// consecutive 32-bit columns from `taddr` (lane field included): thread t
+// receives lane (base + t).
+__device__ __forceinline__ void ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+}  // namespace tc05
 }  // namespace pkv

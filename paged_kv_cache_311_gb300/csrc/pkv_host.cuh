@@ -8,6 +8,7 @@
 #include <utility>
 
 #include "pa_cascade.cuh"
+#include "pa_cascade_tc05.cuh"
 #include "pa_merge.cuh"
 
 namespace pkv {
@@ -32,8 +33,10 @@ struct DecodeLaunch {
 // shared memory as [chunk][row][128 bytes] with 128-byte swizzling.
 // Dimension order (innermost first): elements of a 128-byte chunk, row of
 // the block, 128-byte chunk of the row, kv head, block.
+// The box is box_rows rows of box_chunks chunks (0: all chunks of a row).
 int encode_kv_map(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
-                  int head_dim, int block_size, int num_kv_heads, int64_t num_blocks, int box_rows);
+                  int head_dim, int block_size, int num_kv_heads, int64_t num_blocks, int box_rows,
+                  int box_chunks = 0);
 
 // Marks a kernel as allowed to use `bytes` of dynamic shared memory on the
 // current device (cached per device).
@@ -103,32 +106,46 @@ int run_decode(const DecodeLaunch &a)
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
-// Shared-prefix (cascade) path: one CTA per (kv head, planned item), then the
+// Shared-prefix (cascade) path: one CTA per (kv head, work list), then the
 // merge of multi-item sequences as a programmatic dependent launch (its CTAs
 // take the slots the first grid frees and wait for it to complete, so no
-// launch gap separates the two).
-template <typename T, int D, int BS, int G>
+// launch gap separates the two).  TC05: the tcgen05 kernel (head_dim 128),
+// else the warp-level MMA kernel.
+template <typename T, int D, int BS, int G, bool TC05>
 int run_cascade(const DecodeLaunch &a)
 {
-    using CC = CascadeCfg<T, D, BS, G>;
     const DecodeParams &p = a.p;
     alignas(64) CUtensorMap tmk;
     alignas(64) CUtensorMap tmv;
+    int box_rows, box_chunks, smem;
+    void (*kern)(DecodeParams, CUtensorMap, CUtensorMap, const int32_t *);
+    if constexpr (TC05) {
+        using CC = Tc05Cfg<T, D, BS, G>;
+        box_rows = CC::BOX_ROWS;
+        box_chunks = 1;   // one 64-element chunk plane per load
+        smem = CC::SMEM_BYTES;
+        kern = pa_cascade_tc05_kernel<T, D, BS, G>;
+    } else {
+        using CC = CascadeCfg<T, D, BS, G>;
+        box_rows = CC::C::BOX_ROWS;
+        box_chunks = 0;
+        smem = CC::SMEM_BYTES;
+        kern = pa_cascade_kernel<T, D, BS, G>;
+    }
     int rc = encode_kv_map(&tmk, a.k_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
-                           p.num_blocks, CC::C::BOX_ROWS);
+                           p.num_blocks, box_rows, box_chunks);
     if (rc)
         return rc;
     rc = encode_kv_map(&tmv, a.v_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
-                       p.num_blocks, CC::C::BOX_ROWS);
+                       p.num_blocks, box_rows, box_chunks);
     if (rc)
         return rc;
     static unsigned long long done = 0;
-    auto kern = pa_cascade_kernel<T, D, BS, G>;
-    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), CC::SMEM_BYTES, &done);
+    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem, &done);
     if (rc)
         return rc;
     dim3 grid(p.num_kv_heads, a.num_lists, 1);
-    rc = launch_pdl(kern, grid, dim3(CC::C::NW * 32), CC::SMEM_BYTES, a.stream, p, tmk, tmv, a.plan);
+    rc = launch_pdl(kern, grid, dim3(128), smem, a.stream, p, tmk, tmv, a.plan);
     if (rc)
         return rc;
 
@@ -142,7 +159,7 @@ int run_cascade(const DecodeLaunch &a)
     if (rc)
         return rc;
     if (a.engine_used)
-        *a.engine_used = kEngineTensorCore;
+        *a.engine_used = TC05 ? kEngineTcgen05 : kEngineTensorCore;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -154,13 +171,25 @@ template <typename T, int D, int BS, int G>
 int run_engine(const DecodeLaunch &a)
 {
     if constexpr (Elem<T>::bytes == 2) {
-        if (a.shared)
-            return run_cascade<T, D, BS, G>(a);
+        if (a.shared) {
+            // shared prefix: the warp-level MMA kernel (measured faster so
+            // far), the tcgen05 one at head_dim 128 on request; per sequence:
+            // warp-level MMA (a tcgen05 request included: a decode tile of <= 8
+            // query rows is HBM-bound there)
+            if constexpr (D == 128) {
+                if (a.engine == kEngineTcgen05)
+                    return run_cascade<T, D, BS, G, true>(a);
+            } else {
+                if (a.engine == kEngineTcgen05)
+                    return PKV_EUNSUPPORTED;
+            }
+            return run_cascade<T, D, BS, G, false>(a);
+        }
         const bool tc = a.engine != kEngineCudaCore;
         if (tc)
             return run_decode<T, D, BS, G, true>(a);
     } else {
-        if (a.engine == kEngineTensorCore || a.shared)
+        if (a.engine == kEngineTensorCore || a.engine == kEngineTcgen05 || a.shared)
             return PKV_EUNSUPPORTED;
     }
     return run_decode<T, D, BS, G, false>(a);

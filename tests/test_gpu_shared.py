@@ -19,6 +19,19 @@ import oracle
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["auto", "tcgen05"])
+def shared_engine(request):
+    """Every case on both shared-prefix kernels: "auto" takes the warp-level
+    MMA kernel, "tcgen05" the tcgen05 kernel at head_dim 128 (head_dim 64 has
+    none: PKV_EUNSUPPORTED)."""
+    import paged_kv_cache_311_gb300 as pkv
+    pkv.set_decode_engine(request.param)
+    _ENGINE_NOW[0] = pkv.ENGINES[request.param]
+    yield request.param
+    pkv.set_decode_engine("auto")
+    _ENGINE_NOW[0] = 0
+
+
 def shared_case(seed, *, dtype="bf16", H=8, Hk=2, D=128, bs=16, groups=((300, (5, 40, 1, 70)),)):
     """groups: (prompt length, tail lengths of its members); a member with
     tail -1 is a singleton sequence of the given prompt length (no sharing)."""
@@ -103,9 +116,19 @@ def run_shared(case, P=0, out_dtype=torch.float32, tables=None, plan_tables=None
                                           max_context_len=mcl, device_status=st)
         torch.cuda.synchronize()
         assert pkv.last_decode_launches() == 2
+        engine = int(pkv.load_library().pkv_last_decode_engine())
+        if case["dtype"] != "f32":
+            assert engine == (3 if _engine_now() == 3 else 2)
     # the device only reads the plan
     np.testing.assert_array_equal(plan_dev.cpu().numpy(), plan.host)
     return out.double().cpu().numpy(), int(st.item())
+
+
+_ENGINE_NOW = [0]   # the engine code the fixture set
+
+
+def _engine_now():
+    return _ENGINE_NOW[0]
 
 
 def oracle_out(case, tables=None):
@@ -179,12 +202,20 @@ def test_plan_made_for_other_lengths_is_rejected_on_the_device():
     assert max_err(got[keep], ref[keep]) <= TOL["bf16"]
 
 
-def test_shared_prefix_head_dim_64_and_half_output():
+@pytest.mark.parametrize("D", [64, 128])
+def test_shared_prefix_half_output(D, shared_engine):
     """bf16 output is the fp32 result rounded to nearest even (bit-exact
     against the same plan with fp32 output), so it lies within one bf16 ulp
     of the oracle rounded to bf16, plus the fp32 result's own error; also
-    for the plan cut into many 64-token items (one kv head fills the GPU)."""
-    case = shared_case(3, dtype="bf16", H=8, Hk=1, D=64, bs=16, groups=GROUPS[:2])
+    for the plan cut into many 64-token items (one kv head fills the GPU).
+    The tcgen05 kernel takes head_dim 128 only."""
+    import paged_kv_cache_311_gb300 as pkv
+    case = shared_case(3, dtype="bf16", H=8, Hk=1, D=D, bs=16, groups=GROUPS[:2])
+    if D == 64 and shared_engine == "tcgen05":
+        with pytest.raises(pkv.PkvError) as e:
+            run_shared(case)
+        assert e.value.status == -2
+        return
     ref, _ = oracle_out(case)
     from tests.gpu_support import ulp_bound
     rne = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
