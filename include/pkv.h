@@ -376,15 +376,17 @@ int pkv_paged_attention_decode_static(void *out, int out_dtype, const void *q,
 size_t pkv_static_workspace_capacity(void);
 
 /*
- * Engine of the decode kernel, process-wide (tests and benchmarks compare the
- * two): 0 = automatic (tensor cores for 16-bit caches, CUDA cores for fp32
- * caches), 1 = CUDA cores, 2 = tensor cores
- * (16-bit caches only; fp32 caches then return PKV_EUNSUPPORTED).
- * Returns PKV_EINVAL for other values.
+ * Engine of the decode kernels, process-wide (tests and benchmarks compare
+ * them): 0 = automatic (warp-level tensor-core MMA for 16-bit caches, CUDA
+ * cores for fp32 caches), 1 = CUDA cores, 2 = warp-level tensor-core MMA
+ * (16-bit caches only; fp32 caches then return PKV_EUNSUPPORTED), 3 =
+ * tcgen05: the shared-prefix decode on tcgen05 MMAs with accumulators in
+ * tensor memory (head_dim 128; other head dims return PKV_EUNSUPPORTED), the
+ * per-sequence decode as for 2.  Returns PKV_EINVAL for other values.
  */
 int pkv_decode_set_engine(int engine);
 
-/* Engine (1 or 2) of the last successful decode call on this host thread. */
+/* Engine (1, 2 or 3) of the last successful decode call on this host thread. */
 int pkv_last_decode_engine(void);
 
 /* Static, NUL-terminated description of a pkv_status value. */
