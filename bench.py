@@ -418,63 +418,82 @@ def traffic_for(cfg, algo_bytes):
     return int(e["traffic_per_algorithmic_byte"] * algo_bytes)
 
 
+_PACK_ALIGN = 256   # every piece of a packed step starts on a 256-byte boundary
+
+
+def _pack_pinned(tensors):
+    """One pinned host buffer holding the given CPU tensors back to back
+    (each 256-byte aligned), and where each one sits: the step's inputs then
+    cross to the device in one copy instead of one per tensor."""
+    layout, off = {}, 0
+    for name, t in tensors.items():
+        t = t.contiguous()
+        nbytes = t.numel() * t.element_size()
+        layout[name] = (off, tuple(t.shape), t.dtype, nbytes)
+        off += -(-nbytes // _PACK_ALIGN) * _PACK_ALIGN
+    buf = torch.empty(max(off, _PACK_ALIGN), dtype=torch.uint8)
+    if torch.cuda.is_available():
+        buf = buf.pin_memory()
+    for name, t in tensors.items():
+        o, shape, dtype, nbytes = layout[name]
+        if nbytes:
+            buf[o:o + nbytes].copy_(t.contiguous().reshape(-1).view(torch.uint8))
+    return buf, layout
+
+
+def _unpack(dev_buf, layout):
+    """Device views of a packed step's tensors."""
+    out = {}
+    for name, (o, shape, dtype, nbytes) in layout.items():
+        out[name] = dev_buf[o:o + nbytes].view(dtype).view(shape)
+    return out
+
+
 def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
-    """Same step, inputs from pinned host memory, output read back, all timed."""
+    """Same step, inputs from pinned host memory, output read back, all timed.
+    Each step's inputs (q, new K/V, slot mapping, block tables, lengths,
+    copy-on-write pairs, the shared-prefix plan) were packed into one pinned
+    buffer when the step was prepared, so a step makes one host-to-device
+    copy and one device-to-host copy of the output."""
     import paged_kv_cache_311_gb300 as pkv
-    cfg = state.cfg
     stream = torch.cuda.current_stream()
     dev = state.device
-    pinned = []
+    packed = []
     for s in steps:
-        d = {k: getattr(s, k).cpu().pin_memory() for k in
+        d = {k: getattr(s, k).cpu() for k in
              ("q", "key", "value", "slot_mapping", "block_tables", "context_lens")}
         if s.cow_pairs is not None:
-            d["cow_pairs"] = s.cow_pairs.cpu().pin_memory()
+            d["cow_pairs"] = s.cow_pairs.cpu()
         if s.plan is not None:
-            d["plan"] = torch.from_numpy(s.plan.host).pin_memory()
-        pinned.append(d)
-    dev_bufs = {k: torch.empty_like(getattr(steps[0], k)) for k in
-                ("q", "slot_mapping", "context_lens")}
+            d["plan"] = torch.from_numpy(s.plan.host)
+        packed.append(_pack_pinned(d))
+    dev_buf = torch.empty(max(b.numel() for b, _ in packed), dtype=torch.uint8, device=dev)
+    # each step's device views of the staging buffer, made with the step
+    views = [_unpack(dev_buf, layout) for _, layout in packed]
     out_host = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
     h2d = d2h = 0
     total_ms = 0.0
-    for i, (s, hp) in enumerate(zip(steps, pinned)):
+    for s, (hbuf, _), t in zip(steps, packed, views):
+        dst = dev_buf[:hbuf.numel()]
         _flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        q = torch.empty(hp["q"].shape, dtype=hp["q"].dtype, device=dev)
-        q.copy_(hp["q"], non_blocking=True)
-        key = torch.empty(hp["key"].shape, dtype=hp["key"].dtype, device=dev)
-        key.copy_(hp["key"], non_blocking=True)
-        val = torch.empty(hp["value"].shape, dtype=hp["value"].dtype, device=dev)
-        val.copy_(hp["value"], non_blocking=True)
-        sm = torch.empty(hp["slot_mapping"].shape, dtype=torch.int64, device=dev)
-        sm.copy_(hp["slot_mapping"], non_blocking=True)
-        bt = torch.empty(hp["block_tables"].shape, dtype=torch.int32, device=dev)
-        bt.copy_(hp["block_tables"], non_blocking=True)
-        cl = torch.empty(hp["context_lens"].shape, dtype=torch.int32, device=dev)
-        cl.copy_(hp["context_lens"], non_blocking=True)
-        nb = sum(t.numel() * t.element_size() for t in hp.values())
-        if "cow_pairs" in hp:
-            cp = torch.empty(hp["cow_pairs"].shape, dtype=torch.int64, device=dev)
-            cp.copy_(hp["cow_pairs"], non_blocking=True)
-            pkv.copy_blocks([state.k_cache], [state.v_cache], cp, device_status=state.status)
-        plan_dev = None
-        if "plan" in hp:
-            plan_dev = torch.empty(hp["plan"].shape, dtype=torch.int32, device=dev)
-            plan_dev.copy_(hp["plan"], non_blocking=True)
-        pkv.reshape_and_cache(key, val, state.k_cache, state.v_cache, sm, device_status=state.status)
-        _decode(pkv, state, s, q, bt, cl, plan_dev, P)
+        dst.copy_(hbuf, non_blocking=True)
+        if "cow_pairs" in t:
+            pkv.copy_blocks([state.k_cache], [state.v_cache], t["cow_pairs"], device_status=state.status)
+        pkv.reshape_and_cache(t["key"], t["value"], state.k_cache, state.v_cache, t["slot_mapping"],
+                              device_status=state.status)
+        _decode(pkv, state, s, t["q"], t["block_tables"], t["context_lens"], t.get("plan"), P)
         out_host.copy_(state.out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         total_ms += e0.elapsed_time(e1)
-        h2d += nb
+        h2d += hbuf.numel()
         d2h += out_host.numel() * out_host.element_size()
     n = len(steps)
     return {"value": round(bytes_step / (total_ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d / n), "d2h_bytes_per_step": int(d2h / n),
-            "ms_per_step": round(total_ms / n, 5)}
+            "ms_per_step": round(total_ms / n, 5), "h2d_copies_per_step": 1}
 
 
 # ------------------------------------------------------------- CPU oracle

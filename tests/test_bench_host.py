@@ -15,3 +15,22 @@ def test_split_partition_only_for_two_launches():
     assert bench._split_partition(0, 30000, 1) == 0
     assert bench._split_partition(0, 30000, 2) == 512
     assert bench._split_partition(256, 30000, 2) == 256
+
+
+def test_packed_step_round_trip():
+    """The e2e step's inputs packed into one buffer come back bit for bit,
+    each piece 256-byte aligned."""
+    import torch
+    g = torch.Generator().manual_seed(1)
+    ts = {"q": torch.randn(3, 5, 8, generator=g).to(torch.bfloat16),
+          "slot_mapping": torch.arange(7, dtype=torch.int64) * 3,
+          "block_tables": torch.randint(0, 99, (3, 4), generator=g, dtype=torch.int32),
+          "empty": torch.empty(0, 2, dtype=torch.int64),
+          "plan": torch.from_numpy(np.arange(11, dtype=np.int32))}
+    buf, layout = bench._pack_pinned(ts)
+    back = bench._unpack(buf, layout)
+    for k, t in ts.items():
+        assert layout[k][0] % 256 == 0
+        assert back[k].dtype == t.dtype and back[k].shape == t.shape
+        assert torch.equal(back[k].view(torch.uint8) if t.numel() else back[k],
+                           t.view(torch.uint8) if t.numel() else t)
