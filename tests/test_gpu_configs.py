@@ -54,3 +54,15 @@ def test_long_context_sampled(bs):
     pool_bytes = min(cfg.pool_value, 0.8 * free)
     nb = int(pool_bytes // (2 * cfg.block_bytes))
     run_config(cfg, SEED_BASE + 4, steps=2, samples=2, pool_blocks=nb)
+
+
+@pytest.mark.parametrize("idx", [3, 5])
+def test_shared_presets_sampled_on_tcgen05(idx):
+    """The two shared-prefix presets at full size on the tcgen05 kernel."""
+    import paged_kv_cache_311_gb300 as pkv
+    pkv.set_decode_engine("tcgen05")
+    try:
+        run_config(CONFIGS[idx], SEED_BASE + idx, steps=3, samples=6)
+        assert pkv.last_decode_engine() == "tcgen05"
+    finally:
+        pkv.set_decode_engine("auto")

@@ -290,3 +290,39 @@ def test_sharers_scattered_through_the_batch():
         got, st = run_shared(shuffled, P=P)
         assert st == 0
         assert max_err(got, ref) <= TOL["bf16"], f"P={P}"
+
+
+def growing_scores_case(seed, dtype="bf16", bs=16):
+    """Keys carry a component along a fixed direction proportional to their
+    logical position, and every query has that direction: scores climb by
+    about 12 (log2 units) every 16 tokens, more than the kernels' 2^8 slack
+    on a row's reference maximum, so every tile moves the running maxima and
+    rescales the accumulators (on the tcgen05 kernel, O in tensor memory)."""
+    case = shared_case(seed, dtype=dtype, H=8, Hk=2, D=128, bs=bs, groups=GROUPS)
+    bt, lens = case["block_tables"], case["context_lens"]
+    pos = {}
+    for s in range(len(lens)):
+        for j in range(-(-int(lens[s]) // bs)):
+            for o in range(bs):
+                pos[(int(bt[s, j]), o)] = j * bs + o   # shared blocks sit at the same position
+    u = torch.zeros(128)
+    u[:8] = 1.0
+    kc = case["k_cache"].float()
+    for (b, o), t in pos.items():
+        kc[b, :, o, :] += 0.75 * t * u
+    q = case["q"].float() + u
+    return dict(case, k_cache=kc.to(DT[dtype]), q=q.to(DT[dtype]))
+
+
+@pytest.mark.parametrize("bs", [8, 32])
+def test_growing_scores_rescale_every_tile(bs, shared_engine):
+    from tests.gpu_support import gpu_decode
+    case = growing_scores_case(31 + bs, bs=bs)
+    ref, st = oracle_out(case)
+    assert st == 0
+    for P in (0, 64):
+        got, gst = run_shared(case, P=P)
+        assert gst == 0
+        assert max_err(got, ref) <= TOL["bf16"], f"shared P={P}"
+    per_seq, pst, _ = gpu_decode(case)     # the per-sequence kernel's rescale too
+    assert pst == 0 and max_err(per_seq, ref) <= TOL["bf16"]
