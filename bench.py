@@ -19,6 +19,7 @@ region.  cpu_baseline = the CPU oracle on a bounded sample of the same steps.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -204,6 +205,8 @@ def run_native(args):
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index) if rank == 0 else None
+    gc.collect()      # no collector pass inside the timed steps
+    gc.disable()
     torch.cuda.nvtx.range_push("timed_steps")
     for i, s in enumerate(steps[args.warmup:]):
         _flush_l2(flush)
@@ -226,6 +229,7 @@ def run_native(args):
         e2.record(stream)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
+    gc.enable()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop() if clocks else None
@@ -473,6 +477,8 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
     out_host = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
     h2d = d2h = 0
     total_ms = 0.0
+    gc.collect()      # no collector pass inside the timed steps
+    gc.disable()
     for s, (hbuf, _), t in zip(steps, packed, views):
         dst = dev_buf[:hbuf.numel()]
         _flush_l2(flush)
@@ -490,6 +496,7 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
         total_ms += e0.elapsed_time(e1)
         h2d += hbuf.numel()
         d2h += out_host.numel() * out_host.element_size()
+    gc.enable()
     n = len(steps)
     return {"value": round(bytes_step / (total_ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d / n), "d2h_bytes_per_step": int(d2h / n),
