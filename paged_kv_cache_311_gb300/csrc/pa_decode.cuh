@@ -435,16 +435,6 @@ struct TcEngine {
         }
     };
 
-    // Both halves back to back: all loads first, then all stores (a store
-    // between two loads would keep the second load from issuing before the
-    // first returns).
-    __device__ static void stage_q_rows(const DecodeParams &p, uint8_t *qs, const CtaWork &w)
-    {
-        QRows q;
-        q.load(p, w);
-        q.store(qs);
-    }
-
     __device__ void init(const DecodeParams &p, uint8_t *qs, const CtaWork &w, int, int lane)
     {
         g = lane >> 2;
