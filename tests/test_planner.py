@@ -277,3 +277,51 @@ def test_sharers_are_grouped_wherever_they_sit_in_the_batch():
     items, expected = check_coverage(plan, bt, lens, G, 4)
     groups = {frozenset(it[7]) for it in items if it[1] > G}
     assert groups == {frozenset(i for i, w_ in enumerate(which) if w_ == p) for p in (0, 1)}
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_batches_cover_exactly_within_budget(seed):
+    """Random batches: a few prompts forked into members with random tails,
+    singletons and empty contexts, in shuffled batch order, with random
+    block size, query group and target.  Every token is covered once per
+    query row, lists are well formed and within their budget, and the plan
+    fits the size bound."""
+    rng = np.random.default_rng(1000 + seed)
+    bs = int(rng.choice([8, 16, 32]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hk = int(rng.integers(1, 4))
+    rows, lens, nxt = [], [], 0
+    for _ in range(int(rng.integers(1, 5))):           # forked prompts
+        P_ = int(rng.integers(1, 700))
+        full, rem = divmod(P_, bs)
+        shared = list(range(nxt, nxt + full))
+        nxt += full
+        for _m in range(int(rng.integers(1, 9))):
+            L = P_ + int(rng.integers(0, 200))
+            own = -(-L // bs) - full
+            rows.append(shared + list(range(nxt, nxt + own)))
+            nxt += own
+            lens.append(L)
+    for _ in range(int(rng.integers(0, 4))):           # singletons and empty contexts
+        L = int(rng.integers(0, 400))
+        nb = -(-L // bs)
+        rows.append(list(range(nxt, nxt + nb)))
+        nxt += nb
+        lens.append(L)
+    order = rng.permutation(len(rows))
+    rows = [rows[i] for i in order]
+    lens = np.array([lens[i] for i in order], np.int32)
+    MB = max(1, max(len(r) for r in rows))
+    bt = np.full((len(rows), MB), -1, np.int32)
+    for i, r in enumerate(rows):
+        bt[i, :len(r)] = r
+    # automatic, or an explicit target: a multiple of 32 and of bs, at most 64 blocks
+    target = int(rng.choice([0, 0, max(bs, 32) * int(rng.integers(1, 9))]))
+    mcl = max(int(lens.max()), 1)
+    plan = pkv.plan_shared_prefix(bt, lens, G * Hk, Hk, 128, bs, mcl, target)
+    assert plan.host.size <= pkv.load_library().pkv_shared_plan_max_ints(len(lens), G * Hk, Hk, mcl, target)
+    items, expected = check_coverage(plan, bt, lens, G, Hk, bs=bs)
+    if items and any(it[3] for it in items):
+        budget, costs = check_budget(plan, len(lens))
+        if target:
+            assert budget <= target // 16    # the explicit target caps every list's cost
