@@ -259,6 +259,8 @@ def run_native(args):
     dec_mean_ms = sum(dec_ms) / len(dec_ms)
     achieved = bytes_dec / len(dec_ms) / (dec_mean_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
+    main_kernel = (("pa_cascade_tc05_kernel" if engine_used == "tcgen05" else "pa_cascade_kernel")
+                   if shared else "pa_decode_kernel")
 
     unflushed = _unflushed_decode(pkv, state, steps[-1], P, dec_bytes[-1], peak)
 
@@ -293,12 +295,11 @@ def run_native(args):
             "unflushed": unflushed,
             "pct_of_peak": round(100 * value / peak, 2),
             "roofline": {"bound": "hbm",
-                         "kernel": ((("pa_cascade_tc05_kernel" if engine_used == "tcgen05" else "pa_cascade_kernel")
-                                     + "+pa_cascade_merge_kernel") if shared else
-                                    "pa_decode_kernel" + ("+pa_merge_kernel" if decode_launches[0] == 2 else "")),
+                         "kernel": main_kernel + ("+pa_cascade_merge_kernel" if shared else
+                                                  "+pa_merge_kernel" if decode_launches[0] == 2 else ""),
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                         "traffic": traffic_for(cfg, bytes_dec / len(dec_ms)),
+                         "traffic": traffic_for(cfg, main_kernel, bytes_dec / len(dec_ms)),
                          "algorithmic_bytes_per_launch": int(bytes_dec / len(dec_ms)),
                          "mean_launch_ms": round(dec_mean_ms, 5)},
             "clocks": clk,
@@ -389,35 +390,42 @@ def _split_partition(P, max_len, launches):
     return P if P > 0 else 512
 
 
-KERNEL_SOURCES = ("pa_decode.cuh", "pa_cascade.cuh", "pa_cascade_tc05.cuh", "pa_merge.cuh",
-                  "pkv_device.cuh", "cascade_plan.h")
+# the sources each timed decode kernel is compiled from (its own file and
+# every header it includes): a traffic figure stays valid while these are
+# unchanged, whatever else in the library changes
+_COMMON_SOURCES = ("pa_decode.cuh", "pa_merge.cuh", "pkv_device.cuh")
+KERNEL_SOURCES = {
+    "pa_decode_kernel": _COMMON_SOURCES,
+    "pa_cascade_kernel": _COMMON_SOURCES + ("pa_cascade.cuh", "cascade_plan.h"),
+    "pa_cascade_tc05_kernel": _COMMON_SOURCES + ("pa_cascade.cuh", "cascade_plan.h",
+                                                 "pa_cascade_tc05.cuh"),
+}
 
 
-def kernel_source_sha():
-    """sha256 prefix over the decode kernels' sources: a traffic figure taken
+def kernel_source_sha(kernel):
+    """sha256 prefix over one decode kernel's sources: a traffic figure taken
     on other sources is stale."""
     import hashlib
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "paged_kv_cache_311_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_for(cfg, algo_bytes):
+def traffic_for(cfg, kernel, algo_bytes):
     """Per-launch DRAM traffic (read + write) of the decode kernel, from the
     committed ncu capture's traffic / algorithmic-bytes ratio scaled to this
-    run's launches; None unless that capture was taken on the current kernel
-    source for this workload."""
+    run's launches; None unless that capture was taken on this workload, with
+    this kernel, on its current sources."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    e = d.get(cfg.name)
-    h = kernel_source_sha()
-    if not e or e.get("source_sha") != h:
+    e = d.get(cfg.name, {}).get(kernel)   # {workload: {kernel: figure}}
+    if not e or e.get("source_sha") != kernel_source_sha(kernel):
         return None
     return int(e["traffic_per_algorithmic_byte"] * algo_bytes)
 

@@ -45,17 +45,18 @@ struct Tc05Cfg {
     static constexpr int NW = 4;
     static constexpr int TILE = plan::kTileTokens;   // 16 tokens
     static constexpr int TOK = 2 * TILE;             // tokens per stage
+    static constexpr int GRP = 8;                    // tokens per group: one 8-row swizzle atom
     static constexpr int NSLOT = 4;                  // stages in the ring
     static constexpr int CHUNKS = D * 2 / 128;       // 64-element chunks per row
-    static constexpr int PLANE = TOK * 128;          // one chunk plane of a stage
-    static constexpr int MAT = CHUNKS * PLANE;       // K (or V) of a stage
-    static constexpr int SLOT = 2 * MAT;
-    static constexpr int BOX_ROWS = BS < TILE ? BS : TILE;
-    static constexpr int BOXES = TILE / BOX_ROWS;
-    static constexpr int BOX_BYTES = BOX_ROWS * 128;  // one chunk of one box
+    static constexpr int ATOM = GRP * 128;           // one chunk of one group's rows
+    // a group's period: [K chunk 0][K chunk 1][V chunk 0][V chunk 1]
+    static constexpr int PERIOD = 4 * ATOM;
+    static constexpr int V_OFF = 2 * ATOM;
+    static constexpr int SLOT = (TOK / GRP) * PERIOD;
+    static constexpr int BOX_ROWS = GRP;
     static constexpr int RQ = plan::kMaxRows;        // query rows of an item
+    static constexpr int RPL = RQ / 4;               // query rows per lane (four lanes per token)
     static constexpr int QPLANE = RQ * 128;
-    static constexpr int P_LO = PLANE;               // P^T [token][rows]: low half after the high half
     static constexpr int TM_COLS = 64;               // S^T at column 0, O^T at column 32
     static constexpr int MAXSEG = plan::max_segments(G);
     static constexpr int ITEM_INTS = plan::item_ints(G);
@@ -63,7 +64,7 @@ struct Tc05Cfg {
     static constexpr int SEGS = plan::item_segments_offset();
     static constexpr int TABLE_CAP = plan::kTableCap;
     // ring | q rows | barriers (full[NSLOT], empty[NSLOT], scores) | TMEM
-    // address, flag, stages issued | per-warp row reductions [2][RQ], the
+    // address, flag, stages issued | per-warp row reductions [NW][RQ], the
     // rows' reference maxima and rescale factors | item copy, segment /
     // member / row flags | the list's next item
     static constexpr int OFF_RING = 0;
@@ -72,7 +73,7 @@ struct Tc05Cfg {
     static constexpr int OFF_TMEM = OFF_BAR + (2 * NSLOT + 1) * 8;
     static constexpr int OFF_FLAG = OFF_TMEM + 8;
     static constexpr int OFF_RED = OFF_FLAG + 8;
-    static constexpr int OFF_ITEM = (OFF_RED + 4 * RQ * 4 + 15) / 16 * 16;
+    static constexpr int OFF_ITEM = (OFF_RED + (NW + 2) * RQ * 4 + 15) / 16 * 16;
     static constexpr int EXTRA_INTS = ITEM_INTS + MAXSEG + RQ + 2;
     static constexpr int OFF_NEXT = (OFF_ITEM + EXTRA_INTS * 4 + 15) / 16 * 16;
     static constexpr bool PREFETCH = 3 * (OFF_NEXT + ITEM_INTS * 4 + 2048) <= 228 * 1024;
@@ -80,11 +81,14 @@ struct Tc05Cfg {
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
     static_assert(3 * (SMEM_BYTES + 1024) <= 228 * 1024, "three CTAs per SM");
     static_assert(3 * TM_COLS <= 512, "TMEM of three CTAs per SM");
-    static_assert(SLOT % 1024 == 0 && OFF_Q % 1024 == 0 && QPLANE % 1024 == 0 && PLANE % 1024 == 0,
+    static_assert(SLOT % 1024 == 0 && OFF_Q % 1024 == 0 && QPLANE % 1024 == 0 && ATOM == 1024,
                   "128-byte swizzle atoms are 1024-byte aligned");
-    static_assert(2 * P_LO <= MAT, "P (high and low) fits over the stage's K");
-    static_assert(TILE % BOX_ROWS == 0 && BOX_BYTES % 1024 == 0, "boxes");
-    static_assert(plan::kNT * 8 == RQ, "n-tiles");
+    // S^T's A operand spans 16 atoms from a slot's chunk-1 start: the last
+    // one reads the 1 KiB after the slot (the next slot, or the q rows); an
+    // M = 128 product's N rounded up to 32 reads q rows 24-31 past the staged
+    // ones (in shared memory; their columns are never read)
+    static_assert(OFF_Q >= SLOT && CHUNKS == 2 && TOK / GRP == NW, "layout");
+    static_assert(plan::kNT * 8 == RQ && RQ % 4 == 0 && (RPL % 2) == 0, "n-tiles");
 };
 
 template <typename T, int D, int BS, int G>
@@ -108,8 +112,8 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + CC::OFF_TMEM);
     uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + CC::OFF_FLAG);
     int32_t *n_issued = reinterpret_cast<int32_t *>(cta_flag + 1);   // stages of the item issued
-    float *red = reinterpret_cast<float *>(smem + CC::OFF_RED);   // [2][RQ]
-    float *mref = red + 2 * RQ;   // the rows' reference maxima (log2 domain), CTA-uniform
+    float *red = reinterpret_cast<float *>(smem + CC::OFF_RED);   // [NW][RQ]
+    float *mref = red + NW * RQ;  // the rows' reference maxima (log2 domain), CTA-uniform
     float *alph = mref + RQ;      // rescale factors of a moved reference
     int32_t *it = reinterpret_cast<int32_t *>(smem + CC::OFF_ITEM);
     int32_t *segbad = it + CC::ITEM_INTS;
@@ -216,38 +220,40 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
         // (block 0 is loaded in its place).
         auto issue = [&](int s) {
             const int gs = g + s, sl = gs % NSLOT;
-            uint8_t *kd = smem + CC::OFF_RING + sl * CC::SLOT;
-            int kk[2], t0[2], nbox[2];
+            uint8_t *base = smem + CC::OFF_RING + sl * CC::SLOT;
+            int kk[2], t0[2], te[2];
             uint32_t bytes = 0;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int tt = 2 * s + u;
-                nbox[u] = 0;
+                te[u] = 0;
+                t0[u] = 0;
                 if (tt < total) {
                     kk[u] = seg_of(tt, k_issue);
                     const int *gg = seg(kk[u]);
                     t0[u] = gg[plan::S_BEGIN] + (tt - gg[plan::S_FIRST_TILE]) * TILE;
-                    nbox[u] = min(CC::BOXES, (gg[plan::S_END] - t0[u] + CC::BOX_ROWS - 1) / CC::BOX_ROWS);
-                    bytes += (uint32_t)(nbox[u] * CC::CHUNKS * 2 * CC::BOX_BYTES);
+                    te[u] = min(gg[plan::S_END], t0[u] + TILE);
+                    bytes += (uint32_t)(((te[u] - t0[u] + CC::GRP - 1) / CC::GRP) * 4 * CC::ATOM);
                 }
             }
             mbar_arrive_expect_tx(&full[sl], bytes);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                for (int b = 0; b < nbox[u]; ++b) {
+                for (int gi = 0; gi < 2; ++gi) {
+                    const int tok = t0[u] + gi * CC::GRP;
+                    if (tok >= te[u])
+                        continue;
                     const int *gg = seg(kk[u]);
-                    const int tok = t0[u] + b * CC::BOX_ROWS;
                     int phys = ids[gg[plan::S_ID_OFF] + tok / BS - gg[plan::S_BEGIN] / BS];
                     if (phys < 0 || (int64_t)phys >= p.num_blocks) {
                         segbad[kk[u]] = 1;
                         phys = 0;
                     }
-                    const int row = u * TILE + b * CC::BOX_ROWS;
+                    uint8_t *gb = base + (2 * u + gi) * CC::PERIOD;
 #pragma unroll
                     for (int c = 0; c < CC::CHUNKS; ++c) {
-                        uint8_t *dk = kd + c * CC::PLANE + row * 128;
-                        tma_load_5d(dk, &tmk, &full[sl], 0, tok % BS, c, kvh, phys);
-                        tma_load_5d(dk + CC::MAT, &tmv, &full[sl], 0, tok % BS, c, kvh, phys);
+                        tma_load_5d(gb + c * CC::ATOM, &tmk, &full[sl], 0, tok % BS, c, kvh, phys);
+                        tma_load_5d(gb + CC::V_OFF + c * CC::ATOM, &tmv, &full[sl], 0, tok % BS, c, kvh, phys);
                     }
                 }
             }
@@ -343,14 +349,20 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
         // next stage's S^T as soon as this stage's scores are in registers,
         // this stage's O^T once its P is in shared memory; lane 0 of warp 3
         // refills the ring.
-        float ls[RQ];
+        float ls[CC::RPL];   // this lane's token's share of its rows' sums
 #pragma unroll
-        for (int r = 0; r < RQ; ++r)
-            ls[r] = 0.f;
-        const uint32_t id_qk = tc05::idesc<T>(64, 8 * ntl, false, false);
-        const uint32_t id_pv = tc05::idesc<T>(128, 8 * ntl, true, true);
+        for (int j = 0; j < CC::RPL; ++j)
+            ls[j] = 0.f;
+        // M = 128 products take N a multiple of 16: the query rows' n-tiles
+        // rounded up to 16 or 32 columns (the extra ones are never read)
+        const int n16 = 16 * ((ntl + 1) / 2);
+        const uint32_t id_qk = tc05::idesc<T>(128, n16, false, false);
+        const uint32_t id_pv = tc05::idesc<T>(128, n16, true, true);
         const uint64_t q_desc = tc05::sdesc(qb, 16, 1024);
-        // S^T of stage s into TMEM (the stage's K, A K-major; q rows, B K-major)
+        // S^T of stage s into TMEM (the stage's K, A K-major; q rows, B K-major).
+        // A is 128 rows of 8-row atoms 1 KiB apart from a chunk's first atom:
+        // atom 4w is group w's K, so group w's 8 tokens land in TMEM lanes
+        // 32w .. 32w + 7, warp w's quarter; the other rows are ignored.
         auto issue_qk = [&](int st) {
             const int gs = g + st, sl = gs % NSLOT;
             const uint64_t k_desc = tc05::sdesc(smem_u32(smem + CC::OFF_RING + sl * CC::SLOT), 16, 1024);
@@ -361,7 +373,7 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
             tc05::fence_after_sync();
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (uint32_t)((ks / 4) * CC::PLANE + (ks % 4) * 32);
+                const uint32_t off = (uint32_t)((ks / 4) * CC::ATOM + (ks % 4) * 32);
                 const uint32_t qoff = (uint32_t)((ks / 4) * CC::QPLANE + (ks % 4) * 32);
                 tc05::mma(tS, k_desc + (off >> 4), q_desc + (qoff >> 4), id_qk, ks > 0);
             }
@@ -382,46 +394,56 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
             }
             tc05::fence_after_sync();
 
-            // scores of this warp's tile (warps 0 and 1; lane = token < 16)
-            float x[RQ];
-            bool tile_here = false;
-            int nvalid = 0;
-            if (warp < 2) {
-                const int tt = 2 * s + warp;
-                int rlo = 0, rhi = 0;
-                if (tt < total) {
-                    const int k = seg_of(tt, k_use);
-                    const int *gg = seg(k);
-                    const int t0 = gg[plan::S_BEGIN] + (tt - gg[plan::S_FIRST_TILE]) * TILE;
-                    nvalid = min(TILE, gg[plan::S_END] - t0);
-                    rlo = gg[plan::S_ROW_LO];
-                    rhi = min(gg[plan::S_ROW_HI], nrows);
-                    tile_here = true;
-                }
+            // scores of this warp's group: tokens 8w .. 8w + 7 of the stage
+            // (tile w / 2), read from lanes 0-7 of the warp's TMEM quarter and
+            // shuffled out: lane = 8 rq + t takes token t's query rows
+            // [RPL rq, RPL rq + RPL)
+            const int tt = 2 * s + (warp >> 1), t = lane & 7, rq = lane >> 3;
+            const int g_tok0 = (warp & 1) * CC::GRP;   // the group's first token in its tile
+            int nvalid = 0, rlo = 0, rhi = 0;
+            const bool tile_here = tt < total;
+            if (tile_here) {
+                const int k = seg_of(tt, k_use);
+                const int *gg = seg(k);
+                const int t0 = gg[plan::S_BEGIN] + (tt - gg[plan::S_FIRST_TILE]) * TILE;
+                nvalid = min(TILE, gg[plan::S_END] - t0);
+                rlo = gg[plan::S_ROW_LO];
+                rhi = min(gg[plan::S_ROW_HI], nrows);
+            }
+            const bool valid = tile_here && g_tok0 + t < nvalid;
+            float x[CC::RPL];
+            {
                 uint32_t sv[NT][8];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        sv[nt][j] = 0u;
                     if (nt < ntl)
                         tc05::ld8(tS + tlane + 8 * nt, sv[nt]);
+                }
                 tc05::wait_ld();
-                const bool valid = tile_here && lane < nvalid;
+                float got[CC::RPL];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int k = 0; k < 4; ++k)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int r = 8 * nt + j;
-                        const bool live = valid && nt < ntl && r >= rlo && r < rhi;
-                        x[r] = live ? __uint_as_float(sv[nt][j]) * p.qscale : -INFINITY;
+                    for (int j = 0; j < CC::RPL; ++j) {
+                        const int r = CC::RPL * k + j;
+                        const uint32_t v = __shfl_sync(0xffffffffu, sv[r / 8][r % 8], t);
+                        if (rq == k)
+                            got[j] = __uint_as_float(v);
                     }
-            } else {
 #pragma unroll
-                for (int r = 0; r < RQ; ++r)
-                    x[r] = -INFINITY;
+                for (int j = 0; j < CC::RPL; ++j) {
+                    const int r = CC::RPL * rq + j;
+                    const bool live = valid && r >= rlo && r < rhi;
+                    x[j] = live ? got[j] * p.qscale : -INFINITY;
+                }
             }
             bool over = false;
 #pragma unroll
-            for (int r = 0; r < RQ; ++r)
-                over |= x[r] > mref[r] + kSlack;
+            for (int j = 0; j < CC::RPL; ++j)
+                over |= x[j] > mref[CC::RPL * rq + j] + kSlack;
             tc05::fence_before_sync();
             const bool any_over = __syncthreads_or(over);
             // the scores are in registers: S^T may take the next stage
@@ -442,32 +464,37 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
                 }
             }
             if (any_over) {
-                // exact running maxima: per warp over its tokens, then over
-                // warps 0 and 1 in shared memory
-                if (warp < 2) {
+                // exact running maxima: per warp over its 8 tokens (the lanes
+                // of one rq), then over the warps in shared memory
 #pragma unroll
-                    for (int r = 0; r < RQ; ++r) {
-                        float t = x[r];
-                        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 1));
-                        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 2));
-                        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 4));
-                        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
-                        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
-                        if (lane == 0)
-                            red[warp * RQ + r] = t;
-                    }
+                for (int j = 0; j < CC::RPL; ++j) {
+                    float m8 = x[j];
+                    m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 1));
+                    m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 2));
+                    m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 4));
+                    if (t == 0)
+                        red[warp * RQ + CC::RPL * rq + j] = m8;
                 }
                 __syncthreads();
+                auto stage_max = [&](int r) {
+                    float mx = red[r];
+#pragma unroll
+                    for (int w2 = 1; w2 < NW; ++w2)
+                        mx = fmaxf(mx, red[w2 * RQ + r]);
+                    return mx;
+                };
                 bool grew = false;
 #pragma unroll
-                for (int r = 0; r < RQ; ++r) {
-                    const float mo = mref[r], mn = fmaxf(mo, fmaxf(red[r], red[RQ + r]));
-                    grew |= mn != mo;
-                    ls[r] *= mn == -INFINITY ? 1.f : exp2f(mo - mn);
+                for (int j = 0; j < CC::RPL; ++j) {
+                    const int r = CC::RPL * rq + j;
+                    const float mo = mref[r], mn = fmaxf(mo, stage_max(r));
+                    ls[j] *= mn == -INFINITY ? 1.f : exp2f(mo - mn);
                 }
+                for (int r = 0; r < RQ; ++r)
+                    grew |= fmaxf(mref[r], stage_max(r)) != mref[r];
                 __syncthreads();   // every thread has read the old references
                 if (tid < RQ) {
-                    const float mo = mref[tid], mn = fmaxf(mo, fmaxf(red[tid], red[RQ + tid]));
+                    const float mo = mref[tid], mn = fmaxf(mo, stage_max(tid));
                     alph[tid] = mn == -INFINITY ? 1.f : exp2f(mo - mn);
                     mref[tid] = mn;
                 }
@@ -500,44 +527,35 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
                     break;
                 }
             }
-
             // probabilities against the reference; P^T = hi + lo over the
-            // stage's K as [token][query rows] (the B operand MN-major): a
-            // token's 24 rows are three 16-byte pieces per half
-            if (warp < 2) {
-                const int tok = TILE * warp + lane;
-                float pr[RQ];
+            // group's K atoms as [token][query rows] (the B operand MN-major,
+            // swizzled like the ring): this lane's RPL rows are RPL / 2
+            // 32-bit words of token t's row
+            {
+                uint8_t *grp = slot_p + warp * CC::PERIOD;
 #pragma unroll
-                for (int r = 0; r < RQ; ++r) {
-                    pr[r] = x[r] == -INFINITY ? 0.f : exp2f(x[r] - fmaxf(mref[r], -1e30f));
-                    ls[r] += pr[r];
+                for (int i = 0; i < CC::RPL / 2; ++i) {
+                    const int r = CC::RPL * rq + 2 * i;
+                    const float a0 = x[2 * i] == -INFINITY ? 0.f : exp2f(x[2 * i] - fmaxf(mref[r], -1e30f));
+                    const float a1 =
+                        x[2 * i + 1] == -INFINITY ? 0.f : exp2f(x[2 * i + 1] - fmaxf(mref[r + 1], -1e30f));
+                    ls[2 * i] += a0;
+                    ls[2 * i + 1] += a1;
+                    const uint32_t h = Mma<T>::pack(a0, a1);
+                    const float2 hf = Mma<T>::unpack(h);
+                    const uint32_t l = Mma<T>::pack(a0 - hf.x, a1 - hf.y);
+                    const int byte = r * 2;
+                    const int off = t * 128 + ((((byte >> 4) ^ t)) << 4) + (byte & 15);
+                    *reinterpret_cast<uint32_t *>(grp + off) = h;
+                    *reinterpret_cast<uint32_t *>(grp + CC::ATOM + off) = l;
                 }
-                if (lane < TILE) {
+                // rows of V past the tile's valid tokens may hold anything (even
+                // NaN patterns): zero them so that 0 * v stays 0
+                if (tile_here && !valid && rq < CC::CHUNKS) {
+                    uint4 *vrow = reinterpret_cast<uint4 *>(grp + CC::V_OFF + rq * CC::ATOM + t * 128);
 #pragma unroll
-                    for (int pc = 0; pc < NT; ++pc) {
-                        uint32_t h[4], l[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float a0 = pr[8 * pc + 2 * e], a1 = pr[8 * pc + 2 * e + 1];
-                            h[e] = Mma<T>::pack(a0, a1);
-                            const float2 hf = Mma<T>::unpack(h[e]);
-                            l[e] = Mma<T>::pack(a0 - hf.x, a1 - hf.y);
-                        }
-                        const int off = tok * 128 + ((pc ^ (tok & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(slot_p + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                        *reinterpret_cast<uint4 *>(slot_p + CC::P_LO + off) = make_uint4(l[0], l[1], l[2], l[3]);
-                    }
-                }
-                // rows of V past the tile's valid tokens may hold anything
-                // (even NaN patterns): zero them so that 0 * v stays 0
-                if (tile_here && lane < TILE && lane >= nvalid) {
-#pragma unroll
-                    for (int c = 0; c < CC::CHUNKS; ++c) {
-                        uint4 *vrow = reinterpret_cast<uint4 *>(slot_p + CC::MAT + c * CC::PLANE + tok * 128);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            vrow[q] = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                    for (int q = 0; q < 8; ++q)
+                        vrow[q] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async_smem();
@@ -545,14 +563,15 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
             __syncthreads();
             if (tid == kIssuer) {
                 tc05::fence_after_sync();
-                const uint32_t vb = smem_u32(slot_p) + CC::MAT, pb = smem_u32(slot_p);
+                const uint32_t sb = smem_u32(slot_p);
                 const int nk = 2 * s + 1 < total ? 2 : 1;
                 for (int j = 0; j < nk; ++j) {
-                    const uint64_t a = tc05::sdesc(vb + (uint32_t)(j * TILE * 128), CC::PLANE, 1024);
-                    tc05::mma(tO, a, tc05::sdesc(pb + (uint32_t)(j * TILE * 128), 4096, 1024), id_pv,
-                              s > 0 || j > 0);
-                    tc05::mma(tO, a, tc05::sdesc(pb + CC::P_LO + (uint32_t)(j * TILE * 128), 4096, 1024),
-                              id_pv, true);
+                    // tokens 16j .. 16j + 15: groups 2j, 2j + 1, one period apart;
+                    // V^T MN-major (chunks one atom apart), P^T MN-major
+                    const uint32_t gb = sb + (uint32_t)(2 * j * CC::PERIOD);
+                    const uint64_t a = tc05::sdesc(gb + CC::V_OFF, CC::ATOM, CC::PERIOD);
+                    tc05::mma(tO, a, tc05::sdesc(gb, CC::PERIOD, CC::PERIOD), id_pv, s > 0 || j > 0);
+                    tc05::mma(tO, a, tc05::sdesc(gb + CC::ATOM, CC::PERIOD, CC::PERIOD), id_pv, true);
                 }
                 tc05::commit(&empty[sl]);
             }
@@ -589,18 +608,15 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
         g += n_st;
 
         // ---- row sums over the tokens' lanes, bad rows, results
-        if (warp < 2) {
+        // row sums: over a warp's 8 token lanes, then over the warps
 #pragma unroll
-            for (int r = 0; r < RQ; ++r) {
-                float t = ls[r];
-                t += __shfl_xor_sync(0xffffffffu, t, 1);
-                t += __shfl_xor_sync(0xffffffffu, t, 2);
-                t += __shfl_xor_sync(0xffffffffu, t, 4);
-                t += __shfl_xor_sync(0xffffffffu, t, 8);
-                t += __shfl_xor_sync(0xffffffffu, t, 16);
-                if (lane == 0)
-                    red[warp * RQ + r] = t;
-            }
+        for (int j = 0; j < CC::RPL; ++j) {
+            float sm = ls[j];
+            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 4);
+            if ((lane & 7) == 0)
+                red[warp * RQ + CC::RPL * (lane >> 3) + j] = sm;
         }
         if (tid == 0) {
             bool any = invalid_item;
@@ -648,7 +664,7 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
         for (int r = 0; r < RQ; ++r) {
             if (r < nrows) {
                 const bool bad_r = failed_all || ((*badrows >> r) & 1u);
-                const float L = red[r] + red[RQ + r];
+                const float L = red[r] + red[RQ + r] + red[2 * RQ + r] + red[3 * RQ + r];
                 const int64_t sh = row_head(p, w, G, r);
                 if (exp_s[r / G] == 1) {
                     const float inv = !bad_r && L > 0.f ? 1.f / L : 0.f;

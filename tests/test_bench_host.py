@@ -34,3 +34,27 @@ def test_packed_step_round_trip():
         assert back[k].dtype == t.dtype and back[k].shape == t.shape
         assert torch.equal(back[k].view(torch.uint8) if t.numel() else back[k],
                            t.view(torch.uint8) if t.numel() else t)
+
+
+def test_traffic_only_for_the_kernel_it_was_captured_on():
+    """A stored DRAM-traffic ratio scales to the run's bytes only for its own
+    workload and kernel, and only while that kernel's sources are unchanged."""
+    import json
+    import os
+    from types import SimpleNamespace
+    with open(os.path.join(bench.ROOT, "profiles", "decode_traffic.json")) as f:
+        stored = json.load(f)
+    for name, per_kernel in stored.items():
+        cfg = SimpleNamespace(name=name)
+        for k in bench.KERNEL_SOURCES:
+            e = per_kernel.get(k)
+            fresh = e is not None and e["source_sha"] == bench.kernel_source_sha(k)
+            want = int(e["traffic_per_algorithmic_byte"] * 1_000_000) if fresh else None
+            assert bench.traffic_for(cfg, k, 1_000_000) == want
+        assert set(per_kernel) <= set(bench.KERNEL_SOURCES)
+    assert bench.traffic_for(SimpleNamespace(name="no_such_workload"), "pa_decode_kernel", 1) is None
+    # every kernel's sources include the headers its file includes
+    for k, srcs in bench.KERNEL_SOURCES.items():
+        assert len(set(srcs)) == len(srcs)
+        assert bench.kernel_source_sha(k) != ""
+    assert set(bench.KERNEL_SOURCES["pa_cascade_kernel"]) < set(bench.KERNEL_SOURCES["pa_cascade_tc05_kernel"])
