@@ -380,7 +380,7 @@ def plan_shared_prefix(block_tables, context_lens, num_heads: int, num_kv_heads:
     L = load_library()
     cap = int(L.pkv_shared_plan_max_ints(B, num_heads, num_kv_heads, max_context_len,
                                           partition_size))
-    plan = np.zeros(max(cap, 16), dtype=np.int32)
+    plan = np.empty(max(cap, 16), dtype=np.int32)   # the planner writes every int it returns
     n_ints, ws = ctypes.c_size_t(0), ctypes.c_size_t(0)
     rc = L.pkv_plan_shared_prefix(bt.ctypes.data, cl.ctypes.data, B, MB, block_size, num_heads,
                                   num_kv_heads, head_dim, max_context_len, partition_size,

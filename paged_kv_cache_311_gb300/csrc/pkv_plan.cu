@@ -43,13 +43,28 @@ struct Seg {
     int table_seq, tok_begin, tok_end, row_lo, row_hi;
 };
 
+// A work item; its segments and members live in flat arrays.
 struct Item {
     int seq0, nrows, slot;
-    std::vector<Seg> segs;
-    long long weight;  // tokens streamed
-    int entries;       // block-table entries of all segments
-    std::vector<int> members;  // the sequences whose rows the item serves
+    int seg_begin, seg_count;   // in the segment array
+    int mem_begin, mem_count;   // the sequences whose rows it serves: order[mem_begin ..]
+    int entries;                // block-table entries of all segments
 };
+
+// First j < n with a[j] != b[j], else n.  Tables that share a long prefix
+// (a cached prompt, forked samples) are compared 16 entries at a time.
+int first_diff(const int32_t *a, const int32_t *b, int n)
+{
+    constexpr int kChunk = 16;
+    int j = 0;
+    if (n > 0 && a[0] != b[0])
+        return 0;
+    while (j + kChunk <= n && std::memcmp(a + j, b + j, kChunk * sizeof(int32_t)) == 0)
+        j += kChunk;
+    while (j < n && a[j] == b[j])
+        ++j;
+    return j;
+}
 
 int blocks_between(int tb, int te, int bs) { return (te + bs - 1) / bs - tb / bs; }
 
@@ -119,7 +134,8 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     // Sequences that share leading blocks are grouped wherever they sit in
     // the batch (forked samples are neighbours, requests that reuse a cached
     // system prompt need not be): order them by the block ids of their
-    // tables, valid contexts first and batch order among equal prefixes.
+    // tables, lexicographically (a table that is a prefix of another first),
+    // valid contexts first and batch order among equal tables.
     auto nblk = [&](int s) { return len_ok(s) ? (context_lens[s] + bs - 1) / bs : 0; };
     std::vector<int> order(B);
     for (int s = 0; s < B; ++s)
@@ -129,10 +145,8 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         if ((na > 0) != (nb > 0))
             return na > 0;
         const int32_t *ta = block_tables + (long long)a * MB, *tb = block_tables + (long long)b * MB;
-        for (int j = 0, n = std::min(na, nb); j < n; ++j)
-            if (ta[j] != tb[j])
-                return ta[j] < tb[j];
-        return false;
+        const int n = std::min(na, nb), j = first_diff(ta, tb, n);
+        return j < n ? ta[j] < tb[j] : na < nb;
     });
 
     // tokens that order[k] shares with order[k - 1]
@@ -145,9 +159,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         const int n = std::min(nblk(sa), nblk(sb));
         const int32_t *a = block_tables + (long long)sa * MB;
         const int32_t *b = block_tables + (long long)sb * MB;
-        int c = 0;
-        while (c < n && a[c] == b[c])
-            ++c;
+        const int c = first_diff(a, b, n);
         sp[k] = std::min(c * bs, std::min(la, lb)) / align * align;
     }
 
@@ -179,43 +191,43 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     };
     struct Unit {
         int seq0, nrows;
-        std::vector<int> members;
-        std::vector<Part> parts;
-        long long t0 = 0, tiles = 0;   // place in the kv head's stream
-        int pieces = 0;
+        int mem_begin, mem_count;   // members: order[mem_begin ..]
+        int part_begin, part_end;   // in the part array
+        long long t0, tiles;        // place in the kv head's stream
+        int pieces;
     };
     auto tiles_of = [](int tb, int te) { return (long long)((te - tb + kTileTokens - 1) / kTileTokens); };
     std::vector<Unit> units;
-    std::vector<int> empty;   // sequences with an empty or invalid context
+    std::vector<Part> parts;
+    std::vector<int> empty;   // order positions of sequences with an empty or invalid context
+    units.reserve(groups.size());
+    parts.reserve((size_t)B + groups.size());
     long long W = 0;
     for (const Group &g : groups) {
         const int s = order[g.first];
-        Unit u;
-        u.seq0 = s;
-        u.members.assign(order.begin() + g.first, order.begin() + g.first + g.cnt);
-        u.nrows = g.cnt * G;
+        if (g.cnt == 1 && !len_ok(s)) {
+            empty.push_back(g.first);
+            continue;
+        }
+        Unit u{s, g.cnt * G, g.first, g.cnt, (int)parts.size(), 0, W, 0, 0};
         auto add = [&](int seq, int tb, int te, int lo, int hi) {
             const long long t = tiles_of(tb, te);
-            u.parts.push_back(Part{seq, tb, te, lo, hi, u.tiles, t});
+            parts.push_back(Part{seq, tb, te, lo, hi, u.tiles, t});
             u.tiles += t;
         };
         if (g.cnt == 1) {
-            if (!len_ok(s)) {
-                empty.push_back(s);
-                continue;
-            }
             add(s, 0, context_lens[s], 0, G);
         } else {
             add(s, 0, g.S, 0, u.nrows);
             for (int m = 0; m < g.cnt; ++m) {
-                const int L = context_lens[u.members[m]];
+                const int L = context_lens[order[g.first + m]];
                 if (L > g.S)
-                    add(u.members[m], g.S, L, m * G, (m + 1) * G);
+                    add(order[g.first + m], g.S, L, m * G, (m + 1) * G);
             }
         }
-        u.t0 = W;
+        u.part_end = (int)parts.size();
         W += u.tiles;
-        units.push_back(std::move(u));
+        units.push_back(u);
     }
 
     // ---- lists: the stream cut into consecutive ranges, one CTA each (per
@@ -282,7 +294,11 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     // items: the pieces of units that each list's range covers, in stream
     // order; a piece serves all its unit's rows, with the unit's parts (or
     // pieces of them) inside its range as segments
-    std::vector<std::vector<Item>> lists((size_t)std::max(1LL, nl));
+    std::vector<Item> store;
+    std::vector<Seg> segs;
+    std::vector<std::vector<int>> lists((size_t)std::max(1LL, nl));   // indices into store
+    store.reserve(units.size() + (size_t)nl + empty.size());
+    segs.reserve(parts.size() + 2 * (size_t)nl);
     {
         size_t u = 0;
         for (long long k = 0; k < nl; ++k) {
@@ -294,33 +310,40 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
                 const long long b0 = std::min(cuts[k + 1], un.t0 + un.tiles) - un.t0;
                 if (a0 >= b0)
                     continue;
-                Item it{un.seq0, un.nrows, un.pieces++, {}, 0, 0, un.members};
-                for (const Part &pt : un.parts) {
+                Item it{un.seq0, un.nrows, un.pieces++, (int)segs.size(), 0, un.mem_begin, un.mem_count, 0};
+                for (int p = un.part_begin; p < un.part_end; ++p) {
+                    const Part &pt = parts[(size_t)p];
                     const long long x = std::max(a0, pt.t0), y = std::min(b0, pt.t0 + pt.tiles);
                     if (x >= y)
                         continue;
                     const int tb = pt.tb + (int)((x - pt.t0) * kTileTokens);
                     const int te = std::min(pt.te, pt.tb + (int)((y - pt.t0) * kTileTokens));
-                    it.segs.push_back(Seg{pt.table_seq, tb, te, pt.row_lo, pt.row_hi});
-                    it.weight += te - tb;
+                    segs.push_back(Seg{pt.table_seq, tb, te, pt.row_lo, pt.row_hi});
                     it.entries += blocks_between(tb, te, bs);
                 }
-                lists[(size_t)k].push_back(std::move(it));
+                it.seg_count = (int)segs.size() - it.seg_begin;
+                lists[(size_t)k].push_back((int)store.size());
+                store.push_back(it);
             }
         }
     }
-    for (size_t e = 0; e < empty.size(); ++e)   // zero output, no loads: any list
-        lists[e % lists.size()].push_back(Item{empty[e], G, 0, {}, 0, 0, {empty[e]}});
+    for (size_t e = 0; e < empty.size(); ++e) {   // zero output, no loads: any list
+        const int pos = empty[e];
+        lists[e % lists.size()].push_back((int)store.size());
+        store.push_back(Item{order[pos], G, 0, (int)segs.size(), 0, pos, 1, 0});
+    }
     for (const Unit &un : units)
-        for (int m : un.members)
-            expected[m] = un.pieces;
+        for (int m = 0; m < un.mem_count; ++m)
+            expected[order[un.mem_begin + m]] = un.pieces;
 
     // list k starts at item k; the rest follow, each list's items chained
-    std::vector<Item> items;
+    std::vector<int> items;   // plan position -> store index
     std::vector<int> next;
+    items.reserve(store.size());
     for (auto &l : lists)
         items.push_back(l[0]);
     next.assign(items.size(), -1);
+    next.reserve(store.size());
     for (size_t k = 0; k < lists.size(); ++k) {
         int prev = (int)k;
         for (size_t j = 1; j < lists[k].size(); ++j) {
@@ -345,7 +368,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     if (!plan || plan_capacity_ints < need)
         return PKV_EWORKSPACE;
 
-    for (const Item &it : items)
+    for (const Item &it : store)
         if (it.entries > kTableCap)   // cannot happen: items are cut to fit
             return PKV_EUNSUPPORTED;
     std::memset(plan, 0, need * sizeof(int32_t));
@@ -361,19 +384,19 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     std::copy(context_lens, context_lens + B, plan + kHeader + B);
     int32_t *dst = plan + kHeader + 2 * (size_t)B;
     for (size_t i = 0; i < items.size(); ++i) {
-        const Item &it = items[i];
+        const Item &it = store[(size_t)items[i]];
         dst[I_NEXT] = next[i];
         const int nmem = it.nrows / G;
         int tiles = 0, nids = 0, checks = 0;
         dst[I_SEQ0] = it.seq0;
         for (int m = 0; m < kMaxRows; ++m)
-            dst[kItemHead + m] = m < (int)it.members.size() ? it.members[m] : -1;
+            dst[kItemHead + m] = m < it.mem_count ? order[it.mem_begin + m] : -1;
         dst[I_NROWS] = it.nrows;
         dst[I_SLOT] = it.slot;
-        dst[I_NSEG] = (int)it.segs.size();
+        dst[I_NSEG] = it.seg_count;
         int32_t *ids = dst + item_ids_offset(G);
-        for (size_t k = 0; k < it.segs.size(); ++k) {
-            const Seg &g = it.segs[k];
+        for (int k = 0; k < it.seg_count; ++k) {
+            const Seg &g = segs[(size_t)(it.seg_begin + k)];
             const int nb = blocks_between(g.tok_begin, g.tok_end, bs);
             const bool shared = g.row_lo == 0 && g.row_hi == it.nrows && nmem > 1;
             int32_t *q = dst + item_segments_offset() + kSegInts * k;
@@ -389,8 +412,7 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
             nids += nb;
             checks += (shared ? nmem : 1) * nb;
             const int32_t *row = block_tables + (long long)g.table_seq * MB;
-            for (int j = g.tok_begin / bs; j < (g.tok_end + bs - 1) / bs; ++j)
-                *ids++ = row[j];
+            ids = std::copy(row + g.tok_begin / bs, row + (g.tok_end + bs - 1) / bs, ids);
         }
         dst[I_TILES] = tiles;
         dst[I_IDS] = nids;

@@ -53,9 +53,14 @@ MIN_PIECE = 4        # fewest tiles a list starts another unit with
 
 def list_costs(plan, B):
     """A list's cost as the planner balances it: its tiles plus ITEM_COST
-    for every item after the first."""
-    lists = plan_lists(plan, B)
-    return [t + ITEM_COST * (len(c) - 1) for t, c in zip(list_tiles(plan, B), lists)]
+    for every item after the first that streams tiles (the zero-output items
+    of empty contexts are appended outside the balanced stream)."""
+    h, iints = plan.host, int(plan.host[4])
+    costs = []
+    for t, chain in zip(list_tiles(plan, B), plan_lists(plan, B)):
+        n = sum(1 for i in chain if int(h[8 + 2 * B + i * iints + 4]) > 0)
+        costs.append(t + ITEM_COST * max(0, n - 1))
+    return costs
 
 
 def check_budget(plan, B):
@@ -279,17 +284,12 @@ def test_sharers_are_grouped_wherever_they_sit_in_the_batch():
     assert groups == {frozenset(i for i, w_ in enumerate(which) if w_ == p) for p in (0, 1)}
 
 
-@pytest.mark.parametrize("seed", range(24))
-def test_random_batches_cover_exactly_within_budget(seed):
-    """Random batches: a few prompts forked into members with random tails,
-    singletons and empty contexts, in shuffled batch order, with random
-    block size, query group and target.  Every token is covered once per
-    query row, lists are well formed and within their budget, and the plan
-    fits the size bound."""
-    rng = np.random.default_rng(1000 + seed)
+def random_batch(rng, prefix_rate=0.0):
+    """A few prompts forked into members with random tails, singletons and
+    empty contexts, in shuffled batch order.  With prefix_rate, a member's
+    context may end inside its prompt: its table is then a prefix of the
+    prompt's shared blocks (plus its own copy of a partial block)."""
     bs = int(rng.choice([8, 16, 32]))
-    G = int(rng.choice([1, 2, 4, 8]))
-    Hk = int(rng.integers(1, 4))
     rows, lens, nxt = [], [], 0
     for _ in range(int(rng.integers(1, 5))):           # forked prompts
         P_ = int(rng.integers(1, 700))
@@ -297,9 +297,13 @@ def test_random_batches_cover_exactly_within_budget(seed):
         shared = list(range(nxt, nxt + full))
         nxt += full
         for _m in range(int(rng.integers(1, 9))):
-            L = P_ + int(rng.integers(0, 200))
-            own = -(-L // bs) - full
-            rows.append(shared + list(range(nxt, nxt + own)))
+            if rng.random() < prefix_rate:
+                L = int(rng.integers(1, P_ + 1))
+            else:
+                L = P_ + int(rng.integers(0, 200))
+            nb = -(-L // bs)
+            own = max(0, nb - full)
+            rows.append(shared[:nb] + list(range(nxt, nxt + own)))
             nxt += own
             lens.append(L)
     for _ in range(int(rng.integers(0, 4))):           # singletons and empty contexts
@@ -315,6 +319,13 @@ def test_random_batches_cover_exactly_within_budget(seed):
     bt = np.full((len(rows), MB), -1, np.int32)
     for i, r in enumerate(rows):
         bt[i, :len(r)] = r
+    return bs, bt, lens
+
+
+def check_random_batch(rng, prefix_rate):
+    bs, bt, lens = random_batch(rng, prefix_rate)
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hk = int(rng.integers(1, 4))
     # automatic, or an explicit target: a multiple of 32 and of bs, at most 64 blocks
     target = int(rng.choice([0, 0, max(bs, 32) * int(rng.integers(1, 9))]))
     mcl = max(int(lens.max()), 1)
@@ -325,3 +336,41 @@ def test_random_batches_cover_exactly_within_budget(seed):
         budget, costs = check_budget(plan, len(lens))
         if target:
             assert budget <= target // 16    # the explicit target caps every list's cost
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_batches_cover_exactly_within_budget(seed):
+    """Random batches, block size, query group and target: every token is
+    covered once per query row, lists are well formed and within their
+    budget, and the plan fits the size bound."""
+    check_random_batch(np.random.default_rng(1000 + seed), 0.0)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_batches_with_prefix_tables(seed):
+    """As above, with members whose context ends inside their prompt, so
+    that some tables are prefixes of others (the ordering that brings
+    sharers together is then still a strict one)."""
+    check_random_batch(np.random.default_rng(2000 + seed), 0.3)
+
+
+def test_prefix_table_sorts_before_its_extensions():
+    """A table that is a prefix of others (a request whose context ends
+    inside a cached prompt) is ordered before them and grouped with them,
+    wherever it sits in the batch: the group's shared part is the prefix's
+    full blocks."""
+    bs = 16
+    prompt = list(range(10))                       # 160 tokens of cached prompt
+    rows = [prompt + [100], prompt[:4], prompt + [101], list(range(200, 203)), prompt + [102]]
+    lens = np.array([161, 64, 170, 40, 175], np.int32)
+    bt = np.full((len(rows), 11), -1, np.int32)
+    for i, r in enumerate(rows):
+        bt[i, :len(r)] = r
+    plan = pkv.plan_shared_prefix(bt, lens, 8, 2, 128, bs, int(lens.max()), 0)
+    items, _ = check_coverage(plan, bt, lens, 4, 2, bs=bs)
+    grouped = [it for it in items if len(it[7]) > 1]
+    assert grouped and {frozenset(it[7]) for it in grouped} == {frozenset({1, 0, 2, 4})}
+    # the group lists the prefix's sequence first and shares its 64 tokens
+    assert all(it[7][0] == 1 for it in grouped)
+    shared = [seg for it in grouped for seg in it[3] if seg[3] == 0 and seg[4] == it[1]]
+    assert shared and max(seg[2] for seg in shared) == 64
