@@ -118,11 +118,13 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
  * sequences forked from one prompt (parallel sampling, beam search, a common
  * system prompt; "Advanced Features", KV-Cache Sharing and Prefix Caching)
  * point their tables at the same physical blocks for the shared part.  The
- * planner finds runs of consecutive sequences whose block tables start with
- * the same block ids, groups them (at most 24 / G sequences per group, G =
- * num_heads / num_kv_heads) and cuts the attention into work items: each
- * partition of a group's shared prefix once for all members' query heads,
- * and every member's own tail.
+ * planner orders the sequences by their block tables (lexicographically by
+ * block id, valid contexts first, batch order among equal tables), so that
+ * sequences whose tables start with the same block ids become neighbours
+ * wherever they sit in the batch; it groups runs of such neighbours (at most
+ * 24 / G sequences per group, G = num_heads / num_kv_heads) and cuts the
+ * attention into work items: each partition of a group's shared prefix once
+ * for all members' query heads, and every member's own tail.
  *
  *   block_tables, context_lens  HOST copies of the arrays the decode call
  *              will get on the device (same layout as for decode)
@@ -134,9 +136,11 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
  *              Per kv head the work is one stream of 16-token tiles: each
  *              group's shared prefix (once for all members' query heads), then
  *              each member's own tail, then the next group or ungrouped
- *              sequence.  The stream is cut into lists of nearly equal tiles;
- *              a list holds the pieces of the groups and sequences its range
- *              covers (work items), and each piece writes one partial per row.
+ *              sequence.  The stream is cut into lists of nearly equal cost
+ *              (tiles, plus ten tiles for every item after a list's first:
+ *              what a CTA's switch between items costs); a list holds the
+ *              pieces of the groups and sequences its range covers (work
+ *              items), and each piece writes one partial per row.
  *   plan       HOST int32 buffer of plan_capacity_ints entries; receives the
  *              plan (opaque apart from plan[0] = number of lists, plan[1] =
  *              partial slots per (sequence, head) and plan[7] = number of
