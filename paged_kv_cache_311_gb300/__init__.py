@@ -368,8 +368,9 @@ def kv_cache_usage(block_tables, context_lens, block_size: int, num_blocks: int)
 def plan_shared_prefix(block_tables, context_lens, num_heads: int, num_kv_heads: int,
                        head_dim: int, block_size: int, max_context_len: Optional[int] = None,
                        partition_size: int = 0) -> SharedPrefixPlan:
-    """Host planner: groups consecutive sequences whose block tables start
-    with the same block ids and cuts the attention into work items.
+    """Host planner: orders the sequences by their block tables so that those
+    whose tables start with the same block ids become neighbours, groups them
+    and cuts the attention into work items.
     block_tables, context_lens: host int32 arrays (numpy or CPU tensors)."""
     import numpy as np
     bt = np.ascontiguousarray(np.asarray(block_tables), dtype=np.int32)

@@ -1,11 +1,11 @@
 // pkv_plan.cu -- host planner of the shared-prefix (cascade) decode path.
 //
 // Runs on the host, next to the block manager that owns the block tables:
-// it finds runs of consecutive sequences whose tables start with the same
-// physical block ids (forked samples, beams, a common system prompt), groups
-// them, and cuts the attention work into items (cascade_plan.h).  The kernel
-// side re-checks on the device that the members of a group really share the
-// blocks it was told about.
+// it brings together the sequences whose tables start with the same physical
+// block ids (forked samples, beams, a common system prompt) wherever they sit
+// in the batch, groups them, and cuts the attention work into items
+// (cascade_plan.h).  The kernel side re-checks on the device that the members
+// of a group really share the blocks it was told about.
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
