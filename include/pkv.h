@@ -132,7 +132,9 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
  *              list): a multiple of 32 and of block_size, at most 64 *
  *              block_size (PKV_EINVAL otherwise); 0 = automatic: one list per
  *              resident CTA slot of the current GPU (three per SM) over all kv
- *              heads, at least 64 tokens each.
+ *              heads, at least 64 tokens each.  A cut into more than 65,535
+ *              lists (the grid's y extent: a partition_size far too small for
+ *              the batch) returns PKV_EUNSUPPORTED.
  *              Per kv head the work is one stream of 16-token tiles: each
  *              group's shared prefix (once for all members' query heads), then
  *              each member's own tail, then the next group or ungrouped
