@@ -374,3 +374,16 @@ def test_prefix_table_sorts_before_its_extensions():
     assert all(it[7][0] == 1 for it in grouped)
     shared = [seg for it in grouped for seg in it[3] if seg[3] == 0 and seg[4] == it[1]]
     assert shared and max(seg[2] for seg in shared) == 64
+
+
+def test_too_many_lists_is_refused():
+    """An explicit target far too small for the batch would need more lists
+    than a grid's y extent (65,535): the planner refuses it."""
+    bs, B, L = 16, 512, 4096                      # 256 tiles each, no sharing
+    bt = np.arange(B * (L // bs), dtype=np.int32).reshape(B, L // bs)
+    lens = np.full(B, L, np.int32)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.plan_shared_prefix(bt, lens, 4, 1, 128, bs, L, 32)   # 2 tiles per list: 65,536 lists
+    assert e.value.status == -2
+    plan = pkv.plan_shared_prefix(bt, lens, 4, 1, 128, bs, L, 64)   # 4 tiles per list: 32,768
+    assert plan.num_lists == B * 256 // 4
