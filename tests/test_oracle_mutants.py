@@ -34,6 +34,14 @@ MUTANTS = {
                                "memcpy((char *)k_caches[l] + (size_t)src * block_bytes,\n                   (const char *)k_caches[l] + (size_t)dst * block_bytes"),
     "swap_direction_inverted": ("            if (direction == 0) {\n                memcpy(hk, gk, block_bytes);",
                                 "            if (direction != 0) {\n                memcpy(hk, gk, block_bytes);"),
+    "bf16_shift_15": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    "attend_drops_last_token": ("    for (int i = 0; i < L; ++i) {\n        double p = exp(z[i] - m);",
+                                "    for (int i = 0; i < L - 1; ++i) {\n        double p = exp(z[i] - m);"),
+    "partitions_overlap_by_one": ("int i0 = p * P, i1 = i0 + P < L ? i0 + P : L;",
+                                  "int i0 = p * P, i1 = i0 + P + 1 < L ? i0 + P + 1 : L;"),
+    "merge_exponent_flipped": ("double w = lp[p] * exp(mp[p] - M);", "double w = lp[p] * exp(M - mp[p]);"),
+    "scatter_slot0_is_padding": ("        if (slot < 0)\n            continue;",
+                                 "        if (slot <= 0)\n            continue;"),
     "swap_host_index_is_gpu_index": ("char *hk = (char *)host_k[l] + (size_t)h * block_bytes;",
                                      "char *hk = (char *)host_k[l] + (size_t)(g % host_blocks) * block_bytes;"),
 }

@@ -310,7 +310,9 @@ def test_reshape_and_cache_matches_fancy_index(oracle_lib, dtype):
     vc = torch.randn(NB, Hk, bs, D, generator=g).to(dt)
     key = torch.randn(T, Hk, D, generator=g).to(dt)
     val = torch.randn(T, Hk, D, generator=g).to(dt)
-    slots = torch.randperm(NB * bs, generator=g)[:T].numpy().astype(np.int64)
+    # distinct slots, the pool's first and last among them
+    inner = torch.randperm(NB * bs - 2, generator=g)[:T - 2].numpy().astype(np.int64) + 1
+    slots = np.concatenate([[0], inner, [NB * bs - 1]]).astype(np.int64)
     slots[3] = -1                                   # padding token: skipped
     k_or, v_or = raw_np(kc).copy(), raw_np(vc).copy()
     st = oracle_lib.reshape_and_cache(raw_np(key), raw_np(val), k_or, v_or, slots)
