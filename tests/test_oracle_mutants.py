@@ -62,3 +62,44 @@ def test_pins_reject_mutant(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
+
+
+# Planted mistakes in the oracle's Python block manager (on-demand blocks,
+# fork, copy-on-write, free): the mutated module is put in place of
+# oracle.block_manager before the pin suite imports it.
+BM_MUTANTS = {
+    "cow_on_any_write": ("            if self.refcount[b] > 1:", "            if self.refcount[b] >= 1:"),
+    "cow_keeps_old_reference": ("                self.refcount[b] -= 1\n                table[j] = nb",
+                                "                table[j] = nb"),
+    "fork_takes_no_reference": ("        for b in self.tables[child]:\n            self.refcount[b] += 1",
+                                "        for b in self.tables[child]:\n            pass"),
+    "free_never_returns_blocks": ("            if self.refcount[b] == 0:\n                self.free.append(b)",
+                                  "            if self.refcount[b] < 0:\n                self.free.append(b)"),
+    "blocks_rounded_down": ("    return -(-n_tokens // block_size)", "    return n_tokens // block_size"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BM_MUTANTS))
+def test_pins_reject_block_manager_mutant(name, tmp_path):
+    old, new = BM_MUTANTS[name]
+    path = os.path.join(ROOT, "oracle", "block_manager.py")
+    src = open(path).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutant = tmp_path / "block_manager.py"
+    mutant.write_text(src.replace(old, new))
+    code = (
+        "import importlib.util, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import oracle, pytest\n"
+        f"spec = importlib.util.spec_from_file_location('oracle.block_manager', {str(mutant)!r})\n"
+        "mod = importlib.util.module_from_spec(spec)\n"
+        "spec.loader.exec_module(mod)\n"
+        "sys.modules['oracle.block_manager'] = mod\n"
+        "oracle.block_manager = mod\n"
+        f"sys.exit(pytest.main(['-x', '-q', '-p', 'no:cacheprovider', "
+        f"{os.path.join(ROOT, 'tests', 'test_oracle_pins.py')!r}]))\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
+    # a pin failed (status 1), not the import or collection (status 2 and up)
+    assert r.returncode == 1, f"pytest status {r.returncode}:\n{r.stdout[-2000:]}{r.stderr[-2000:]}"

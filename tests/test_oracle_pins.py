@@ -71,6 +71,22 @@ def test_blocks_on_demand():
     assert len(set(bm.tables[0])) == len(bm.tables[0])
 
 
+def test_blocks_return_when_their_last_sharer_frees():
+    """A finished sequence's blocks go back to the pool; a block it shares
+    with a fork stays held until the fork finishes too (reference counts;
+    "Advanced Features", KV-Cache Sharing)."""
+    from oracle.block_manager import OracleBlockManager
+    bm = OracleBlockManager(num_blocks=16, block_size=16)
+    bm.add_sequence(0, 40)          # blocks for tokens 0-15, 16-31, 32-39
+    bm.fork(0, 1)
+    bm.append_token(1)              # the shared partial block is copied for the fork
+    assert len(bm.free) == 16 - 4
+    bm.free_sequence(0)             # the two full blocks stay with the fork
+    assert len(bm.free) == 16 - 3
+    bm.free_sequence(1)
+    assert len(bm.free) == 16 and all(r == 0 for r in bm.refcount)
+
+
 def test_page_table_example(oracle_lib):
     """Logical block 0 -> physical 47, logical 1 -> physical 123: with a single
     dominant key at logical position p the output is exactly the V row stored
