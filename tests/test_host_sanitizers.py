@@ -1,0 +1,46 @@
+"""The library's host code (shared-prefix planner, block pool, cache-usage
+accounting) built with AddressSanitizer and UndefinedBehaviorSanitizer and
+run on random inputs by tests/sanitize/host_driver.cpp.  CPU only."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "paged_kv_cache_311_gb300", "csrc")
+HOST_SOURCES = ["pkv_plan.cu", "pkv_block_pool.cu", "pkv_usage.cu"]
+
+
+def _cuda_root():
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    return os.environ.get("CUDA_HOME", "/usr/local/cuda")
+
+
+def test_host_code_is_clean_under_asan_and_ubsan(tmp_path):
+    cxx = shutil.which("g++")
+    if cxx is None:
+        pytest.skip("no g++")
+    cuda = _cuda_root()
+    exe = tmp_path / "host_driver"
+    cmd = [cxx, "-std=c++17", "-O1", "-g", "-fno-omit-frame-pointer",
+           "-fsanitize=address,undefined", f"-I{cuda}/include"]
+    for src in HOST_SOURCES:   # plain host C++ in .cu files
+        cmd += ["-x", "c++", os.path.join(CSRC, src)]
+    cmd += ["-x", "c++", os.path.join(ROOT, "tests", "sanitize", "host_driver.cpp"),
+            "-o", str(exe), f"-L{cuda}/lib64", "-lcudart"]
+    b = subprocess.run(cmd, capture_output=True, text=True)
+    if b.returncode != 0 and "sanitize" in b.stderr and "cannot find" in b.stderr:
+        pytest.skip("no sanitizer runtime for this compiler")
+    assert b.returncode == 0, b.stderr[-3000:]
+    env = dict(os.environ,
+               LD_LIBRARY_PATH=f"{cuda}/lib64:" + os.environ.get("LD_LIBRARY_PATH", ""),
+               ASAN_OPTIONS="detect_leaks=1:protect_shadow_gap=0",
+               UBSAN_OPTIONS="halt_on_error=1:print_stacktrace=1")
+    r = subprocess.run([str(exe)], capture_output=True, text=True, env=env, timeout=600)
+    report = r.stdout[-3000:] + r.stderr[-3000:]
+    assert r.returncode == 0, report
+    assert "runtime error" not in r.stderr and "AddressSanitizer" not in r.stderr, report
+    assert r.stdout.startswith("planned ")
