@@ -44,3 +44,36 @@ def test_host_code_is_clean_under_asan_and_ubsan(tmp_path):
     assert r.returncode == 0, report
     assert "runtime error" not in r.stderr and "AddressSanitizer" not in r.stderr, report
     assert r.stdout.startswith("planned ")
+
+
+def test_oracle_pins_are_clean_under_asan_and_ubsan(tmp_path):
+    """The oracle's C source built with both sanitizers: its pin suite runs
+    against it (the sanitizer runtimes preloaded into the interpreter)
+    without a report."""
+    import sys
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    rt = []
+    for name in ("libasan.so", "libubsan.so"):
+        p = subprocess.run([gcc, f"-print-file-name={name}"], capture_output=True,
+                           text=True).stdout.strip()
+        if not os.path.isabs(p):
+            pytest.skip(f"no {name} for this compiler")
+        rt.append(p)
+    lib = tmp_path / "liboracle_san.so"
+    b = subprocess.run([gcc, "-std=c11", "-O1", "-g", "-fno-omit-frame-pointer",
+                        "-fsanitize=address,undefined", "-fPIC", "-shared",
+                        "-D_POSIX_C_SOURCE=200809L", os.path.join(ROOT, "oracle", "pkv_oracle.c"),
+                        "-o", str(lib), "-lm", "-lpthread"], capture_output=True, text=True)
+    assert b.returncode == 0, b.stderr[-3000:]
+    env = dict(os.environ, PKV_ORACLE_LIB=str(lib), LD_PRELOAD=":".join(rt),
+               ASAN_OPTIONS="detect_leaks=0:protect_shadow_gap=0",   # the interpreter's own
+               UBSAN_OPTIONS="halt_on_error=1:print_stacktrace=1")
+    # -s: a sanitizer aborts the process, so its report must not sit in pytest's capture
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-s", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    report = r.stdout[-3000:] + r.stderr[-3000:]
+    assert r.returncode == 0, report
+    assert "runtime error" not in report and "AddressSanitizer" not in report, report
