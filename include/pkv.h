@@ -51,7 +51,10 @@ typedef enum {
     PKV_EINVAL = -1,        /* bad pointer, size, shape or alignment */
     PKV_EUNSUPPORTED = -2,  /* valid request outside the built kernel set */
     PKV_ECUDA = -3,         /* a CUDA runtime/driver call failed */
-    PKV_EWORKSPACE = -4     /* workspace missing or too small */
+    PKV_EWORKSPACE = -4,    /* workspace missing or too small */
+    PKV_EHOSTMEM = -5       /* a host-side allocation failed (the planner, the usage
+                               accounting or the block pool; a pool that returns it
+                               may be left part way through the call) */
 } pkv_status;
 
 /* Bits OR-ed into *device_status by the kernels. */
@@ -233,8 +236,9 @@ int pkv_kv_cache_usage(const int32_t *block_tables, const int32_t *context_lens,
  */
 typedef struct pkv_block_pool pkv_block_pool;
 
-/* A pool of num_blocks blocks of block_size tokens; NULL on bad sizes or
- * when memory for it cannot be had.  Block 0 is handed out first. */
+/* A pool of num_blocks (1 .. 2^31 - 1) blocks of block_size (1 .. 65536)
+ * tokens; NULL on other sizes or when memory for it cannot be had.  Block 0
+ * is handed out first. */
 pkv_block_pool *pkv_block_pool_create(int64_t num_blocks, int block_size);
 void pkv_block_pool_destroy(pkv_block_pool *pool);
 

@@ -143,6 +143,7 @@ const char *pkv_status_string(int status)
     case PKV_EUNSUPPORTED: return "unsupported configuration (head_dim, block_size, group or dtype)";
     case PKV_ECUDA: return "CUDA runtime or driver call failed";
     case PKV_EWORKSPACE: return "workspace missing or too small";
+    case PKV_EHOSTMEM: return "host memory allocation failed";
     default: return "unknown status";
     }
 }

@@ -125,13 +125,27 @@ bool valid_table(const pkv_block_pool *p, const int32_t *table, int n)
     return true;
 }
 
+// Runs the body of a pool call that may allocate (a cache entry, an
+// eviction-order node): a failed host allocation becomes a status instead of
+// an exception through the C ABI (the pool may then be left part way
+// through the call).
+template <typename F>
+int guarded(F &&body)
+{
+    try {
+        return body();
+    } catch (const std::bad_alloc &) {
+        return PKV_EHOSTMEM;
+    }
+}
+
 }  // namespace
 
 extern "C" {
 
 pkv_block_pool *pkv_block_pool_create(int64_t num_blocks, int block_size)
 {
-    if (num_blocks <= 0 || num_blocks > INT32_MAX || block_size <= 0)
+    if (num_blocks <= 0 || num_blocks > INT32_MAX || block_size <= 0 || block_size > 65536)
         return nullptr;
     pkv_block_pool *p = new (std::nothrow) pkv_block_pool;
     if (!p)
@@ -193,35 +207,38 @@ int pkv_block_pool_allocate_prompt(pkv_block_pool *pool, const int32_t *tokens, 
     if (!pool || num_tokens < 0 || (num_tokens > 0 && (!tokens || !table)) || !cached_tokens)
         return PKV_EINVAL;
     const int bs = pool->block_size;
-    const int nb = (num_tokens + bs - 1) / bs, full = num_tokens / bs;
-    if (nb > table_capacity)
+    const int64_t nb64 = ((int64_t)num_tokens + bs - 1) / bs;
+    if (nb64 > table_capacity)
         return PKV_EINVAL;
-    // the longest run of leading full blocks the cache holds
-    int reused = 0;
-    uint64_t k = kRootKey;
-    for (; reused < full; ++reused) {
-        const int32_t *toks = tokens + (size_t)reused * bs;
-        const uint64_t kn = chain_key(k, toks, bs);
-        ++pool->lookups;
-        const int32_t b = pool->find(kn, k, toks);
-        if (b < 0)
-            break;
-        ++pool->hits;
-        table[reused] = b;
-        k = kn;
-    }
-    // holding the reused blocks first keeps them out of the eviction order
-    for (int i = 0; i < reused; ++i)
-        pool->hold(table[i]);
-    if (pool->available() < nb - reused) {
+    const int nb = (int)nb64, full = num_tokens / bs;
+    return guarded([&] {
+        // the longest run of leading full blocks the cache holds
+        int reused = 0;
+        uint64_t k = kRootKey;
+        for (; reused < full; ++reused) {
+            const int32_t *toks = tokens + (size_t)reused * bs;
+            const uint64_t kn = chain_key(k, toks, bs);
+            ++pool->lookups;
+            const int32_t b = pool->find(kn, k, toks);
+            if (b < 0)
+                break;
+            ++pool->hits;
+            table[reused] = b;
+            k = kn;
+        }
+        // holding the reused blocks first keeps them out of the eviction order
         for (int i = 0; i < reused; ++i)
-            pool->drop(table[i]);
-        return PKV_EWORKSPACE;
-    }
-    for (int i = reused; i < nb; ++i)
-        table[i] = pool->take();
-    *cached_tokens = reused * bs;
-    return PKV_OK;
+            pool->hold(table[i]);
+        if (pool->available() < nb - reused) {
+            for (int i = 0; i < reused; ++i)
+                pool->drop(table[i]);
+            return (int)PKV_EWORKSPACE;
+        }
+        for (int i = reused; i < nb; ++i)
+            table[i] = pool->take();
+        *cached_tokens = reused * bs;
+        return (int)PKV_OK;
+    });
 }
 
 int pkv_block_pool_commit_prompt(pkv_block_pool *pool, const int32_t *tokens, int num_tokens,
@@ -232,21 +249,23 @@ int pkv_block_pool_commit_prompt(pkv_block_pool *pool, const int32_t *tokens, in
     const int bs = pool->block_size, full = num_tokens / bs;
     if (!valid_table(pool, table, full))
         return PKV_EINVAL;
-    uint64_t k = kRootKey;
-    for (int i = 0; i < full; ++i) {
-        const int32_t *toks = tokens + (size_t)i * bs;
-        const uint64_t kn = chain_key(k, toks, bs);
-        const int32_t b = table[i];
-        if (!pool->cached[b] && pool->by_key.find(kn) == pool->by_key.end()) {
-            pool->cached[b] = 1;
-            pool->key[b] = kn;
-            pool->parent[b] = k;
-            std::memcpy(&pool->tokens[(size_t)b * bs], toks, sizeof(int32_t) * bs);
-            pool->by_key.emplace(kn, b);
+    return guarded([&] {
+        uint64_t k = kRootKey;
+        for (int i = 0; i < full; ++i) {
+            const int32_t *toks = tokens + (size_t)i * bs;
+            const uint64_t kn = chain_key(k, toks, bs);
+            const int32_t b = table[i];
+            if (!pool->cached[b] && pool->by_key.find(kn) == pool->by_key.end()) {
+                pool->cached[b] = 1;
+                pool->key[b] = kn;
+                pool->parent[b] = k;
+                std::memcpy(&pool->tokens[(size_t)b * bs], toks, sizeof(int32_t) * bs);
+                pool->by_key.emplace(kn, b);
+            }
+            k = kn;
         }
-        k = kn;
-    }
-    return PKV_OK;
+        return (int)PKV_OK;
+    });
 }
 
 int pkv_block_pool_fork(pkv_block_pool *pool, const int32_t *table, int num_blocks)
@@ -262,9 +281,11 @@ int pkv_block_pool_release(pkv_block_pool *pool, const int32_t *table, int num_b
 {
     if (!pool || !valid_table(pool, table, num_blocks))
         return PKV_EINVAL;
-    for (int i = 0; i < num_blocks; ++i)
-        pool->drop(table[i]);
-    return PKV_OK;
+    return guarded([&] {
+        for (int i = 0; i < num_blocks; ++i)
+            pool->drop(table[i]);
+        return (int)PKV_OK;
+    });
 }
 
 int pkv_block_pool_prepare_write(pkv_block_pool *pool, int32_t *table, int logical_block,
@@ -278,12 +299,14 @@ int pkv_block_pool_prepare_write(pkv_block_pool *pool, int32_t *table, int logic
         return 0;                      // the writer is its only holder
     if (pool->available() < 1)
         return PKV_EWORKSPACE;
-    const int32_t nb = pool->take();
-    pool->drop(b);
-    table[logical_block] = nb;
-    copy_pair[0] = b;
-    copy_pair[1] = nb;
-    return 1;
+    return guarded([&] {
+        const int32_t nb = pool->take();
+        pool->drop(b);
+        table[logical_block] = nb;
+        copy_pair[0] = b;
+        copy_pair[1] = nb;
+        return 1;
+    });
 }
 
 int pkv_block_pool_stats(const pkv_block_pool *pool, int64_t *free_blocks, int64_t *cached_blocks,

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cstring>
+#include <new>
 #include <vector>
 
 #include "../../include/pkv.h"
@@ -68,12 +69,23 @@ int first_diff(const int32_t *a, const int32_t *b, int n)
 
 int blocks_between(int tb, int te, int bs) { return (te + bs - 1) / bs - tb / bs; }
 
-size_t split_total(long long seqs, long long heads, long long slots, long long head_dim)
+// Bytes of the split workspace (see DecodeParams): (max, sum) pairs, then the
+// accumulators, 256-byte aligned.  False if the size does not fit in 64 bits.
+bool split_total(uint64_t seqs, uint64_t heads, uint64_t slots, uint64_t head_dim, size_t *bytes)
 {
-    const size_t ml = (size_t)(seqs * heads * slots * 2) * sizeof(float);
-    const size_t acc_off = (ml + 255) & ~size_t(255);
-    return acc_off + (size_t)(seqs * heads * slots * head_dim) * sizeof(float);
+    uint64_t rows, ml, acc;
+    if (__builtin_mul_overflow(seqs, heads, &rows) || __builtin_mul_overflow(rows, slots, &rows) ||
+        __builtin_mul_overflow(rows, (uint64_t)(2 * sizeof(float)), &ml) ||
+        __builtin_mul_overflow(rows, head_dim * sizeof(float), &acc) || ml > UINT64_MAX - 256 ||
+        ((ml + 255) & ~uint64_t(255)) > UINT64_MAX - acc)
+        return false;
+    *bytes = (size_t)(((ml + 255) & ~uint64_t(255)) + acc);
+    return true;
 }
+
+// Longest context the planner takes: far beyond any cache, small enough
+// that token and tile arithmetic stays inside int.
+constexpr int kMaxContext = 1 << 30;
 
 }  // namespace
 
@@ -93,22 +105,25 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
     // the table capacity allows (block size 8); items: every unit's first
     // piece (at most one per sequence) plus one more per list boundary
     using namespace pkv::plan;
-    const long long W = (long long)num_seqs * ((max_context_len + kTileTokens - 1) / kTileTokens);
+    const long long W = (long long)num_seqs * (((long long)max_context_len + kTileTokens - 1) / kTileTokens);
     const long long q_cap = (long long)(kTableCap - 2 * max_segments(G)) * 8 / kTileTokens;
     long long lists = (W + q_cap - 1) / q_cap + 1;
     if (partition_size > 0)
         lists = std::max(lists, W / std::max(1, partition_size / kTileTokens) + 1);
     else
         lists = std::max(lists, 3LL * gpu_sm_count() / num_kv_heads + 1);
+    lists = std::min(lists, 65536LL);   // a plan never has more (PKV_EUNSUPPORTED)
     return (size_t)kHeader + 2 * (size_t)num_seqs +
            (size_t)(num_seqs + lists) * item_ints(G);
 }
 
-int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
-                           int max_blocks_per_seq, int block_size, int num_heads,
-                           int num_kv_heads, int head_dim, int max_context_len,
-                           int partition_size, int32_t *plan, size_t plan_capacity_ints,
-                           size_t *plan_ints, size_t *workspace_bytes)
+// The planner proper; pkv_plan_shared_prefix below only turns a failed host
+// allocation into a status instead of an exception through the C ABI.
+static int plan_shared_prefix(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                              int max_blocks_per_seq, int block_size, int num_heads,
+                              int num_kv_heads, int head_dim, int max_context_len,
+                              int partition_size, int32_t *plan, size_t plan_capacity_ints,
+                              size_t *plan_ints, size_t *workspace_bytes)
 {
     using namespace pkv::plan;
     if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
@@ -119,6 +134,10 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         return PKV_EINVAL;
     const int G = num_heads / num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8)
+        return PKV_EUNSUPPORTED;
+    // what the decode kernels take (the plan is made for them)
+    if ((block_size != 8 && block_size != 16 && block_size != 32) || (head_dim != 64 && head_dim != 128) ||
+        max_context_len > kMaxContext)
         return PKV_EUNSUPPORTED;
     if (partition_size > 0 &&
         (partition_size % 32 || partition_size % block_size || partition_size / block_size > kTableCap / 4))
@@ -361,8 +380,11 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
     const size_t need = (size_t)kHeader + 2 * (size_t)B + items.size() * iints;
     if (plan_ints)
         *plan_ints = need;
+    size_t ws_bytes = 0;
+    if (!split_total((uint64_t)B, (uint64_t)num_heads, (uint64_t)slots, (uint64_t)head_dim, &ws_bytes))
+        return PKV_EUNSUPPORTED;
     if (workspace_bytes)
-        *workspace_bytes = split_total(B, num_heads, slots, head_dim);
+        *workspace_bytes = ws_bytes;
     if (items.size() > INT32_MAX / 2 || lists.size() > 65535)
         return PKV_EUNSUPPORTED;
     if (!plan || plan_capacity_ints < need)
@@ -420,6 +442,24 @@ int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_l
         dst += iints;
     }
     return PKV_OK;
+}
+
+int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                           int max_blocks_per_seq, int block_size, int num_heads,
+                           int num_kv_heads, int head_dim, int max_context_len,
+                           int partition_size, int32_t *plan, size_t plan_capacity_ints,
+                           size_t *plan_ints, size_t *workspace_bytes)
+{
+    try {
+        return plan_shared_prefix(block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                                  block_size, num_heads, num_kv_heads, head_dim, max_context_len,
+                                  partition_size, plan, plan_capacity_ints, plan_ints,
+                                  workspace_bytes);
+    } catch (const std::bad_alloc &) {
+        return PKV_EHOSTMEM;
+    } catch (...) {   // a size no vector can hold (std::length_error)
+        return PKV_EINVAL;
+    }
 }
 
 }  // extern "C"

@@ -2,11 +2,13 @@
 // shared-prefix planner, the block pool and the cache-usage accounting,
 // called through their C ABI on random inputs, including the awkward ones
 // (empty, negative and over-the-bound lengths, tables that are prefixes of
-// others, out-of-range block ids, a pool that runs dry).  The checks of what
+// others, out-of-range block ids, a pool that runs dry, scalar arguments at
+// and past their limits).  The checks of what
 // the calls compute live in the Python tests; this program only has to run
 // to the end without a sanitizer report.  Built and run by
 // tests/test_host_sanitizers.py.
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -178,6 +180,61 @@ void pool_case()
     pkv_block_pool_destroy(pool);
 }
 
+// Scalar arguments at and past their limits (sizes near INT_MAX, negative
+// ones, a pool of huge blocks) with small valid arrays: every call must come
+// back with a status, with no overflow and no exception through the C ABI.
+long extreme_arguments()
+{
+    const int ext[] = {INT32_MIN, -1, 0, 1, 7, 16, 24, 65535, 1 << 20, INT32_MAX - 15, INT32_MAX};
+    long calls = 0;
+    for (int a : ext)
+        for (int b : ext)
+            for (int c : ext)
+                for (int d : ext)
+                    for (int e : ext) {
+                        (void)pkv_shared_plan_max_ints(a, b, c, d, e);
+                        ++calls;
+                    }
+    std::vector<int32_t> bt(4 * 8), cl(4, 5), plan(1 << 16);
+    std::iota(bt.begin(), bt.end(), 0);
+    size_t need = 0, ws = 0;
+    for (int bs : ext)
+        for (int H : ext)
+            for (int Hk : ext)
+                for (int D : ext)
+                    for (int mcl : ext)
+                        for (int P : ext) {
+                            (void)pkv_plan_shared_prefix(bt.data(), cl.data(), 4, 8, bs, H, Hk, D, mcl, P,
+                                                         plan.data(), plan.size(), &need, &ws);
+                            ++calls;
+                        }
+    int64_t tokens = 0, blocks = 0, slots = 0;
+    for (int bs : ext)
+        for (int mb = 1; mb <= 8; ++mb)
+            for (int64_t nb : {INT64_MIN, (int64_t)-1, (int64_t)0, (int64_t)1, (int64_t)64, INT64_MAX}) {
+                (void)pkv_kv_cache_usage(bt.data(), cl.data(), 4, mb, bs, nb, &tokens, &blocks, &slots);
+                ++calls;
+            }
+    for (int64_t nb : {INT64_MIN, (int64_t)-1, (int64_t)0, (int64_t)1, (int64_t)64})
+        for (int bs : ext) {
+            pkv_block_pool *pool = pkv_block_pool_create(nb, bs);
+            if (pool) {
+                int32_t out[4];
+                for (int k : ext)
+                    if (k <= 4)
+                        (void)pkv_block_pool_allocate(pool, k, out);
+                std::vector<int32_t> toks(64, 3), table(80);
+                int cached = 0;
+                for (int n : ext)
+                    if (n <= 64)
+                        (void)pkv_block_pool_allocate_prompt(pool, toks.data(), n, table.data(), 80, &cached);
+                pkv_block_pool_destroy(pool);
+            }
+            ++calls;
+        }
+    return calls;
+}
+
 }  // namespace
 
 int main()
@@ -189,6 +246,7 @@ int main()
         usage_case();
     for (int i = 0; i < 300; ++i)
         pool_case();
-    std::printf("planned %ld refused %ld\n", planned, refused);
+    const long extreme = extreme_arguments();
+    std::printf("planned %ld refused %ld extreme-argument calls %ld\n", planned, refused, extreme);
     return 0;
 }

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings(lib):
     assert pkv.status_string(0) == "ok"
-    for code in (-1, -2, -3, -4):
+    for code in (-1, -2, -3, -4, -5):
         assert pkv.status_string(code) != "unknown status"
     assert pkv.status_string(99) == "unknown status"
 
