@@ -76,13 +76,19 @@ struct SplitLayout {
     size_t total;
 };
 
-SplitLayout split_layout(long long seqs, long long heads, long long np, long long head_dim)
+// False when the sizes do not fit in 64 bits (no real call comes near).
+bool split_layout(uint64_t seqs, uint64_t heads, uint64_t np, uint64_t head_dim, SplitLayout *s)
 {
-    SplitLayout s;
-    s.ml_bytes = (size_t)(seqs * heads * np * 2) * sizeof(float);
-    s.acc_off = (s.ml_bytes + 255) & ~size_t(255);
-    s.total = s.acc_off + (size_t)(seqs * heads * np * head_dim) * sizeof(float);
-    return s;
+    uint64_t rows, ml, acc;
+    if (__builtin_mul_overflow(seqs, heads, &rows) || __builtin_mul_overflow(rows, np, &rows) ||
+        __builtin_mul_overflow(rows, (uint64_t)(2 * sizeof(float)), &ml) ||
+        __builtin_mul_overflow(rows, head_dim * sizeof(float), &acc) || ml > UINT64_MAX - 256 ||
+        ((ml + 255) & ~uint64_t(255)) > UINT64_MAX - acc)
+        return false;
+    s->ml_bytes = (size_t)ml;
+    s->acc_off = (size_t)((ml + 255) & ~uint64_t(255));
+    s->total = s->acc_off + (size_t)acc;
+    return true;
 }
 
 }  // namespace
@@ -170,7 +176,9 @@ size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_heads, int max_
     const long long np = ((long long)max_context_len + P - 1) / P;
     if (np <= 1)
         return 0;
-    return split_layout(num_seqs, num_heads, np, head_dim).total;
+    SplitLayout s;
+    return split_layout((uint64_t)num_seqs, (uint64_t)num_heads, (uint64_t)np, (uint64_t)head_dim, &s)
+               ? s.total : 0;
 }
 
 int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const void *k_cache,
@@ -223,7 +231,7 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
         P = partition_size;
     } else {
         const long long ctas = (long long)num_seqs * num_kv_heads;
-        const bool fits = (maxL + block_size - 1) / block_size <= kTableCap;
+        const bool fits = ((long long)maxL + block_size - 1) / block_size <= kTableCap;
         const bool fills = ctas >= 4LL * sm_count(dev);
         P = (fits && fills) ? maxL : PKV_DEFAULT_PARTITION;
     }
@@ -258,7 +266,9 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
     p.split = np > 1;
     p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax via exp2
     if (p.split) {
-        const SplitLayout s = split_layout(num_seqs, num_heads, np, head_dim);
+        SplitLayout s;
+        if (!split_layout((uint64_t)num_seqs, (uint64_t)num_heads, (uint64_t)np, (uint64_t)head_dim, &s))
+            return PKV_EUNSUPPORTED;
         if (!workspace || workspace_bytes < s.total || !aligned16(workspace))
             return PKV_EWORKSPACE;
         p.ws_ml = static_cast<float *>(workspace);
@@ -328,7 +338,9 @@ int pkv_paged_attention_decode_shared(void *out, int out_dtype, const void *q, c
         return PKV_EUNSUPPORTED;
     if (num_kv_heads > 65535)
         return PKV_EUNSUPPORTED;
-    const SplitLayout lay = split_layout(num_seqs, num_heads, slots, head_dim);
+    SplitLayout lay;
+    if (!split_layout((uint64_t)num_seqs, (uint64_t)num_heads, (uint64_t)slots, (uint64_t)head_dim, &lay))
+        return PKV_EUNSUPPORTED;
     if (!workspace || workspace_bytes < lay.total || !aligned16(workspace))
         return PKV_EWORKSPACE;
 
@@ -380,6 +392,8 @@ int pkv_reshape_and_cache(const void *key, const void *value, void *k_cache, voi
 {
     if (!valid_dtype(dtype) || num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0)
+        return PKV_EINVAL;
+    if ((int64_t)head_dim * elem_bytes(dtype) > INT32_MAX)
         return PKV_EINVAL;
     const int row_bytes = head_dim * elem_bytes(dtype);
     if (row_bytes % 16)

@@ -81,10 +81,16 @@ int pkv_paged_attention_decode_static(void *out, int out_dtype, const void *q,
     // laid out as the split path expects.
     const long long maxL = max_context_len > 0 ? max_context_len : 1;
     const long long np = (maxL + P - 1) / P;
-    const long long rows = (long long)num_seqs * num_heads * np;
+    // (sizes beyond 64 bits cannot fit either)
+    uint64_t rows, acc;
+    if (__builtin_mul_overflow((uint64_t)num_seqs, (uint64_t)num_heads, &rows) ||
+        __builtin_mul_overflow(rows, (uint64_t)np, &rows) ||
+        __builtin_mul_overflow(rows, (uint64_t)head_dim * sizeof(float), &acc) ||
+        rows > kStaticWsBytes || acc > kStaticWsBytes)
+        return PKV_EWORKSPACE;
     const size_t ml = (size_t)rows * 2 * sizeof(float);
     const size_t acc_off = (ml + 255) & ~size_t(255);
-    const size_t need = acc_off + (size_t)rows * head_dim * sizeof(float);
+    const size_t need = acc_off + (size_t)acc;
     if (need > kStaticWsBytes)
         return PKV_EWORKSPACE;
 

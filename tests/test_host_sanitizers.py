@@ -78,3 +78,35 @@ def test_oracle_pins_are_clean_under_asan_and_ubsan(tmp_path):
     report = r.stdout[-3000:] + r.stderr[-3000:]
     assert r.returncode == 0, report
     assert "runtime error" not in report and "AddressSanitizer" not in report, report
+
+
+@pytest.mark.slow
+def test_gpu_entry_points_host_checks_are_clean_under_ubsan(tmp_path):
+    """The library built with UndefinedBehaviorSanitizer on its host code; the
+    GPU entry points' argument checks get sizes at and past their limits
+    (tests/sanitize/abi_extremes.py) with no CUDA device visible."""
+    import sys
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a CUDA device is visible: this probe runs on machines without one")
+    except ImportError:
+        pass
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    ubsan = subprocess.run([gcc, "-print-file-name=libubsan.so"], capture_output=True,
+                           text=True).stdout.strip()
+    if not os.path.isabs(ubsan):
+        pytest.skip("no libubsan for this compiler")
+    from paged_kv_cache_311_gb300 import build as libbuild
+    lib = libbuild.build(extra_flags=["-Xcompiler", "-fsanitize=undefined",
+                                      "-Xcompiler", "-fno-sanitize-recover=undefined"],
+                         out_path=str(tmp_path / "libpkv_ubsan.so"))
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", LD_PRELOAD=ubsan,
+               UBSAN_OPTIONS="halt_on_error=1:print_stacktrace=1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "sanitize", "abi_extremes.py"), lib],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    report = r.stdout[-3000:] + r.stderr[-3000:]
+    assert r.returncode == 0, report
+    assert "runtime error" not in report and r.stdout.startswith("calls "), report
