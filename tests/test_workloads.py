@@ -88,3 +88,57 @@ def test_long_context_pool_is_about_60_gb():
         pool_bytes = w.num_blocks * 2 * cfg.with_(block_size=bs).block_bytes
         assert 59e9 < pool_bytes <= 60e9
         assert w.init_lens.min() >= 16384 and w.init_lens.max() <= 32768
+
+
+def test_system_prompt_requests_share_their_prompt_blocks_only():
+    """Request i starts with system prompt i % 4 (1024-2048 tokens) and adds
+    32-256 tokens of its own. The prompt's full blocks are held once, by
+    exactly the requests on that prompt. Every other block is a single
+    request's own."""
+    cfg = get("system_prompt_bf16")
+    w = PagedDecodeWorkload(cfg, 311 * 100 + 5, total_steps=3)
+    inp = w.next_step()
+    bs, B = cfg.block_size, w.num_seqs
+    assert B == 256 and len(w.prompt_lens) == 4
+    assert ((w.prompt_lens >= 1024) & (w.prompt_lens <= 2048)).all()
+    np.testing.assert_array_equal(w.prompt_of, np.arange(B) % 4)
+    own = inp.context_lens - w.prompt_lens[w.prompt_of]
+    assert own.min() >= 32 + 1 and own.max() <= 256 + 1       # + the token of this step
+    holders = {}
+    for s in range(B):
+        n = blocks_for_tokens(int(inp.context_lens[s]), bs)
+        for j, b in enumerate(inp.block_tables[s, :n].tolist()):
+            holders.setdefault(b, set()).add((s, j))
+    for p in range(4):
+        full = int(w.prompt_lens[p]) // bs
+        members = [s for s in range(B) if s % 4 == p]
+        first = inp.block_tables[members[0], :full]
+        for s in members:
+            np.testing.assert_array_equal(inp.block_tables[s, :full], first)
+        for j, b in enumerate(first.tolist()):
+            assert holders[b] == {(s, j) for s in members}
+    shared = {int(b) for p in range(4)
+              for b in inp.block_tables[p, :int(w.prompt_lens[p]) // bs].tolist()}
+    for b, who in holders.items():
+        if b not in shared:
+            assert len(who) == 1, f"block {b} held by {who}"
+    _check_tables(w, inp)
+
+
+def test_llama_shaped_length_mixes():
+    """Llama-7B-shaped batch: 64 sequences of U{128..2048} cached tokens.
+    Llama-13B-shaped batch: 256 lengths round(600 e^(0.8 N)) clipped to
+    [16, 4096], so the median sits near 600 and the tails reach the clips.
+    Both add the token of the step."""
+    w7 = PagedDecodeWorkload(get("llama7b_f16"), 311 * 100 + 1, total_steps=2)
+    assert w7.num_seqs == 64
+    assert w7.init_lens.min() >= 128 and w7.init_lens.max() <= 2048
+    np.testing.assert_array_equal(w7.next_step().context_lens, w7.init_lens + 1)
+    cfg13 = get("llama13b_cb_bf16")
+    w13 = PagedDecodeWorkload(cfg13, 311 * 100 + 2, total_steps=2)
+    L = w13.init_lens
+    assert w13.num_seqs == 256 and L.min() >= 16 and L.max() <= 4096
+    assert 450 <= np.median(L) <= 800
+    # the log of the unclipped lengths has spread sigma = 0.8 around log 600
+    inner = L[(L > 16) & (L < 4096)]
+    assert 0.6 <= np.std(np.log(inner)) <= 1.0
