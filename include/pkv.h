@@ -154,7 +154,10 @@ int pkv_paged_attention_decode(void *out, int out_dtype, const void *q, const vo
  *   plan_ints  out: entries the plan needs
  *   workspace_bytes  out: workspace the decode call needs for this plan
  * Returns PKV_EWORKSPACE (after filling both outputs) when plan is NULL or
- * too small; pkv_shared_plan_max_ints bounds the size in advance.
+ * too small; pkv_shared_plan_max_ints bounds the size in advance.  Takes
+ * what the decode kernels take: block_size 8, 16 or 32, head_dim 64 or 128,
+ * num_heads / num_kv_heads 1, 2, 4 or 8, max_context_len up to 2^30
+ * (PKV_EUNSUPPORTED otherwise); PKV_EHOSTMEM if its host memory runs out.
  */
 int pkv_plan_shared_prefix(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                            int max_blocks_per_seq, int block_size, int num_heads,
