@@ -279,6 +279,27 @@ int pkv_block_pool_release(pkv_block_pool *pool, const int32_t *table, int num_b
 int pkv_block_pool_prepare_write(pkv_block_pool *pool, int32_t *table, int logical_block,
                                  int64_t *copy_pair);
 
+/* Room for one more token in each of n sequences, in one call (a decode
+ * step's bookkeeping; "The PagedAttention Algorithm", Steps 1-3, and
+ * "Advanced Features", KV-Cache Sharing).  Sequence s holds lens[s] tokens
+ * in row s of tables (int32 [n, table_stride], host); its new token goes to
+ * position lens[s]: a fresh block when that position starts a block (written
+ * at index lens[s] / block_size), else the row's last block, copied first
+ * (as prepare_write does) if another sequence or the prefix cache holds it.
+ * Sequences are served in batch order, as one call each would be.
+ *   slots       out, int64 [n]: block * block_size + offset of each new token
+ *               (the slot mapping pkv_reshape_and_cache takes)
+ *   copy_pairs  out, int64 [n, 2]: (source, copy) of each block copied, in
+ *               order (what pkv_copy_blocks takes); *num_pairs of them
+ *   num_done    out: sequences served
+ * Every row is checked before anything changes (PKV_EINVAL: a negative
+ * length, no room for the new block index, or a block nobody holds).
+ * PKV_EWORKSPACE when the pool runs out: the first *num_done sequences are
+ * served, the rest untouched.  PKV_EHOSTMEM as for the other pool calls. */
+int pkv_block_pool_append_slots(pkv_block_pool *pool, int32_t *tables, int table_stride,
+                                const int32_t *lens, int n, int64_t *slots, int64_t *copy_pairs,
+                                int *num_pairs, int *num_done);
+
 /* Blocks a new holder can get (free + cached ones nobody holds), -1 for a
  * NULL pool; holders of a block; whether it is a cache entry (-1 if out of
  * range); and counters (any pointer may be NULL). */

@@ -94,6 +94,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_block_pool_release.restype = i32
     L.pkv_block_pool_prepare_write.argtypes = [vp, vp, i32, vp]
     L.pkv_block_pool_prepare_write.restype = i32
+    L.pkv_block_pool_append_slots.argtypes = [vp, vp, i32, vp, i32, vp, vp, ctypes.POINTER(i32),
+                                              ctypes.POINTER(i32)]
+    L.pkv_block_pool_append_slots.restype = i32
     L.pkv_block_pool_available.argtypes = [vp]
     L.pkv_block_pool_available.restype = i64
     L.pkv_block_pool_refcount.argtypes = [vp, i32]
@@ -308,6 +311,29 @@ class BlockPool:
         if rc < 0:
             _check(rc, "pkv_block_pool_prepare_write")
         return (int(pair[0]), int(pair[1])) if rc == 1 else None
+
+    def append_slots(self, tables, lens):
+        """Room for one more token in every sequence of a batch, in one call:
+        tables (numpy int32 [n, MB], C-contiguous, rewritten in place where a
+        block is added or copied) and lens (the tokens each holds before this
+        one) -> (slots int64 [n], copy pairs int64 [k, 2]).  If the pool runs
+        out, raises PkvError with ``done``, the number of sequences served."""
+        import numpy as np
+        assert tables.dtype == np.int32 and tables.flags.c_contiguous and tables.ndim == 2
+        ln = self._i32(lens)
+        n = tables.shape[0]
+        assert ln.shape == (n,)
+        slots = np.empty(max(n, 1), np.int64)
+        pairs = np.empty((max(n, 1), 2), np.int64)
+        k, done = ctypes.c_int32(0), ctypes.c_int32(0)
+        rc = self._L.pkv_block_pool_append_slots(self._p, tables.ctypes.data, tables.shape[1],
+                                                 ln.ctypes.data, n, slots.ctypes.data,
+                                                 pairs.ctypes.data, ctypes.byref(k), ctypes.byref(done))
+        if rc != 0:
+            e = PkvError(rc, "pkv_block_pool_append_slots")
+            e.done = done.value
+            raise e
+        return slots[:n].copy(), pairs[:k.value].copy()
 
     def available(self) -> int:
         return int(self._L.pkv_block_pool_available(self._p))

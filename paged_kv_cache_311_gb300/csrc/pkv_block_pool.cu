@@ -309,6 +309,51 @@ int pkv_block_pool_prepare_write(pkv_block_pool *pool, int32_t *table, int logic
     });
 }
 
+int pkv_block_pool_append_slots(pkv_block_pool *pool, int32_t *tables, int table_stride,
+                                const int32_t *lens, int n, int64_t *slots, int64_t *copy_pairs,
+                                int *num_pairs, int *num_done)
+{
+    if (!pool || n < 0 || table_stride <= 0 || !num_pairs || !num_done ||
+        (n > 0 && (!tables || !lens || !slots || !copy_pairs)))
+        return PKV_EINVAL;
+    *num_pairs = 0;
+    *num_done = 0;
+    const int bs = pool->block_size;
+    // every row checked before any changes: lengths, room for the new block
+    // index, and the blocks holding the tokens so far held by someone
+    for (int s = 0; s < n; ++s) {
+        const int L = lens[s];
+        if (L < 0 || L / bs >= table_stride ||
+            !valid_table(pool, tables + (int64_t)s * table_stride, (int)(((int64_t)L + bs - 1) / bs)))
+            return PKV_EINVAL;
+    }
+    // in batch order, as one call per sequence would: a sibling that shares
+    // the block a copy left behind may then write it in place
+    return guarded([&] {
+        for (int s = 0; s < n; ++s) {
+            int32_t *t = tables + (int64_t)s * table_stride;
+            const int j = lens[s] / bs, off = lens[s] % bs;
+            if (off == 0) {                       // the token starts a block
+                if (pool->available() < 1)
+                    return (int)PKV_EWORKSPACE;
+                t[j] = pool->take();
+            } else if (pool->refs[t[j]] > 1 || pool->cached[t[j]]) {   // shared: copy first
+                if (pool->available() < 1)
+                    return (int)PKV_EWORKSPACE;
+                const int32_t b = t[j], nb = pool->take();
+                pool->drop(b);
+                t[j] = nb;
+                copy_pairs[2 * (int64_t)*num_pairs] = b;
+                copy_pairs[2 * (int64_t)*num_pairs + 1] = nb;
+                ++*num_pairs;
+            }
+            slots[s] = (int64_t)t[j] * bs + off;
+            ++*num_done;
+        }
+        return (int)PKV_OK;
+    });
+}
+
 int pkv_block_pool_stats(const pkv_block_pool *pool, int64_t *free_blocks, int64_t *cached_blocks,
                          int64_t *evictable_blocks, uint64_t *lookups, uint64_t *hits)
 {

@@ -163,11 +163,32 @@ void pool_case()
                 continue;
             int64_t pair[2] = {-1, -1};
             pkv_block_pool_prepare_write(pool, live[k].data(), uni(0, (int)live[k].size() - 1), pair);
-        } else {
+        } else if (op < 0.9) {
             const size_t k = (size_t)uni(0, (int)live.size() - 1);
             int32_t fresh = -1;
             if (pkv_block_pool_allocate(pool, 1, &fresh) == PKV_OK)
                 live[k].push_back(fresh);
+        } else {
+            // one token more for every live sequence, in one call: rows padded
+            // to a common stride, a random position inside each last block or
+            // at the start of the next
+            const int n = (int)live.size(), stride = 72;
+            std::vector<int32_t> rows((size_t)n * stride, -1), lens(n);
+            for (int i = 0; i < n; ++i) {
+                const auto &t = live[(size_t)i];
+                std::copy(t.begin(), t.begin() + std::min<size_t>(t.size(), stride), rows.begin() + (size_t)i * stride);
+                lens[i] = t.empty() ? 0 : ((int)t.size() - 1) * bs + uni(1, bs);
+            }
+            std::vector<int64_t> slots((size_t)std::max(n, 1)), pairs((size_t)std::max(n, 1) * 2);
+            int np = 0, done = 0;
+            const int rc = pkv_block_pool_append_slots(pool, rows.data(), stride, lens.data(), n,
+                                                       slots.data(), pairs.data(), &np, &done);
+            if (rc == PKV_OK || rc == PKV_EWORKSPACE)
+                for (int i = 0; i < done; ++i) {
+                    const int held = (lens[i] + bs - 1) / bs, now = lens[i] / bs + 1;
+                    live[(size_t)i].assign(rows.begin() + (size_t)i * stride,
+                                           rows.begin() + (size_t)i * stride + std::max(held, now));
+                }
         }
         int64_t free_blocks, cached_blocks, evictable;
         uint64_t lookups, hits;

@@ -293,3 +293,126 @@ def test_system_prompt_requests_share_cached_blocks_and_group():
     items, _ = check_coverage(plan, bt, np.array(lens, np.int32), G, 4)
     groups = {frozenset(it[7]) for it in items if it[1] > G}
     assert groups == {frozenset(range(p, 18, 3)) for p in range(3)}
+
+
+def _per_sequence_append(pool, tables, lens):
+    """One call per sequence, in batch order: the reference for append_slots."""
+    bs = pool.block_size
+    slots, pairs = [], []
+    for s in range(len(tables)):
+        j, off = divmod(int(lens[s]), bs)
+        if off == 0:
+            tables[s] = np.append(tables[s], pool.allocate(1)).astype(np.int32)
+        else:
+            pair = pool.prepare_write(tables[s], j)
+            if pair:
+                pairs.append(pair)
+        slots.append(int(tables[s][j]) * bs + off)
+    return slots, pairs
+
+
+def test_append_slots_equals_one_call_per_sequence():
+    """Random histories (prompts reusing cached prefixes, forks, releases)
+    kept in two pools: one steps its batch with append_slots, the other with
+    a call per sequence. Tables, slots, copy pairs, holders and the free
+    count agree at every step."""
+    rng = np.random.default_rng(31)
+    bs, NB, MB = 8, 300, 64
+    a, b = pkv.BlockPool(NB, bs), pkv.BlockPool(NB, bs)
+    prefixes = [rng.integers(0, 40, int(rng.integers(8, 60))).astype(np.int32) for _ in range(3)]
+    seqs = []   # (table for pool a as a padded row, table for pool b, length)
+    for step in range(150):
+        op = rng.random()
+        if op < 0.25 or not seqs:
+            pre = prefixes[int(rng.integers(0, 3))]
+            toks = np.concatenate([pre, rng.integers(0, 40, int(rng.integers(0, 12)))]).astype(np.int32)
+            if a.available() < toks.size // bs + 4:
+                continue
+            ta, _ = a.allocate_prompt(toks)
+            tb, _ = b.allocate_prompt(toks)
+            assert np.array_equal(ta, tb)
+            if rng.random() < 0.7:
+                a.commit_prompt(toks, ta)
+                b.commit_prompt(toks, tb)
+            seqs.append([ta, tb, toks.size])
+        elif op < 0.35:
+            k = int(rng.integers(0, len(seqs)))
+            a.fork(seqs[k][0])
+            b.fork(seqs[k][1])
+            seqs.append([seqs[k][0].copy(), seqs[k][1].copy(), seqs[k][2]])
+        elif op < 0.45:
+            k = int(rng.integers(0, len(seqs)))
+            ta, tb, _ = seqs.pop(k)
+            a.release(ta)
+            b.release(tb)
+        else:
+            live = [s for s in seqs if s[2] // bs < MB]
+            if not live or a.available() < len(live):
+                continue
+            rows = np.full((len(live), MB), -1, np.int32)
+            for i, s in enumerate(live):
+                rows[i, :s[0].size] = s[0]
+            lens = np.array([s[2] for s in live], np.int32)
+            slots, pairs = a.append_slots(rows, lens)
+            tabs_b = [s[1] for s in live]
+            want_slots, want_pairs = _per_sequence_append(b, tabs_b, lens)
+            assert slots.tolist() == want_slots
+            assert [tuple(p) for p in pairs.tolist()] == want_pairs
+            for i, s in enumerate(live):
+                n = -(-(int(lens[i]) + 1) // bs)
+                s[0] = rows[i, :n].copy()
+                s[1] = tabs_b[i]
+                s[2] += 1
+                assert np.array_equal(s[0], s[1])
+        assert a.available() == b.available()
+    for blk in range(NB):
+        assert a.refcount(blk) == b.refcount(blk) and a.is_cached(blk) == b.is_cached(blk)
+
+
+def test_append_slots_copy_on_write_rule_in_one_call():
+    """Six samples forked from a 37-token prompt, stepped in one call: samples
+    0-4 copy the shared partial block, sample 5 writes in place, and every
+    slot is offset 5 of the sample's third block ("Advanced Features",
+    KV-Cache Sharing)."""
+    bs = 16
+    pool = pkv.BlockPool(64, bs)
+    t0 = pool.allocate(3)
+    for _ in range(5):
+        pool.fork(t0)
+    rows = np.tile(np.append(t0, [-1, -1]).astype(np.int32), (6, 1))
+    slots, pairs = pool.append_slots(rows, np.full(6, 37, np.int32))
+    assert pairs.shape == (5, 2) and (pairs[:, 0] == t0[2]).all()
+    assert len(set(pairs[:, 1].tolist())) == 5
+    assert rows[5, 2] == t0[2] and all(rows[s, 2] != t0[2] for s in range(5))
+    assert (slots == rows[:, 2].astype(np.int64) * bs + 5).all()
+    assert (rows[:, :2] == t0[:2]).all() and pool.refcount(int(t0[0])) == 6
+
+
+def test_append_slots_stops_where_the_pool_runs_out():
+    bs = 8
+    pool = pkv.BlockPool(5, bs)
+    t = pool.allocate(4)                       # four one-block sequences, each full
+    rows = np.full((4, 4), -1, np.int32)
+    rows[:, 0] = t
+    before = rows.copy()
+    with pytest.raises(pkv.PkvError) as e:
+        pool.append_slots(rows, np.full(4, bs, np.int32))   # each needs a new block; 1 is left
+    assert e.value.status == -4 and e.value.done == 1
+    assert rows[0, 1] >= 0 and (rows[1:] == before[1:]).all()
+    assert pool.available() == 0
+
+
+def test_append_slots_checks_every_row_first():
+    bs = 8
+    pool = pkv.BlockPool(16, bs)
+    t = pool.allocate(2)
+    rows = np.array([[t[0], -1], [t[1], -1]], np.int32)
+    # a negative length; no room for block index 2; a block nobody holds
+    for lens in ([3, -1], [3, 16], [8, 5]):
+        r = rows.copy()
+        if lens == [8, 5]:
+            r[1, 0] = 15                           # a block nobody holds
+        with pytest.raises(pkv.PkvError) as e:
+            pool.append_slots(r, np.array(lens, np.int32))
+        assert e.value.status == -1
+        assert pool.available() == 14
