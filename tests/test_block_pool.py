@@ -416,3 +416,57 @@ def test_append_slots_checks_every_row_first():
             pool.append_slots(r, np.array(lens, np.int32))
         assert e.value.status == -1
         assert pool.available() == 14
+
+
+def test_append_slots_follows_the_oracle_block_manager():
+    """Random adds, forks and frees; at each decode step every live sequence
+    gets its next token through one append_slots call, and the oracle's block
+    manager takes the same tokens one sequence at a time in batch order:
+    slots, copy pairs, tables and holder counts agree."""
+    rng = np.random.default_rng(47)
+    bs, NB, MB = 16, 500, 40
+    pool, ref = pkv.BlockPool(NB, bs), OracleBlockManager(NB, bs)
+    tables, lens, nxt = {}, {}, 0
+    for step in range(300):
+        op = rng.random()
+        live = sorted(tables)
+        if op < 0.15 or not live:
+            n = int(rng.integers(1, 120))
+            if pool.available() < -(-n // bs) + 40:
+                continue
+            tb, _ = pool.allocate_prompt(rng.integers(0, 1000, n))
+            assert list(tb) == ref.add_sequence(nxt, n)
+            tables[nxt], lens[nxt] = tb, n
+            nxt += 1
+        elif op < 0.3:
+            s = int(rng.choice(live))
+            pool.fork(tables[s])
+            ref.fork(s, nxt)
+            tables[nxt], lens[nxt] = tables[s].copy(), lens[s]
+            nxt += 1
+        elif op < 0.4:
+            s = int(rng.choice(live))
+            pool.release(tables.pop(s))
+            lens.pop(s)
+            ref.free_sequence(s)
+        else:
+            batch = [s for s in live if lens[s] // bs < MB]
+            if not batch or pool.available() < len(batch):
+                continue
+            rows = np.full((len(batch), MB), -1, np.int32)
+            for i, s in enumerate(batch):
+                rows[i, :tables[s].size] = tables[s]
+            slots, pairs = pool.append_slots(rows, np.array([lens[s] for s in batch], np.int32))
+            want_pairs = []
+            for i, s in enumerate(batch):
+                slot, pair = ref.append_token(s)
+                assert slots[i] == slot
+                if pair:
+                    want_pairs.append(pair)
+                lens[s] += 1
+                tables[s] = rows[i, :-(-lens[s] // bs)].copy()
+                assert list(tables[s]) == ref.tables[s]
+            assert [tuple(p) for p in pairs.tolist()] == want_pairs
+    for b in range(NB):
+        assert pool.refcount(b) == ref.refcount[b]
+    assert pool.available() == len(ref.free)
