@@ -22,7 +22,11 @@
  *     i % block_size; its slot number is block * block_size + i % block_size.
  *   - Pointers are DEVICE pointers unless stated otherwise.  The caller owns
  *     every buffer, including the workspace; the library allocates no device
- *     memory and keeps no per-call state.  Every call is asynchronous on
+ *     memory; the one device buffer it has is the static 32 MiB array
+ *     compiled into it for pkv_paged_attention_decode_static.  Its
+ *     only state between calls is the engine choice (process-wide) and the
+ *     last decode call's engine and launch count (per host thread).  Every
+ *     call is asynchronous on
  *     `stream` (a cudaStream_t; NULL = the legacy default stream) and returns
  *     after enqueueing its kernels.
  *   - Host-side argument errors return a negative pkv_status and enqueue
@@ -104,7 +108,8 @@ size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_heads, int max_
  *              pkv_paged_attention_workspace_bytes(...) bytes when the split
  *              path runs (may be NULL otherwise)
  * Supported: head_dim in {64, 128}; block_size in {8, 16, 32};
- * num_heads / num_kv_heads in {1, 2, 4, 8}; dtypes as pkv_dtype.
+ * num_heads / num_kv_heads in {1, 2, 4, 8}; num_seqs and num_kv_heads up to
+ * 65,535 (grid extents); dtypes as pkv_dtype.  PKV_EUNSUPPORTED otherwise.
  * Device errors: PKV_DEV_BAD_BLOCK / PKV_DEV_BAD_CONTEXT_LEN -> that
  * sequence's output rows (for the kv head group touched) are zero.
  */
