@@ -49,8 +49,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=95)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--op", default="decode", choices=["decode", "swap_blocks"],
-                    help="swap_blocks: time the block swap of a preempted tenth of the batch")
+    ap.add_argument("--op", default="decode", choices=["decode", "swap_blocks", "host_step"],
+                    help="swap_blocks: time the block swap of a preempted tenth of the batch; "
+                         "host_step: time a step's host bookkeeping (no GPU)")
     ap.add_argument("--config", default="llama7b_f16")
     ap.add_argument("--block-size", type=int, default=0)
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling cases)")
@@ -782,12 +783,73 @@ def run_swap(args):
     print(json.dumps(line))
 
 
+def run_host_step(args):
+    """A decode step's host bookkeeping for the workload's batch, timed on the
+    host cores (no GPU): the block pool giving every sequence its next slot
+    in one call (append_slots) and one call per sequence, and, for workloads
+    with shared prompts, the shared-prefix planner on the step's tables.
+    Prints one JSON line of medians in microseconds per step."""
+    import paged_kv_cache_311_gb300 as pkv
+    cfg = get(args.config)
+    if args.block_size:
+        cfg = cfg.with_(block_size=args.block_size)
+    seed = SEED_BASE + CONFIGS.index(get(args.config))
+    steps = max(args.steps, 3)
+    w = PagedDecodeWorkload(cfg, seed, total_steps=max(steps + args.warmup, 2),
+                            num_seqs=args.num_seqs or None, pool_blocks=None if cfg.pool != "bytes" else 1 << 20)
+    inputs = [w.next_step() for _ in range(args.warmup + steps)]
+    bs, B = cfg.block_size, w.num_seqs
+    res = {}
+    # the pool: the batch's first-step lengths, then one token per sequence per step
+    first = inputs[0]
+    MB = int(first.block_tables.shape[1]) + steps + 2
+    nb_total = int(sum(-(-int(L) // bs) + steps // bs + 2 for L in first.context_lens))
+    for mode in ("append_slots", "per_sequence"):
+        pool = pkv.BlockPool(nb_total + B, bs)
+        rows = np.full((B, MB), -1, np.int32)
+        lens = np.asarray(first.context_lens, np.int32).copy()
+        for s in range(B):
+            t = pool.allocate(-(-int(lens[s]) // bs))
+            rows[s, :t.size] = t
+        ts = []
+        for i in range(args.warmup + steps):
+            t0 = time.perf_counter()
+            if mode == "append_slots":
+                pool.append_slots(rows, lens)
+            else:
+                for s in range(B):
+                    j, off = divmod(int(lens[s]), bs)
+                    if off == 0:
+                        rows[s, j] = pool.allocate(1)[0]
+                    else:
+                        pool.prepare_write(rows[s], j)
+            ts.append(time.perf_counter() - t0)
+            lens += 1
+        res[f"pool_{mode}_us"] = round(1e6 * statistics.median(ts[args.warmup:]), 1)
+    if cfg.kind in ("shared_prefix", "system_prompt"):
+        ts = []
+        for inp in inputs:
+            t0 = time.perf_counter()
+            pkv.plan_shared_prefix(inp.block_tables, inp.context_lens, cfg.num_heads, cfg.num_kv_heads,
+                                   cfg.head_dim, bs, int(inp.context_lens.max()), 0)
+            ts.append(time.perf_counter() - t0)
+        res["plan_shared_prefix_us"] = round(1e6 * statistics.median(ts[args.warmup:]), 1)
+    import platform
+    print(json.dumps({"metric": "host bookkeeping per decode step (median us)", "op": "host_step",
+                      "unit": "us", "higher_is_better": False, "steps": steps, "warmup": args.warmup,
+                      "config": {"workload": cfg.name, "num_seqs": B, "block_size": bs},
+                      "host": {"machine": platform.machine(), "cores": os.cpu_count()},
+                      **res}))
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "swap_blocks":
         run_swap(args)
+    elif args.op == "host_step":
+        run_host_step(args)
     else:
         run_native(args)
 

@@ -58,3 +58,21 @@ def test_traffic_only_for_the_kernel_it_was_captured_on():
         assert len(set(srcs)) == len(srcs)
         assert bench.kernel_source_sha(k) != ""
     assert set(bench.KERNEL_SOURCES["pa_cascade_kernel"]) < set(bench.KERNEL_SOURCES["pa_cascade_tc05_kernel"])
+
+
+def test_host_step_op_runs_without_a_gpu():
+    """bench.py --op host_step times a step's host bookkeeping on the host
+    cores alone and prints one JSON line with the pool and planner figures."""
+    import json
+    import os
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--op", "host_step",
+                        "--config", "shared_prefix_bf16", "--steps", "3", "--warmup", "1"],
+                       cwd=bench.ROOT, capture_output=True, text=True, timeout=600,
+                       env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["op"] == "host_step" and line["config"]["workload"] == "shared_prefix_bf16"
+    for k in ("pool_append_slots_us", "pool_per_sequence_us", "plan_shared_prefix_us"):
+        assert line[k] > 0
