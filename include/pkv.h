@@ -64,8 +64,13 @@ typedef enum {
 /* Bits OR-ed into *device_status by the kernels. */
 #define PKV_DEV_BAD_BLOCK 1u        /* block id outside [0, num_blocks) */
 #define PKV_DEV_BAD_SLOT 2u         /* slot outside [0, num_blocks * block_size) */
-#define PKV_DEV_TIMEOUT 4u          /* a bounded wait on a TMA barrier gave up */
+#define PKV_DEV_TIMEOUT 4u          /* a bounded wait on a TMA or tensor-core barrier gave up
+                                       (2 s): the rows it served are zero */
 #define PKV_DEV_BAD_CONTEXT_LEN 8u  /* context_lens[s] < 0 or beyond the table / max */
+#define PKV_DEV_DRAIN_TIMEOUT 16u   /* after a timeout, the wait for the copies or products
+                                       already issued gave up too: a CTA may have exited with
+                                       them still writing its shared memory; treat the
+                                       context as unreliable */
 
 /* Supported shapes of the decode kernel. */
 #define PKV_DEFAULT_PARTITION 512    /* tokens per split-context partition */
@@ -381,27 +386,31 @@ int pkv_swap_blocks(void *const *gpu_k, void *const *gpu_v, void *const *host_k,
  * paged_attention_decode_static -- the same attention as
  * pkv_paged_attention_decode, for callers that cannot allocate device
  * memory.  (The pages have no counterpart; this is a convenience of this
- * library.)  Callers of this kind include code running while a stream is
- * captured into a CUDA graph (cudaMalloc is not allowed during capture),
- * plugins whose host engine owns all device memory and gives them none, and
- * latency-critical loops that must not call cudaMalloc because it may
- * synchronise the device.
+ * library.)  Callers of this kind include plugins whose host engine owns all
+ * device memory and gives them none, code running under an allocator that
+ * is full or must not grow, and latency-critical loops that must not call
+ * cudaMalloc because it may synchronise the device.
  *
- * It always takes the split-context path and keeps the partials in a buffer
- * that lives inside libpkv.so: pkv_static_workspace_capacity() bytes (32 MiB)
- * on every GPU that uses it, held until the process exits.  It calls no
- * allocator.  The first call on a device looks up that buffer's address for
- * the device (cudaGetSymbolAddress); make that first call before any stream
- * capture begins.
+ * A context longer than one partition takes the split-context path, whose
+ * partials live in a buffer inside libpkv.so: pkv_static_workspace_capacity()
+ * bytes (32 MiB) on every GPU that uses it, held until the process exits.  A
+ * batch whose contexts all fit one partition (max_context_len <=
+ * partition_size) takes the single pass and uses no buffer.  It calls no
+ * allocator.  The first call on a device looks up the buffer's address for
+ * that device (cudaGetSymbolAddress, with the device current) and keeps it;
+ * make that first call before any stream capture begins, and do not use the
+ * library across a cudaDeviceReset (the kept address would be stale).
  *
  * Arguments as for pkv_paged_attention_decode, without the workspace;
  * partition_size 0 means PKV_DEFAULT_PARTITION tokens.  Returns
- * PKV_EWORKSPACE when num_seqs * num_heads * ceil(max_context_len /
- * partition_size) * (2 + head_dim) * 4 bytes (plus alignment) exceed the
- * capacity.  All calls on one device share the buffer: calls whose kernels
- * may overlap on the GPU (different streams without ordering) race and give
- * wrong results; calls ordered on one stream are safe.  The buffer keeps the
- * last call's partials; nothing in it needs to start at zero.
+ * PKV_EWORKSPACE when the split path's num_seqs * num_heads *
+ * ceil(max_context_len / partition_size) * (2 + head_dim) * 4 bytes (plus
+ * alignment) exceed the capacity.  All calls on one device share the
+ * buffer: calls whose kernels may overlap on the GPU (different streams
+ * without ordering) race and give wrong results; calls ordered on one stream
+ * are safe.  The buffer keeps the last call's partials; nothing in it needs
+ * to start at zero (the partition pass writes every partial the reduce
+ * reads).
  */
 int pkv_paged_attention_decode_static(void *out, int out_dtype, const void *q,
                                       const void *k_cache, const void *v_cache, int kv_dtype,
@@ -430,6 +439,22 @@ int pkv_last_decode_engine(void);
 
 /* Static, NUL-terminated description of a pkv_status value. */
 const char *pkv_status_string(int status);
+
+/*
+ * Test hook of the kernels' bounded waits (no counterpart on the pages: it
+ * exists so that the error path of a wait that gives up can run on a GPU
+ * without faulting or hanging it).  Enqueues one CTA that waits, with the
+ * bounded wait every decode kernel uses, on an mbarrier phase that nothing
+ * completes (no arrival, no copy), then runs the drain wait that follows a
+ * timeout in those kernels on the same phase.  Both give up after limit_ns
+ * nanoseconds (1 .. 2e9) or max_polls polls (0: limit_ns / 4 polls, more than
+ * the time limit lets through),
+ * whichever comes first, and the CTA returns; *device_status (required)
+ * then holds PKV_DEV_TIMEOUT | PKV_DEV_DRAIN_TIMEOUT.  The context stays
+ * usable.  PKV_EINVAL for a NULL status or a limit outside the range.
+ */
+int pkv_test_bounded_wait(uint64_t limit_ns, uint64_t max_polls, uint32_t *device_status,
+                          void *stream);
 
 /* Number of kernels the last successful pkv_paged_attention_decode call on
  * this host thread enqueued (1 = single pass, 2 = partition pass + reduce). */

@@ -29,7 +29,8 @@ __all__ = [
     "paged_attention_decode_shared", "plan_shared_prefix", "SharedPrefixPlan",
     "set_decode_engine", "last_decode_engine", "kv_cache_usage", "KvCacheUsage", "swap_blocks",
     "SWAP_OUT", "SWAP_IN", "BlockPool",
-    "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "HEADER_PATH",
+    "DEV_BAD_BLOCK", "DEV_BAD_SLOT", "DEV_TIMEOUT", "DEV_BAD_CONTEXT_LEN", "DEV_DRAIN_TIMEOUT",
+    "HEADER_PATH", "bounded_wait_hook",
 ]
 
 HEADER_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
@@ -38,7 +39,7 @@ HEADER_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__fil
 PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
 _DTYPE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 
-DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_TIMEOUT, DEV_BAD_CONTEXT_LEN = 1, 2, 4, 8
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_TIMEOUT, DEV_BAD_CONTEXT_LEN, DEV_DRAIN_TIMEOUT = 1, 2, 4, 8, 16
 
 _lib = None
 
@@ -120,6 +121,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     L.pkv_last_decode_engine.restype = i32
     L.pkv_decode_set_engine.argtypes = [i32]
     L.pkv_decode_set_engine.restype = i32
+    L.pkv_test_bounded_wait.argtypes = [ctypes.c_uint64, ctypes.c_uint64, vp, vp]
+    L.pkv_test_bounded_wait.restype = i32
     if path is None:
         _lib = L
     return L
@@ -451,6 +454,15 @@ def paged_attention_decode_shared(out: torch.Tensor, q: torch.Tensor, k_cache: t
         _stream(stream))
     _check(rc, "pkv_paged_attention_decode_shared")
     return out
+
+
+def bounded_wait_hook(device_status: torch.Tensor, limit_ns: int, max_polls: int = 0,
+                      stream=None) -> None:
+    """Test hook: one CTA whose bounded wait (and the drain after it) must
+    give up; device_status then holds DEV_TIMEOUT | DEV_DRAIN_TIMEOUT."""
+    _need_cuda(device_status)
+    _check(load_library().pkv_test_bounded_wait(int(limit_ns), int(max_polls), _ptr(device_status),
+                                                _stream(stream)), "pkv_test_bounded_wait")
 
 
 def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,

@@ -114,4 +114,26 @@ swap_blocks_kernel(const __grid_constant__ SwapBlocksParams ptrs, const int64_t 
     }
 }
 
+// Test hook of the bounded waits: one CTA waits on an mbarrier whose phase
+// nothing completes (no thread arrives, no copy is issued), with the same
+// bounded wait the decode kernels use, so the wait must give up; then the
+// drain that follows a timeout in those kernels runs on the same phase and
+// gives up too.  Expected result: PKV_DEV_TIMEOUT | PKV_DEV_DRAIN_TIMEOUT in
+// *status, and a kernel that returns.
+__global__ void __launch_bounds__(32)
+bounded_wait_test_kernel(uint64_t limit_ns, uint64_t max_polls, uint32_t *status)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(&bar, 0, limit_ns, max_polls)) {
+        if (threadIdx.x == 0)
+            report(status, PKV_DEV_TIMEOUT);
+        drain_wait(&bar, 0, threadIdx.x == 0 ? status : nullptr, limit_ns, max_polls);
+    }
+}
+
 }  // namespace pkv

@@ -305,7 +305,7 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                 const int last = min(my_n, failed_at + S);
                 for (int i = failed_at; i < last; ++i) {
                     const int a = ring + i;
-                    mbar_wait_bounded(&bars[a % S], (uint32_t)((a / S) & 1), 200000000ull);
+                    drain_wait(&bars[a % S], (uint32_t)((a / S) & 1), p.status);
                 }
                 if (lane == 0) {
                     report(p.status, PKV_DEV_TIMEOUT);

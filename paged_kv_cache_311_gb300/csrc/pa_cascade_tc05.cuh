@@ -587,13 +587,13 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
             const int issued = *reinterpret_cast<volatile int32_t *>(n_issued);
             for (int i = done_st; i < issued && i < n_st; ++i) {
                 const int gi = g + i;
-                mbar_wait_bounded(&full[gi % NSLOT], (uint32_t)((gi / NSLOT) & 1), 200000000ull);
+                drain_wait(&full[gi % NSLOT], (uint32_t)((gi / NSLOT) & 1), p.status);
             }
             if (done_st < n_st)   // an S^T issued for a stage not consumed
-                mbar_wait_bounded(sbar, (uint32_t)((g + done_st) & 1), 200000000ull);
+                drain_wait(sbar, (uint32_t)((g + done_st) & 1), p.status);
             if (done_st > 0)
-                mbar_wait_bounded(&empty[(g + done_st - 1) % NSLOT],
-                                  (uint32_t)(((g + done_st - 1) / NSLOT) & 1), 200000000ull);
+                drain_wait(&empty[(g + done_st - 1) % NSLOT],
+                           (uint32_t)(((g + done_st - 1) / NSLOT) & 1), p.status);
         } else if (n_st > 0) {
             // every product of the item done (one commit covers all before it)
             const int gl = g + n_st - 1;

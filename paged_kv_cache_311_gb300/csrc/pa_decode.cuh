@@ -791,7 +791,7 @@ __device__ __forceinline__ void decode_cta(const DecodeParams &p, const CUtensor
         // exit, then mark the CTA's result invalid.
         const int last = min(my_n, failed_at + S);
         for (int i = failed_at; i < last; ++i)
-            mbar_wait_bounded(&bars[(base + i) % S], (uint32_t)(((base + i) / S) & 1), 200000000ull);
+            drain_wait(&bars[(base + i) % S], (uint32_t)(((base + i) / S) & 1), p.status);
         if (lane == 0) {
             report(p.status, PKV_DEV_TIMEOUT);
             atomicOr(cta_flag, 1u);

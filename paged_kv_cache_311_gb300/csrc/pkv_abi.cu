@@ -494,4 +494,14 @@ int pkv_swap_blocks(void *const *gpu_k, void *const *gpu_v, void *const *host_k,
     return PKV_OK;
 }
 
+int pkv_test_bounded_wait(uint64_t limit_ns, uint64_t max_polls, uint32_t *device_status,
+                          void *stream)
+{
+    if (!device_status || limit_ns == 0 || limit_ns > kWaitLimitNs)
+        return PKV_EINVAL;
+    bounded_wait_test_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, max_polls,
+                                                                               device_status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 }  // extern "C"

@@ -226,14 +226,18 @@ int pkv_block_pool_allocate_prompt(pkv_block_pool *pool, const int32_t *tokens, 
             table[reused] = b;
             k = kn;
         }
+        // reused blocks nobody holds sit in the eviction order but cannot
+        // serve as this request's fresh blocks; a request that cannot be
+        // served is refused before anything changes (the eviction order
+        // included)
+        int64_t idle = 0;
+        for (int i = 0; i < reused; ++i)
+            idle += pool->refs[table[i]] == 0;
+        if (pool->available() - idle < nb - reused)
+            return (int)PKV_EWORKSPACE;
         // holding the reused blocks first keeps them out of the eviction order
         for (int i = 0; i < reused; ++i)
             pool->hold(table[i]);
-        if (pool->available() < nb - reused) {
-            for (int i = 0; i < reused; ++i)
-                pool->drop(table[i]);
-            return (int)PKV_EWORKSPACE;
-        }
         for (int i = reused; i < nb; ++i)
             table[i] = pool->take();
         *cached_tokens = reused * bs;

@@ -60,21 +60,44 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// Limit of every wait on a load or a tensor-core product (and of the drain
+// that follows a wait that gave up): 2 s of %globaltimer time.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 // Waits until the barrier's phase with the given parity has completed.
-// Gives up after `limit_ns` of wall time and returns false; the caller then
-// reports PKV_DEV_TIMEOUT instead of spinning forever.
+// Gives up and returns false after `limit_ns` of wall time or `max_polls`
+// polls of the barrier, whichever comes first (0: one poll per 4 ns of the
+// limit; a poll takes longer than that, so the time limit decides unless the
+// timer stalls); the caller then reports PKV_DEV_TIMEOUT instead of spinning
+// forever.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  uint64_t limit_ns = 2000000000ull)
+                                                  uint64_t limit_ns = kWaitLimitNs,
+                                                  uint64_t max_polls = 0)
 {
     if (mbar_try_wait(bar, parity))
         return true;
+    const uint64_t cap = max_polls ? max_polls : limit_ns >> 2;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
+    for (uint64_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns)
+        if ((it & 255u) == 0 && (globaltimer_ns() - t0 > limit_ns || it >= cap))
             return false;
     }
+}
+
+__device__ __forceinline__ void report(uint32_t *status, uint32_t bits);
+
+// After a wait gave up: waits (bounded as any wait) for a phase whose copies
+// or products were already issued, so that the CTA does not leave with them
+// still writing into its shared memory or tensor memory.  If this wait gives
+// up too, PKV_DEV_DRAIN_TIMEOUT reports that the CTA may have exited with
+// them in flight.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                           uint64_t limit_ns = kWaitLimitNs, uint64_t max_polls = 0)
+{
+    if (!mbar_wait_bounded(bar, parity, limit_ns, max_polls))
+        report(status, PKV_DEV_DRAIN_TIMEOUT);
 }
 
 // Orders this thread's earlier generic-proxy shared-memory accesses before

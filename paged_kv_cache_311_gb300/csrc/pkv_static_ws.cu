@@ -1,19 +1,22 @@
 // pkv_static_ws.cu -- paged decode attention for callers that cannot
 // allocate device memory.
 //
-// Some callers have no way to obtain a workspace: code that runs while a
-// CUDA stream is being captured into a graph (cudaMalloc is not allowed
-// there), plugins whose host engine owns every device allocation and hands
-// them none, and latency-critical loops that must not call cudaMalloc because
-// it can synchronise the device.  pkv_paged_attention_decode_static serves
-// them: it always runs the split-context path (partition pass + log-sum-exp
-// reduce) and keeps the partials in a fixed array that lives in this library
-// (kStaticWsBytes per GPU, held from the first use of the library on that GPU
-// until the process exits).  It never allocates.
+// Some callers have no way to obtain a workspace: plugins whose host engine
+// owns every device allocation and hands them none, code running under an
+// allocator that is already full or must not grow, and latency-critical
+// loops that must not call cudaMalloc because it can synchronise the device.
+// pkv_paged_attention_decode_static serves them.  When a context spans more
+// than one partition it runs the split-context path (partition pass +
+// log-sum-exp reduce) and keeps the partials in a fixed array that lives in
+// this library (kStaticWsBytes per GPU, held from the first use of the
+// library on that GPU until the process exits); a batch whose contexts fit
+// one partition takes the single pass, which needs no workspace.  It never
+// allocates.
 //
 // Host code cannot use the array's name as a device address, so each device
 // gets the real address once, with that device current, from
-// cudaGetSymbolAddress; the address is cached per device.
+// cudaGetSymbolAddress; the address is cached per device (a cudaDeviceReset
+// invalidates it: the library must not be used across one).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -81,6 +84,12 @@ int pkv_paged_attention_decode_static(void *out, int out_dtype, const void *q,
     // laid out as the split path expects.
     const long long maxL = max_context_len > 0 ? max_context_len : 1;
     const long long np = (maxL + P - 1) / P;
+    if (np == 1)   // one partition: the single pass, no workspace
+        return pkv_paged_attention_decode(out, out_dtype, q, k_cache, v_cache, kv_dtype,
+                                          block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                          num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                          max_context_len, scale, P, nullptr, 0, device_status,
+                                          stream);
     // (sizes beyond 64 bits cannot fit either)
     uint64_t rows, acc;
     if (__builtin_mul_overflow((uint64_t)num_seqs, (uint64_t)num_heads, &rows) ||
@@ -101,8 +110,8 @@ int pkv_paged_attention_decode_static(void *out, int out_dtype, const void *q,
     const int rc = static_ws_address(dev, &ws);
     if (rc != PKV_OK)
         return rc;
-    // A partition size below the longest context forces the split path, which
-    // is the only one that needs the workspace; a single partition needs none.
+    // A partition size below the longest context forces the split path, the
+    // only one that needs the workspace.
     return pkv_paged_attention_decode(out, out_dtype, q, k_cache, v_cache, kv_dtype, block_tables,
                                       max_blocks_per_seq, context_lens, num_seqs, num_heads,
                                       num_kv_heads, head_dim, block_size, num_blocks,

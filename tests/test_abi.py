@@ -105,3 +105,14 @@ def test_cache_ops_host_validation(lib):
 def test_package_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         pkv.load_library(str(tmp_path / "missing.so"))
+
+
+def test_bounded_wait_hook_checks_its_arguments_on_the_host(lib):
+    """The test hook rejects a missing status word and a limit outside
+    (0, 2 s] before any CUDA call."""
+    lib.pkv_test_bounded_wait.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p,
+                                          ctypes.c_void_p]
+    assert lib.pkv_test_bounded_wait(1_000_000, 0, None, None) == -1
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.pkv_test_bounded_wait(0, 0, fake, None) == -1
+    assert lib.pkv_test_bounded_wait(2_000_000_001, 0, fake, None) == -1

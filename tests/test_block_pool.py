@@ -3,16 +3,17 @@
 Without prefix caching the pool must hand out exactly the blocks the
 oracle's block manager does (on-demand allocation, forks, copy-on-write and
 frees on the page "PagedAttention: Efficient LLM Serving with vLLM", "The
-PagedAttention Algorithm" and "Advanced Features"); with it, a request whose
-prompt starts with the tokens of committed full blocks reuses exactly those
-blocks ("Advanced Features", Prefix Caching)."""
+PagedAttention Algorithm" and "Advanced Features"); with it, exactly the
+blocks of the oracle's prefix-cache model: a request whose prompt starts with
+the tokens of committed full blocks reuses those blocks ("Advanced
+Features", Prefix Caching)."""
 import os
 
 import numpy as np
 import pytest
 
 import paged_kv_cache_311_gb300 as pkv
-from oracle.block_manager import OracleBlockManager
+from oracle.block_manager import OracleBlockManager, OraclePrefixCache
 from paged_kv_cache_311_gb300.build import build, library_path
 from tests.util import read_golden
 
@@ -164,87 +165,33 @@ def test_writing_into_a_cached_block_copies_it():
     assert pool.prepare_write(t, 2) is None               # the copy is private
 
 
-class PoolModel:
-    """Plain reference of the prefix cache for the random test below: the
-    cache maps a prompt's token prefix up to a block boundary to its block."""
-
-    def __init__(self, nb, bs):
-        self.bs, self.free = bs, list(range(nb))[::-1]
-        self.refs = [0] * nb
-        self.entry = {}          # tuple(tokens[:k * bs]) -> block
-        self.key_of = {}         # block -> key
-        self.lru = []            # cached blocks nobody holds, least recent first
-
-    def available(self):
-        return len(self.free) + len(self.lru)
-
-    def take(self):
-        if self.free:
-            b = self.free.pop()
-        else:
-            b = self.lru.pop(0)
-            del self.entry[self.key_of.pop(b)]
-        self.refs[b] = 1
-        return b
-
-    def hold(self, b):
-        if self.refs[b] == 0 and b in self.key_of:
-            self.lru.remove(b)
-        self.refs[b] += 1
-
-    def drop(self, b):
-        self.refs[b] -= 1
-        if self.refs[b] == 0:
-            (self.lru if b in self.key_of else self.free).append(b)
-
-    def allocate_prompt(self, toks):
-        bs, n = self.bs, len(toks)
-        table = []
-        for k in range(n // bs):
-            b = self.entry.get(tuple(toks[:(k + 1) * bs]))
-            if b is None:
-                break
-            table.append(b)
-        for b in table:
-            self.hold(b)
-        need = -(-n // bs) - len(table)
-        if self.available() < need:
-            for b in table:
-                self.drop(b)
-            return None
-        reused = len(table)
-        table += [self.take() for _ in range(need)]
-        return table, reused * bs
-
-    def commit(self, toks, table):
-        for k in range(len(toks) // self.bs):
-            key = tuple(toks[:(k + 1) * self.bs])
-            b = table[k]
-            if b not in self.key_of and key not in self.entry:
-                self.entry[key], self.key_of[b] = b, key
-
-
-def test_prefix_cache_against_a_reference_model():
+def test_prefix_cache_follows_the_oracle_model():
+    """A random walk of prompts over five shared prefixes (some committed,
+    some not), releases and refused requests: the pool hands out the tables
+    and cached-token counts of the oracle's prefix-cache model, and holder
+    counts, cache entries and the free count agree throughout.  The model is
+    pinned to the page's prefix-caching statements in the oracle pins."""
     rng = np.random.default_rng(21)
     bs, NB = 8, 60
-    pool, model = pkv.BlockPool(NB, bs), PoolModel(NB, bs)
+    pool, model = pkv.BlockPool(NB, bs), OraclePrefixCache(NB, bs)
     prefixes = [rng.integers(0, 50, int(rng.integers(4, 40))) for _ in range(5)]
     live = []
+    refused = 0
     for step in range(800):
-        if live and (rng.random() < 0.45 or model.available() < 12):
+        if live and (rng.random() < 0.4 or model.available() < 2):
             i = int(rng.integers(0, len(live)))
             toks, table = live.pop(i)
             pool.release(table)
-            for b in table:
-                model.drop(b)
+            model.release(list(table))
         else:
             pre = prefixes[int(rng.integers(0, len(prefixes)))]
             toks = np.concatenate([pre[:int(rng.integers(0, len(pre) + 1))],
                                    rng.integers(0, 50, int(rng.integers(0, 20)))]).astype(np.int32)
             if toks.size == 0:
                 continue
-            want = model.allocate_prompt(list(toks))
+            want = model.allocate_prompt(toks.tolist())
             if want is None:
+                refused += 1
                 with pytest.raises(pkv.PkvError):
                     pool.allocate_prompt(toks)
                 continue
@@ -252,13 +199,37 @@ def test_prefix_cache_against_a_reference_model():
             assert (list(table), cached) == (want[0], want[1])
             if rng.random() < 0.8:
                 pool.commit_prompt(toks, table)
-                model.commit(list(toks), list(table))
+                model.commit_prompt(toks.tolist(), list(table))
             live.append((toks, table))
         assert pool.available() == model.available()
     for b in range(NB):
-        assert pool.refcount(b) == model.refs[b]
-        assert pool.is_cached(b) == (b in model.key_of)
-    assert pool.stats()["hits"] > 100          # the walk reused cached prefixes often
+        assert pool.refcount(b) == model.holders[b]
+        assert pool.is_cached(b) == model.is_cached(b)
+    st = pool.stats()
+    assert (st["lookups"], st["hits"]) == (model.lookups, model.hits)
+    assert st["hits"] > 100          # the walk reused cached prefixes often
+    assert refused > 0               # and ran into a full pool
+
+
+def test_refused_prompt_leaves_the_eviction_order_alone():
+    """A refused request takes nothing and leaves the order in which idle
+    cached blocks are evicted as it was."""
+    bs = 8
+    pool, model = pkv.BlockPool(6, bs), OraclePrefixCache(6, bs)
+    p1, p2 = np.arange(16, dtype=np.int32), np.arange(100, 116, dtype=np.int32)
+    for p in (p1, p2):
+        t, _ = pool.allocate_prompt(p); pool.commit_prompt(p, t)
+        u = model.allocate_prompt(p.tolist())[0]; model.commit_prompt(p.tolist(), u)
+        pool.release(t); model.release(u)
+    assert list(pool.allocate(1)) == model.allocate(1) == [4]
+    # p1 + 4 more blocks: 2 reused (idle) + 4 fresh, but only 1 free + 2 other idle blocks
+    big = np.concatenate([p1, np.arange(500, 532, dtype=np.int32)])
+    assert model.allocate_prompt(big.tolist()) is None
+    with pytest.raises(pkv.PkvError):
+        pool.allocate_prompt(big)
+    # the free block, then p1's blocks: still the ones released longest ago
+    assert list(pool.allocate(3)) == model.allocate(3) == [5, 0, 1]
+    assert not pool.is_cached(0) and pool.is_cached(2)
 
 
 def test_system_prompt_requests_share_cached_blocks_and_group():
@@ -470,3 +441,36 @@ def test_append_slots_follows_the_oracle_block_manager():
     for b in range(NB):
         assert pool.refcount(b) == ref.refcount[b]
     assert pool.available() == len(ref.free)
+
+
+def test_decode_batch_system_prompt_follows_the_oracle_model():
+    """DecodeBatch on the pool: 40 requests over 3 system prompts, then 20
+    decode steps; every table, cached count, slot and copy pair matches the
+    oracle's prefix-cache model."""
+    from tests.pool_lockstep import Lockstep, build_system_prompt, system_prompt_requests
+    bs = 16
+    reqs, prompts = system_prompt_requests(5, 40, 3, (100, 300), (1, 40))
+    ls = Lockstep(600, bs, 40, 32)
+    pre = build_system_prompt(ls, reqs)
+    # the first request of each prompt computes it; later ones reuse its full blocks
+    assert [c for _, c in pre] == [0, 0, 0] + [len(prompts[i % 3]) // bs * bs for i in range(3, 40)]
+    assert [s.size for s, _ in pre] == [len(r) - c for r, (_, c) in zip(reqs, pre)]
+    for _ in range(20):
+        ls.step(40)
+    ls.check_holders()
+
+
+def test_decode_batch_sampling_follows_the_oracle_model():
+    """Eight prompts forked into six samples each, then 20 steps: the first
+    step copies every shared partial last block (five copies per prompt whose
+    length is not a multiple of the block size), as the oracle model does."""
+    from tests.pool_lockstep import Lockstep, build_sampling, sampling_prompts
+    bs, S = 16, 6
+    prompts = sampling_prompts(6, 8, (40, 200))
+    ls = Lockstep(400, bs, 8 * S, 32)
+    build_sampling(ls, prompts, S)
+    _, pairs = ls.step(8 * S)
+    assert pairs.shape[0] == 5 * sum(1 for p in prompts if p.size % bs)
+    for _ in range(19):
+        ls.step(8 * S)
+    ls.check_holders()

@@ -66,3 +66,42 @@ def test_shared_presets_sampled_on_tcgen05(idx):
         assert pkv.last_decode_engine() == "tcgen05"
     finally:
         pkv.set_decode_engine("auto")
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_full_step_in_the_cache_dtype_every_sequence(idx):
+    """One full-size step of the Llama-7B (fp16) and Llama-13B (bf16)
+    workloads with the output in the cache's dtype, as the benchmark runs it,
+    checked on every sequence: the 16-bit output is the fp32 result of the
+    same step rounded to nearest even (bit for bit), the fp32 result is within
+    the attention tolerance of the oracle, and so the 16-bit output lies
+    within one unit in the last place of the oracle's value rounded to that
+    dtype, plus the fp32 result's own error."""
+    import paged_kv_cache_311_gb300 as pkv
+    from tests.gpu_support import ulp_bound
+    from tests.util import DT
+    cfg = CONFIGS[idx]
+    seed = SEED_BASE + idx
+    tdt = DT[cfg.dtype]
+    w = PagedDecodeWorkload(cfg, seed, total_steps=1)
+    state = DeviceState(cfg, w, seed, out_dtype=tdt)
+    inp = w.next_step()
+    orc = SampledOracle(state, list(range(w.num_seqs)), [inp])   # before any library kernel
+    ds = state.to_device(inp, value_device="cpu")
+    state.run_step(ds)                   # copy-on-write, scatter, decode into the 16-bit output
+    out32 = torch.empty(state.out.shape, dtype=torch.float32, device=state.out.device)
+    pkv.paged_attention_decode(out32, ds.q, state.k_cache, state.v_cache, ds.block_tables,
+                               ds.context_lens, cfg.softmax_scale,
+                               max_context_len=ds.max_context_len,
+                               partition_size=cfg.partition_size, workspace=state.workspace,
+                               device_status=state.status)
+    torch.cuda.synchronize()
+    assert state.status.item() == 0
+    orc.apply_step(inp, ds.key.cpu(), ds.value.cpu())
+    ref = orc.attention(inp, ds.q.cpu())
+    got16 = state.out.double().cpu().numpy()
+    got32 = out32.double().cpu().numpy()
+    assert max_err(got32, ref) <= TOL[cfg.dtype]
+    np.testing.assert_array_equal(got16, out32.to(tdt).double().cpu().numpy())
+    rne = torch.from_numpy(ref).to(tdt).double().numpy()
+    assert np.all(np.abs(got16 - rne) <= ulp_bound(ref, tdt) + np.abs(got32 - ref))

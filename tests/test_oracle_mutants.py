@@ -65,7 +65,7 @@ def test_pins_reject_mutant(name, tmp_path):
 
 
 # Planted mistakes in the oracle's Python block manager (on-demand blocks,
-# fork, copy-on-write, free): the mutated module is put in place of
+# fork, copy-on-write, free, prefix caching): the mutated module is put in place of
 # oracle.block_manager before the pin suite imports it.
 BM_MUTANTS = {
     "cow_on_any_write": ("            if self.refcount[b] > 1:", "            if self.refcount[b] >= 1:"),
@@ -76,6 +76,18 @@ BM_MUTANTS = {
     "free_never_returns_blocks": ("            if self.refcount[b] == 0:\n                self.free.append(b)",
                                   "            if self.refcount[b] < 0:\n                self.free.append(b)"),
     "blocks_rounded_down": ("    return -(-n_tokens // block_size)", "    return n_tokens // block_size"),
+    # prefix caching
+    "prefix_key_is_the_block_alone": ("        return toks[:(k + 1) * self.block_size]",
+                                      "        return toks[k * self.block_size:(k + 1) * self.block_size]"),
+    "reused_blocks_not_held": ("        for b in reused:\n            self._hold(b)",
+                               "        for b in reused:\n            pass"),
+    "evicts_latest_released": ("            b = self.idle.pop(0)", "            b = self.idle.pop()"),
+    "cached_block_written_in_place": ("        if self.holders[b] == 1 and b not in self.key:",
+                                      "        if self.holders[b] == 1:"),
+    "refusal_counts_idle_reused_as_free": ("        if self.available() - idle_reused < fresh:",
+                                           "        if self.available() < fresh:"),
+    "second_commit_replaces_entry": ("            if b not in self.key and prefix not in self.entry:",
+                                     "            if b not in self.key:"),
 }
 
 

@@ -436,3 +436,170 @@ def test_copy_on_write_rule():
     for c in range(1, 6):
         bm2.fork(0, c)
     assert all(bm2.append_token(s)[1] is None for s in range(6))
+
+
+# ---------------------------------------------------------- prefix caching
+# The page "PagedAttention: Efficient LLM Serving with vLLM", "Advanced
+# Features": Prefix Caching (the first request with a prefix computes its KV
+# blocks and caches them; later requests with the same prefix reuse them) and
+# KV-Cache Sharing (only the divergent tokens get new blocks).  Every count
+# below is worked out by hand from those statements and the block-count rule
+# (100 tokens at 16 per block: 6 full blocks + 4 tokens in a 7th).
+
+def _prompt(n, seed):
+    return [int(x) for x in np.random.default_rng(seed).integers(0, 32000, n)]
+
+
+def test_prefix_cache_first_request_computes_later_ones_reuse():
+    from oracle.block_manager import OraclePrefixCache
+    bs, system = 16, _prompt(100, 1)
+    pc = OraclePrefixCache(num_blocks=64, block_size=bs)
+    reqs = [system + _prompt(20, 10 + i) for i in range(5)]       # 120 tokens: 8 blocks each
+    first, cached = pc.allocate_prompt(reqs[0])
+    assert cached == 0 and len(first) == 8 and len(set(first)) == 8
+    pc.commit_prompt(reqs[0], first)
+    tables = [first]
+    for r in reqs[1:]:
+        t, cached = pc.allocate_prompt(r)
+        assert cached == 96                        # the 6 full system-prompt blocks
+        assert t[:6] == first[:6]                  # reused, not recomputed
+        assert len(t) == 8 and not set(t[6:]) & set(b for u in tables for b in u)
+        pc.commit_prompt(r, t)
+        tables.append(t)
+    assert all(pc.holders[b] == 5 for b in first[:6])
+    assert all(pc.holders[b] == 1 for t in tables for b in t[6:])
+    # 6 shared + 5 x 2 own blocks, against 5 x 8 without the cache
+    assert len({b for t in tables for b in t}) == 16
+    assert pc.available() == 64 - 16
+    # two requests for a new prompt that arrive before either is committed
+    # both compute it; the first commit's blocks are the ones later reused
+    other = _prompt(48, 2)
+    a, _ = pc.allocate_prompt(other)
+    b, _ = pc.allocate_prompt(other)
+    pc.commit_prompt(other, a)
+    pc.commit_prompt(other, b)
+    c, cached = pc.allocate_prompt(other + [7])
+    assert cached == 48 and c[:3] == a[:3] and not set(c[:3]) & set(b)
+
+
+def test_prefix_cache_key_covers_every_earlier_token():
+    from oracle.block_manager import OraclePrefixCache
+    bs, p = 16, _prompt(64, 3)
+    pc = OraclePrefixCache(num_blocks=32, block_size=bs)
+    t, _ = pc.allocate_prompt(p)
+    pc.commit_prompt(p, t)
+    # blocks 1..3 hold the same tokens after a different block 0: no reuse
+    q = list(p)
+    q[3] += 1
+    u, cached = pc.allocate_prompt(q)
+    assert cached == 0 and not set(u) & set(t)
+    # the same first 40 tokens: the 2 full blocks they cover
+    v, cached = pc.allocate_prompt(p[:40] + _prompt(30, 4))
+    assert cached == 32 and v[:2] == t[:2] and v[2] not in t
+    # block 0 of another committed prompt, then block 1 of p: block 0 is
+    # reused, block 1 is not (its K/V in p was computed after p's block 0)
+    x = _prompt(32, 7)
+    tx, _ = pc.allocate_prompt(x)
+    pc.commit_prompt(x, tx)
+    mixed = x[:16] + p[16:32]
+    w, cached = pc.allocate_prompt(mixed)
+    assert cached == 16 and w[0] == tx[0] and w[1] not in t and w[1] != tx[1]
+
+
+def test_only_divergent_tokens_get_new_blocks():
+    """Six samples of one 100-token prompt: they share its 7 blocks; each
+    sample's first new token copies the shared partial block (samples 0-4;
+    sample 5 is its last holder and writes in place); 20 tokens later every
+    sample holds one more block of its own."""
+    from oracle.block_manager import OraclePrefixCache
+    bs = 16
+    pc = OraclePrefixCache(num_blocks=64, block_size=bs)
+    prompt, _ = pc.allocate_prompt(_prompt(100, 5))
+    tables = [list(prompt)]
+    for _ in range(5):
+        pc.fork(prompt)
+        tables.append(list(prompt))
+    pairs = []
+    for s in range(6):
+        slot, pair = pc.append_token(tables[s], 100)
+        assert slot == tables[s][6] * bs + 4
+        if pair:
+            pairs.append(pair)
+    assert len(pairs) == 5 and all(p[0] == prompt[6] for p in pairs)
+    assert tables[5][6] == prompt[6]
+    for n in range(101, 120):
+        for s in range(6):
+            assert pc.append_token(tables[s], n)[1] is None
+    assert all(t[:6] == prompt[:6] for t in tables)
+    assert all(pc.holders[b] == 6 for b in prompt[:6])
+    # 6 shared + 6 partial-block copies (5 copies + the original) + 6 new
+    assert len({b for t in tables for b in t}) == 18
+    assert all(len(t) == 8 for t in tables)
+
+
+def test_cached_block_is_copied_before_a_write():
+    """A committed block is read by every later request that reuses it, so
+    its only holder writes into a copy; the entry stays reusable."""
+    from oracle.block_manager import OraclePrefixCache
+    bs, p = 8, _prompt(24, 6)
+    pc = OraclePrefixCache(num_blocks=16, block_size=bs)
+    t, _ = pc.allocate_prompt(p)
+    pc.commit_prompt(p, t)
+    old = t[2]
+    assert pc.prepare_write(t, 2) == (old, t[2]) and t[2] != old
+    assert pc.holders[old] == 0 and pc.is_cached(old)
+    assert pc.prepare_write(t, 2) is None                  # the copy is private
+    again, cached = pc.allocate_prompt(p)
+    assert cached == 24 and again == [t[0], t[1], old]
+
+
+def test_released_prefix_stays_reusable_and_the_longest_released_goes_first():
+    """The eviction rule: a cached block nobody holds keeps its entry until a
+    block is needed and none is free; then the one released longest ago."""
+    from oracle.block_manager import OraclePrefixCache
+    bs, NB = 8, 12
+    pc = OraclePrefixCache(num_blocks=NB, block_size=bs)
+    p1, p2 = list(range(16)), list(range(100, 116))
+    t1, _ = pc.allocate_prompt(p1)
+    pc.commit_prompt(p1, t1)
+    t2, _ = pc.allocate_prompt(p2)
+    pc.commit_prompt(p2, t2)
+    assert (t1, t2) == ([0, 1], [2, 3])                   # block 0 first
+    pc.release(t1)                                        # released first
+    pc.release(t2)
+    assert pc.available() == NB and pc.idle == [0, 1, 2, 3]
+    again, cached = pc.allocate_prompt(p1)                # still reusable
+    assert cached == 16 and again == t1
+    pc.release(again)                                     # p1 is now the latest released
+    assert pc.idle == [2, 3, 0, 1]
+    assert sorted(pc.allocate(8)) == list(range(4, 12))   # the free blocks go first
+    assert pc.allocate(2) == [2, 3]                       # then p2's: released longest ago
+    assert not pc.is_cached(2) and not pc.is_cached(3)
+    _, cached = pc.allocate_prompt(p2)
+    assert cached == 0
+    pc2 = OraclePrefixCache(num_blocks=NB, block_size=bs)
+    u1, _ = pc2.allocate_prompt(p1)
+    pc2.commit_prompt(p1, u1)
+    pc2.release(u1)
+    pc2.allocate(NB - 2)
+    _, cached = pc2.allocate_prompt(p1)                   # p1 survived
+    assert cached == 16
+
+
+def test_refused_request_changes_nothing():
+    """A request that cannot get every block it needs takes none and leaves
+    the pool as it was: a reused block nobody holds cannot also serve as
+    one of the request's fresh blocks."""
+    from oracle.block_manager import OraclePrefixCache
+    bs = 8
+    pc = OraclePrefixCache(num_blocks=4, block_size=bs)
+    p = list(range(16))
+    t, _ = pc.allocate_prompt(p)
+    pc.commit_prompt(p, t)
+    pc.release(t)                                   # 2 idle cached + 2 free
+    keep = pc.allocate(1)                           # 2 idle + 1 free
+    state = (list(pc.free), list(pc.idle), list(pc.holders))
+    assert pc.allocate_prompt(p + list(range(50, 66))) is None   # 2 reused + 2 fresh > 1 free
+    assert (list(pc.free), list(pc.idle), list(pc.holders)) == state
+    t3, cached = pc.allocate_prompt(p + [1, 2])     # 2 reused + 1 fresh: fits
+    assert cached == 16 and t3[:2] == t and t3[2] not in keep

@@ -1,13 +1,19 @@
 """pkv_paged_attention_decode_static: decode attention without any allocation.
 
 This entry point exists for callers that cannot allocate device memory --
-code running under CUDA-graph stream capture, plugins whose host engine owns
-all device memory, and latency-critical loops that must not call cudaMalloc.
-It keeps the split-context partials in a buffer inside the library instead
-of a caller workspace.  The test calls it through the C ABI twice in a row
-(on two different batches) and compares each result with the allocating
-entry point pkv_paged_attention_decode at the tolerance the other attention
-tests use.  It runs last so that a failure here cannot hide other results.
+plugins whose host engine owns all device memory and gives them none, code
+under an allocator that is full or must not grow, and latency-critical loops
+that must not call cudaMalloc because it may synchronise the device.  When a
+context spans several partitions it keeps the split-context partials in a
+buffer inside the library instead of a caller workspace.
+
+The test calls it through the C ABI twice in a row (on two different
+batches, each at two partition sizes) and compares each result with the
+allocating entry point pkv_paged_attention_decode and with the CPU oracle, at
+the tolerance the other attention tests use.  It also checks that a large
+batch whose contexts fit one partition runs (single pass, no buffer) and that
+a split request beyond the buffer is refused.  It runs last so that a
+failure here cannot hide other results.
 """
 import ctypes
 
@@ -15,7 +21,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_support import TOL
+from tests.gpu_support import TOL, max_err, oracle_decode
 from tests.util import small_case
 
 pytestmark = pytest.mark.gpu
@@ -62,7 +68,7 @@ def _allocating(case, d, P):
     return out
 
 
-def test_static_workspace_matches_allocating_decode_twice():
+def test_static_workspace_matches_allocating_decode_and_oracle_twice():
     L = _lib()
     cases = [
         small_case(41, dtype="bf16", B=5, H=16, Hk=2, D=128, bs=16, lens=(1, 700, 513, 2000, 4097)),
@@ -70,17 +76,39 @@ def test_static_workspace_matches_allocating_decode_twice():
     ]
     for case in cases:                      # two calls in a row, different batches
         d = _device(case)
+        ref, ost = oracle_decode(case)
+        assert ost == 0
         for P in (512, 256):
-            ref = _allocating(case, d, P)
-            out = torch.full_like(ref, float("nan"))
+            alloc = _allocating(case, d, P)
+            out = torch.full_like(alloc, float("nan"))
             st = torch.zeros(1, dtype=torch.int32, device="cuda")
             rc = _static_call(L, case, d, out, st, P)
             assert rc == 0
             torch.cuda.synchronize()
             assert st.item() == 0
-            err = (out.double() - ref.double()).abs().max().item()
-            assert err <= TOL[case["dtype"]], err
             assert torch.isfinite(out).all()
+            got = out.double().cpu().numpy()
+            assert max_err(got, alloc.double().cpu().numpy()) <= TOL[case["dtype"]]
+            assert max_err(got, ref) <= TOL[case["dtype"]]
+
+
+def test_single_partition_batch_needs_no_buffer():
+    """2048 sequences x 64 heads whose contexts fit one partition: the split
+    path's partials would take 2048 * 64 * (2 + 128) * 4 bytes (> 32 MiB), but
+    the single pass uses none, so the call runs and matches the oracle."""
+    L = _lib()
+    B = 2048
+    lens = tuple(int(x) for x in np.random.default_rng(5).integers(1, 65, B))
+    case = small_case(44, dtype="bf16", B=B, H=64, Hk=8, D=128, bs=16, lens=lens)
+    assert B * 64 * (2 + 128) * 4 > L.pkv_static_workspace_capacity()
+    d = _device(case)
+    out = torch.full(d["q"].shape, float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert _static_call(L, case, d, out, st, 512) == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ref, ost = oracle_decode(case)
+    assert ost == 0 and max_err(out.double().cpu().numpy(), ref) <= TOL["bf16"]
 
 
 def test_static_workspace_rejects_oversized_requests():
