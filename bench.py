@@ -2,17 +2,29 @@
 
 A step is one pass of the whole hot path over one batch: copy-on-write block
 copies (when the step has any), the scatter of the new tokens into their
-slots, and paged decode attention (single pass, or partition pass plus
-log-sum-exp reduce).  Default workload: the Llama-7B-shaped fp16 decode
-(batch 64, 32 heads, head_dim 128, block 16, lengths U{128..2048}, 100 steps).
+slots, and paged decode attention (single pass, split-context partitions plus
+log-sum-exp reduce, or the shared-prefix kernel plus its merge).
 
-Prints ONE JSON line (rank 0).  value = algorithmic bytes of the step / device
-time of the step, with every input resident in HBM; L2 is flushed (256 MiB
-read) before every step, outside the timed events.  roofline = the decode
-kernel's own algorithmic bytes per launch / its mean launch time against the
-measured HBM copy bandwidth.  e2e = the same metric with the step's inputs
-copied from pinned host memory and the output read back inside the timed
-region.  cpu_baseline = the CPU oracle on a bounded sample of the same steps.
+Default line: the largest workload that fits one GPU, the long-context decode
+(batch 16, 64 query / 8 kv heads, head_dim 128, block 16, contexts of 16K-32K
+tokens whose blocks are scattered over a ~60 GB pool, 512-token partitions).
+At one GPU the same line carries ``per_config``: every workload -- Llama-7B
+fp16, Llama-13B continuous batching, parallel sampling with shared prefixes,
+the long-context decode at block sizes 8 / 16 / 32, and cached system prompts
+-- each over its own step count, with the same figures as the headline.
+
+Figures (rank 0 prints ONE JSON line):
+  value      algorithmic bytes of the steps / device time of the steps, every
+             input resident in HBM; L2 is flushed (256 MiB read) before every
+             step, outside the timed events.
+  roofline   the decode's own algorithmic bytes per launch / its mean
+             event-timed duration, against the measured HBM copy bandwidth.
+  e2e        the same metric with the step's inputs copied from pinned host
+             memory and the output read back inside the device-timed region.
+  host_e2e   a serving loop's steps timed by the host's wall clock: block-pool
+             bookkeeping, the shared-prefix planner, packing, copies, library
+             calls and a stream synchronise.
+  cpu_baseline  the CPU oracle on a bounded sample of the same steps.
 
 --impl reference times the oracle itself as the reference arm.
 """
@@ -46,13 +58,13 @@ SEED_BASE = 311 * 100
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=95)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--op", default="decode", choices=["decode", "swap_blocks", "host_step"],
                     help="swap_blocks: time the block swap of a preempted tenth of the batch; "
                          "host_step: time a step's host bookkeeping (no GPU)")
-    ap.add_argument("--config", default="llama7b_f16")
+    ap.add_argument("--config", default=HEADLINE[0])
     ap.add_argument("--block-size", type=int, default=0)
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling cases)")
     ap.add_argument("--pool-gb", type=float, default=0.0,
@@ -60,10 +72,14 @@ def parse_args():
     ap.add_argument("--partition-size", type=int, default=-1, help="-1: the preset's choice")
     ap.add_argument("--engine", default="auto", choices=["auto", "cuda_core", "tensor_core", "tcgen05"])
     ap.add_argument("--no-shared", action="store_true",
-                    help="shared-prefix workload: use the per-sequence entry point")
+                    help="shared-prefix workloads: use the per-sequence entry point")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-host-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="only the headline workload (per_config is on by default at one GPU)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--per-config-cpu-seconds", type=float, default=4.0)
     ap.add_argument("--identity-tables", action="store_true",
                     help="place every sequence's blocks contiguously (gather-overhead comparison)")
     return ap.parse_args()
@@ -163,43 +179,104 @@ class ClockSampler:
 def run_native(args):
     dist, rank, world = dist_setup()
     dev = local_device()
-    cfg = get(args.config)
-    if args.block_size:
-        cfg = cfg.with_(block_size=args.block_size)
-    seed = SEED_BASE + CONFIGS.index(get(args.config)) + 1000 * rank
-    total = args.warmup + args.steps
+    head = measure(args, args.config, args.block_size, args.steps, args.warmup, dist, rank, world,
+                   dev, cpu_seconds=args.cpu_seconds)
+    per_config = None
+    if world == 1 and not args.no_per_config and args.op == "decode":
+        per_config = {}
+        for name, bs in PER_CONFIG:
+            key = name if name != "long_context_bf16" else f"{name}/bs{bs}"
+            if (name, bs or get(name).block_size) == (head["config"]["workload"],
+                                                      head["config"]["block_size"]):
+                per_config[key] = _compact(head)
+                continue
+            cfg = get(name)
+            r = measure(args, name, bs, cfg.steps - PER_CONFIG_WARMUP if cfg.steps > 10 else cfg.steps,
+                        PER_CONFIG_WARMUP, None, 0, 1, dev, cpu_seconds=args.per_config_cpu_seconds,
+                        engine="auto", shared_default=True)
+            per_config[key] = _compact(r)
+    if rank == 0:
+        line = {"metric": METRIC, **{k: head[k] for k in (
+            "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+            "scaling", "vs_baseline", "dtype", "data", "config", "seq_steps_per_s", "step_ms",
+            "decode_ms", "unflushed", "pct_of_peak", "roofline", "clocks", "gpu_launches", "e2e",
+            "host_e2e", "cpu_baseline", "kv_memory")}}
+        if per_config is not None:
+            line["per_config"] = per_config
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# The headline line: the largest configuration that fits one GPU -- the
+# long-context decode (batch 16, 64 q / 8 kv heads, 16K-32K tokens) over a
+# ~60 GB pool, split-context partitions and their merge.  per_config: every
+# workload of the survey at one GPU, each over its own step count.
+HEADLINE = ("long_context_bf16", 16)
+PER_CONFIG = [("llama7b_f16", 0), ("llama13b_cb_bf16", 0), ("shared_prefix_bf16", 0),
+              ("long_context_bf16", 8), ("long_context_bf16", 16), ("long_context_bf16", 32),
+              ("system_prompt_bf16", 0)]
+PER_CONFIG_WARMUP = 3
+
+
+def _compact(r):
+    """A per_config entry: the measured figures of one workload."""
+    keep = ("value", "unit", "steps", "warmup", "ms_per_step", "seq_steps_per_s", "decode_ms",
+            "roofline", "clocks", "gpu_launches", "e2e", "host_e2e", "cpu_baseline", "kv_memory")
+    out = {k: r[k] for k in keep}
+    c = r["config"]
+    out["config"] = {k: c[k] for k in ("workload", "kv_dtype", "num_seqs", "num_heads",
+                                       "num_kv_heads", "block_size", "partition_size",
+                                       "decode_launches_per_step", "engine", "pool_gb", "path")}
+    return out
+
+
+def measure(args, name, block_size, steps, warmup, dist, rank, world, dev, cpu_seconds,
+            engine=None, shared_default=None):
+    """One workload: device-timed steps, the unflushed repeat, e2e through
+    the C ABI with host buffers, the wall-clock host_e2e serving loop, the
+    CPU oracle on a bounded sample, and memory accounting."""
+    import paged_kv_cache_311_gb300 as pkv
+    cfg = get(name)
+    if block_size:
+        cfg = cfg.with_(block_size=block_size)
+    engine = args.engine if engine is None else engine
+    no_shared = args.no_shared if shared_default is None else not shared_default
+    seed = SEED_BASE + CONFIGS.index(get(name)) + 1000 * rank
+    total = warmup + steps
     w = PagedDecodeWorkload(cfg, seed, total_steps=max(total, cfg.steps),
-                            contiguous=args.identity_tables, num_seqs=args.num_seqs or None,
-                            pool_blocks=_pool_blocks(cfg, dev, args.pool_gb))
-    P = cfg.partition_size if args.partition_size < 0 else args.partition_size
+                            contiguous=args.identity_tables and name == args.config,
+                            num_seqs=(args.num_seqs or None) if name == args.config else None,
+                            pool_blocks=_pool_blocks(cfg, dev, args.pool_gb if name == args.config
+                                                     else 0.0))
+    P = cfg.partition_size if (args.partition_size < 0 or name != args.config) else args.partition_size
     out_dtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[cfg.dtype]
     state = DeviceState(cfg, w, seed, device=dev, out_dtype=out_dtype)
     host_inputs = [w.next_step() for _ in range(total)]
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(cfg, state, host_inputs, args.cpu_seconds, seed)
+    if rank == 0 and world == 1 and not args.no_cpu and cpu_seconds > 0:
+        cpu = cpu_baseline(cfg, state, host_inputs, cpu_seconds, seed)
 
-    import paged_kv_cache_311_gb300 as pkv
-    shared = cfg.kind in ("shared_prefix", "system_prompt") and not args.no_shared
-    if shared and args.partition_size < 0:
+    shared = cfg.kind in ("shared_prefix", "system_prompt") and not no_shared
+    if shared and (args.partition_size < 0 or name != args.config):
         P = 0   # the shared-prefix planner's own default partition
-    steps = [state.to_device(inp, shared=shared, partition_size=P) for inp in host_inputs]
-    pkv.set_decode_engine(args.engine)
-    for s in steps:
+    steps_dev = [state.to_device(inp, shared=shared, partition_size=P) for inp in host_inputs]
+    pkv.set_decode_engine(engine)
+    for s in steps_dev:
         state.ensure_workspace(s.max_context_len, P, s.plan)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     out_bytes = torch.tensor([], dtype=out_dtype).element_size()
 
     # warm-up
-    for s in steps[:args.warmup]:
+    for s in steps_dev[:warmup]:
         state.run_step(s, partition_size=P)
     torch.cuda.synchronize()
     state.status.zero_()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     launches = 0
     decode_launches = []
     if dist is not None:
@@ -209,7 +286,7 @@ def run_native(args):
     gc.collect()      # no collector pass inside the timed steps
     gc.disable()
     torch.cuda.nvtx.range_push("timed_steps")
-    for i, s in enumerate(steps[args.warmup:]):
+    for i, s in enumerate(steps_dev[warmup:]):
         _flush_l2(flush)
         _preroll()
         e0, e1, e2 = ev[i]
@@ -235,24 +312,20 @@ def run_native(args):
         dist.barrier()
     clk = clocks.stop() if clocks else None
     if state.status.item() != 0:
-        raise RuntimeError(f"device status {state.status.item()} during the timed steps")
+        raise RuntimeError(f"{cfg.name}: device status {state.status.item()} during the timed steps")
 
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     dec_ms = [b.elapsed_time(c) for _, b, c in ev]
     tot_ms = sum(step_ms)
     bytes_step, bytes_dec, seqs = 0, 0, 0
     dec_bytes = []
-    for s, n in zip(steps[args.warmup:], decode_launches):
-        if shared:
-            expected = s.plan.host[8:8 + w.num_seqs]
-            ab = algorithmic_bytes(cfg, s.host, w.num_seqs, out_bytes=out_bytes, partials=expected)
-        else:
-            Pp = _split_partition(P, s.max_context_len, n)
-            ab = algorithmic_bytes(cfg, s.host, w.num_seqs, split_partition=Pp, out_bytes=out_bytes)
+    for s, n in zip(steps_dev[warmup:], decode_launches):
+        ab = _step_bytes(cfg, s.host, w.num_seqs, out_bytes, s.plan, P, n)
         bytes_step += ab["total"]
         bytes_dec += ab["attention"]
         dec_bytes.append(ab["attention"])
         seqs += w.num_seqs
+    plan_s = sum(s.plan_seconds for s in steps_dev[warmup:])
     t_max = max_over_ranks(dist, tot_ms / 1e3)
     bytes_all = sum_over_ranks(dist, bytes_step)
     seqs_all = sum_over_ranks(dist, seqs)
@@ -263,55 +336,78 @@ def run_native(args):
     main_kernel = (("pa_cascade_tc05_kernel" if engine_used == "tcgen05" else "pa_cascade_kernel")
                    if shared else "pa_decode_kernel")
 
-    unflushed = _unflushed_decode(pkv, state, steps[-1], P, dec_bytes[-1], peak)
+    unflushed = _unflushed_decode(pkv, state, steps_dev[-1], P, dec_bytes[-1], peak)
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(state, steps[args.warmup:], host_inputs[args.warmup:], P, flush, bytes_step)
+        e2e = run_e2e(state, steps_dev[warmup:], host_inputs[warmup:], P, flush, bytes_step)
     # memory accounting of the paged cache at the first timed step
-    first = host_inputs[args.warmup]
+    first = host_inputs[warmup]
     use = pkv.kv_cache_usage(first.block_tables, first.context_lens, cfg.block_size, w.num_blocks)
     kv_memory = {"block_size": cfg.block_size, "tokens": use.tokens, "blocks": use.blocks,
                  "paged_waste": round(use.paged_waste, 4),
                  "reserve_longest_waste": round(use.reserved_waste(int(first.context_lens.max())), 4)}
+    host = None
+    if not args.no_host_e2e and world == 1:
+        # last: it writes its own prefill into the same cache
+        host = run_host_e2e(cfg, w, state, shared, P, engine, flush, seed,
+                            steps=min(steps, HOST_E2E_STEPS), warmup=min(warmup, 3))
+    pkv.set_decode_engine("auto")
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max * 1e3 / args.steps, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": cfg.name, "kv_dtype": cfg.dtype, "num_seqs": w.num_seqs,
-                       "num_heads": cfg.num_heads, "num_kv_heads": cfg.num_kv_heads,
-                       "head_dim": cfg.head_dim, "block_size": cfg.block_size,
-                       "partition_size": P, "decode_launches_per_step": decode_launches[0],
-                       "engine": engine_used,
-                       "pool_gb": round(2 * w.num_blocks * cfg.block_bytes / 1e9, 3),
-                       "parallelism": f"replicas x{world} (sequences sharded, no collective)",
-                       "l2": "flushed (256 MiB read) before every timed step, outside the events",
-                       "block_placement": "contiguous" if args.identity_tables else "random"},
-            "seq_steps_per_s": round(seqs_all / t_max, 1),
-            "step_ms": _spread(step_ms),
-            "decode_ms": _spread(dec_ms),
-            "unflushed": unflushed,
-            "pct_of_peak": round(100 * value / peak, 2),
-            "roofline": {"bound": "hbm",
-                         "kernel": main_kernel + ("+pa_cascade_merge_kernel" if shared else
-                                                  "+pa_merge_kernel" if decode_launches[0] == 2 else ""),
-                         "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                         "traffic": traffic_for(cfg, main_kernel, bytes_dec / len(dec_ms)),
-                         "algorithmic_bytes_per_launch": int(bytes_dec / len(dec_ms)),
-                         "mean_launch_ms": round(dec_mean_ms, 5)},
-            "clocks": clk,
-            "gpu_launches": launches,
-            "e2e": e2e,
-            "cpu_baseline": cpu,
-            "kv_memory": kv_memory,
-        }
-        print(json.dumps(line))
-    if dist is not None:
-        dist.destroy_process_group()
+    pool_gb = round(2 * w.num_blocks * cfg.block_bytes / 1e9, 3)
+    res = {
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": round(t_max * 1e3 / steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "kv_dtype": cfg.dtype, "num_seqs": w.num_seqs,
+                   "num_heads": cfg.num_heads, "num_kv_heads": cfg.num_kv_heads,
+                   "head_dim": cfg.head_dim, "block_size": cfg.block_size,
+                   "partition_size": P, "decode_launches_per_step": decode_launches[0],
+                   "engine": engine_used,
+                   "path": "shared prefix" if shared else (
+                       "split-context + merge" if decode_launches[0] == 2 else "single pass"),
+                   "pool_gb": pool_gb,
+                   "parallelism": f"replicas x{world} (sequences sharded, no collective)",
+                   "l2": "flushed (256 MiB read) before every timed step, outside the events",
+                   "block_placement": "contiguous" if args.identity_tables and name == args.config
+                   else "random",
+                   "timed_steps": f"steps {warmup}..{warmup + steps - 1} of the workload"},
+        # shared paths: the host planner's time for each step counts too
+        "seq_steps_per_s": round(seqs_all / (t_max + max_over_ranks(dist, plan_s)), 1),
+        "step_ms": _spread(step_ms),
+        "decode_ms": _spread(dec_ms),
+        "unflushed": unflushed,
+        "pct_of_peak": round(100 * value / peak, 2),
+        "roofline": {"bound": "hbm",
+                     "kernel": main_kernel + ("+pa_cascade_merge_kernel" if shared else
+                                              "+pa_merge_kernel" if decode_launches[0] == 2 else ""),
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": traffic_for(cfg, main_kernel, bytes_dec / len(dec_ms)),
+                     "algorithmic_bytes_per_launch": int(bytes_dec / len(dec_ms)),
+                     "mean_launch_ms": round(dec_mean_ms, 5)},
+        "clocks": clk,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "host_e2e": host,
+        "cpu_baseline": cpu,
+        "kv_memory": kv_memory,
+    }
+    if shared:
+        res["config"]["planner_ms_per_step"] = round(plan_s * 1e3 / steps, 4)
+    del state, steps_dev, flush
+    gc.collect()
+    torch.cuda.empty_cache()
+    return res
+
+
+def _step_bytes(cfg, inp, num_seqs, out_bytes, plan, P, launches):
+    """Algorithmic bytes of one step (attention, scatter, copies)."""
+    if plan is not None:
+        expected = plan.host[8:8 + num_seqs]
+        return algorithmic_bytes(cfg, inp, num_seqs, out_bytes=out_bytes, partials=expected)
+    return algorithmic_bytes(cfg, inp, num_seqs, split_partition=_split_partition(P, 0, launches),
+                             out_bytes=out_bytes)
 
 
 def _decode(pkv, state, s, q, bt, cl, plan_dev, P):
@@ -514,6 +610,225 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
     return {"value": round(bytes_step / (total_ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d / n), "d2h_bytes_per_step": int(d2h / n),
             "ms_per_step": round(total_ms / n, 5), "h2d_copies_per_step": 1}
+
+
+# ----------------------------------------------------- wall-clock serving loop
+HOST_E2E_STEPS = 20
+
+
+def _host_cpu():
+    """Host core model and count, for the wall-clock figures."""
+    import platform
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k = line.split(":")[0].strip().lower()
+                if k in ("model name", "cpu part") and not model:
+                    model = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    parts = {"0xd4f": "Neoverse-V2", "0xd40": "Neoverse-V1", "0xd0c": "Neoverse-N1"}
+    return {"machine": platform.machine(), "cores": os.cpu_count(),
+            "model": parts.get(model.lower(), model)}
+
+
+class _Staging:
+    """A pinned host buffer and its device twin for one step's small inputs
+    (tables, lengths, slots, copy pairs, plan), packed 256-byte aligned so
+    that they cross in one copy."""
+
+    def __init__(self, nbytes, dev):
+        self.host = torch.empty(nbytes, dtype=torch.uint8)
+        if torch.cuda.is_available():
+            self.host = self.host.pin_memory()
+        self.hnp = self.host.numpy()
+        self.dev = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def pack(self, arrays):
+        off, views = 0, {}
+        for name, a in arrays:
+            a = np.ascontiguousarray(a)
+            n = a.nbytes
+            if off + n > self.hnp.size:
+                raise ValueError("staging buffer too small")
+            self.hnp[off:off + n] = a.reshape(-1).view(np.uint8)
+            views[name] = (off, a.shape, a.dtype, n)
+            off += -(-n // _PACK_ALIGN) * _PACK_ALIGN
+        return off, views
+
+    def device_views(self, views):
+        tdt = {np.dtype(np.int32): torch.int32, np.dtype(np.int64): torch.int64}
+        return {k: self.dev[o:o + n].view(tdt[dt]).view(shape) for k, (o, shape, dt, n) in views.items()}
+
+
+def run_host_e2e(cfg, w, state, shared, P, engine, flush, seed, steps, warmup):
+    """A serving loop's decode steps through the public API, timed by the
+    host's wall clock (time.perf_counter) with no GPU pre-roll: each step's
+    block bookkeeping on the product's block pool (continuous batching: the
+    finished sequences' release and the new requests' prompt blocks; then
+    every sequence's next slot and the copy-on-write pairs, DecodeBatch.step
+    -> pkv_block_pool_append_slots), the shared-prefix planner for the shared
+    paths, packing the step's tables, lengths, slots, pairs and plan into one
+    pinned buffer, its host-to-device copy and those of q and the new K/V
+    (prepared beforehand: in a model they come from the layers before), the
+    library calls (copy_blocks, reshape_and_cache, decode), the copy of the
+    output back to pinned memory and a stream synchronise.  The batch has
+    the workload's shapes (lengths, prompts shared or forked as the workload
+    shares them), but its blocks are the ones the pool hands out: their
+    K/V is written by a prefill scatter before the timed steps."""
+    import paged_kv_cache_311_gb300 as pkv
+    from paged_kv_cache_311_gb300.batch import DecodeBatch
+    from workloads.gen import StepInputs
+    dev = state.device
+    bs, B, Hk, D, H = cfg.block_size, w.num_seqs, cfg.num_kv_heads, cfg.head_dim, cfg.num_heads
+    dt = state.k_cache.dtype
+    rng = np.random.default_rng(seed + 77)
+    total = warmup + steps
+    n_rep = int(round(cfg.replace_fraction * B)) if cfg.kind == "continuous" else 0
+    longest = int(max(int(np.max(w.init_lens)), cfg.new_len_hi if n_rep else 0)) + total + bs
+    MB = -(-longest // bs)
+    pool = pkv.BlockPool(w.num_blocks, bs)
+    batch = DecodeBatch(pool, B, MB)
+
+    # the batch's requests, shaped as the workload's
+    prefill = []
+    if cfg.kind == "shared_prefix":
+        S = cfg.samples_per_prompt
+        for p, lp in enumerate(w.prompt_lens):
+            prefill.append(batch.add_prompt(p * S, rng.integers(0, 32000, int(lp)))[0])
+            for k in range(1, S):
+                batch.fork(p * S, p * S + k)
+    elif cfg.kind == "system_prompt":
+        sys_toks = [rng.integers(0, 32000, int(lp)) for lp in w.prompt_lens]
+        for i in range(B):
+            toks = np.concatenate([sys_toks[int(w.prompt_of[i])],
+                                   rng.integers(0, 32000, int(w.own_lens[i]))])
+            prefill.append(batch.add_prompt(i, toks)[0])
+            batch.commit(i, toks)
+    else:
+        for i in range(B):
+            prefill.append(batch.add_prompt(i, rng.integers(0, 32000, int(w.init_lens[i])))[0])
+    pre = np.concatenate(prefill)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed + 78)
+    chunk = max(1, (64 << 20) // (Hk * D * 4))
+    for c in range(0, pre.size, chunk):
+        sl = torch.from_numpy(pre[c:c + chunk]).to(dev)
+        k = torch.randn((sl.numel(), Hk, D), generator=gen, device=dev).to(dt)
+        v = torch.randn((sl.numel(), Hk, D), generator=gen, device=dev).to(dt)
+        pkv.reshape_and_cache(k, v, state.k_cache, state.v_cache, sl, device_status=state.status)
+    torch.cuda.synchronize()
+
+    # per step: the replaced rows and their prompts (continuous batching)
+    plans = []
+    for _ in range(total):
+        rows = rng.choice(B, size=n_rep, replace=False) if n_rep else []
+        plans.append([(int(r), rng.integers(0, 32000, int(rng.integers(cfg.new_len_lo,
+                                                                          cfg.new_len_hi + 1))))
+                      for r in rows])
+    t_max = B + n_rep * (cfg.new_len_hi if n_rep else 0)
+    hq = _normal_pinned((B, H, D), dt, gen)
+    hk = _normal_pinned((t_max, Hk, D), dt, gen)
+    hv = _normal_pinned((t_max, Hk, D), dt, gen)
+    dq = torch.empty_like(hq, device=dev)
+    dk = torch.empty_like(hk, device=dev)
+    dv = torch.empty_like(hv, device=dev)
+    out_host = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
+    meta_bytes = B * MB * 4 + B * 4 + t_max * 8 + B * 16 + 8 * _PACK_ALIGN
+    if shared:
+        meta_bytes += 4 * int(pkv.load_library().pkv_shared_plan_max_ints(
+            B, H, Hk, longest, 0))
+    stage = _Staging(meta_bytes, dev)
+    stream = torch.cuda.current_stream()
+    ws = state.workspace
+    pkv.set_decode_engine(engine)
+
+    wall, book, plan_t, bytes_ = [], [], [], []
+    h2d = d2h = 0
+    gc.collect()
+    gc.disable()
+    for i in range(total):
+        _flush_l2(flush)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        pre_slots = []
+        for row, toks in plans[i]:
+            batch.release(row)
+            pre_slots.append(batch.add_prompt(row, toks)[0])
+        dec_slots, pairs = batch.step(B)
+        slots = np.concatenate(pre_slots + [dec_slots]) if pre_slots else dec_slots
+        tables, lens = batch.tables[:B], batch.lens[:B]
+        max_len = int(lens.max())
+        t1 = time.perf_counter()
+        plan = None
+        arrays = [("bt", tables), ("cl", lens), ("slots", slots)]
+        if pairs.shape[0]:
+            arrays.append(("pairs", pairs))
+        if shared:
+            plan = pkv.plan_shared_prefix(tables, lens, H, Hk, D, bs, max_len, 0)
+            arrays.append(("plan", plan.host))
+        t2 = time.perf_counter()
+        nbytes, views = stage.pack(arrays)
+        T = slots.size
+        stage.dev[:nbytes].copy_(stage.host[:nbytes], non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        dk[:T].copy_(hk[:T], non_blocking=True)
+        dv[:T].copy_(hv[:T], non_blocking=True)
+        d = stage.device_views(views)
+        need = (plan.workspace_bytes if shared else
+                pkv.paged_attention_workspace_bytes(B, H, max_len, D, P))
+        if need and (ws is None or ws.numel() < need):
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        if pairs.shape[0]:
+            pkv.copy_blocks([state.k_cache], [state.v_cache], d["pairs"], device_status=state.status)
+        pkv.reshape_and_cache(dk[:T], dv[:T], state.k_cache, state.v_cache, d["slots"],
+                              device_status=state.status)
+        if shared:
+            pkv.paged_attention_decode_shared(state.out, dq, state.k_cache, state.v_cache, d["bt"],
+                                              d["cl"], cfg.softmax_scale, plan, d["plan"],
+                                              max_context_len=max_len, workspace=ws,
+                                              device_status=state.status)
+        else:
+            pkv.paged_attention_decode(state.out, dq, state.k_cache, state.v_cache, d["bt"], d["cl"],
+                                       cfg.softmax_scale, max_context_len=max_len,
+                                       partition_size=P, workspace=ws, device_status=state.status)
+        launches = pkv.last_decode_launches()
+        out_host.copy_(state.out, non_blocking=True)
+        stream.synchronize()
+        t3 = time.perf_counter()
+        if i >= warmup:
+            wall.append(t3 - t0)
+            book.append(t1 - t0)
+            plan_t.append(t2 - t1)
+            inp = StepInputs(step=i, slot_mapping=slots, token_seq=np.zeros(T, np.int64),
+                             token_pos=np.zeros(T, np.int64), context_lens=lens.copy(),
+                             block_tables=tables.copy(), cow_pairs=pairs, max_context_len=max_len)
+            bytes_.append((inp, plan, launches))
+            h2d += nbytes + dq.numel() * dq.element_size() + 2 * T * Hk * D * dk.element_size()
+            d2h += out_host.numel() * out_host.element_size()
+    gc.enable()
+    pkv.set_decode_engine("auto")
+    if state.status.item() != 0:
+        raise RuntimeError(f"{cfg.name}: device status {state.status.item()} in the host_e2e steps")
+    out_bytes = state.out.element_size()
+    nb = sum(_step_bytes(cfg, inp, B, out_bytes, plan, P, n)["total"] for inp, plan, n in bytes_)
+    tot = sum(wall)
+    n = len(wall)
+    return {"value": round(nb / tot / 1e9, 2), "unit": "GB/s", "steps": n, "warmup": warmup,
+            "ms_per_step": round(1e3 * tot / n, 4), "seq_steps_per_s": round(B * n / tot, 1),
+            "h2d_bytes_per_step": int(h2d / n), "d2h_bytes_per_step": int(d2h / n),
+            "host_ms": {"bookkeeping_median": round(1e3 * statistics.median(book), 4),
+                        "planner_median": round(1e3 * statistics.median(plan_t), 4),
+                        "step_median": round(1e3 * statistics.median(wall), 4)},
+            "host": _host_cpu(),
+            "timed": "wall clock per step: pool bookkeeping, planner, packing, copies in and out, "
+                     "library calls, stream synchronise; no GPU pre-roll, L2 flushed before each"}
+
+
+def _normal_pinned(shape, dt, gen):
+    x = torch.randn(shape, generator=gen, device=gen.device).to(dt)
+    return x.cpu().pin_memory()
 
 
 # ------------------------------------------------------------- CPU oracle

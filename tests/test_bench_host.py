@@ -76,3 +76,22 @@ def test_host_step_op_runs_without_a_gpu():
     assert line["op"] == "host_step" and line["config"]["workload"] == "shared_prefix_bf16"
     for k in ("pool_append_slots_us", "pool_per_sequence_us", "plan_shared_prefix_us"):
         assert line[k] > 0
+
+
+def test_staging_packs_a_step_and_views_it_back():
+    """The wall-clock loop's per-step staging: tables, lengths, slots, pairs
+    and plan packed 256-byte aligned come back bit for bit as typed views."""
+    import torch
+    rng = np.random.default_rng(3)
+    st = bench._Staging(1 << 16, torch.device("cpu"))
+    arrays = [("bt", rng.integers(-1, 999, (5, 7)).astype(np.int32)),
+              ("cl", rng.integers(0, 99, 5).astype(np.int32)),
+              ("slots", rng.integers(0, 1 << 40, 9).astype(np.int64)),
+              ("pairs", rng.integers(0, 99, (2, 2)).astype(np.int64)),
+              ("plan", np.arange(13, dtype=np.int32))]
+    n, views = st.pack(arrays)
+    assert n % 256 == 0 and all(o % 256 == 0 for o, *_ in views.values())
+    st.dev[:n].copy_(st.host[:n])
+    back = st.device_views(views)
+    for name, a in arrays:
+        assert np.array_equal(back[name].numpy(), a)

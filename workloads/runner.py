@@ -34,6 +34,7 @@ class DeviceStep:
     host: StepInputs
     plan: object = None                     # SharedPrefixPlan (shared-prefix workloads)
     plan_device: Optional[torch.Tensor] = None
+    plan_seconds: float = 0.0               # host time the planner took for this step
 
 
 class DeviceState:
@@ -67,11 +68,16 @@ class DeviceState:
         if inp.cow_pairs.shape[0]:
             pairs = torch.as_tensor(inp.cow_pairs, dtype=torch.int64).to(dev)
         plan = plan_dev = None
+        plan_s = 0.0
         if shared:
+            import time
+
             import paged_kv_cache_311_gb300 as pkv
+            t0 = time.perf_counter()
             plan = pkv.plan_shared_prefix(inp.block_tables, inp.context_lens, cfg.num_heads,
                                           cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
                                           inp.max_context_len, partition_size)
+            plan_s = time.perf_counter() - t0
             plan_dev = plan.to(dev)
         return DeviceStep(
             step=inp.step, q=q.to(dev), key=k.to(dev), value=v.to(dev),
@@ -79,7 +85,7 @@ class DeviceState:
             block_tables=torch.as_tensor(inp.block_tables).to(dev),
             context_lens=torch.as_tensor(inp.context_lens).to(dev),
             cow_pairs=pairs, max_context_len=inp.max_context_len, host=inp,
-            plan=plan, plan_device=plan_dev)
+            plan=plan, plan_device=plan_dev, plan_seconds=plan_s)
 
     def ensure_workspace(self, max_context_len: int, partition_size: int,
                          plan=None) -> None:
