@@ -261,8 +261,8 @@ def measure(args, name, block_size, steps, warmup, dist, rank, world, dev, cpu_s
     shared = cfg.kind in ("shared_prefix", "system_prompt") and not no_shared
     if shared and (args.partition_size < 0 or name != args.config):
         P = 0   # the shared-prefix planner's own default partition
+    pkv.set_decode_engine(engine)   # before planning: the automatic plan follows the kernel
     steps_dev = [state.to_device(inp, shared=shared, partition_size=P) for inp in host_inputs]
-    pkv.set_decode_engine(engine)
     for s in steps_dev:
         state.ensure_workspace(s.max_context_len, P, s.plan)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

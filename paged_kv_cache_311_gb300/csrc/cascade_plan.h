@@ -62,4 +62,12 @@ constexpr int item_ids_offset(int group) { return item_segments_offset() + kSegI
 constexpr int item_ints(int group) { return item_ids_offset(group) + kTableCap; }
 
 }  // namespace plan
+
+// How the shared-prefix kernel that the current engine choice runs takes a
+// plan (defined beside that choice, in pkv_abi.cu): resident CTAs per SM
+// (3 for the warp-level kernel, 1 for the tcgen05 kernel) and what a CTA's
+// switch from one item to the next costs in 16-token tiles streamed.
+int shared_ctas_per_sm(int head_dim);
+int shared_item_cost_tiles(int head_dim);
+
 }  // namespace pkv

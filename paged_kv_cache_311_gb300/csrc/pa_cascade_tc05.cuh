@@ -1,691 +1,855 @@
 // pa_cascade_tc05.cuh -- shared-prefix (cascade) decode on the 5th-generation
-// tensor cores (tcgen05).
+// tensor cores (tcgen05), one warp-specialised CTA per SM.
 //
-// Same plan, items, device checks and partials as pa_cascade_kernel
+// Same plan, items, device checks, outputs and partials as pa_cascade_kernel
 // (cascade_plan.h; PagedAttention: Efficient LLM Serving with vLLM,
-// "Advanced Features", KV-Cache Sharing), with the attention products moved
-// from per-warp mma.sync to tcgen05.mma issued by one thread, accumulators in
-// tensor memory (TMEM):
-//   * A CTA-wide ring of four 32-token stages (two 16-token tiles each): per
-//     stage K and V, each as two planes [64-element chunk][32 rows][128 B]
-//     with 128-byte swizzling, written by one TMA load per block box and
-//     chunk.
-//   * S^T = K q^T: M = 64 tokens (the stage's 32 and 32 ignored rows), N = 8
-//     x the item's n-tiles of query rows, K = head_dim, into TMEM columns
-//     [0, 24); row r of S^T sits in TMEM lane 32 (r / 16) + r % 16, so warps
-//     0 and 1 read the scores of their tile's 16 tokens from their own lane
-//     quarters.
-//   * Online softmax in the log2 domain against a CTA-wide reference maximum
-//     per query row, kept while every new score stays within kSlack of it;
-//     otherwise the CTA moves to the exact running maxima and rescales O in
-//     TMEM.  P (<= 2^kSlack) is split into a 16-bit high part and remainder,
-//     written over the stage's K (no longer needed) as [query row][token].
-//   * O^T += V^T P^T: M = 128 dims (V read MN-major), N = query rows, K = 16
-//     tokens per instruction, high and low parts into the same accumulator
-//     (TMEM columns [32, 56)); its completion frees the stage for the TMA.
-//   * End of an item: O^T read from TMEM (thread = one dim, registers = rows),
-//     row sums reduced across the tokens' lanes, output or partial written.
+// "Advanced Features", KV-Cache Sharing): for every row of an item (query
+// head h of member m), the softmax-weighted sum of V over the item's tokens,
+// written as the output when the item holds the sequence entirely, else as
+// an unnormalised partial (max, sum, acc) for pa_cascade_merge_kernel.
+//
+// Work: the plan's (list, kv head) units are dealt round-robin to one CTA
+// per SM; a CTA walks its units' items one after the other.  Each item's
+// 16-token tiles are grouped into stages of 128 tokens (8 tiles; an item's
+// last stage may be partly empty).  Roles, one CTA:
+//   * loader warp: copies the next item's record into a two-slot record
+//     ring, then stages its query rows (the B operand of S^T), then runs the
+//     device checks (block ids in range and equal to the device tables,
+//     lengths equal to the plan's), each step released on its own barrier;
+//   * producer warp: TMA loads of each stage's K and V (one box per block
+//     piece and 64-element chunk plane, the 32 lanes issuing in parallel)
+//     into a three-stage ring;
+//   * MMA thread: S^T = K q^T (M = 128 tokens, N = 32 query-row columns,
+//     K = 128 dims) into one of two TMEM score buffers, then O^T += V^T P^T
+//     for the stage before (M = 128 dims, N = 32, K = the stage's valid
+//     16-token tiles) into one TMEM accumulator; each completion is
+//     signalled with tcgen05.commit on a per-stage mbarrier;
+//   * twelve softmax warps, four per group of 8 query rows (one per TMEM
+//     lane quarter): thread = one token of the stage, for its group's rows.  Online softmax in the log2 domain against a reference maximum
+//     per query row shared by the CTA, kept while every new score stays
+//     within 2^8 of it (a per-stage OR over the four warps); otherwise the
+//     exact stage maxima (warp shuffles, then shared memory) move the
+//     references and O is rescaled in TMEM.  P = hi + lo 16-bit parts, so the
+//     products keep fp32-level accuracy, written over the stage's K (used
+//     by then) as [token][query rows], the B operand read MN-major.  At the
+//     end of an item the same warps read O^T (thread = one dim) and write
+//     the rows' outputs or partials.
+// Every hand-off is an mbarrier phase (K, V full; scores full / free; P full;
+// stage free; record, q rows, checks full; record free), so no role waits for another's slowest
+// warp, and the next item's loads stream while an item's epilogue runs.
+// Every wait is bounded (PKV_DEV_TIMEOUT); the softmax warps take their
+// decisions together through a named-barrier OR.
 #pragma once
 
 #include "pa_cascade.cuh"
 
 namespace pkv {
 
-// fp32 -> the cache's 16-bit type, round to nearest even
-template <typename T> __device__ __forceinline__ T to_elem(float v);
-template <> __device__ __forceinline__ __nv_bfloat16 to_elem<__nv_bfloat16>(float v)
-{
-    return __float2bfloat16_rn(v);
-}
-template <> __device__ __forceinline__ __half to_elem<__half>(float v) { return __float2half_rn(v); }
-
 template <typename T, int D, int BS, int G>
 struct Tc05Cfg {
     static_assert(D == 128, "the tcgen05 cascade kernel takes head_dim 128");
-    static constexpr int NW = 4;
     static constexpr int TILE = plan::kTileTokens;   // 16 tokens
-    static constexpr int TOK = 2 * TILE;             // tokens per stage
-    static constexpr int GRP = 8;                    // tokens per group: one 8-row swizzle atom
-    static constexpr int NSLOT = 4;                  // stages in the ring
-    static constexpr int CHUNKS = D * 2 / 128;       // 64-element chunks per row
-    static constexpr int ATOM = GRP * 128;           // one chunk of one group's rows
-    // a group's period: [K chunk 0][K chunk 1][V chunk 0][V chunk 1]
-    static constexpr int PERIOD = 4 * ATOM;
-    static constexpr int V_OFF = 2 * ATOM;
-    static constexpr int SLOT = (TOK / GRP) * PERIOD;
-    static constexpr int BOX_ROWS = GRP;
-    static constexpr int RQ = plan::kMaxRows;        // query rows of an item
-    static constexpr int RPL = RQ / 4;               // query rows per lane (four lanes per token)
-    static constexpr int QPLANE = RQ * 128;
-    static constexpr int TM_COLS = 64;               // S^T at column 0, O^T at column 32
+    static constexpr int TOK = 128;                  // tokens per stage: M of S^T
+    static constexpr int TPS = TOK / TILE;           // tiles per stage
+    static constexpr int NSTAGE = 3;
+    static constexpr int PLANE = TOK * 128;          // one 64-element chunk of a stage's rows
+    static constexpr int KV_BYTES = 2 * PLANE;       // K (or V) of one stage
+    static constexpr int STAGE = 2 * KV_BYTES;       // K then V
+    static constexpr int RQ = plan::kMaxRows;        // query rows of an item (24)
+    static constexpr int N = 32;                     // MMA N: the rows padded to 32
+    static constexpr int QPLANE = N * 128;
+    static constexpr int QBUF = 2 * QPLANE;          // q rows of one item: [chunk][32 rows][128 B]
+    static constexpr int BOX_ROWS = BS < TILE ? BS : TILE;
+    static constexpr int BOX_BYTES = BOX_ROWS * 128; // one box: BOX_ROWS rows of one chunk
     static constexpr int MAXSEG = plan::max_segments(G);
     static constexpr int ITEM_INTS = plan::item_ints(G);
     static constexpr int IDS = plan::item_ids_offset(G);
     static constexpr int SEGS = plan::item_segments_offset();
     static constexpr int TABLE_CAP = plan::kTableCap;
-    // ring | q rows | barriers (full[NSLOT], empty[NSLOT], scores) | TMEM
-    // address, flag, stages issued | per-warp row reductions [NW][RQ], the
-    // rows' reference maxima and rescale factors | item copy, segment /
-    // member / row flags | the list's next item
-    static constexpr int OFF_RING = 0;
-    static constexpr int OFF_Q = NSLOT * SLOT;
-    static constexpr int OFF_BAR = OFF_Q + CHUNKS * QPLANE;
-    static constexpr int OFF_TMEM = OFF_BAR + (2 * NSLOT + 1) * 8;
-    static constexpr int OFF_FLAG = OFF_TMEM + 8;
-    static constexpr int OFF_RED = OFF_FLAG + 8;
-    static constexpr int OFF_ITEM = (OFF_RED + (NW + 2) * RQ * 4 + 15) / 16 * 16;
-    static constexpr int EXTRA_INTS = ITEM_INTS + MAXSEG + RQ + 2;
-    static constexpr int OFF_NEXT = (OFF_ITEM + EXTRA_INTS * 4 + 15) / 16 * 16;
-    static constexpr bool PREFETCH = 3 * (OFF_NEXT + ITEM_INTS * 4 + 2048) <= 228 * 1024;
-    static constexpr int SMEM_USED = OFF_NEXT + (PREFETCH ? ITEM_INTS * 4 : 0);
+    // an item's slot of the record ring: what the loader worked out (the M_*
+    // ints), the record, then per-segment bad flags and the members' expected
+    // partial counts
+    enum { M_NST = 0, M_END, M_FAILED, M_ZERO, M_BADROWS, M_KVH, M_FINAL, M_HEAD };
+    static constexpr int META_INTS = M_HEAD + ITEM_INTS + MAXSEG + RQ;
+    static constexpr int META_BYTES = (META_INTS * 4 + 15) / 16 * 16;
+    static constexpr int OFF_Q = NSTAGE * STAGE;
+    static constexpr int OFF_META = OFF_Q + 2 * QBUF;
+    static constexpr int OFF_RED = OFF_META + 2 * META_BYTES;   // [2][4 warps][32 rows] floats
+    static constexpr int OFF_BAR = OFF_RED + 2 * 4 * N * 4;
+    enum {
+        B_KFULL = 0,
+        B_VFULL = B_KFULL + NSTAGE,
+        B_SFULL = B_VFULL + NSTAGE,
+        B_SFREE = B_SFULL + 2,
+        B_PFULL = B_SFREE + 2,
+        B_STFREE = B_PFULL + NSTAGE,
+        B_RECFULL = B_STFREE + NSTAGE,
+        B_QFULL = B_RECFULL + 2,
+        B_METAFULL = B_QFULL + 2,
+        B_RECEMPTY = B_METAFULL + 2,
+        B_MMADONE = B_RECEMPTY + 2,
+        B_DONE = B_MMADONE + 1,
+        NBAR = B_DONE + 1
+    };
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM address, abort flag
+    static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
-    static_assert(3 * (SMEM_BYTES + 1024) <= 228 * 1024, "three CTAs per SM");
-    static_assert(3 * TM_COLS <= 512, "TMEM of three CTAs per SM");
-    static_assert(SLOT % 1024 == 0 && OFF_Q % 1024 == 0 && QPLANE % 1024 == 0 && ATOM == 1024,
+    // softmax warps: three row groups (query rows 8j .. 8j + 7) of four warps,
+    // one per TMEM lane quarter
+    static constexpr int NRG = RQ / 8;
+    static constexpr int SWARPS = 4 * NRG;
+    static constexpr int WARPS = 3 + SWARPS;              // producer, MMA, loader, softmax
+    static constexpr int THREADS = WARPS * 32;
+    static constexpr int TM_COLS = 128;                   // S^T at 0 and 32, O^T at 64
+    static constexpr int kRecEmptyArrivals = 2 + SWARPS;  // producer, MMA commit, softmax warps
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(PLANE % 1024 == 0 && STAGE % 1024 == 0 && OFF_Q % 1024 == 0 && QPLANE % 1024 == 0,
                   "128-byte swizzle atoms are 1024-byte aligned");
-    // S^T's A operand spans 16 atoms from a slot's chunk-1 start: the last
-    // one reads the 1 KiB after the slot (the next slot, or the q rows); an
-    // M = 128 product's N rounded up to 32 reads q rows 24-31 past the staged
-    // ones (in shared memory; their columns are never read)
-    static_assert(OFF_Q >= SLOT && CHUNKS == 2 && TOK / GRP == NW, "layout");
-    static_assert(plan::kNT * 8 == RQ && RQ % 4 == 0 && (RPL % 2) == 0, "n-tiles");
+    static_assert(BOX_ROWS % 8 == 0, "boxes start on 8-row atoms");
+    static_assert(RQ <= N && RQ % 8 == 0 && RQ <= 32, "query rows");
 };
 
+// Named barrier of the twelve softmax warps (id 1, 384 threads): a sync, and
+// an OR of one predicate over them.
+__device__ __forceinline__ void softmax_sync()
+{
+    __syncwarp();
+    asm volatile("bar.sync 1, 384;" ::: "memory");
+}
+__device__ __forceinline__ bool softmax_any(bool v)
+{
+    uint32_t r;
+    __syncwarp();
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+                 "bar.red.or.pred p, 1, 384, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
+
+// 2^x, the special-function unit's approximation (relative error far below
+// the 2^-16 of the P split it feeds)
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(128, 3)
+__global__ void __launch_bounds__(Tc05Cfg<T, D, BS, G>::THREADS, 1)
 pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv, const int32_t *plan_buf)
+                       const __grid_constant__ CUtensorMap tmv, const int32_t *plan_buf, int num_lists)
 {
     using CC = Tc05Cfg<T, D, BS, G>;
-    constexpr int NW = CC::NW, TILE = CC::TILE, NSLOT = CC::NSLOT, RQ = CC::RQ, NT = plan::kNT;
+    constexpr int NSTAGE = CC::NSTAGE, RQ = CC::RQ, TILE = CC::TILE, TPS = CC::TPS;
     constexpr float kSlack = 8.f;
-    constexpr int kIssuer = 64;     // lane 0 of warp 2: issues the MMAs
-    constexpr int kProducer = 96;   // lane 0 of warp 3: issues the TMA loads
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = aligned_smem(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kvh = blockIdx.x;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + CC::OFF_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + CC::OFF_MISC);
+    uint32_t *abort_flag = tslot + 1;
 
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + CC::OFF_BAR);
-    uint64_t *empty = full + NSLOT;
-    uint64_t *sbar = empty + NSLOT;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + CC::OFF_TMEM);
-    uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + CC::OFF_FLAG);
-    int32_t *n_issued = reinterpret_cast<int32_t *>(cta_flag + 1);   // stages of the item issued
-    float *red = reinterpret_cast<float *>(smem + CC::OFF_RED);   // [NW][RQ]
-    float *mref = red + NW * RQ;  // the rows' reference maxima (log2 domain), CTA-uniform
-    float *alph = mref + RQ;      // rescale factors of a moved reference
-    int32_t *it = reinterpret_cast<int32_t *>(smem + CC::OFF_ITEM);
-    int32_t *segbad = it + CC::ITEM_INTS;
-    int32_t *exp_s = segbad + CC::MAXSEG;
-    uint32_t *badrows = reinterpret_cast<uint32_t *>(exp_s + RQ);
-    uint32_t *lenbad = badrows + 1;
-    int32_t *next_buf = reinterpret_cast<int32_t *>(smem + CC::OFF_NEXT);
-    const uint32_t qb = smem_u32(smem + CC::OFF_Q);
-
-    const int B = p.num_seqs, slots = p.num_partitions;
+    const int B = p.num_seqs, slots = p.num_partitions, Hk = p.num_kv_heads;
     const int32_t *expected = plan_buf + plan::kHeader;
     const int32_t *plan_lens = expected + B;
     const int32_t *items = plan_buf + plan::kHeader + 2 * B;
 
     if (tid == 0) {
-        for (int i = 0; i < 2 * NSLOT + 1; ++i)
-            mbar_init(&full[i], 1);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&bars[CC::B_KFULL + i], 1);
+            mbar_init(&bars[CC::B_VFULL + i], 1);
+            mbar_init(&bars[CC::B_PFULL + i], CC::SWARPS);
+            mbar_init(&bars[CC::B_STFREE + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[CC::B_SFULL + i], 1);
+            mbar_init(&bars[CC::B_SFREE + i], CC::SWARPS);
+            mbar_init(&bars[CC::B_RECFULL + i], 1);
+            mbar_init(&bars[CC::B_QFULL + i], 1);
+            mbar_init(&bars[CC::B_METAFULL + i], 1);
+            mbar_init(&bars[CC::B_RECEMPTY + i], CC::kRecEmptyArrivals);
+        }
+        mbar_init(&bars[CC::B_MMADONE], 1);
+        mbar_init(&bars[CC::B_DONE], CC::WARPS);
         fence_mbar_init();
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
-        *cta_flag = 0;
+        *abort_flag = 0;
     }
-    if (warp == 0)
+    if (warp == 1)
         tc05::alloc(tslot, CC::TM_COLS);
     tc05::fence_before_sync();
     __syncthreads();
     tc05::fence_after_sync();
-    const uint32_t tS = *tslot, tO = tS + 32;
-    const uint32_t tlane = (uint32_t)(32 * warp) << 16;   // this warp's lane quarter
+    const uint32_t tS = *tslot, tO = tS + 64;
     // launched as a programmatic dependent of the previous kernel: nothing it
-    // may write is read before this wait; only then may the merge kernel
-    // behind this grid start (it reads the plan before its own wait)
+    // may write is read before this wait; then the merge kernel behind this
+    // grid may start (it reads the plan before its own wait)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    int g = 0;   // stages this CTA has started, over all its items
-    bool fetched = false;
-    for (int item = blockIdx.y; item >= 0 && item < p.num_items;) {
-        if (tid == 0)
-            *lenbad = 0;
-        if (tid < CC::MAXSEG)
-            segbad[tid] = 0;
-        if (fetched) {
-            cp_async_wait_all();
-            __syncthreads();
-            for (int i = tid; i < CC::ITEM_INTS; i += NW * 32)
-                it[i] = next_buf[i];
-        } else {
-            const int32_t *src = items + (int64_t)item * CC::ITEM_INTS;
-            constexpr int PER = (CC::ITEM_INTS + NW * 32 - 1) / (NW * 32);
-            int32_t v[PER];
-#pragma unroll
-            for (int u = 0; u < PER; ++u) {
-                const int i = tid + u * NW * 32;
-                v[u] = i < CC::ITEM_INTS ? src[i] : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < PER; ++u) {
-                const int i = tid + u * NW * 32;
-                if (i < CC::ITEM_INTS)
-                    it[i] = v[u];
-            }
-        }
-        __syncthreads();
+    auto meta = [&](int b) { return reinterpret_cast<int32_t *>(smem + CC::OFF_META + b * CC::META_BYTES); };
+    auto rec_of = [&](int32_t *m) { return m + CC::M_HEAD; };
+    auto segbad_of = [&](int32_t *m) { return m + CC::M_HEAD + CC::ITEM_INTS; };
+    auto exp_of = [&](int32_t *m) { return m + CC::M_HEAD + CC::ITEM_INTS + CC::MAXSEG; };
+    auto aborted = [&]() { return *reinterpret_cast<volatile uint32_t *>(abort_flag) != 0; };
+    // a bounded wait; giving up stops the CTA's work (every role sees the flag)
+    auto wait = [&](int bar, uint32_t parity) {
+        if (mbar_wait_bounded(&bars[bar], parity))
+            return true;
+        if (atomicOr(abort_flag, 1u) == 0)
+            report(p.status, PKV_DEV_TIMEOUT);
+        return false;
+    };
 
-        const int seq0 = it[plan::I_SEQ0], nrows = it[plan::I_NROWS], slot = it[plan::I_SLOT];
-        const int nseg = it[plan::I_NSEG], total = it[plan::I_TILES];
-        const int next = it[plan::I_NEXT] > item && it[plan::I_NEXT] < p.num_items ? it[plan::I_NEXT] : -1;
-        fetched = CC::PREFETCH && next >= 0;
-        if (fetched) {
-            const int32_t *src = items + (int64_t)next * CC::ITEM_INTS;
-            for (int i = tid; i < CC::ITEM_INTS; i += NW * 32)
-                cp_async4(next_buf + i, src + i);
-        }
-        const int nmem = nrows / G;
-        const int32_t *members = it + plan::kItemHead;
-        const CtaWork w{seq0, nrows, kvh, 0, 0, slot, seq0, members};
-        if (nseg == 0) {  // empty or invalid context: zero rows, nothing to merge
-            const int L = p.context_lens[seq0];
-            if ((L < 0 || L > p.max_context_len) && tid == 0 && kvh == 0)
-                report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
-            for (int idx = tid; idx < nrows * D; idx += blockDim.x)
-                store_out(p.out, p.out_dtype, row_head(p, w, G, idx / D) * D + idx % D, 0.f);
-            __syncthreads();
-            item = next;
-            continue;
-        }
-        auto seg = [&](int k) { return it + CC::SEGS + plan::kSegInts * k; };
-        int32_t *ids = it + CC::IDS;
-        const bool dead = *reinterpret_cast<volatile uint32_t *>(cta_flag) != 0;
-        const bool invalid_item =
-            it[plan::I_IDS] > CC::TABLE_CAP || nseg > CC::MAXSEG || nrows > RQ || nrows <= 0;
-        auto seg_of = [&](int tile, int &k) {
-            while (k + 1 < nseg && seg(k + 1)[plan::S_FIRST_TILE] <= tile)
-                ++k;
-            return k;
-        };
-        const int n_st = invalid_item || dead ? 0 : (total + 1) / 2;
-        const int ntl = (nrows + 7) / 8;
-        int k_issue = 0;
-        // Stage s of the item (its tiles 2s, 2s + 1) into the ring slot of
-        // CTA stage g + s: one TMA load per block box, chunk plane and
-        // matrix.  A block id outside the pool invalidates its segment's rows
-        // (block 0 is loaded in its place).
-        auto issue = [&](int s) {
-            const int gs = g + s, sl = gs % NSLOT;
-            uint8_t *base = smem + CC::OFF_RING + sl * CC::SLOT;
-            int kk[2], t0[2], te[2];
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int tt = 2 * s + u;
-                te[u] = 0;
-                t0[u] = 0;
-                if (tt < total) {
-                    kk[u] = seg_of(tt, k_issue);
-                    const int *gg = seg(kk[u]);
-                    t0[u] = gg[plan::S_BEGIN] + (tt - gg[plan::S_FIRST_TILE]) * TILE;
-                    te[u] = min(gg[plan::S_END], t0[u] + TILE);
-                    bytes += (uint32_t)(((te[u] - t0[u] + CC::GRP - 1) / CC::GRP) * 4 * CC::ATOM);
-                }
-            }
-            mbar_arrive_expect_tx(&full[sl], bytes);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                for (int gi = 0; gi < 2; ++gi) {
-                    const int tok = t0[u] + gi * CC::GRP;
-                    if (tok >= te[u])
-                        continue;
-                    const int *gg = seg(kk[u]);
-                    int phys = ids[gg[plan::S_ID_OFF] + tok / BS - gg[plan::S_BEGIN] / BS];
-                    if (phys < 0 || (int64_t)phys >= p.num_blocks) {
-                        segbad[kk[u]] = 1;
-                        phys = 0;
-                    }
-                    uint8_t *gb = base + (2 * u + gi) * CC::PERIOD;
-#pragma unroll
-                    for (int c = 0; c < CC::CHUNKS; ++c) {
-                        tma_load_5d(gb + c * CC::ATOM, &tmk, &full[sl], 0, tok % BS, c, kvh, phys);
-                        tma_load_5d(gb + CC::V_OFF + c * CC::ATOM, &tmv, &full[sl], 0, tok % BS, c, kvh, phys);
-                    }
-                }
-            }
-        };
-        if (tid == kProducer) {
-            *n_issued = min(n_st, NSLOT - 1);
-            for (int s = 0; s < min(n_st, NSLOT - 1); ++s)
-                issue(s);
-        }
-
-        // ---- while the first stages load, one round trip of global loads:
-        // the device table entries to check against the plan's block ids,
-        // the q rows and the members' expected partial counts and lengths
-        const int vtotal = invalid_item ? 0 : it[plan::I_CHECKS];
-        int got[4], want[4], kk4[4];
-        auto load_checks = [&](int x0) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int x = x0 + u * NW * 32 + tid;
-                kk4[u] = -1;
-                got[u] = want[u] = 0;
-                if (x < vtotal) {
-                    int k = 0;
-                    while (k + 1 < nseg && seg(k + 1)[plan::S_CHECK_OFF] <= x)
-                        ++k;
-                    const int *gg = seg(k);
-                    const int nb = (k + 1 < nseg ? seg(k + 1)[plan::S_ID_OFF] : it[plan::I_IDS]) -
-                                   gg[plan::S_ID_OFF];
-                    const int local = x - gg[plan::S_CHECK_OFF];
-                    const int m = local / nb, i = local % nb;
-                    const bool shared = gg[plan::S_ROW_LO] == 0 && gg[plan::S_ROW_HI] == nrows && nmem > 1;
-                    const int sq = shared ? members[m] : gg[plan::S_TABLE_SEQ];
-                    got[u] = p.block_tables[(int64_t)sq * p.max_blocks_per_seq + gg[plan::S_BEGIN] / BS + i];
-                    want[u] = ids[gg[plan::S_ID_OFF] + i];
-                    kk4[u] = k;
-                }
-            }
-        };
-        auto fold_checks = [&]() {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (kk4[u] >= 0 && got[u] != want[u])
-                    segbad[kk4[u]] = 1;
-        };
-        // q rows as the B operand of S^T: [chunk][RQ rows][128 B], swizzled,
-        // rows >= nrows zero
-        constexpr int QPCS = D * 2 / 16;
-        constexpr int QPER = (RQ * QPCS + NW * 32 - 1) / (NW * 32);
-        uint4 qv[QPER];
-        load_checks(0);
-#pragma unroll
-        for (int u = 0; u < QPER; ++u) {
-            const int i = tid + u * NW * 32, r = i / QPCS;
-            qv[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < RQ * QPCS && r < nrows && !invalid_item)
-                qv[u] = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.q) +
-                                                        row_head(p, w, G, r) * D)[i % QPCS];
-        }
-        int m_exp = 0, m_plen = 0, m_len = 0;
-        if (tid < nmem) {
-            const int sq = members[tid];
-            m_exp = expected[sq];
-            m_plen = plan_lens[sq];
-            m_len = p.context_lens[sq];
-        }
-        fold_checks();
-#pragma unroll
-        for (int u = 0; u < QPER; ++u) {
-            const int i = tid + u * NW * 32;
-            if (i < RQ * QPCS) {
-                const int r = i / QPCS, pc = i % QPCS, c = pc / 8, q8 = pc % 8;
-                *reinterpret_cast<uint4 *>(smem + CC::OFF_Q + c * CC::QPLANE + r * 128 +
-                                           ((q8 ^ (r & 7)) << 4)) = qv[u];
-            }
-        }
-        if (tid < nmem) {
-            exp_s[tid] = m_exp;
-            if (m_plen != m_len)
-                atomicOr(lenbad, 1u << tid);
-        }
-        if (tid < RQ)
-            mref[tid] = -INFINITY;
-        for (int x0 = 4 * NW * 32; x0 < vtotal; x0 += 4 * NW * 32) {
-            load_checks(x0);
-            fold_checks();
-        }
-        fence_proxy_async_smem();   // q rows (generic stores) before the MMAs read them
-        tc05::fence_before_sync();
-        __syncthreads();
-
-        // ---- the stages.  Warps 0 and 1 run the softmax of a stage's two
-        // tiles (one token per lane); lane 0 of warp 2 issues the MMAs -- the
-        // next stage's S^T as soon as this stage's scores are in registers,
-        // this stage's O^T once its P is in shared memory; lane 0 of warp 3
-        // refills the ring.
-        float ls[CC::RPL];   // this lane's token's share of its rows' sums
-#pragma unroll
-        for (int j = 0; j < CC::RPL; ++j)
-            ls[j] = 0.f;
-        // M = 128 products take N a multiple of 16: the query rows' n-tiles
-        // rounded up to 16 or 32 columns (the extra ones are never read)
-        const int n16 = 16 * ((ntl + 1) / 2);
-        const uint32_t id_qk = tc05::idesc<T>(128, n16, false, false);
-        const uint32_t id_pv = tc05::idesc<T>(128, n16, true, true);
-        const uint64_t q_desc = tc05::sdesc(qb, 16, 1024);
-        // S^T of stage s into TMEM (the stage's K, A K-major; q rows, B K-major).
-        // A is 128 rows of 8-row atoms 1 KiB apart from a chunk's first atom:
-        // atom 4w is group w's K, so group w's 8 tokens land in TMEM lanes
-        // 32w .. 32w + 7, warp w's quarter; the other rows are ignored.
-        auto issue_qk = [&](int st) {
-            const int gs = g + st, sl = gs % NSLOT;
-            const uint64_t k_desc = tc05::sdesc(smem_u32(smem + CC::OFF_RING + sl * CC::SLOT), 16, 1024);
-            if (!mbar_wait_bounded(&full[sl], (uint32_t)((gs / NSLOT) & 1))) {
-                atomicOr(cta_flag, 2u);
-                return;
-            }
-            tc05::fence_after_sync();
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (uint32_t)((ks / 4) * CC::ATOM + (ks % 4) * 32);
-                const uint32_t qoff = (uint32_t)((ks / 4) * CC::QPLANE + (ks % 4) * 32);
-                tc05::mma(tS, k_desc + (off >> 4), q_desc + (qoff >> 4), id_qk, ks > 0);
-            }
-            tc05::commit(sbar);
-        };
-        if (tid == kIssuer && n_st > 0)
-            issue_qk(0);
-        int k_use = 0;
-        bool failed = false;
-        int s = 0;
-        for (; s < n_st; ++s) {
-            const int gs = g + s, sl = gs % NSLOT;
-            uint8_t *slot_p = smem + CC::OFF_RING + sl * CC::SLOT;
-            bool bad = !mbar_wait_bounded(sbar, (uint32_t)(gs & 1));
-            if (__syncthreads_or(bad || (*reinterpret_cast<volatile uint32_t *>(cta_flag) & 2u))) {
-                failed = true;
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        // The warp issues a stage's loads together: lane 4u + 2c + v takes
+        // tile u of the stage, 64-dim chunk plane c, K (v = 0) or V (v = 1),
+        // and issues that plane's box(es) of the tile (one thread issuing
+        // every box of a stage was measured at ~120 ns per box, the
+        // pipeline's limit).
+        const int u = lane >> 2, c = (lane >> 1) & 1, v = lane & 1;
+        const CUtensorMap *map = v ? &tmv : &tmk;
+        int g = 0;
+        for (int n = 0;; ++n) {
+            const int b = n & 1;
+            const bool okr = wait(CC::B_RECFULL + b, (uint32_t)((n >> 1) & 1));
+            if (!__all_sync(0xffffffffu, okr))
                 break;
-            }
-            tc05::fence_after_sync();
-
-            // scores of this warp's group: tokens 8w .. 8w + 7 of the stage
-            // (tile w / 2), read from lanes 0-7 of the warp's TMEM quarter and
-            // shuffled out: lane = 8 rq + t takes token t's query rows
-            // [RPL rq, RPL rq + RPL)
-            const int tt = 2 * s + (warp >> 1), t = lane & 7, rq = lane >> 3;
-            const int g_tok0 = (warp & 1) * CC::GRP;   // the group's first token in its tile
-            int nvalid = 0, rlo = 0, rhi = 0;
-            const bool tile_here = tt < total;
-            if (tile_here) {
-                const int k = seg_of(tt, k_use);
-                const int *gg = seg(k);
-                const int t0 = gg[plan::S_BEGIN] + (tt - gg[plan::S_FIRST_TILE]) * TILE;
-                nvalid = min(TILE, gg[plan::S_END] - t0);
-                rlo = gg[plan::S_ROW_LO];
-                rhi = min(gg[plan::S_ROW_HI], nrows);
-            }
-            const bool valid = tile_here && g_tok0 + t < nvalid;
-            float x[CC::RPL];
-            {
-                uint32_t sv[NT][8];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        sv[nt][j] = 0u;
-                    if (nt < ntl)
-                        tc05::ld8(tS + tlane + 8 * nt, sv[nt]);
-                }
-                tc05::wait_ld();
-                float got[CC::RPL];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll
-                    for (int j = 0; j < CC::RPL; ++j) {
-                        const int r = CC::RPL * k + j;
-                        const uint32_t v = __shfl_sync(0xffffffffu, sv[r / 8][r % 8], t);
-                        if (rq == k)
-                            got[j] = __uint_as_float(v);
-                    }
-#pragma unroll
-                for (int j = 0; j < CC::RPL; ++j) {
-                    const int r = CC::RPL * rq + j;
-                    const bool live = valid && r >= rlo && r < rhi;
-                    x[j] = live ? got[j] * p.qscale : -INFINITY;
-                }
-            }
-            bool over = false;
-#pragma unroll
-            for (int j = 0; j < CC::RPL; ++j)
-                over |= x[j] > mref[CC::RPL * rq + j] + kSlack;
-            tc05::fence_before_sync();
-            const bool any_over = __syncthreads_or(over);
-            // the scores are in registers: S^T may take the next stage
-            if (tid == kIssuer && s + 1 < n_st)
-                issue_qk(s + 1);
-            // refill: stage s + NSLOT - 1 goes to the slot stage s - 1 used
-            if (tid == kProducer && s + NSLOT - 1 < n_st) {
-                bool ok = true;
-                if (s >= 1) {
-                    const int gp = gs - 1;
-                    ok = mbar_wait_bounded(&empty[gp % NSLOT], (uint32_t)((gp / NSLOT) & 1));
-                }
-                if (ok) {
-                    issue(s + NSLOT - 1);
-                    *n_issued = s + NSLOT;
-                } else {
-                    atomicOr(cta_flag, 2u);
-                }
-            }
-            if (any_over) {
-                // exact running maxima: per warp over its 8 tokens (the lanes
-                // of one rq), then over the warps in shared memory
-#pragma unroll
-                for (int j = 0; j < CC::RPL; ++j) {
-                    float m8 = x[j];
-                    m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 1));
-                    m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 2));
-                    m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 4));
-                    if (t == 0)
-                        red[warp * RQ + CC::RPL * rq + j] = m8;
-                }
-                __syncthreads();
-                auto stage_max = [&](int r) {
-                    float mx = red[r];
-#pragma unroll
-                    for (int w2 = 1; w2 < NW; ++w2)
-                        mx = fmaxf(mx, red[w2 * RQ + r]);
-                    return mx;
-                };
-                bool grew = false;
-#pragma unroll
-                for (int j = 0; j < CC::RPL; ++j) {
-                    const int r = CC::RPL * rq + j;
-                    const float mo = mref[r], mn = fmaxf(mo, stage_max(r));
-                    ls[j] *= mn == -INFINITY ? 1.f : exp2f(mo - mn);
-                }
-                for (int r = 0; r < RQ; ++r)
-                    grew |= fmaxf(mref[r], stage_max(r)) != mref[r];
-                __syncthreads();   // every thread has read the old references
-                if (tid < RQ) {
-                    const float mo = mref[tid], mn = fmaxf(mo, stage_max(tid));
-                    alph[tid] = mn == -INFINITY ? 1.f : exp2f(mo - mn);
-                    mref[tid] = mn;
-                }
-                __syncthreads();
-                if (grew && s > 0) {
-                    // O holds earlier stages: rescale it once their products
-                    // are done (each warp its quarter of the dims)
-                    const int gp = gs - 1;
-                    bad = !mbar_wait_bounded(&empty[gp % NSLOT], (uint32_t)((gp / NSLOT) & 1));
-                    if (!bad) {
-                        tc05::fence_after_sync();
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            if (nt < ntl) {
-                                uint32_t ov[8];
-                                tc05::ld8(tO + tlane + 8 * nt, ov);
-                                tc05::wait_ld();
-#pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alph[8 * nt + j]);
-                                tc05::st8(tO + tlane + 8 * nt, ov);
-                            }
-                        tc05::wait_st();
-                    }
-                }
-                tc05::fence_before_sync();
-                if (__syncthreads_or(bad)) {
-                    failed = true;
-                    ++s;   // the next stage's S^T may be in flight: drained below
+            int32_t *m = meta(b);
+            if (m[CC::M_END])
+                break;
+            const int32_t *it = rec_of(m);
+            const int n_st = m[CC::M_NST], kvh = m[CC::M_KVH];
+            const int nseg = it[plan::I_NSEG], total = it[plan::I_TILES];
+            const int32_t *ids = it + CC::IDS;
+            auto seg = [&](int k) { return it + CC::SEGS + plan::kSegInts * k; };
+            int kcur = 0;
+            bool stop = false;
+            for (int s = 0; s < n_st; ++s, ++g) {
+                const int slot = g % NSTAGE;
+                const bool oks = g < NSTAGE || wait(CC::B_STFREE + slot, (uint32_t)(((g / NSTAGE) - 1) & 1));
+                if (!__all_sync(0xffffffffu, oks)) {
+                    stop = true;
                     break;
                 }
-            }
-            // probabilities against the reference; P^T = hi + lo over the
-            // group's K atoms as [token][query rows] (the B operand MN-major,
-            // swizzled like the ring): this lane's RPL rows are RPL / 2
-            // 32-bit words of token t's row
-            {
-                uint8_t *grp = slot_p + warp * CC::PERIOD;
-#pragma unroll
-                for (int i = 0; i < CC::RPL / 2; ++i) {
-                    const int r = CC::RPL * rq + 2 * i;
-                    const float a0 = x[2 * i] == -INFINITY ? 0.f : exp2f(x[2 * i] - fmaxf(mref[r], -1e30f));
-                    const float a1 =
-                        x[2 * i + 1] == -INFINITY ? 0.f : exp2f(x[2 * i + 1] - fmaxf(mref[r + 1], -1e30f));
-                    ls[2 * i] += a0;
-                    ls[2 * i + 1] += a1;
-                    const uint32_t h = Mma<T>::pack(a0, a1);
-                    const float2 hf = Mma<T>::unpack(h);
-                    const uint32_t l = Mma<T>::pack(a0 - hf.x, a1 - hf.y);
-                    const int byte = r * 2;
-                    const int off = t * 128 + ((((byte >> 4) ^ t)) << 4) + (byte & 15);
-                    *reinterpret_cast<uint32_t *>(grp + off) = h;
-                    *reinterpret_cast<uint32_t *>(grp + CC::ATOM + off) = l;
+                // this lane's tile: its token range and boxes
+                const int tile = TPS * s + u;
+                int t0 = 0, te = 0, sid = 0, sb0 = 0;
+                if (tile < total) {
+                    while (kcur + 1 < nseg && seg(kcur + 1)[plan::S_FIRST_TILE] <= tile)
+                        ++kcur;
+                    const int *gg = seg(kcur);
+                    t0 = gg[plan::S_BEGIN] + (tile - gg[plan::S_FIRST_TILE]) * TILE;
+                    te = min(gg[plan::S_END], t0 + TILE);
+                    sid = gg[plan::S_ID_OFF];
+                    sb0 = gg[plan::S_BEGIN] / BS;
                 }
-                // rows of V past the tile's valid tokens may hold anything (even
-                // NaN patterns): zero them so that 0 * v stays 0
-                if (tile_here && !valid && rq < CC::CHUNKS) {
-                    uint4 *vrow = reinterpret_cast<uint4 *>(grp + CC::V_OFF + rq * CC::ATOM + t * 128);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        vrow[q] = make_uint4(0u, 0u, 0u, 0u);
+                const int nbox = (te - t0 + CC::BOX_ROWS - 1) / CC::BOX_ROWS;
+                // bytes each of K and V: the boxes of every tile, both planes
+                const uint32_t bytes = __reduce_add_sync(0xffffffffu, (c == 0 && v == 0) ? (uint32_t)nbox : 0u) *
+                                       (uint32_t)(2 * CC::BOX_BYTES);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[CC::B_KFULL + slot], bytes);
+                    mbar_arrive_expect_tx(&bars[CC::B_VFULL + slot], bytes);
                 }
-            }
-            fence_proxy_async_smem();
-            tc05::fence_before_sync();
-            __syncthreads();
-            if (tid == kIssuer) {
-                tc05::fence_after_sync();
-                const uint32_t sb = smem_u32(slot_p);
-                const int nk = 2 * s + 1 < total ? 2 : 1;
-                for (int j = 0; j < nk; ++j) {
-                    // tokens 16j .. 16j + 15: groups 2j, 2j + 1, one period apart;
-                    // V^T MN-major (chunks one atom apart), P^T MN-major
-                    const uint32_t gb = sb + (uint32_t)(2 * j * CC::PERIOD);
-                    const uint64_t a = tc05::sdesc(gb + CC::V_OFF, CC::ATOM, CC::PERIOD);
-                    tc05::mma(tO, a, tc05::sdesc(gb, CC::PERIOD, CC::PERIOD), id_pv, s > 0 || j > 0);
-                    tc05::mma(tO, a, tc05::sdesc(gb + CC::ATOM, CC::PERIOD, CC::PERIOD), id_pv, true);
-                }
-                tc05::commit(&empty[sl]);
-            }
-        }
-        const int done_st = s;   // stages whose S^T was consumed (failed: maybe fewer)
-        if (failed) {
-            // let the copies and products in flight finish before the memory
-            // they write is reused or released
-            if (tid == 0) {
-                report(p.status, PKV_DEV_TIMEOUT);
-                atomicOr(cta_flag, 1u);
-            }
-            const int issued = *reinterpret_cast<volatile int32_t *>(n_issued);
-            for (int i = done_st; i < issued && i < n_st; ++i) {
-                const int gi = g + i;
-                drain_wait(&full[gi % NSLOT], (uint32_t)((gi / NSLOT) & 1), p.status);
-            }
-            if (done_st < n_st)   // an S^T issued for a stage not consumed
-                drain_wait(sbar, (uint32_t)((g + done_st) & 1), p.status);
-            if (done_st > 0)
-                drain_wait(&empty[(g + done_st - 1) % NSLOT],
-                           (uint32_t)(((g + done_st - 1) / NSLOT) & 1), p.status);
-        } else if (n_st > 0) {
-            // every product of the item done (one commit covers all before it)
-            const int gl = g + n_st - 1;
-            if (!mbar_wait_bounded(&empty[gl % NSLOT], (uint32_t)((gl / NSLOT) & 1))) {
-                if (tid == 0) {
-                    report(p.status, PKV_DEV_TIMEOUT);
-                    atomicOr(cta_flag, 1u);
+                __syncwarp();
+                uint8_t *dst = smem + slot * CC::STAGE + v * CC::KV_BYTES + c * CC::PLANE + u * TILE * 128;
+                uint64_t *bar = &bars[(v ? CC::B_VFULL : CC::B_KFULL) + slot];
+                for (int bx = 0; bx < nbox; ++bx) {
+                    const int tok = t0 + bx * CC::BOX_ROWS;
+                    int phys = ids[sid + tok / BS - sb0];
+                    if (phys < 0 || (int64_t)phys >= p.num_blocks)
+                        phys = 0;   // flagged by the loader's checks
+                    tma_load_5d(dst + bx * CC::BOX_BYTES, map, bar, 0, tok % BS, c, kvh, phys);
                 }
             }
-            tc05::fence_after_sync();
+            if (stop)
+                break;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars[CC::B_RECEMPTY + b]);
         }
-        g += n_st;
-
-        // ---- row sums over the tokens' lanes, bad rows, results
-        // row sums: over a warp's 8 token lanes, then over the warps
-#pragma unroll
-        for (int j = 0; j < CC::RPL; ++j) {
-            float sm = ls[j];
-            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-            sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-            sm += __shfl_xor_sync(0xffffffffu, sm, 4);
-            if ((lane & 7) == 0)
-                red[warp * RQ + CC::RPL * (lane >> 3) + j] = sm;
+        // no load may still be writing the ring when the CTA leaves: the
+        // last stage issued into each slot has landed (in normal runs the
+        // consumers already waited for every one of them)
+        if (lane == 0) {
+            for (int x = g - NSTAGE < 0 ? 0 : g - NSTAGE; x < g; ++x) {
+                drain_wait(&bars[CC::B_KFULL + x % NSTAGE], (uint32_t)((x / NSTAGE) & 1), p.status);
+                drain_wait(&bars[CC::B_VFULL + x % NSTAGE], (uint32_t)((x / NSTAGE) & 1), p.status);
+            }
         }
-        if (tid == 0) {
-            bool any = invalid_item;
-            uint32_t mask = 0;
-            for (int k = 0; k < nseg && k < CC::MAXSEG; ++k)
-                if (segbad[k]) {
-                    any = true;
-                    for (int r = seg(k)[plan::S_ROW_LO]; r < seg(k)[plan::S_ROW_HI] && r < 32; ++r)
-                        mask |= 1u << r;
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA
+        // One thread, an event loop: the PV of the oldest stage whose P is
+        // written (it frees that ring slot for the producer), else the S^T of
+        // the next stage once its K has landed and its score buffer is free.
+        // Neither waits for the other, so a slot is held only from its load
+        // to its PV.
+        if (lane == 0) {
+            const uint32_t id_qk = tc05::idesc<T>(128, CC::N, false, false);
+            const uint32_t id_pv = tc05::idesc<T>(128, CC::N, true, true);
+            int gq = 0, gp = 0;                  // stages with S^T issued / with PV issued
+            int pk[4] = {0, 0, 0, 0};            // per issued stage (gq - gp <= 2): valid tiles,
+            bool pf[4] = {false, false, false, false};   // and whether it starts its item
+            int n = 0, cur_b = 0, q_s = 0, q_nst = -1, q_total = 0;
+            uint32_t qb = 0;
+            bool items_done = false, ok = true;
+            uint64_t t_idle = 0;
+            for (uint32_t spin = 0;; ++spin) {
+                bool progress = false;
+                if (gp < gq) {
+                    const int slot = gp % NSTAGE;
+                    const uint32_t par = (uint32_t)((gp / NSTAGE) & 1);
+                    if (mbar_test_wait(&bars[CC::B_PFULL + slot], par) &&
+                        mbar_test_wait(&bars[CC::B_VFULL + slot], par)) {
+                        // O^T += V^T P^T over the stage's valid tiles: A = V^T
+                        // MN-major (64-dim chunk planes PLANE apart, 8-token
+                        // groups 1 KiB apart), B = P^T MN-major over the stage's
+                        // K (hi, then lo one plane on)
+                        tc05::fence_after_sync();
+                        const uint32_t kb = smem_u32(smem + slot * CC::STAGE), vb = kb + CC::KV_BYTES;
+                        const int nk = pk[gp & 3];
+                        for (int k = 0; k < nk; ++k) {
+                            const uint64_t a = tc05::sdesc(vb + k * 2048, CC::PLANE, 1024);
+                            const uint64_t bh = tc05::sdesc(kb + k * 2048, CC::PLANE, 1024);
+                            const uint64_t bl = tc05::sdesc(kb + CC::PLANE + k * 2048, CC::PLANE, 1024);
+                            tc05::mma(tO, a, bh, id_pv, !(pf[gp & 3] && k == 0));
+                            tc05::mma(tO, a, bl, id_pv, true);
+                        }
+                        tc05::commit(&bars[CC::B_STFREE + slot]);
+                        ++gp;
+                        progress = true;
+                    }
                 }
-            const uint32_t lb = *lenbad;
-            for (int mm = 0; mm < nmem; ++mm)
-                if ((lb >> mm) & 1u)
-                    mask |= ((1u << G) - 1u) << (mm * G);
-            *badrows = mask;
-            if (any)
-                report(p.status, PKV_DEV_BAD_BLOCK);
-            if (lb)
-                report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+                if (!items_done && q_nst < 0) {
+                    // the next item's q rows (every item releases its record
+                    // slot once its S^T products have read them)
+                    const int b = n & 1;
+                    if (mbar_test_wait(&bars[CC::B_QFULL + b], (uint32_t)((n >> 1) & 1))) {
+                        int32_t *m = meta(b);
+                        ++n;
+                        progress = true;
+                        if (m[CC::M_END]) {
+                            items_done = true;
+                        } else if (m[CC::M_NST] == 0) {
+                            tc05::commit(&bars[CC::B_RECEMPTY + b]);
+                        } else {
+                            cur_b = b;
+                            q_nst = m[CC::M_NST];
+                            q_total = rec_of(m)[plan::I_TILES];
+                            q_s = 0;
+                            qb = smem_u32(smem + CC::OFF_Q + b * CC::QBUF);
+                        }
+                    }
+                }
+                if (q_nst > 0 && gq - gp < 2) {
+                    const int slot = gq % NSTAGE, sb = gq & 1;
+                    if (mbar_test_wait(&bars[CC::B_KFULL + slot], (uint32_t)((gq / NSTAGE) & 1)) &&
+                        (gq < 2 || mbar_test_wait(&bars[CC::B_SFREE + sb], (uint32_t)(((gq >> 1) - 1) & 1)))) {
+                        // S^T = K q^T: both operands K-major, 128-byte swizzled;
+                        // a 16-dim k-step moves 32 bytes along the row, the
+                        // second 64-dim chunk is the next plane
+                        tc05::fence_after_sync();
+                        const uint32_t kb = smem_u32(smem + slot * CC::STAGE);
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint64_t a = tc05::sdesc(kb + (ks / 4) * CC::PLANE + (ks % 4) * 32, 16, 1024);
+                            const uint64_t bq = tc05::sdesc(qb + (ks / 4) * CC::QPLANE + (ks % 4) * 32, 16, 1024);
+                            tc05::mma(tS + sb * 32, a, bq, id_qk, ks > 0);
+                        }
+                        tc05::commit(&bars[CC::B_SFULL + sb]);
+                        pk[gq & 3] = min(TPS, q_total - TPS * q_s);
+                        pf[gq & 3] = q_s == 0;
+                        ++gq;
+                        progress = true;
+                        if (++q_s == q_nst) {
+                            tc05::commit(&bars[CC::B_RECEMPTY + cur_b]);   // its q rows are read
+                            q_nst = -1;
+                        }
+                    }
+                }
+                if (items_done && gp == gq)
+                    break;
+                // bounded: give up after the wait limit without any progress;
+                // idle polls back off briefly so that the softmax warp on this
+                // SM sub-partition keeps its issue slots
+                if (progress) {
+                    t_idle = 0;
+                    continue;
+                }
+                __nanosleep(32);
+                if ((spin & 63u) == 0) {
+                    const uint64_t now = globaltimer_ns();
+                    if (t_idle == 0) {
+                        t_idle = now;
+                    } else if (now - t_idle > kWaitLimitNs || aborted()) {
+                        if (atomicOr(abort_flag, 1u) == 0)
+                            report(p.status, PKV_DEV_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            (void)ok;
+            // every product done before the TMEM goes
+            tc05::commit(&bars[CC::B_MMADONE]);
+            drain_wait(&bars[CC::B_MMADONE], 0u, p.status);
         }
-        __syncthreads();
-        const bool failed_all = invalid_item || failed || n_st == 0 ||
-                                *reinterpret_cast<volatile uint32_t *>(cta_flag) != 0;
-        // O^T: this thread's dim d = 32 warp + lane, one register per row
-        float o[RQ];
+    } else if (warp == 2) {
+        // -------------------------------------------------------- loader
+        // Per item, in order: the record (-> RECFULL: the producer and the
+        // softmax warps may start), the query rows (-> QFULL: the MMA may
+        // start), the device checks and the members' partial counts
+        // (-> METAFULL: needed by the item's epilogue).
+        const int units = Hk * num_lists;
+        constexpr int RPL = (CC::ITEM_INTS + 31) / 32;   // record ints per lane
+        int n = 0;
+        bool stop = false;
+        auto next_slot = [&]() {
+            const int b = n & 1;
+            if (n >= 2 && !wait(CC::B_RECEMPTY + b, (uint32_t)(((n >> 1) - 1) & 1)))
+                return -1;
+            return b;
+        };
+        for (int un = blockIdx.x; un < units && !stop; un += gridDim.x) {
+            const int kvh = un % Hk;
+            for (int item = un / Hk; item >= 0 && item < p.num_items;) {
+                // the record's loads leave before the wait for its slot
+                int32_t rv[RPL];
+                const int32_t *src = items + (int64_t)item * CC::ITEM_INTS;
 #pragma unroll
-        for (int r = 0; r < RQ; ++r)
-            o[r] = 0.f;
-        if (!failed_all) {
-            uint32_t ov[NT][8];
+                for (int k = 0; k < RPL; ++k) {
+                    const int i = lane + 32 * k;
+                    rv[k] = i < CC::ITEM_INTS ? src[i] : 0;
+                }
+                const int b = next_slot();
+                if (b < 0) {
+                    stop = true;
+                    break;
+                }
+                int32_t *m = meta(b);
+                int32_t *it = rec_of(m);
+                int32_t *segbad = segbad_of(m);
+                int32_t *exps = exp_of(m);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                if (nt < ntl)
-                    tc05::ld8(tO + tlane + 8 * nt, ov[nt]);
-            tc05::wait_ld();
+                for (int k = 0; k < RPL; ++k) {
+                    const int i = lane + 32 * k;
+                    if (i < CC::ITEM_INTS)
+                        it[i] = rv[k];
+                }
+                if (lane < CC::MAXSEG)
+                    segbad[lane] = 0;
+                __syncwarp();
+                const int nseg = it[plan::I_NSEG], total = it[plan::I_TILES], nrows = it[plan::I_NROWS];
+                const int nxt = it[plan::I_NEXT] > item && it[plan::I_NEXT] < p.num_items ? it[plan::I_NEXT] : -1;
+                const bool invalid = nseg > 0 && (it[plan::I_IDS] > CC::TABLE_CAP || nseg > CC::MAXSEG ||
+                                                  nrows > RQ || nrows <= 0 || total <= 0);
+                const bool dead = aborted();
+                const int n_st = (nseg <= 0 || invalid || dead) ? 0 : (total + TPS - 1) / TPS;
+                if (lane == 0) {
+                    m[CC::M_NST] = n_st;
+                    m[CC::M_END] = 0;
+                    m[CC::M_FAILED] = invalid || dead;
+                    m[CC::M_ZERO] = nseg <= 0;
+                    m[CC::M_BADROWS] = 0;
+                    m[CC::M_FINAL] = nseg <= 0 ? -1 : 0;
+                    m[CC::M_KVH] = kvh;
+                    mbar_arrive(&bars[CC::B_RECFULL + b]);   // the producer and softmax may start
+                }
+                const int nmem = nrows > 0 && nrows <= RQ ? nrows / G : 0;
+                const int32_t *members = it + plan::kItemHead;
+                const CtaWork w{it[plan::I_SEQ0], nrows, kvh, 0, 0, it[plan::I_SLOT], it[plan::I_SEQ0], members};
+                if (n_st > 0) {
+                    // q rows -> [chunk][32 rows][128 B], 128-byte swizzled, and
+                    // the members' expected partial counts and lengths: all
+                    // loads in flight before the first store
+                    uint8_t *qs = smem + CC::OFF_Q + b * CC::QBUF;
+                    constexpr int PCS = D * 2 / 16;   // 16-byte pieces per row
+                    constexpr int PER = (RQ * PCS + 31) / 32;
+                    uint4 qv[PER];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                    for (int k = 0; k < PER; ++k) {
+                        const int i = lane + 32 * k, r = i / PCS;
+                        qv[k] = make_uint4(0u, 0u, 0u, 0u);
+                        if (r < nrows)
+                            qv[k] = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.q) +
+                                                                    row_head(p, w, G, r) * D)[i % PCS];
+                    }
+                    int m_exp = 0, m_plen = 0, m_len = 0;
+                    if (lane < nmem) {
+                        const int sq = members[lane];
+                        m_exp = expected[sq];
+                        m_plen = plan_lens[sq];
+                        m_len = p.context_lens[sq];
+                    }
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (nt < ntl)
-                        o[8 * nt + j] = __uint_as_float(ov[nt][j]);
-        }
-        const int d = 32 * warp + lane;
+                    for (int k = 0; k < PER; ++k) {
+                        const int i = lane + 32 * k;
+                        if (i < RQ * PCS) {
+                            const int r = i / PCS, pc = i % PCS, ch = pc / 8, q8 = pc % 8;
+                            *reinterpret_cast<uint4 *>(qs + ch * CC::QPLANE + r * 128 + ((q8 ^ (r & 7)) << 4)) = qv[k];
+                        }
+                    }
+                    fence_proxy_async_smem();   // the q rows (generic stores) before the MMAs read them
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bars[CC::B_QFULL + b]);
+                    if (lane < nmem)
+                        exps[lane] = m_exp;
+                    const uint32_t lb = __reduce_or_sync(0xffffffffu, (lane < nmem && m_plen != m_len) ? 1u << lane : 0u);
+                    // device checks, all loads of a round in flight together
+                    const int vtotal = it[plan::I_CHECKS];
+                    auto seg = [&](int k) { return it + CC::SEGS + plan::kSegInts * k; };
+                    for (int x0 = 0; x0 < vtotal; x0 += 32 * 8) {
+                        int got[8], want[8], kk[8];
 #pragma unroll
-        for (int r = 0; r < RQ; ++r) {
-            if (r < nrows) {
-                const bool bad_r = failed_all || ((*badrows >> r) & 1u);
-                const float L = red[r] + red[RQ + r] + red[2 * RQ + r] + red[3 * RQ + r];
-                const int64_t sh = row_head(p, w, G, r);
-                if (exp_s[r / G] == 1) {
-                    const float inv = !bad_r && L > 0.f ? 1.f / L : 0.f;
-                    store_out(p.out, p.out_dtype, sh * D + d, bad_r ? 0.f : o[r] * inv);
+                        for (int k = 0; k < 8; ++k) {
+                            const int x = x0 + 32 * k + lane;
+                            kk[k] = -1;
+                            got[k] = want[k] = 0;
+                            if (x < vtotal) {
+                                int sg = 0;
+                                while (sg + 1 < nseg && seg(sg + 1)[plan::S_CHECK_OFF] <= x)
+                                    ++sg;
+                                const int *gg = seg(sg);
+                                const int nb = (sg + 1 < nseg ? seg(sg + 1)[plan::S_ID_OFF] : it[plan::I_IDS]) -
+                                               gg[plan::S_ID_OFF];
+                                const int local = x - gg[plan::S_CHECK_OFF];
+                                const int mi = local / nb, i = local % nb;
+                                const bool shared = gg[plan::S_ROW_LO] == 0 && gg[plan::S_ROW_HI] == nrows &&
+                                                    nmem > 1;
+                                const int sq = shared ? members[mi] : gg[plan::S_TABLE_SEQ];
+                                got[k] = p.block_tables[(int64_t)sq * p.max_blocks_per_seq +
+                                                        gg[plan::S_BEGIN] / BS + i];
+                                want[k] = it[CC::IDS + gg[plan::S_ID_OFF] + i];
+                                kk[k] = sg;
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (kk[k] >= 0 && (got[k] != want[k] || want[k] < 0 ||
+                                               (int64_t)want[k] >= p.num_blocks))
+                                segbad[kk[k]] = 1;
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        bool any = false;
+                        uint32_t mask = 0;
+                        for (int k = 0; k < nseg; ++k)
+                            if (segbad[k]) {
+                                any = true;
+                                for (int r = seg(k)[plan::S_ROW_LO]; r < seg(k)[plan::S_ROW_HI] && r < 32; ++r)
+                                    mask |= 1u << r;
+                            }
+                        for (int mi = 0; mi < nmem; ++mi)
+                            if ((lb >> mi) & 1u)
+                                mask |= ((1u << G) - 1u) << (mi * G);
+                        m[CC::M_BADROWS] = (int32_t)mask;
+                        uint32_t fin = 0;   // rows whose sequence the item holds entirely
+                        for (int r = 0; r < nrows; ++r)
+                            if (exps[r / G] == 1)
+                                fin |= 1u << r;
+                        m[CC::M_FINAL] = (int32_t)fin;
+                        if (any)
+                            report(p.status, PKV_DEV_BAD_BLOCK);
+                        if (lb)
+                            report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+                    }
                 } else {
-                    __stcg(p.ws_acc + (sh * slots + slot) * D + d, bad_r ? 0.f : o[r]);
-                    if (d == 0)
-                        __stcg(reinterpret_cast<float2 *>(p.ws_ml) + sh * slots + slot,
-                               make_float2(bad_r ? -INFINITY : mref[r], bad_r ? -1.f : L));
+                    if (nseg <= 0) {
+                        if (lane == 0 && kvh == 0) {
+                            const int L = p.context_lens[it[plan::I_SEQ0]];
+                            if (L < 0 || L > p.max_context_len)
+                                report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+                        }
+                    } else {
+                        // an item the CTA cannot run (a malformed record, or the
+                        // CTA gave up after a timeout): its rows fail
+                        if (lane < nmem)
+                            exps[lane] = expected[members[lane]];
+                        __syncwarp();
+                        if (lane == 0) {
+                            m[CC::M_BADROWS] = -1;
+                            uint32_t fin = 0;
+                            for (int r = 0; r < nrows && r < RQ; ++r)
+                                if (exps[r / G] == 1)
+                                    fin |= 1u << r;
+                            m[CC::M_FINAL] = (int32_t)fin;
+                            if (invalid)
+                                report(p.status, PKV_DEV_BAD_BLOCK);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bars[CC::B_QFULL + b]);
                 }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars[CC::B_METAFULL + b]);
+                ++n;
+                item = nxt;
             }
         }
-        tc05::fence_before_sync();
-        __syncthreads();
-        tc05::fence_after_sync();
-        item = next;
+        if (!stop) {
+            const int b = next_slot();
+            if (b >= 0 && lane == 0) {
+                meta(b)[CC::M_END] = 1;
+                mbar_arrive(&bars[CC::B_RECFULL + b]);
+                mbar_arrive(&bars[CC::B_QFULL + b]);
+                mbar_arrive(&bars[CC::B_METAFULL + b]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- softmax
+        const int sw = warp - 3;                    // softmax warp 0 .. SWARPS - 1
+        const int j = sw >> 2;                      // row group: query rows 8j .. 8j + 7
+        const int r0 = 8 * j;
+        const int qw = warp & 3;                    // TMEM lane quarter
+        const int t = 32 * qw + lane;               // this thread's token; its dim at the end
+        const uint32_t tl = (uint32_t)(32 * qw) << 16;
+        float *red = reinterpret_cast<float *>(smem + CC::OFF_RED);   // [4][32] stage maxima
+        float *red2 = red + 4 * CC::N;                                 // [4][32] row sums
+        float mref[8], lsum[8];
+        int g = 0;
+        for (int n = 0;; ++n) {
+            const int b = n & 1;
+            const bool okm = wait(CC::B_RECFULL + b, (uint32_t)((n >> 1) & 1));
+            if (softmax_any(!okm))
+                break;
+            int32_t *m = meta(b);
+            if (m[CC::M_END])
+                break;
+            const int32_t *it = rec_of(m);
+            const int n_st = m[CC::M_NST], kvh = m[CC::M_KVH];
+            const int nseg = it[plan::I_NSEG], total = it[plan::I_TILES], nrows = it[plan::I_NROWS];
+            auto seg = [&](int k) { return it + CC::SEGS + plan::kSegInts * k; };
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mref[i] = -INFINITY;
+                lsum[i] = 0.f;
+            }
+            int kcur = 0;
+            bool fail = false;
+            for (int s = 0; s < n_st; ++s, ++g) {
+                const int slot = g % NSTAGE, sb = g & 1;
+                const bool oks = wait(CC::B_SFULL + sb, (uint32_t)((g >> 1) & 1));
+                if (softmax_any(!oks || aborted())) {
+                    fail = true;
+                    break;
+                }
+                tc05::fence_after_sync();
+                uint32_t sv[8];
+                tc05::ld8(tS + sb * 32 + r0 + tl, sv);
+                tc05::wait_ld();
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars[CC::B_SFREE + sb]);   // the score buffer may take stage g + 2
+
+                // this token's place: tile, segment, rows it serves
+                const int tile = TPS * s + t / TILE;
+                const bool loaded = tile < total;
+                bool valid = false;
+                int rlo = 0, rhi = 0;
+                if (loaded) {
+                    while (kcur + 1 < nseg && seg(kcur + 1)[plan::S_FIRST_TILE] <= tile)
+                        ++kcur;
+                    const int *gg = seg(kcur);
+                    const int tok = gg[plan::S_BEGIN] + (tile - gg[plan::S_FIRST_TILE]) * TILE + t % TILE;
+                    valid = tok < gg[plan::S_END];
+                    rlo = gg[plan::S_ROW_LO];
+                    rhi = min(gg[plan::S_ROW_HI], nrows);
+                }
+                float x[8];
+                bool over = false;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const bool live = valid && r0 + i >= rlo && r0 + i < rhi;
+                    x[i] = live ? __uint_as_float(sv[i]) * p.qscale : -INFINITY;
+                    over |= x[i] > mref[i] + kSlack;   // a row with no token yet: any live score
+                }
+                if (softmax_any(over)) {
+                    // exact maxima of this stage's scores per row: over the
+                    // warp's 32 tokens, then over the four lane quarters
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float v = x[i];
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+                        if (lane == i)
+                            red[qw * CC::N + r0 + i] = v;
+                    }
+                    softmax_sync();
+                    float alpha[8];
+                    bool grew = false;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = r0 + i;
+                        const float sm = fmaxf(fmaxf(red[r], red[CC::N + r]),
+                                               fmaxf(red[2 * CC::N + r], red[3 * CC::N + r]));
+                        const float mn = fmaxf(mref[i], sm);
+                        // a row with no token so far keeps nothing to rescale
+                        alpha[i] = mn == -INFINITY ? 1.f : fast_exp2(mref[i] - mn);
+                        grew |= mn != mref[i];
+                        mref[i] = mn;
+                    }
+                    bool okr = true;
+                    if (grew && s > 0) {
+                        // O holds this item's earlier stages: rescale this row
+                        // group's columns once their products are done
+                        okr = wait(CC::B_STFREE + (g - 1) % NSTAGE, (uint32_t)(((g - 1) / NSTAGE) & 1));
+                        if (okr) {
+                            tc05::fence_after_sync();
+                            uint32_t ov[8];
+                            tc05::ld8(tO + r0 + tl, ov);
+                            tc05::wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha[i]);
+                            tc05::st8(tO + r0 + tl, ov);
+                            tc05::wait_st();
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        lsum[i] *= alpha[i];
+                    if (softmax_any(!okr)) {
+                        fail = true;
+                        break;
+                    }
+                }
+                // P = hi + lo: this token's 8 rows of the B operand [token][rows]
+                // over the stage's K, one 16-byte piece (the row group's),
+                // swizzled by the token's row within its 8-token atom
+                uint8_t *kb = smem + slot * CC::STAGE;
+                {
+                    uint32_t h[4], lo[4];
+#pragma unroll
+                    for (int w2 = 0; w2 < 4; ++w2) {
+                        const float a0 = x[2 * w2] == -INFINITY ? 0.f : fast_exp2(x[2 * w2] - mref[2 * w2]);
+                        const float a1 = x[2 * w2 + 1] == -INFINITY ? 0.f
+                                                                     : fast_exp2(x[2 * w2 + 1] - mref[2 * w2 + 1]);
+                        lsum[2 * w2] += a0;
+                        lsum[2 * w2 + 1] += a1;
+                        h[w2] = Mma<T>::pack(a0, a1);
+                        const float2 hf = Mma<T>::unpack(h[w2]);
+                        lo[w2] = Mma<T>::pack(a0 - hf.x, a1 - hf.y);
+                    }
+                    const uint32_t a = smem_u32(kb) + (uint32_t)((t >> 3) * 1024 + (t & 7) * 128) +
+                                       (uint32_t)(((j ^ (t & 7)) & 7) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h[0]), "r"(h[1]),
+                                 "r"(h[2]), "r"(h[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a + CC::PLANE), "r"(lo[0]),
+                                 "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
+                                 : "memory");
+                }
+                // a loaded tile's rows past its segment may hold anything (even
+                // NaN patterns): row group 0 zeroes such a token's V row so that
+                // 0 * v stays 0
+                if (j == 0 && loaded && !valid) {
+                    if (wait(CC::B_VFULL + slot, (uint32_t)((g / NSTAGE) & 1))) {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            uint4 *vr = reinterpret_cast<uint4 *>(kb + CC::KV_BYTES + c * CC::PLANE + t * 128);
+#pragma unroll
+                            for (int q8 = 0; q8 < 8; ++q8)   // pieces staggered across the rows' banks
+                                vr[(q8 ^ t) & 7] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();   // P and the zeroed rows before the MMAs read them
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars[CC::B_PFULL + slot]);
+            }
+            if (fail)
+                break;
+
+            // ---- end of the item: row sums, O^T, outputs or partials (the
+            // loader's check results are needed from here on)
+            {
+                bool oke = wait(CC::B_METAFULL + b, (uint32_t)((n >> 1) & 1));
+                if (n_st > 0)
+                    oke = oke && wait(CC::B_STFREE + (g - 1) % NSTAGE, (uint32_t)(((g - 1) / NSTAGE) & 1));
+                if (softmax_any(!oke))
+                    break;
+                if (n_st > 0)
+                    tc05::fence_after_sync();
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float v = lsum[i];
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                if (lane == i)
+                    red2[qw * CC::N + r0 + i] = v;
+            }
+            uint32_t ov[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                ov[i] = 0u;
+            if (n_st > 0) {
+                tc05::ld8(tO + r0 + tl, ov);
+                tc05::wait_ld();
+            }
+            tc05::fence_before_sync();
+            softmax_sync();
+            const int32_t *members = it + plan::kItemHead;
+            const CtaWork w{it[plan::I_SEQ0], nrows, kvh, 0, 0, it[plan::I_SLOT], it[plan::I_SEQ0], members};
+            const uint32_t badrows = (uint32_t)m[CC::M_BADROWS], fin = (uint32_t)m[CC::M_FINAL];
+            const bool zero = m[CC::M_ZERO] != 0, failed_all = m[CC::M_FAILED] != 0;
+            const int rows = nrows > 0 && nrows <= RQ ? nrows : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + i;
+                if (r < rows) {
+                    const float L = (red2[r] + red2[CC::N + r]) + (red2[2 * CC::N + r] + red2[3 * CC::N + r]);
+                    const int64_t sh = row_head(p, w, G, r);
+                    const bool bad = failed_all || ((badrows >> r) & 1u);
+                    const float o = __uint_as_float(ov[i]);
+                    if ((fin >> r) & 1u) {
+                        store_out(p.out, p.out_dtype, sh * D + t,
+                                  (zero || bad || !(L > 0.f)) ? 0.f : o * (1.f / L));
+                    } else {
+                        const int64_t base = sh * slots + it[plan::I_SLOT];
+                        __stcg(p.ws_acc + base * D + t, bad ? 0.f : o);
+                        if (t == 0)
+                            __stcg(reinterpret_cast<float2 *>(p.ws_ml) + base,
+                                   make_float2(bad ? -INFINITY : mref[i], bad ? -1.f : L));
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars[CC::B_RECEMPTY + b]);
+        }
     }
+
+    // every warp's last access to the tensor memory precedes its arrival
+    // here; the allocating warp frees it once all have arrived (no CTA-wide
+    // barrier: the roles' lane 0 threads reconverge with their warps first)
+    __syncwarp();
     tc05::fence_before_sync();
-    __syncthreads();
-    if (warp == 0)
-        tc05::dealloc(*tslot, CC::TM_COLS);
+    if (lane == 0)
+        mbar_arrive(&bars[CC::B_DONE]);
+    if (warp == 1) {
+        drain_wait(&bars[CC::B_DONE], 0u, p.status);
+        tc05::fence_after_sync();
+        tc05::dealloc(tS, CC::TM_COLS);
+    }
 }
 
 }  // namespace pkv

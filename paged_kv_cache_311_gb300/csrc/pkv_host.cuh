@@ -64,6 +64,26 @@ int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaS
                                                                                       : PKV_ECUDA;
 }
 
+// SMs of the current device (cached per device; 152, a GB300's count, if it
+// cannot be read).
+inline int device_sm_count()
+{
+    static int cache[64] = {};
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    if (cache[dev] > 0)
+        return cache[dev];
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+        (void)cudaGetLastError();
+        v = 152;
+    }
+    cache[dev] = v;
+    return v;
+}
+
 int launch_decode_f32(const DecodeLaunch &a);
 int launch_decode_f16(const DecodeLaunch &a);
 int launch_decode_bf16(const DecodeLaunch &a);
@@ -118,19 +138,19 @@ int run_cascade(const DecodeLaunch &a)
     alignas(64) CUtensorMap tmk;
     alignas(64) CUtensorMap tmv;
     int box_rows, box_chunks, smem;
-    void (*kern)(DecodeParams, CUtensorMap, CUtensorMap, const int32_t *);
+    const void *kern;
     if constexpr (TC05) {
         using CC = Tc05Cfg<T, D, BS, G>;
         box_rows = CC::BOX_ROWS;
         box_chunks = 1;   // one 64-element chunk plane per load
         smem = CC::SMEM_BYTES;
-        kern = pa_cascade_tc05_kernel<T, D, BS, G>;
+        kern = reinterpret_cast<const void *>(pa_cascade_tc05_kernel<T, D, BS, G>);
     } else {
         using CC = CascadeCfg<T, D, BS, G>;
         box_rows = CC::C::BOX_ROWS;
         box_chunks = 0;
         smem = CC::SMEM_BYTES;
-        kern = pa_cascade_kernel<T, D, BS, G>;
+        kern = reinterpret_cast<const void *>(pa_cascade_kernel<T, D, BS, G>);
     }
     int rc = encode_kv_map(&tmk, a.k_cache, Elem<T>::tma, Elem<T>::bytes, D, BS, p.num_kv_heads,
                            p.num_blocks, box_rows, box_chunks);
@@ -141,11 +161,21 @@ int run_cascade(const DecodeLaunch &a)
     if (rc)
         return rc;
     static unsigned long long done = 0;
-    rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem, &done);
+    rc = ensure_smem_attr(kern, smem, &done);
     if (rc)
         return rc;
-    dim3 grid(p.num_kv_heads, a.num_lists, 1);
-    rc = launch_pdl(kern, grid, dim3(128), smem, a.stream, p, tmk, tmv, a.plan);
+    if constexpr (TC05) {
+        // one CTA per SM, each taking every gridDim.x-th (list, kv head) unit
+        const long long units = (long long)p.num_kv_heads * a.num_lists;
+        const long long sms = device_sm_count();
+        const unsigned ctas = (unsigned)(units < sms ? units : sms);
+        rc = launch_pdl(pa_cascade_tc05_kernel<T, D, BS, G>, dim3(ctas), dim3(Tc05Cfg<T, D, BS, G>::THREADS),
+                        smem, a.stream, p, tmk, tmv, a.plan, a.num_lists);
+    } else {
+        dim3 grid(p.num_kv_heads, a.num_lists, 1);
+        rc = launch_pdl(pa_cascade_kernel<T, D, BS, G>, grid, dim3(128), smem, a.stream, p, tmk, tmv,
+                        a.plan);
+    }
     if (rc)
         return rc;
 

@@ -20,15 +20,12 @@ namespace {
 
 // Smallest automatic list (tokens): below it the per-CTA fixed costs win.
 constexpr int kMinAutoTokens = 64;
-// What a CTA's switch from one item to the next costs, in 16-token tiles
-// streamed: the epilogue of one item and the start of the next (about 6 us
-// on a GB300, against about 0.6 us per tile while all CTAs stream).
-constexpr long long kItemCostTiles = 10;
 // Fewest tiles a list starts another unit with.
 constexpr long long kMinPieceTiles = 4;
 
-// SMs of the current device (the automatic cut targets three resident CTAs
-// per SM); 152, a GB300's count, when no device answers.
+// SMs of the current device (the automatic cut targets one list per
+// resident CTA of the shared-prefix kernel); 152, a GB300's count, when no
+// device answers.
 int gpu_sm_count()
 {
     int dev = 0, n = 0;
@@ -111,7 +108,7 @@ size_t pkv_shared_plan_max_ints(int num_seqs, int num_heads, int num_kv_heads, i
     if (partition_size > 0)
         lists = std::max(lists, W / std::max(1, partition_size / kTileTokens) + 1);
     else
-        lists = std::max(lists, 3LL * gpu_sm_count() / num_kv_heads + 1);
+        lists = std::max(lists, 3LL * gpu_sm_count() / num_kv_heads + 1);   // the most CTAs per SM
     lists = std::min(lists, 65536LL);   // a plan never has more (PKV_EUNSUPPORTED)
     return (size_t)kHeader + 2 * (size_t)num_seqs +
            (size_t)(num_seqs + lists) * item_ints(G);
@@ -251,14 +248,16 @@ static int plan_shared_prefix(const int32_t *block_tables, const int32_t *contex
 
     // ---- lists: the stream cut into consecutive ranges, one CTA each (per
     // kv head), of nearly equal cost whatever the units' sizes.  A list's
-    // cost is its tiles plus kItemCostTiles for every item after its first
-    // (the CTA's epilogue of one item and start of the next stream nothing);
-    // a list does not start another unit with less than kMinPieceTiles of
-    // budget left (no sliver items).  Greedy filling under a budget gives the
-    // fewest lists for that budget; the budget is the smallest whose lists
-    // fit one per resident CTA slot of the GPU (three per SM) over the kv
-    // heads (automatic), or the explicit target.  An item's block ids stay
-    // within the kernel's table capacity whatever the segments' alignment.
+    // cost is its tiles plus the item cost for every item after its first
+    // (what the CTA's switch from one item to the next costs the kernel that
+    // runs the plan); a list does not start another unit with less than
+    // kMinPieceTiles of budget left (no sliver items).  Greedy filling under
+    // a budget gives the fewest lists for that budget; the budget is the
+    // smallest whose lists fit one per resident CTA of that kernel over the
+    // kv heads (automatic), or the explicit target.  An item's block ids
+    // stay within the kernel's table capacity whatever the segments'
+    // alignment.
+    const long long kItemCostTiles = pkv::shared_item_cost_tiles(head_dim);
     const long long q_cap = (long long)(kTableCap - 2 * max_segments(G)) * bs / kTileTokens;
     auto walk = [&](long long budget, std::vector<long long> *cuts) {
         long long pos = 0, n = 0;
@@ -293,7 +292,8 @@ static int plan_shared_prefix(const int32_t *block_tables, const int32_t *contex
     if (partition_size > 0) {
         Q = std::min<long long>(partition_size / kTileTokens, q_cap);
     } else {
-        const long long N = std::max(1LL, 3LL * gpu_sm_count() / num_kv_heads);
+        const long long N = std::max(1LL, (long long)pkv::shared_ctas_per_sm(head_dim) * gpu_sm_count() /
+                                              num_kv_heads);
         long long lo = std::min(q_cap, std::max<long long>(kMinAutoTokens / kTileTokens, (W + N - 1) / N));
         long long hi = lo;
         while (hi < q_cap && walk(hi, nullptr) > N)
