@@ -64,9 +64,12 @@ constexpr int item_ints(int group) { return item_ids_offset(group) + kTableCap; 
 }  // namespace plan
 
 // How the shared-prefix kernel that the current engine choice runs takes a
-// plan (defined beside that choice, in pkv_abi.cu): resident CTAs per SM
-// (3 for the warp-level kernel, 1 for the tcgen05 kernel) and what a CTA's
-// switch from one item to the next costs in 16-token tiles streamed.
+// plan (the planner's automatic cut follows it): resident CTAs per SM (3 for
+// the warp-level kernel, 1 for the tcgen05 kernel) and what a CTA's switch
+// from one item to the next costs in 16-token tiles streamed.  The engine
+// choice (pkv_decode_set_engine) passes its value on with
+// set_shared_plan_engine.  Defined in pkv_plan.cu.
+void set_shared_plan_engine(int engine);
 int shared_ctas_per_sm(int head_dim);
 int shared_item_cost_tiles(int head_dim);
 

@@ -139,21 +139,6 @@ int ensure_smem_attr(const void *func, int bytes, unsigned long long *done_mask)
 
 using namespace pkv;
 
-// The shared-prefix kernel of the current engine choice (see run_engine):
-// the tcgen05 kernel runs one CTA per SM and overlaps an item's epilogue
-// with the next item's loads (a switch costs about one tile); the warp-level
-// kernel runs three CTAs per SM and drains its rings at every switch (about
-// 6 us, ten tiles, measured on a GB300).
-int pkv::shared_ctas_per_sm(int head_dim)
-{
-    return head_dim == 128 && g_engine_override.load(std::memory_order_relaxed) == kEngineTcgen05 ? 1 : 3;
-}
-
-int pkv::shared_item_cost_tiles(int head_dim)
-{
-    return pkv::shared_ctas_per_sm(head_dim) == 1 ? 1 : 10;
-}
-
 extern "C" {
 
 const char *pkv_status_string(int status)
@@ -178,6 +163,7 @@ int pkv_decode_set_engine(int engine)
     if (engine < kEngineAuto || engine > kEngineTcgen05)
         return PKV_EINVAL;
     g_engine_override.store(engine, std::memory_order_relaxed);
+    pkv::set_shared_plan_engine(engine);   // the automatic shared-prefix plan follows the kernel
     return PKV_OK;
 }
 

@@ -7,6 +7,7 @@
 // (cascade_plan.h).  The kernel side re-checks on the device that the members
 // of a group really share the blocks it was told about.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cstring>
@@ -85,6 +86,28 @@ bool split_total(uint64_t seqs, uint64_t heads, uint64_t slots, uint64_t head_di
 constexpr int kMaxContext = 1 << 30;
 
 }  // namespace
+
+namespace pkv {
+
+namespace {
+std::atomic<int> g_plan_engine{0};   // the engine choice (pkv_decode_set_engine)
+constexpr int kTcgen05Engine = 3;
+}  // namespace
+
+void set_shared_plan_engine(int engine) { g_plan_engine.store(engine, std::memory_order_relaxed); }
+
+// The tcgen05 kernel (head_dim 128) runs one CTA per SM and overlaps an
+// item's epilogue with the next item's loads (a switch costs about one
+// tile); the warp-level kernel runs three CTAs per SM and drains its rings
+// at every switch (about 6 us, ten tiles, measured on a GB300).
+int shared_ctas_per_sm(int head_dim)
+{
+    return head_dim == 128 && g_plan_engine.load(std::memory_order_relaxed) == kTcgen05Engine ? 1 : 3;
+}
+
+int shared_item_cost_tiles(int head_dim) { return shared_ctas_per_sm(head_dim) == 1 ? 1 : 10; }
+
+}  // namespace pkv
 
 extern "C" {
 
