@@ -31,7 +31,8 @@
 //     exact stage maxima (warp shuffles, then shared memory) move the
 //     references and O is rescaled in TMEM.  P = hi + lo 16-bit parts, so the
 //     products keep fp32-level accuracy, written over the stage's K (used
-//     by then) as [token][query rows], the B operand read MN-major.  At the
+//     by then) as [token][hi rows | lo rows], one N = 64 B operand read
+//     MN-major (high and low products land in separate O^T columns).  At the
 //     end of an item the same warps read O^T (thread = one dim) and write
 //     the rows' outputs or partials.
 // Every hand-off is an mbarrier phase (K, V full; scores full / free; P full;
@@ -100,7 +101,12 @@ struct Tc05Cfg {
     static constexpr int SWARPS = 4 * NRG;
     static constexpr int WARPS = 3 + SWARPS;              // producer, MMA, loader, softmax
     static constexpr int THREADS = WARPS * 32;
-    static constexpr int TM_COLS = 128;                   // S^T at 0 and 32, O^T at 64
+    // TMEM columns: S^T buffer b in two partial sums (even / odd 16-dim
+    // k-steps) at 64 b and 64 b + 32; O^T in two partial sums (even / odd
+    // 16-token tile) of 64 columns at 128 + 64 k, each [P's high part rows
+    // 0-31 | low part rows 0-31]
+    static constexpr int TM_COLS = 256;
+    static constexpr int TM_O = 128;
     static constexpr int kRecEmptyArrivals = 2 + SWARPS;  // producer, MMA commit, softmax warps
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(PLANE % 1024 == 0 && STAGE % 1024 == 0 && OFF_Q % 1024 == 0 && QPLANE % 1024 == 0,
@@ -184,7 +190,7 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
     tc05::fence_before_sync();
     __syncthreads();
     tc05::fence_after_sync();
-    const uint32_t tS = *tslot, tO = tS + 64;
+    const uint32_t tS = *tslot, tO = tS + CC::TM_O;
     // launched as a programmatic dependent of the previous kernel: nothing it
     // may write is read before this wait; then the merge kernel behind this
     // grid may start (it reads the plan before its own wait)
@@ -203,6 +209,23 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
         if (atomicOr(abort_flag, 1u) == 0)
             report(p.status, PKV_DEV_TIMEOUT);
         return false;
+    };
+    // the same, polling with the non-blocking test and a short back-off, for
+    // the pipeline's hand-offs (a suspended try_wait resumed measurably late)
+    auto wait_poll = [&](int bar, uint32_t parity) {
+        if (mbar_test_wait(&bars[bar], parity))
+            return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            __nanosleep(20);
+            if (mbar_test_wait(&bars[bar], parity))
+                return true;
+            if ((it & 63u) == 0 && (globaltimer_ns() - t0 > kWaitLimitNs || it >= (1u << 30))) {
+                if (atomicOr(abort_flag, 1u) == 0)
+                    report(p.status, PKV_DEV_TIMEOUT);
+                return false;
+            }
+        }
     };
 
     if (warp == 0) {
@@ -232,7 +255,7 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
             bool stop = false;
             for (int s = 0; s < n_st; ++s, ++g) {
                 const int slot = g % NSTAGE;
-                const bool oks = g < NSTAGE || wait(CC::B_STFREE + slot, (uint32_t)(((g / NSTAGE) - 1) & 1));
+                const bool oks = g < NSTAGE || wait_poll(CC::B_STFREE + slot, (uint32_t)(((g / NSTAGE) - 1) & 1));
                 if (!__all_sync(0xffffffffu, oks)) {
                     stop = true;
                     break;
@@ -292,7 +315,9 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
         // to its PV.
         if (lane == 0) {
             const uint32_t id_qk = tc05::idesc<T>(128, CC::N, false, false);
-            const uint32_t id_pv = tc05::idesc<T>(128, CC::N, true, true);
+            // O^T gets P's high and low parts in one product: N = 64 columns,
+            // the low part's rows 32 columns after the high part's
+            const uint32_t id_pv = tc05::idesc<T>(128, 2 * CC::N, true, true);
             int gq = 0, gp = 0;                  // stages with S^T issued / with PV issued
             int pk[4] = {0, 0, 0, 0};            // per issued stage (gq - gp <= 2): valid tiles,
             bool pf[4] = {false, false, false, false};   // and whether it starts its item
@@ -310,16 +335,16 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
                         // O^T += V^T P^T over the stage's valid tiles: A = V^T
                         // MN-major (64-dim chunk planes PLANE apart, 8-token
                         // groups 1 KiB apart), B = P^T MN-major over the stage's
-                        // K (hi, then lo one plane on)
+                        // K, a token's 128-byte row [hi rows 0-31 | lo rows 0-31]
                         tc05::fence_after_sync();
                         const uint32_t kb = smem_u32(smem + slot * CC::STAGE), vb = kb + CC::KV_BYTES;
                         const int nk = pk[gp & 3];
                         for (int k = 0; k < nk; ++k) {
+                            // the item's first stage starts each partial sum
+                            const bool acc = !(pf[gp & 3] && k < 2);
                             const uint64_t a = tc05::sdesc(vb + k * 2048, CC::PLANE, 1024);
-                            const uint64_t bh = tc05::sdesc(kb + k * 2048, CC::PLANE, 1024);
-                            const uint64_t bl = tc05::sdesc(kb + CC::PLANE + k * 2048, CC::PLANE, 1024);
-                            tc05::mma(tO, a, bh, id_pv, !(pf[gp & 3] && k == 0));
-                            tc05::mma(tO, a, bl, id_pv, true);
+                            const uint64_t bp = tc05::sdesc(kb + k * 2048, CC::PLANE, 1024);
+                            tc05::mma(tO + 64 * (k & 1), a, bp, id_pv, acc);
                         }
                         tc05::commit(&bars[CC::B_STFREE + slot]);
                         ++gp;
@@ -360,7 +385,7 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
                         for (int ks = 0; ks < D / 16; ++ks) {
                             const uint64_t a = tc05::sdesc(kb + (ks / 4) * CC::PLANE + (ks % 4) * 32, 16, 1024);
                             const uint64_t bq = tc05::sdesc(qb + (ks / 4) * CC::QPLANE + (ks % 4) * 32, 16, 1024);
-                            tc05::mma(tS + sb * 32, a, bq, id_qk, ks > 0);
+                            tc05::mma(tS + sb * 64 + 32 * (ks & 1), a, bq, id_qk, ks > 1);
                         }
                         tc05::commit(&bars[CC::B_SFULL + sb]);
                         pk[gq & 3] = min(TPS, q_total - TPS * q_s);
@@ -637,14 +662,15 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
             bool fail = false;
             for (int s = 0; s < n_st; ++s, ++g) {
                 const int slot = g % NSTAGE, sb = g & 1;
-                const bool oks = wait(CC::B_SFULL + sb, (uint32_t)((g >> 1) & 1));
+                const bool oks = wait_poll(CC::B_SFULL + sb, (uint32_t)((g >> 1) & 1));
                 if (softmax_any(!oks || aborted())) {
                     fail = true;
                     break;
                 }
                 tc05::fence_after_sync();
-                uint32_t sv[8];
-                tc05::ld8(tS + sb * 32 + r0 + tl, sv);
+                uint32_t sv[8], sv2[8];
+                tc05::ld8(tS + sb * 64 + r0 + tl, sv);
+                tc05::ld8(tS + sb * 64 + 32 + r0 + tl, sv2);
                 tc05::wait_ld();
                 tc05::fence_before_sync();
                 __syncwarp();
@@ -670,7 +696,7 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const bool live = valid && r0 + i >= rlo && r0 + i < rhi;
-                    x[i] = live ? __uint_as_float(sv[i]) * p.qscale : -INFINITY;
+                    x[i] = live ? (__uint_as_float(sv[i]) + __uint_as_float(sv2[i])) * p.qscale : -INFINITY;
                     over |= x[i] > mref[i] + kSlack;   // a row with no token yet: any live score
                 }
                 if (softmax_any(over)) {
@@ -708,13 +734,18 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
                         okr = wait(CC::B_STFREE + (g - 1) % NSTAGE, (uint32_t)(((g - 1) / NSTAGE) & 1));
                         if (okr) {
                             tc05::fence_after_sync();
-                            uint32_t ov[8];
-                            tc05::ld8(tO + r0 + tl, ov);
+                            uint32_t ov[4][8];   // (even, odd tile) x (hi, lo) columns of the group's rows
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                tc05::ld8(tO + 32 * q + r0 + tl, ov[q]);
                             tc05::wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha[i]);
-                            tc05::st8(tO + r0 + tl, ov);
+                            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    ov[q][i] = __float_as_uint(__uint_as_float(ov[q][i]) * alpha[i]);
+                                tc05::st8(tO + 32 * q + r0 + tl, ov[q]);
+                            }
                             tc05::wait_st();
                         }
                     }
@@ -743,12 +774,13 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
                         const float2 hf = Mma<T>::unpack(h[w2]);
                         lo[w2] = Mma<T>::pack(a0 - hf.x, a1 - hf.y);
                     }
-                    const uint32_t a = smem_u32(kb) + (uint32_t)((t >> 3) * 1024 + (t & 7) * 128) +
-                                       (uint32_t)(((j ^ (t & 7)) & 7) << 4);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h[0]), "r"(h[1]),
+                    const uint32_t row = smem_u32(kb) + (uint32_t)((t >> 3) * 1024 + (t & 7) * 128);
+                    const uint32_t ah = row + (uint32_t)(((j ^ (t & 7)) & 7) << 4);
+                    const uint32_t al = row + (uint32_t)((((4 + j) ^ (t & 7)) & 7) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ah), "r"(h[0]), "r"(h[1]),
                                  "r"(h[2]), "r"(h[3])
                                  : "memory");
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a + CC::PLANE), "r"(lo[0]),
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(al), "r"(lo[0]),
                                  "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
                                  : "memory");
                 }
@@ -797,13 +829,23 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
                 if (lane == i)
                     red2[qw * CC::N + r0 + i] = v;
             }
-            uint32_t ov[8];
+            float ov[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                ov[i] = 0u;
+                ov[i] = 0.f;
             if (n_st > 0) {
-                tc05::ld8(tO + r0 + tl, ov);
+                // the four partial sums; the odd-tile ones hold nothing of an
+                // item with a single tile
+                uint32_t o4[4][8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tc05::ld8(tO + 32 * q + r0 + tl, o4[q]);
                 tc05::wait_ld();
+                const bool odd = total > 1;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)   // (even hi + even lo) + (odd hi + odd lo)
+                    ov[i] = (__uint_as_float(o4[0][i]) + __uint_as_float(o4[1][i])) +
+                            (odd ? __uint_as_float(o4[2][i]) + __uint_as_float(o4[3][i]) : 0.f);
             }
             tc05::fence_before_sync();
             softmax_sync();
@@ -819,7 +861,7 @@ pa_cascade_tc05_kernel(const __grid_constant__ DecodeParams p, const __grid_cons
                     const float L = (red2[r] + red2[CC::N + r]) + (red2[2 * CC::N + r] + red2[3 * CC::N + r]);
                     const int64_t sh = row_head(p, w, G, r);
                     const bool bad = failed_all || ((badrows >> r) & 1u);
-                    const float o = __uint_as_float(ov[i]);
+                    const float o = ov[i];
                     if ((fin >> r) & 1u) {
                         store_out(p.out, p.out_dtype, sh * D + t,
                                   (zero || bad || !(L > 0.f)) ? 0.f : o * (1.f / L));
