@@ -530,10 +530,11 @@ def traffic_for(cfg, kernel, algo_bytes):
 _PACK_ALIGN = 256   # every piece of a packed step starts on a 256-byte boundary
 
 
-def _pack_pinned(tensors):
-    """One pinned host buffer holding the given CPU tensors back to back
-    (each 256-byte aligned), and where each one sits: the step's inputs then
-    cross to the device in one copy instead of one per tensor."""
+def _pack_pinned(tensors, pin=True):
+    """One host buffer (pinned unless `pin` is false) holding the given CPU
+    tensors back to back (each 256-byte aligned), and where each one sits:
+    the step's inputs then cross to the device in one copy instead of one
+    per tensor."""
     layout, off = {}, 0
     for name, t in tensors.items():
         t = t.contiguous()
@@ -541,7 +542,7 @@ def _pack_pinned(tensors):
         layout[name] = (off, tuple(t.shape), t.dtype, nbytes)
         off += -(-nbytes // _PACK_ALIGN) * _PACK_ALIGN
     buf = torch.empty(max(off, _PACK_ALIGN), dtype=torch.uint8)
-    if torch.cuda.is_available():
+    if pin and torch.cuda.is_available():
         buf = buf.pin_memory()
     for name, t in tensors.items():
         o, shape, dtype, nbytes = layout[name]
@@ -561,9 +562,11 @@ def _unpack(dev_buf, layout):
 def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
     """Same step, inputs from pinned host memory, output read back, all timed.
     Each step's inputs (q, new K/V, slot mapping, block tables, lengths,
-    copy-on-write pairs, the shared-prefix plan) were packed into one pinned
-    buffer when the step was prepared, so a step makes one host-to-device
-    copy and one device-to-host copy of the output.  As in the device-timed
+    copy-on-write pairs, the shared-prefix plan) were packed into one buffer
+    when the step was prepared; before the step they are placed in the one
+    pinned staging buffer the loop reuses (as a serving loop reuses its
+    own), so a step makes one host-to-device copy and one device-to-host
+    copy of the output.  As in the device-timed
     loop, the GPU is kept busy while the host enqueues a step (a serving loop
     prepares step n + 1 while step n runs), so the events time the copies and
     kernels rather than Python's launch latency."""
@@ -578,8 +581,12 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
             d["cow_pairs"] = s.cow_pairs.cpu()
         if s.plan is not None:
             d["plan"] = torch.from_numpy(s.plan.host)
-        packed.append(_pack_pinned(d))
-    dev_buf = torch.empty(max(b.numel() for b, _ in packed), dtype=torch.uint8, device=dev)
+        packed.append(_pack_pinned(d, pin=False))
+    stage_bytes = max(b.numel() for b, _ in packed)
+    dev_buf = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
+    stage = torch.empty(stage_bytes, dtype=torch.uint8)
+    if torch.cuda.is_available():
+        stage = stage.pin_memory()
     # each step's device views of the staging buffer, made with the step
     views = [_unpack(dev_buf, layout) for _, layout in packed]
     out_host = torch.empty(state.out.shape, dtype=state.out.dtype).pin_memory()
@@ -587,7 +594,9 @@ def run_e2e(state, steps, host_inputs, P, flush, bytes_step):
     total_ms = 0.0
     gc.collect()      # no collector pass inside the timed steps
     gc.disable()
-    for s, (hbuf, _), t in zip(steps, packed, views):
+    for s, (pbuf, _), t in zip(steps, packed, views):
+        hbuf = stage[:pbuf.numel()]
+        hbuf.copy_(pbuf)   # the previous step's copies are done (its end event was waited for)
         dst = dev_buf[:hbuf.numel()]
         _flush_l2(flush)
         _preroll()    # the host enqueues the step while the GPU is busy, as in a pipelined loop

@@ -43,8 +43,8 @@ struct CascadeCfg {
     static constexpr int SEGS = plan::item_segments_offset();
     static constexpr int TABLE_CAP = plan::kTableCap;
     // ring | barriers | flag | q rows | item copy (with its block ids) | bad
-    // flag per segment, members' expected partial counts, bad-row and
-    // bad-length masks | per-row warp weights | the list's next item
+    // flag per segment, members' expected partial counts, a spare int and the
+    // bad-length mask | per-row warp weights | the list's next item
     static constexpr int OFF_STAGES = 0;
     static constexpr int OFF_BAR = C::STAGES_BYTES;
     static constexpr int OFF_FLAG = OFF_BAR + NW * S * 8;
@@ -90,8 +90,8 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     int32_t *it = reinterpret_cast<int32_t *>(smem + CC::OFF_ITEM);
     int32_t *segbad = it + CC::ITEM_INTS;    // segment k addresses a bad block
     int32_t *exp_s = segbad + CC::MAXSEG;    // expected partials per member
-    uint32_t *badrows = reinterpret_cast<uint32_t *>(exp_s + plan::kMaxRows);
-    uint32_t *lenbad = badrows + 1;          // members whose device length differs from the plan's
+    // members whose device length differs from the plan's
+    uint32_t *lenbad = reinterpret_cast<uint32_t *>(exp_s + plan::kMaxRows) + 1;
     uint32_t *cta_flag = reinterpret_cast<uint32_t *>(smem + CC::OFF_FLAG);
     if (tid == 0) {
         prefetch_tensormap(&tmk);
@@ -214,17 +214,16 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                 tma_load_5d(vd + b * C::BOX_BYTES, &tmv, &bars[st], 0, tok % BS, 0, kvh, phys);
             }
         };
-        if (lane == 0)
-            for (int i = 0; i < (my_n < S ? my_n : S); ++i)
-                issue(i, (ring + i) % S);
-
-        // ---- while the first tiles load: the device tables must hold the plan's
-        // block ids (every member's table for a shared prefix segment, the
-        // segment's own table otherwise); q rows to shared memory; the members'
-        // expected partial counts and lengths.  The q rows, the first
-        // 4 * NW * 32 table entries and the members' counts and lengths are all
-        // loaded before any of them is used, so the start costs one round trip;
-        // an item with more entries to check takes more rounds after it.
+        // ---- the item's small loads, then its first tiles: the device tables
+        // must hold the plan's block ids (every member's table for a shared
+        // prefix segment, the segment's own table otherwise); q rows to shared
+        // memory; the members' expected partial counts and lengths.  The q
+        // rows, the first 4 * NW * 32 table entries and the members' counts and
+        // lengths are all requested before any of them is used, and before the
+        // ring's tile loads, so that they do not queue behind a whole grid's
+        // tiles: the start costs one round trip, and the tiles land while the
+        // rows are stored.  An item with more entries to check takes more
+        // rounds after it.
         const int vtotal = invalid_item ? 0 : it[plan::I_CHECKS];
         int got[4], want[4], kk[4];
         auto load_checks = [&](int x0) {
@@ -257,8 +256,8 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                     segbad[kk[u]] = 1;
         };
         typename CC::Engine::QRows qrows;
-        load_checks(0);
         qrows.load(p, w);
+        load_checks(0);
         int m_exp = 0, m_plen = 0, m_len = 0;
         if (tid < nmem) {
             const int sq = members[tid];
@@ -266,6 +265,9 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             m_plen = plan_lens[sq];
             m_len = p.context_lens[sq];
         }
+        if (lane == 0)
+            for (int i = 0; i < (my_n < S ? my_n : S); ++i)
+                issue(i, (ring + i) % S);
         fold_checks();
         qrows.store(smem + CC::OFF_Q);
         if (tid < nmem) {
@@ -316,50 +318,45 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             eng.finish(mw, lw, aw, warp, lane, nrows);
         }
         ring += my_n;
-        // rows served by a segment with a bad or disagreeing block id (marked by
-        // the table check or by any issue of the loop) or of a member whose
-        // length disagrees
-        if (tid == 0) {
-            bool any = invalid_item;
-            uint32_t mask = 0;
-            for (int k = 0; k < nseg && k < CC::MAXSEG; ++k)
-                if (segbad[k]) {
-                    any = true;
-                    for (int r = seg(k)[plan::S_ROW_LO]; r < seg(k)[plan::S_ROW_HI] && r < 32; ++r)
-                        mask |= 1u << r;
-                }
-            const uint32_t lb = *lenbad;
-            for (int m = 0; m < nmem; ++m)
-                if ((lb >> m) & 1u)
-                    mask |= ((1u << G) - 1u) << (m * G);
-            *badrows = mask;
-            if (any)
-                report(p.status, PKV_DEV_BAD_BLOCK);
-            if (lb)
-                report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
-        }
+        // The warps' (max, sum, acc) are in the scratch and every mark of a bad
+        // block is in.
         __syncthreads();
 
         // ---- every row's result: the output itself for a sequence this item
         // holds entirely, otherwise this item's partial (read by the merge
-        // through L2).  One thread per row folds the warps' (max, sum) into
-        // weights in shared memory (1 / sum included for a final row); then
-        // float4 pieces of the accumulators.
+        // through L2).  One thread per row finds whether the row fails -- a
+        // segment serving it addresses a bad or disagreeing block id (marked by
+        // the table check or by any issue of the loop), or its member's length
+        // disagrees -- and folds the warps' (max, sum) into weights in shared
+        // memory (1 / sum included for a final row); then float4 pieces of the
+        // accumulators.
         const bool failed_all =
             invalid_item || *reinterpret_cast<volatile uint32_t *>(cta_flag) != 0;
         if (tid < nrows) {
             const int r = tid;
-            const bool failed = failed_all || ((*badrows >> r) & 1u);
+            const uint32_t lb = *lenbad;
+            bool bad = failed_all || ((lb >> (r / G)) & 1u);
+            for (int k = 0; k < nseg && k < CC::MAXSEG; ++k)
+                bad = bad || (segbad[k] && r >= seg(k)[plan::S_ROW_LO] && r < seg(k)[plan::S_ROW_HI]);
+            if (r == 0) {
+                bool any = invalid_item;
+                for (int k = 0; k < nseg && k < CC::MAXSEG; ++k)
+                    any = any || segbad[k] != 0;
+                if (any)
+                    report(p.status, PKV_DEV_BAD_BLOCK);
+                if (lb)
+                    report(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+            }
             const bool final_row = exp_s[r / G] == 1;
             float M = -INFINITY, den = 0.f, f[NW];
 #pragma unroll
             for (int k = 0; k < NW; ++k)
-                M = fmaxf(M, failed ? -INFINITY : mw[k * RS + r]);
+                M = fmaxf(M, bad ? -INFINITY : mw[k * RS + r]);
 #pragma unroll
             for (int k = 0; k < NW; ++k) {
-                const float mk = failed ? -INFINITY : mw[k * RS + r];
+                const float mk = bad ? -INFINITY : mw[k * RS + r];
                 f[k] = mk == -INFINITY ? 0.f : exp2f(mk - M);
-                den += failed ? 0.f : f[k] * lw[k * RS + r];
+                den += bad ? 0.f : f[k] * lw[k * RS + r];
             }
             const float norm = !final_row ? 1.f : (den > 0.f ? 1.f / den : 0.f);
 #pragma unroll
@@ -368,7 +365,7 @@ pa_cascade_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             if (!final_row) {
                 const int64_t base = row_head(p, w, G, r) * slots + slot;
                 __stcg(reinterpret_cast<float2 *>(p.ws_ml) + base,
-                       make_float2(failed ? -INFINITY : M, failed ? -1.f : den));
+                       make_float2(bad ? -INFINITY : M, bad ? -1.f : den));
             }
         }
         __syncthreads();
