@@ -873,6 +873,11 @@ pa_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__
     init_rings<DecodeCfg<T, D, BS, G, TC>>(smem);
     int ring = 0;
     decode_cta<T, D, BS, G, TC, 1>(p, &tmk, &tmv, smem, w, ring);
+    // split path: the merge grid, queued behind this one as a programmatic
+    // dependent, may be scheduled once every CTA has stored its partials
+    // (it waits for the whole grid before reading them)
+    if (p.split)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace pkv

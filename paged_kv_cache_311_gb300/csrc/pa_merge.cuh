@@ -1,7 +1,7 @@
 // pa_merge.cuh -- the log-sum-exp merge of split-context partials: the
-// half-warp routine merge_partials (also used by pa_cascade_merge_kernel in
-// pa_cascade.cuh) and pa_merge_kernel, which runs it for every (sequence,
-// head) after the split-context pass.
+// half-warp routine merge_partials (pa_cascade_merge_kernel in
+// pa_cascade.cuh runs it for the few partials of a shared-prefix plan) and
+// pa_merge_kernel, one CTA per (sequence, head) after the split-context pass.
 #pragma once
 
 #include "pa_decode.cuh"
@@ -99,26 +99,160 @@ __device__ __forceinline__ void merge_partials(const DecodeParams &p, int64_t sh
                                num[4 * v + 3] * inv));
 }
 
-// Merge after the split-context pass: one half-warp per (sequence, head),
-// eight per CTA; the valid slots are the ceil(L / P) partitions of the
-// context (up to 64 and more for long contexts: chunks of eight slots).
+// Merge after the split-context pass: one CTA of kSplitMergeWarps warps per
+// (sequence, head), whose valid slots are the ceil(L / P) partitions of the
+// context (64 at 32K tokens in 512-token partitions).  The partitions are
+// dealt round-robin to the warps, and within a warp to SPI slot lanes (lane
+// = sub-slot * (D / 4) + float4 piece), so that the loads of up to
+// kSplitMergeWarps * SPI * kSplitMergeU partials leave together: a long
+// context costs one round trip to L2, not one per chunk of slots.  Each lane
+// keeps a running (max, sum, acc piece) over its slots; lanes of one piece
+// combine by shuffles, then the warps in shared memory, each step the same
+// log-sum-exp merge:
+//   out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k,  M = max_k m_k.
+// A partial with l < 0 marks a failed pass and zeroes the row; so does a
+// context length outside [0, max_context_len] (reported once per sequence).
+constexpr int kSplitMergeWarps = 8, kSplitMergeU = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128) pa_merge_kernel(const __grid_constant__ DecodeParams p)
+__global__ void __launch_bounds__(kSplitMergeWarps * 32)
+pa_merge_kernel(const __grid_constant__ DecodeParams p)
 {
-    const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
-    const int64_t sh = (int64_t)blockIdx.x * 8 + hw;
-    if (sh >= (int64_t)p.num_seqs * p.num_heads)
-        return;
+    constexpr int W = kSplitMergeWarps, U = kSplitMergeU;
+    constexpr int PPR = D / 4;          // float4 pieces of a row
+    static_assert(PPR <= 32 && 32 % PPR == 0, "a row's pieces fit one warp");
+    constexpr int SPI = 32 / PPR;       // slots a warp reads side by side
+    constexpr int ST = W * SPI;         // slot stride of one lane
+    __shared__ float s_m[W], s_l[W];
+    __shared__ int s_bad[W];
+    __shared__ float4 s_acc[W][PPR];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int piece = lane % PPR, sub = lane / PPR;
+    const int64_t sh = blockIdx.x;
     const int seq = (int)(sh / p.num_heads);
-    merge_partials<D, 8>(p, sh, p.num_partitions, hl, [&]() {
-        const int L = p.context_lens[seq];
-        if (L < 0 || L > p.max_context_len) {
-            if (hl == 0 && sh % p.num_heads == 0)
-                report(p.status, PKV_DEV_BAD_CONTEXT_LEN);  // the partition pass skipped it silently
-            return kMergeZero;
+    const int slots = p.num_partitions;
+    const int first = warp * SPI + sub;   // this lane's slots: first + j * ST
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + sh * slots;
+    const float4 *acc = reinterpret_cast<const float4 *>(p.ws_acc + sh * slots * D) + piece;
+
+    float2 t[U];
+    float4 a[U];
+    auto load_round = [&](int j0, int lim) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int k = first + (j0 + u) * ST;
+            t[u] = make_float2(-INFINITY, 0.f);
+            a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < lim) {
+                t[u] = __ldcg(ml + k);
+                a[u] = __ldcg(acc + (int64_t)k * PPR);
+            }
         }
-        return (L + p.partition_size - 1) / p.partition_size;
-    });
+    };
+    // launched as a programmatic dependent of the partition pass: the
+    // lengths (an input) may be read at once, the partials only after the
+    // whole pass is done.  The first round's loads then leave before the
+    // length they depend on is used: they lie inside the row's slots
+    // whatever it turns out to be, and slots >= n are ignored below.
+    const int L = p.context_lens[seq];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    load_round(0, slots);
+    const bool bad_len = L < 0 || L > p.max_context_len;
+    if (bad_len && threadIdx.x == 0 && sh % p.num_heads == 0)
+        report(p.status, PKV_DEV_BAD_CONTEXT_LEN);   // the partition pass skipped it silently
+    const int n = bad_len ? 0 : (L + p.partition_size - 1) / p.partition_size;
+
+    float M = -INFINITY, den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool invalid = bad_len;
+    for (int j0 = 0; first + j0 * ST < n; j0 += U) {
+        if (j0 > 0)
+            load_round(j0, n);
+        float Mc = M;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (first + (j0 + u) * ST < n) {
+                Mc = fmaxf(Mc, t[u].x);
+                invalid |= t[u].y < 0.f;
+            }
+        }
+        if (Mc == -INFINITY)
+            continue;   // nothing attended so far
+        const float sc = exp2f(M - Mc);   // 0 while M is still -inf
+        den *= sc;
+        num.x *= sc;
+        num.y *= sc;
+        num.z *= sc;
+        num.w *= sc;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (first + (j0 + u) * ST < n && t[u].x != -INFINITY) {
+                const float f = exp2f(t[u].x - Mc);
+                den += f * t[u].y;
+                num.x += f * a[u].x;
+                num.y += f * a[u].y;
+                num.z += f * a[u].z;
+                num.w += f * a[u].w;
+            }
+        }
+        M = Mc;
+    }
+    // lanes holding the same piece for different sub-slots, then the warps
+#pragma unroll
+    for (int off = PPR; off < 32; off <<= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
+        const float lo = __shfl_xor_sync(0xffffffffu, den, off);
+        float4 no;
+        no.x = __shfl_xor_sync(0xffffffffu, num.x, off);
+        no.y = __shfl_xor_sync(0xffffffffu, num.y, off);
+        no.z = __shfl_xor_sync(0xffffffffu, num.z, off);
+        no.w = __shfl_xor_sync(0xffffffffu, num.w, off);
+        invalid |= __shfl_xor_sync(0xffffffffu, (int)invalid, off) != 0;
+        const float Mn = fmaxf(M, Mo);
+        const float fa = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        const float fb = Mo == -INFINITY ? 0.f : exp2f(Mo - Mn);
+        den = fa * den + fb * lo;
+        num = make_float4(fa * num.x + fb * no.x, fa * num.y + fb * no.y, fa * num.z + fb * no.z,
+                          fa * num.w + fb * no.w);
+        M = Mn;
+    }
+    if (lane < PPR) {
+        s_acc[warp][piece] = num;
+        if (lane == 0) {
+            s_m[warp] = M;
+            s_l[warp] = den;
+            s_bad[warp] = invalid;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < PPR) {
+        float Mt = -INFINITY;
+        bool inv = false;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            Mt = fmaxf(Mt, s_m[w]);
+            inv |= s_bad[w] != 0;
+        }
+        float dt = 0.f;
+        float4 nt = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Mt != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float f = s_m[w] == -INFINITY ? 0.f : exp2f(s_m[w] - Mt);
+                const float4 x = s_acc[w][threadIdx.x];
+                dt += f * s_l[w];
+                nt.x += f * x.x;
+                nt.y += f * x.y;
+                nt.z += f * x.z;
+                nt.w += f * x.w;
+            }
+        }
+        const bool zero = inv || dt == 0.f;
+        const float inv_d = zero ? 0.f : 1.f / dt;
+        store_out4(p.out, p.out_dtype, sh * D + 4 * threadIdx.x,
+                   make_float4(nt.x * inv_d, nt.y * inv_d, nt.z * inv_d, nt.w * inv_d));
+    }
 }
 
 }  // namespace pkv

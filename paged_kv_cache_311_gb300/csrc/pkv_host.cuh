@@ -108,9 +108,10 @@ int run_decode(const DecodeLaunch &a)
     rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), Sh::smem, &done);
     if (rc)
         return rc;
-    // Plain launches: a programmatic dependent launch of these two measured
-    // ~3% slower on the long-context workload (the merge grid's early CTAs
-    // ride along the partition pass's many waves).
+    // The merge is a programmatic dependent of the partition pass, whose CTAs
+    // allow it only as their last act: it is scheduled as the pass's last
+    // wave ends, not beside its many earlier waves (an early trigger measured
+    // ~3% slower on the long-context workload).
     dim3 grid(p.num_partitions, p.num_kv_heads, p.num_seqs);
     kern<<<grid, Sh::threads, Sh::smem, a.stream>>>(p, tmk, tmv);
     if (p.split) {
@@ -118,8 +119,10 @@ int run_decode(const DecodeLaunch &a)
         rc = ensure_smem_attr(reinterpret_cast<const void *>(pa_merge_kernel<D>), 0, &merge_done);
         if (rc)
             return rc;
-        pa_merge_kernel<D><<<(unsigned)(((long long)p.num_seqs * p.num_heads + 7) / 8), 128, 0,
-                             a.stream>>>(p);
+        rc = launch_pdl(pa_merge_kernel<D>, dim3((unsigned)((long long)p.num_seqs * p.num_heads)),
+                        dim3(kSplitMergeWarps * 32), 0, a.stream, p);
+        if (rc)
+            return rc;
     }
     if (a.engine_used)
         *a.engine_used = TC ? kEngineTensorCore : kEngineCudaCore;
