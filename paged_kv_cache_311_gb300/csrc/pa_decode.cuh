@@ -365,6 +365,17 @@ struct CcEngine {
     }
 };
 
+// 2^x on the special-function unit (ex2.approx.ftz: relative error near
+// 2^-22, subnormal results flushed to zero), for the probabilities of the
+// tensor-core engine: each is at most 2^8 and is split into 16-bit high and
+// low parts that keep 16 bits of it, far coarser than that error.
+__device__ __forceinline__ float ex2_fast(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------- tensor cores
 // NT n-tiles of 8 query rows each (NT = 1 for one sequence's G <= 8 heads).
 // QS: the q^T B-fragments are read from a shared-memory copy of the rows
@@ -519,11 +530,13 @@ struct TcEngine {
                     }
             }
         }
+        if constexpr (NT == 1 || !QS) {   // QS with several n-tiles: one chain per n-tile
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                s[nt][j] += s2[nt][j];
+                for (int j = 0; j < 4; ++j)
+                    s[nt][j] += s2[nt][j];
+        }
 
         // ---- online softmax in the log2 domain: this lane holds tokens g,
         // g + 8 of rows 2c, 2c + 1.  Each row keeps a reference maximum m.
@@ -559,8 +572,8 @@ struct TcEngine {
                     // rows still without a token have no live score here: the
                     // finite stand-in keeps 2^(-inf - m) at 0 instead of NaN
                     const float mr = fmaxf(m[nt][j], -1e30f);
-                    p0[nt][j] = exp2f(x0[nt][j] - mr);
-                    p1[nt][j] = exp2f(x1[nt][j] - mr);
+                    p0[nt][j] = ex2_fast(x0[nt][j] - mr);
+                    p1[nt][j] = ex2_fast(x1[nt][j] - mr);
                     lsum[nt][j] += p0[nt][j] + p1[nt][j];
                 }
             }
@@ -578,10 +591,10 @@ struct TcEngine {
                     const float mn = fmaxf(m[nt][j], tm);
                     // a row with no token yet keeps max -inf: nothing to rescale or add
                     const bool none = mn == -INFINITY;
-                    alpha[nt][j] = none ? 1.f : exp2f(m[nt][j] - mn);
+                    alpha[nt][j] = none ? 1.f : ex2_fast(m[nt][j] - mn);
                     grew |= mn != m[nt][j];
-                    p0[nt][j] = none ? 0.f : exp2f(x0[nt][j] - mn);
-                    p1[nt][j] = none ? 0.f : exp2f(x1[nt][j] - mn);
+                    p0[nt][j] = none ? 0.f : ex2_fast(x0[nt][j] - mn);
+                    p1[nt][j] = none ? 0.f : ex2_fast(x1[nt][j] - mn);
                     lsum[nt][j] = lsum[nt][j] * alpha[nt][j] + p0[nt][j] + p1[nt][j];
                     m[nt][j] = mn;
                 }
