@@ -484,17 +484,41 @@ struct TcEngine {
         }
     }
 
-    // Rows outside [row_lo, row_hi) ignore the tile (their state is unchanged);
-    // n-tiles without such a row issue no MMA.
+    // Rows outside [row_lo, row_hi) ignore the tile (their state is unchanged):
+    // only the n-tiles holding such rows run, each range of them in its own
+    // straight-line copy of the tile (a tail tile of one member costs one
+    // n-tile's MMAs and softmax, not NT's).
     __device__ void tile(uint32_t kbase, uint32_t vbase, int nvalid, int lane, int row_lo = 0,
                          int row_hi = 1 << 30)
     {
         const int nlo = row_lo >> 3, nhi = min(ntl, (row_hi + 7) >> 3);
+        if constexpr (NT == 1) {
+            if (nhi > nlo)
+                tile_rows<0, 1>(kbase, vbase, nvalid, lane, row_lo, row_hi);
+        } else {
+            static_assert(NT == 3, "n-tile ranges are dispatched for NT = 1 and 3");
+            switch (nlo * 4 + nhi) {
+            case 0 * 4 + 3: tile_rows<0, 3>(kbase, vbase, nvalid, lane, row_lo, row_hi); break;
+            case 0 * 4 + 1: tile_rows<0, 1>(kbase, vbase, nvalid, lane, row_lo, row_hi); break;
+            case 1 * 4 + 2: tile_rows<1, 2>(kbase, vbase, nvalid, lane, row_lo, row_hi); break;
+            case 2 * 4 + 3: tile_rows<2, 3>(kbase, vbase, nvalid, lane, row_lo, row_hi); break;
+            case 0 * 4 + 2: tile_rows<0, 2>(kbase, vbase, nvalid, lane, row_lo, row_hi); break;
+            case 1 * 4 + 3: tile_rows<1, 3>(kbase, vbase, nvalid, lane, row_lo, row_hi); break;
+            default: break;   // no n-tile holds a row of the tile
+            }
+        }
+    }
+
+    // The tile over n-tiles [N0, N1).
+    template <int N0, int N1>
+    __device__ __forceinline__ void tile_rows(uint32_t kbase, uint32_t vbase, int nvalid, int lane,
+                                              int row_lo, int row_hi)
+    {
         // ---- S^T (16 tokens x 8 query rows per n-tile) = K q^T, as two
         // independent accumulation chains (even / odd k-steps)
         float s[NT][4], s2[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = N0; nt < N1; ++nt)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 s[nt][j] = s2[nt][j] = 0.f;
@@ -507,8 +531,7 @@ struct TcEngine {
                 ldsm_x4(kbase + chunk_off(2 * kp) + koff[(2 * kp) & 3], a0);
                 ldsm_x4(kbase + chunk_off(2 * kp + 1) + koff[(2 * kp + 1) & 3], a1);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    if (nt >= nlo && nt < nhi) {
+                for (int nt = N0; nt < N1; ++nt) {
                         uint32_t b[4];
                         ldsm_x4(qaddr + nt * 8 * QROWB + kp * 64, b);
                         Mma<T>::run(s[nt], a0, b[0], b[1]);
@@ -521,8 +544,7 @@ struct TcEngine {
                 uint32_t a[4];
                 ldsm_x4(kbase + chunk_off(ks) + koff[ks & 3], a);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    if (nt >= nlo && nt < nhi) {
+                for (int nt = N0; nt < N1; ++nt) {
                         if (ks & 1)
                             Mma<T>::run(s2[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
                         else
@@ -532,7 +554,7 @@ struct TcEngine {
         }
         if constexpr (NT == 1 || !QS) {   // QS with several n-tiles: one chain per n-tile
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = N0; nt < N1; ++nt)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     s[nt][j] += s2[nt][j];
@@ -553,7 +575,7 @@ struct TcEngine {
         float x0[NT][2], x1[NT][2], p0[NT][2], p1[NT][2];
         bool over = false;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = N0; nt < N1; ++nt) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int row = 8 * nt + 2 * c + j;
@@ -566,7 +588,7 @@ struct TcEngine {
         }
         if (!__any_sync(0xffffffffu, over)) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = N0; nt < N1; ++nt) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     // rows still without a token have no live score here: the
@@ -581,7 +603,7 @@ struct TcEngine {
             float alpha[NT][2];
             bool grew = false;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = N0; nt < N1; ++nt) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     float tm = fmaxf(x0[nt][j], x1[nt][j]);
@@ -602,7 +624,7 @@ struct TcEngine {
             // rescale the accumulators only when some row's running maximum moved
             if (__any_sync(0xffffffffu, grew)) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int nt = N0; nt < N1; ++nt)
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
                         o[mt][nt][0] *= alpha[nt][0];
@@ -628,7 +650,7 @@ struct TcEngine {
         // ---- P^T B-fragments: P = hi + lo in the cache's 16-bit type
         uint32_t bh[NT][2], bl[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = N0; nt < N1; ++nt) {
             const uint32_t h0 = Mma<T>::pack(p0[nt][0], p0[nt][1]);  // tokens g,   rows 2c, 2c+1
             const uint32_t h1 = Mma<T>::pack(p1[nt][0], p1[nt][1]);  // tokens g+8, rows 2c, 2c+1
             const float2 f0 = Mma<T>::unpack(h0), f1 = Mma<T>::unpack(h1);
@@ -647,11 +669,9 @@ struct TcEngine {
                 uint32_t a[4];
                 ldsm_x4_trans(vbase + chunk_off(mt) + voff[mt & 3], a);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (nt >= nlo && nt < nhi) {
-                        Mma<T>::run(o[mt][nt], a, bh[nt][0], bh[nt][1]);
-                        Mma<T>::run(o[mt][nt], a, bl[nt][0], bl[nt][1]);
-                    }
+                for (int nt = N0; nt < N1; ++nt) {
+                    Mma<T>::run(o[mt][nt], a, bh[nt][0], bh[nt][1]);
+                    Mma<T>::run(o[mt][nt], a, bl[nt][0], bl[nt][1]);
                 }
             }
         }
