@@ -70,6 +70,35 @@ def test_long_context_split_path(engine):
         assert max_err(got, ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("engine", ["cuda_core", "tensor_core"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_split_merge_over_many_rounds(D, engine):
+    """Hundreds of 32-token partitions per context: the merge reads a
+    context's slots in several rounds (eight warps, one slot lane each at
+    head_dim 128 and two at 64, eight slots per lane per round), and keys
+    carry a component along a fixed direction proportional to their
+    position that every query shares, so the scores climb through the
+    context and each round raises the running maxima.  An empty context and
+    a one-partition one sit beside them."""
+    lens = (5000, 1, 0, 2100, 40)
+    case = small_case(77 + D, dtype="bf16", B=5, H=8, Hk=2, D=D, bs=16, lens=lens)
+    bt = case["block_tables"]
+    kc = case["k_cache"].float()
+    u = torch.zeros(D)
+    u[:8] = 1.0
+    for s, L in enumerate(lens):
+        for t in range(L):
+            kc[int(bt[s, t // 16]), :, t % 16, :] += 0.01 * t * u
+    case = dict(case, k_cache=kc.to(torch.bfloat16), q=(case["q"].float() + u).to(torch.bfloat16))
+    ref, st = oracle_decode(case)
+    assert st == 0
+    for P in (32, 64):
+        got, gst, launches = gpu_decode(case, partition_size=P, engine=engine)
+        assert gst == 0 and launches == 2
+        assert not got[2].any()
+        assert max_err(got, ref) <= TOL["bf16"], f"P={P}"
+
+
 @pytest.mark.parametrize("dtype,engine", [("f32", "cuda_core"), ("bf16", "cuda_core"),
                                           ("bf16", "tensor_core"), ("f16", "tensor_core")])
 def test_empty_and_single_token(dtype, engine):
