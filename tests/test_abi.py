@@ -52,6 +52,9 @@ def test_workspace_bytes(lib):
     assert pkv.paged_attention_workspace_bytes(B, H, L, D, 0) == expect
     assert pkv.paged_attention_workspace_bytes(B, H, L, D, 512) == expect
     assert pkv.paged_attention_workspace_bytes(0, H, L, D, 0) == 0
+    # sizes whose byte count passes 64 bits report 0 (the decode call then
+    # refuses them) instead of a wrapped-around size
+    assert pkv.paged_attention_workspace_bytes(65535, 65535, 1 << 30, 128, 32) == 0
 
 
 def _decode(lib, **kw):
